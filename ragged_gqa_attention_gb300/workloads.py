@@ -1,0 +1,220 @@
+"""Seeded synthetic inputs for ragged GQA attention.
+
+This module only draws random numbers and lays them out in the padded_bhnd /
+packed_nhd forms of the "TensorRT Custom Operator Schemas" page (TRT_Attention,
+tensor format notation).  It holds none of the attention arithmetic, so both
+the CUDA path and the CPU oracle can take their inputs from it.
+
+Recipe (every workload): ``torch.Generator('cpu').manual_seed(seed)``; the draw
+order is lengths, Q, K, V, mask; Q/K/V are drawn as fp32 N(0, 1) and cast to
+the workload dtype with round-to-nearest-even; integer lengths are uniform
+with inclusive bounds.  Rows of padded KV at or beyond a sequence's kv length
+hold ``kv_pad`` (NaN by default, so that any read of them shows in the
+output); packed tensors may carry ``tail`` extra rows past the last sequence,
+filled the same way.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+from typing import Optional
+
+import torch
+
+PADDED = "padded"
+PACKED = "packed"
+
+
+@dataclass
+class Case:
+    """One attention problem on host memory (CPU tensors)."""
+    name: str
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    q_form: str
+    kv_form: str
+    batch: int
+    query_lengths: Optional[torch.Tensor]   # int32 [B+1] cumulative, or None
+    kv_lengths: Optional[torch.Tensor]      # int32 [B+1] cumulative or [B]
+    q_lens: list                            # per-batch valid query rows
+    kv_lens: list                           # per-batch valid key rows
+    scale: float = 1.0
+    causal: str = "none"
+    norm: str = "softmax"
+    mask: Optional[torch.Tensor] = None
+    quant: Optional[str] = None
+    quant_scale: Optional[torch.Tensor] = None
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def q_heads(self):
+        return self.q.shape[-2] if self.q_form == PACKED else self.q.shape[1]
+
+    @property
+    def kv_heads(self):
+        return self.k.shape[-2] if self.kv_form == PACKED else self.k.shape[1]
+
+    @property
+    def head_dim(self):
+        return self.q.shape[-1]
+
+
+def _cum(lens):
+    out = [0]
+    for n in lens:
+        out.append(out[-1] + int(n))
+    return torch.tensor(out, dtype=torch.int32)
+
+
+def _randn(g, shape, dtype):
+    return torch.randn(shape, generator=g, dtype=torch.float32).to(dtype)
+
+
+def make_case(name, seed, *, batch, q_heads, kv_heads, head_dim, q_lens,
+              kv_lens=None, q_form=PADDED, kv_form=PADDED, q_seq=None,
+              kv_seq=None, dtype=torch.float16, scale=None, causal="none",
+              norm="softmax", mask=None, quant=None, quant_scale=None,
+              pass_query_lengths=None, pass_kv_lengths=True, kv_pad=math.nan,
+              tail=0, g=None):
+    """Build a Case from explicit per-batch lengths.
+
+    q_lens / kv_lens: per-batch valid lengths (python ints).  For padded forms
+    the padded extent is ``q_seq`` / ``kv_seq`` (default: the max length).
+    ``pass_query_lengths`` (padded Q) passes the optional cumulative
+    query_lengths; ``pass_kv_lengths`` (padded KV) passes the optional [B]
+    kv_lengths.  ``mask`` is either a ready tensor or a callable
+    ``mask(g) -> tensor`` drawn after V.  ``g`` continues an existing
+    generator (used when the lengths were drawn from it).
+    """
+    if g is None:
+        g = torch.Generator("cpu").manual_seed(seed)
+    kv_lens = list(q_lens) if kv_lens is None else list(kv_lens)
+    q_lens = [int(x) for x in q_lens]
+    kv_lens = [int(x) for x in kv_lens]
+    D = head_dim
+    if q_form == PACKED:
+        T = sum(q_lens) + tail
+        q = _randn(g, (T, q_heads, D), dtype)
+        if tail:
+            q[sum(q_lens):] = kv_pad
+        query_lengths = _cum(q_lens)
+    else:
+        q_seq = max(q_lens + [0]) if q_seq is None else q_seq
+        q = _randn(g, (batch, q_heads, q_seq, D), dtype)
+        query_lengths = _cum(q_lens) if pass_query_lengths else None
+    if kv_form == PACKED:
+        Tk = sum(kv_lens) + tail
+        k = _randn(g, (Tk, kv_heads, D), dtype)
+        v = _randn(g, (Tk, kv_heads, D), dtype)
+        if tail:
+            k[sum(kv_lens):] = kv_pad
+            v[sum(kv_lens):] = kv_pad
+        kv_lengths = _cum(kv_lens)
+    else:
+        kv_seq = max(kv_lens + [0]) if kv_seq is None else kv_seq
+        k = _randn(g, (batch, kv_heads, kv_seq, D), dtype)
+        v = _randn(g, (batch, kv_heads, kv_seq, D), dtype)
+        for b, n in enumerate(kv_lens):
+            k[b, :, n:] = kv_pad
+            v[b, :, n:] = kv_pad
+        kv_lengths = (torch.tensor(kv_lens, dtype=torch.int32)
+                      if pass_kv_lengths else None)
+    if callable(mask):
+        mask = mask(g)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if quant is not None and quant_scale is None:
+        quant_scale = torch.tensor(1.0 / 448.0 if quant == "fp8" else 1.0 / 127.0,
+                                   dtype=torch.float32)
+    return Case(name=name, q=q, k=k, v=v, q_form=q_form, kv_form=kv_form,
+                batch=batch, query_lengths=query_lengths,
+                kv_lengths=kv_lengths, q_lens=q_lens, kv_lens=kv_lens,
+                scale=scale, causal=causal, norm=norm, mask=mask, quant=quant,
+                quant_scale=quant_scale)
+
+
+def _uniform_int(g, lo, hi, n):
+    """n integers uniform on [lo, hi] (inclusive)."""
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
+
+
+# The five named workloads.  Each entry: (name, description).
+WORKLOADS = {
+    1: ("padded_selfattn_b2_h4_n64_d64_fp16",
+        "padded_bhnd B=2 Hq=Hkv=4 N=64 D=64 fp16, scale 1/8, no causal"),
+    2: ("packed_ragged_prefill_gqa32x8_d128_bf16",
+        "packed_nhd Q/KV, B=8 lengths U[128,2048], Hq=32 Hkv=8 D=128 bf16, "
+        "upper_left"),
+    3: ("chunked_packedq_paddedkv8192_gqa32x8_d128_bf16",
+        "packed Q chunks U[64,512], padded KV N=8192 with kv_len "
+        "U[q_len,8192], B=16, Hq=32 Hkv=8 D=128 bf16, lower_right"),
+    4: ("decode_b64_gqa64x8_kv4096_d128_bf16",
+        "packed Q (one token each), padded KV N=4096 with kv_len "
+        "U[256,4096], B=64, Hq=64 Hkv=8 D=128 bf16, lower_right"),
+    5: ("quantized_padded_b4_h16_n4096_d128_fp16",
+        "padded B=4 Hq=Hkv=16 N=4096 D=128 fp16, upper_left, bool key-suffix "
+        "mask [B,1,1,N] of 0-25%, P Q/DQ to fp8 (s=1/448) or int8 (s=1/127)"),
+}
+
+
+def workload(index, *, quant="fp8", kv_pad=math.nan, seed=None):
+    """The named workload ``index`` (1..5) as a Case on host memory.
+
+    ``quant`` selects the fp8 or int8 variant of workload 5.
+    """
+    seed = index if seed is None else seed
+    g = torch.Generator("cpu").manual_seed(seed)
+    name = WORKLOADS[index][0]
+    if index == 1:
+        return make_case(name, seed, batch=2, q_heads=4, kv_heads=4,
+                         head_dim=64, q_lens=[64, 64], dtype=torch.float16,
+                         scale=1.0 / 8.0, kv_pad=kv_pad, g=g)
+    if index == 2:
+        lens = _uniform_int(g, 128, 2048, 8)
+        return make_case(name, seed, batch=8, q_heads=32, kv_heads=8,
+                         head_dim=128, q_lens=lens, kv_lens=lens,
+                         q_form=PACKED, kv_form=PACKED, dtype=torch.bfloat16,
+                         causal="upper_left", kv_pad=kv_pad, g=g)
+    if index == 3:
+        qls = _uniform_int(g, 64, 512, 16)
+        kvls = [_uniform_int(g, ql, 8192, 1)[0] for ql in qls]
+        return make_case(name, seed, batch=16, q_heads=32, kv_heads=8,
+                         head_dim=128, q_lens=qls, kv_lens=kvls,
+                         q_form=PACKED, kv_form=PADDED, kv_seq=8192,
+                         dtype=torch.bfloat16, causal="lower_right",
+                         kv_pad=kv_pad, g=g)
+    if index == 4:
+        kvls = _uniform_int(g, 256, 4096, 64)
+        return make_case(name, seed, batch=64, q_heads=64, kv_heads=8,
+                         head_dim=128, q_lens=[1] * 64, kv_lens=kvls,
+                         q_form=PACKED, kv_form=PADDED, kv_seq=4096,
+                         dtype=torch.bfloat16, causal="lower_right",
+                         kv_pad=kv_pad, g=g)
+    if index == 5:
+        N, B = 4096, 4
+
+        def suffix_mask(gen):
+            # masked key suffix of m_b = floor(U[0, 0.25] * N) keys
+            m = torch.floor(torch.rand(B, generator=gen) * 0.25 * N).to(torch.int64)
+            keep = torch.arange(N)[None, :] < (N - m)[:, None]
+            return keep.reshape(B, 1, 1, N)
+
+        c = make_case(name, seed, batch=B, q_heads=16, kv_heads=16,
+                      head_dim=128, q_lens=[N] * B, kv_lens=[N] * B,
+                      dtype=torch.float16, causal="upper_left",
+                      mask=suffix_mask, quant=quant, kv_pad=kv_pad,
+                      pass_kv_lengths=False, g=g)
+        c.name = f"{name}_{quant}"
+        return c
+    raise KeyError(index)
+
+
+def to_device(case: Case, device, non_blocking=False) -> Case:
+    """Copy every tensor of ``case`` to ``device``."""
+    def mv(t):
+        return None if t is None else t.to(device, non_blocking=non_blocking)
+    return replace(case, q=mv(case.q), k=mv(case.k), v=mv(case.v),
+                   query_lengths=mv(case.query_lengths),
+                   kv_lengths=mv(case.kv_lengths), mask=mv(case.mask),
+                   quant_scale=mv(case.quant_scale))
