@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark of the ragged GQA fused attention forward on GB300.
+
+One step = one trt_attention / trt_quantized_attention call over one batch of
+the workload (device-side scheduler + the attention kernel).  The headline is
+the ragged packed GQA prefill workload (8 sequences of 128-2048 tokens,
+Hq=32, Hkv=8, D=128, bf16, upper_left causal) in TFLOP/s, with FLOPs = 4 * D
+* attendable pairs counted exactly.  The other workloads (chunked context,
+decode in KV GB/s, quantized P) are reported under "workloads".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Inputs are synthetic (seeded) and resident
+in HBM for ``value``; ``e2e`` times the same call from pinned host buffers
+with the host<->device copies inside the timed region.  L2 is flushed
+(a 256 MiB write) between timed iterations.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ragged_gqa_attention_gb300 import binding, metrics  # noqa: E402
+from ragged_gqa_attention_gb300 import workloads as W  # noqa: E402
+
+HEADLINE = 2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class Runner:
+    """One prepared call on device-resident inputs (arguments built once)."""
+
+    def __init__(self, dc: W.Case, stream):
+        import ctypes
+        self.ctypes = ctypes
+        self.lib = binding.load()
+        self.dc = dc
+        self.stream = stream
+        self.y = torch.empty_like(dc.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dc.q.device)
+        a = binding.make_args(dc.q, dc.k, dc.v, self.y, q_form=dc.q_form, kv_form=dc.kv_form,
+                              query_lengths=dc.query_lengths, kv_lengths=dc.kv_lengths,
+                              mask=dc.mask, scale=dc.scale, causal=dc.causal, norm=dc.norm,
+                              status=self.status)
+        n = self.lib.rga_attention_workspace_size(ctypes.byref(a))
+        self.ws = torch.empty(n, dtype=torch.uint8, device=dc.q.device)
+        a.workspace, a.workspace_bytes = self.ws.data_ptr(), n
+        self.args = a
+        self.h = ctypes.c_void_p(stream.cuda_stream)
+        if dc.quant is not None:
+            self.qt = binding.QUANT[dc.quant]
+            self.qs = ctypes.c_void_p(dc.quant_scale.data_ptr())
+            self.qsd = binding.DTYPES[dc.quant_scale.dtype]
+
+    def __call__(self):
+        b = self.ctypes.byref(self.args)
+        if self.dc.quant is None:
+            rc = self.lib.trt_attention(b, self.h)
+        else:
+            rc = self.lib.trt_quantized_attention(b, self.qt, self.qs, self.qsd, self.h)
+        if rc != 0:
+            raise binding.RgaError(rc, "bench call")
+
+    def check_status(self):
+        torch.cuda.synchronize()
+        st = int(self.status.item())
+        if st != 0:
+            raise RuntimeError(f"device status {binding.STATUS_NAMES.get(st, st)}")
+
+
+def barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x, dist_on):
+    if not dist_on:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def device_timed(run, stream, steps, warmup, dist_on, sampler_index=None):
+    """Per-step CUDA-event durations (ms) with an L2 flush between steps."""
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")   # 256 MiB
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            run()
+    barrier(dist_on)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    sampler = ClockSampler(sampler_index) if sampler_index is not None else None
+    if sampler:
+        sampler.__enter__()
+    with torch.cuda.stream(stream):
+        for s, e in ev:
+            flush.zero_()
+            s.record(stream)
+            run()
+            e.record(stream)
+    barrier(dist_on)
+    if sampler:
+        sampler.__exit__(None, None, None)
+    times = [s.elapsed_time(e) for s, e in ev]
+    return times, (sampler.summary() if sampler else None)
+
+
+def e2e_timed(case: W.Case, stream, steps, warmup, dist_on):
+    """The public call from pinned host buffers: H2D inputs, attention, D2H Y."""
+    host = {}
+    for name in ("q", "k", "v", "query_lengths", "kv_lengths", "mask", "quant_scale"):
+        t = getattr(case, name)
+        host[name] = None if t is None else t.pin_memory()
+    dev = {n: (None if t is None else torch.empty_like(t, device="cuda")) for n, t in host.items()}
+    dc = W.Case(**{**case.__dict__, **dev})
+    run = Runner(dc, stream)
+    y_host = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
+
+    def step():
+        for n, t in host.items():
+            if t is not None:
+                dev[n].copy_(t, non_blocking=True)
+        run()
+        y_host.copy_(run.y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    barrier(dist_on)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for s, e in ev:
+            s.record(stream)
+            step()
+            e.record(stream)
+    barrier(dist_on)
+    run.check_status()
+    bi = metrics.input_bytes(case)
+    bo = case.q.numel() * case.q.element_size()
+    return [s.elapsed_time(e) for s, e in ev], bi, bo
+
+
+def oracle_sample(case: W.Case, budget_s: float, max_units=None):
+    """Time the CPU oracle, as it stands, on whole sequences of the workload
+    (all heads), shortest first, until ``budget_s`` seconds have been spent.
+    Returns (flops done, seconds, threads, description)."""
+    import oracle   # the CPU baseline leg is one of the oracle's permitted users
+    order = sorted(range(case.batch), key=lambda b: (case.q_lens[b] * case.kv_lens[b], b))
+    threads = os.cpu_count() or 1
+    done_flops, spent, seqs = 0.0, 0.0, []
+    for b in order:
+        sub = single_sequence(case, b)
+        f = metrics.flops(sub)
+        if f == 0:
+            continue
+        t0 = time.perf_counter()
+        oracle.attention(sub.q, sub.k, sub.v, q_form=sub.q_form, kv_form=sub.kv_form,
+                         query_lengths=sub.query_lengths, kv_lengths=sub.kv_lengths,
+                         mask=sub.mask, scale=sub.scale, causal=sub.causal, norm=sub.norm,
+                         quant=sub.quant, quant_scale=sub.quant_scale, nthreads=threads)
+        spent += time.perf_counter() - t0
+        done_flops += f
+        seqs.append(b)
+        if spent >= budget_s or (max_units and len(seqs) >= max_units):
+            break
+    desc = (f"sequences {seqs} of {case.name} (all {case.q_heads} query heads each), "
+            f"oracle fp64 C with {threads} threads")
+    return done_flops, spent, threads, desc
+
+
+def single_sequence(case: W.Case, b: int) -> W.Case:
+    """Sequence b of a case as a batch of one (layout slicing only)."""
+    ql, kl = case.q_lens[b], case.kv_lens[b]
+    if case.q_form == W.PACKED:
+        o = int(case.query_lengths[b])
+        q, qlen = case.q[o:o + ql], torch.tensor([0, ql], dtype=torch.int32)
+    else:
+        q = case.q[b:b + 1]
+        qlen = None if case.query_lengths is None else torch.tensor([0, ql], dtype=torch.int32)
+    if case.kv_form == W.PACKED:
+        o = int(case.kv_lengths[b])
+        k, v, klen = case.k[o:o + kl], case.v[o:o + kl], torch.tensor([0, kl], dtype=torch.int32)
+    else:
+        k, v = case.k[b:b + 1], case.v[b:b + 1]
+        klen = None if case.kv_lengths is None else torch.tensor([kl], dtype=torch.int32)
+    mask = case.mask
+    if mask is not None:
+        m = mask.reshape((1,) * (4 - mask.dim()) + tuple(mask.shape))
+        mask = m[b:b + 1] if m.shape[0] > 1 else m
+    return W.Case(**{**case.__dict__, "q": q, "k": k, "v": v, "batch": 1,
+                     "query_lengths": qlen, "kv_lengths": klen, "q_lens": [ql],
+                     "kv_lens": [kl], "mask": mask})
+
+
+def measure(index, quant, stream, steps, warmup, dist_on, peaks, rank, clocks=False):
+    """Device-timed throughput of one workload (inputs resident in HBM)."""
+    case = W.workload(index, quant=quant, kv_pad=0.0)
+    dc = W.to_device(case, "cuda")
+    run = Runner(dc, stream)
+    times, clk = device_timed(run, stream, steps, warmup, dist_on,
+                              sampler_index=(torch.cuda.current_device() if clocks else None))
+    run.check_status()
+    ms = max_over_ranks(statistics.mean(times), dist_on)
+    dec = metrics.is_decode(case)
+    if dec:
+        work, unit, bound = metrics.decode_bytes(case), "GB/s", "hbm"
+        value = work / (ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+    else:
+        work, unit, bound = metrics.flops(case), "TFLOP/s", "tensor"
+        value = work / (ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+    return dict(case=case, ms=ms, value=value, unit=unit, bound=bound, peak=peak, work=work,
+                clocks=clk, launches_per_step=2, times=times)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=HEADLINE)
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other workloads (headline only)")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle CPU work for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    torch.cuda.set_device(local)
+    if dist_on:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    binding.load(build_if_missing=(rank == 0))
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream()
+
+    head = measure(args.workload, "fp8", stream, args.steps, args.warmup, dist_on, peaks, rank,
+                   clocks=True)
+    case = head["case"]
+    e2e_times, bi, bo = e2e_timed(case, stream, max(3, args.steps // 2), 3, dist_on)
+    e2e_ms = max_over_ranks(statistics.mean(e2e_times), dist_on)
+    scale = 1e12 if head["unit"] == "TFLOP/s" else 1e9
+    e2e_val = head["work"] / (e2e_ms * 1e-3) / scale
+
+    secondary = {}
+    if not args.no_secondary:
+        for idx, q in ((3, "fp8"), (4, "fp8"), (5, "fp8"), (5, "int8")):
+            if idx == args.workload:
+                continue
+            torch.cuda.empty_cache()
+            r = measure(idx, q, stream, max(5, args.steps // 2), 3, dist_on, peaks, rank)
+            secondary[r["case"].name] = {
+                "value": round(r["value"] * world, 3), "unit": r["unit"],
+                "ms_per_step": round(r["ms"], 4), "bound": r["bound"],
+                "frac_of_peak": round(r["value"] / r["peak"], 4),
+                "peak": r["peak"], "peak_source": peak_src}
+            del r
+
+    cpu = None
+    if rank == 0:
+        f, s, thr, desc = oracle_sample(case, args.cpu_budget)
+        cpu = {"value": (f / s / scale) if s > 0 else None, "unit": head["unit"],
+               "cores": thr, "kind": "oracle", "sample": desc, "seconds": round(s, 2)}
+
+    if rank == 0:
+        value = head["value"] * world
+        line = {
+            "metric": "attention TFLOP/s (prefill) / KV-read GB/s (decode) and % of roofline, 1 GB300",
+            "value": round(value, 3), "unit": head["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(head["ms"], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": str(case.q.dtype).replace("torch.", ""),
+            "data": "synthetic (seeded N(0,1) inputs, seeded lengths)",
+            "config": {"workload": case.name, "batch": case.batch, "q_heads": case.q_heads,
+                       "kv_heads": case.kv_heads, "head_dim": case.head_dim,
+                       "q_tokens": sum(case.q_lens), "kv_tokens": sum(case.kv_lens),
+                       "causal": case.causal, "l2": "flushed (256 MiB write) between steps",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": head["bound"], "achieved": round(head["value"], 3),
+                         "peak": head["peak"], "unit": head["unit"],
+                         "frac": round(head["value"] / head["peak"], 4),
+                         "traffic": None, "peak_source": peak_src,
+                         "note": "achieved = algorithmic work / CUDA-event time of the whole "
+                                 "call (scheduler + attention kernel)"},
+            "e2e": {"value": round(e2e_val * world, 3), "unit": head["unit"],
+                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": head["launches_per_step"] * args.steps,
+            "clocks": head["clocks"],
+            "cpu_baseline": cpu,
+            "workloads": secondary,
+        }
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def reference_arm(args, rank, world):
+    """The oracle, as it stands, on the host cores: each step is a bounded
+    sample (whole sequences of the workload) timed on the CPU."""
+    if rank != 0:
+        return
+    case = W.workload(args.workload, kv_pad=0.0)
+    for _ in range(args.warmup):
+        oracle_sample(case, 0.0, max_units=1)
+    flops = secs = 0.0
+    thr, desc = 1, ""
+    for _ in range(args.steps):
+        f, s, thr, desc = oracle_sample(case, 0.0, max_units=1)
+        flops += f
+        secs += s
+    unit = "TFLOP/s"
+    if metrics.is_decode(case):
+        unit = "GB/s"
+    val = flops / secs / 1e12 if secs > 0 else None
+    line = {"impl": "reference", "metric": "attention TFLOP/s (prefill) / KV-read GB/s (decode) "
+            "and % of roofline, 1 GB300", "value": val, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / max(args.steps, 1) * 1e3, "higher_is_better": True,
+            "config": {"workload": case.name}, "dtype": "f64",
+            "cpu_baseline": {"value": val, "unit": unit, "cores": thr, "kind": "oracle",
+                             "sample": desc + " per step"},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

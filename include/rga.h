@@ -1,0 +1,174 @@
+/*
+ * rga.h - C ABI of the ragged GQA fused attention library (GB300, sm_103a).
+ *
+ * The operation is the fused attention forward of the TRT_Attention and
+ * TRT_QuantizedAttention custom operators ("TensorRT Custom Operator
+ * Schemas"), covering the MHA/GQA attention of the AttentionPlugin
+ * ("TensorRT Plugins Guide", AttentionPlugin):
+ *
+ *     Y = softmax(scale * Q K^T + mask) V        (TRT_normalization_op "softmax")
+ *     Y = (scale * Q K^T + mask) V  on allowed pairs   ("none")
+ *
+ * and, for the quantized operator, a quantize/dequantize of the normalised
+ * probabilities to fp8 E4M3 or int8 with a given scale before the second
+ * batched matmul (BMM2).
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *    library never allocates, frees or synchronises; all work is enqueued on
+ *    the caller's stream, so a call can be captured into a CUDA graph.
+ *  - Synchronous argument errors are returned as an rga_status and nothing
+ *    is launched.  Errors that depend on device data (the length inputs) are
+ *    detected on the device: the affected call writes a non-zero code to
+ *    *device_status, enqueues no attention work and leaves Y untouched.
+ *    rga_get_device_status reads that word back.
+ *  - Padded query rows at or beyond a sequence's query length, and packed
+ *    rows beyond the last sequence, are never written.
+ */
+#ifndef RGA_H
+#define RGA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RGA_ABI_VERSION 1
+
+typedef enum {
+    RGA_OK = 0,
+    RGA_ERR_INVALID_ARG = 1,     /* bad pointer, shape, enum or combination */
+    RGA_ERR_UNSUPPORTED = 2,     /* valid per the schema, not implemented here */
+    RGA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
+    RGA_ERR_DEVICE_LENGTHS = 4,  /* device-side: inconsistent length inputs */
+    RGA_ERR_TIMEOUT = 5,         /* device-side: a bounded wait ran out */
+    RGA_ERR_WORKSPACE = 6        /* workspace missing or too small */
+} rga_status;
+
+/* IO forms (TRT_Attention attributes query_form / kv_form):
+ *   PADDED_BHND: 4-D [B, H, N, D], row-major;
+ *   PACKED_NHD:  3-D [T, H, D], row-major, sequences concatenated along T. */
+typedef enum { RGA_FORM_PADDED_BHND = 0, RGA_FORM_PACKED_NHD = 1 } rga_form;
+
+/* causal_kind (TRT_Attention).  For a sequence with q_len query rows and
+ * kv_len keys, query i may attend key j when:
+ *   NONE:        always;
+ *   UPPER_LEFT:  j <= i  (the is_causal of TRT_QuantizedAttention);
+ *   LOWER_RIGHT: j <= i + kv_len - q_len. */
+typedef enum {
+    RGA_CAUSAL_NONE = 0,
+    RGA_CAUSAL_UPPER_LEFT = 1,
+    RGA_CAUSAL_LOWER_RIGHT = 2
+} rga_causal;
+
+/* TRT_normalization_op. */
+typedef enum { RGA_NORM_SOFTMAX = 0, RGA_NORM_NONE = 1 } rga_norm;
+
+/* Element types.  Q, K, V and Y share one of F16 / BF16.  A mask is BOOL
+ * (one byte per element, non-zero = may attend) or additive F16/BF16/F32. */
+typedef enum { RGA_F16 = 0, RGA_BF16 = 1, RGA_F32 = 2, RGA_BOOL = 3 } rga_dtype;
+
+/* normalization_quantize_to_type (TRT_QuantizedAttention). */
+typedef enum { RGA_QUANT_FP8_E4M3 = 0, RGA_QUANT_INT8 = 1 } rga_quant;
+
+/*
+ * Arguments of one attention call ("TensorRT Custom Operator Schemas",
+ * TRT_Attention: attributes, inputs 0-5 and output Y).
+ *
+ * q:  padded [B, Hq, q_seq, D] or packed [q_seq, Hq, D]       (input Q)
+ * k, v: padded [B, Hkv, kv_seq, D] or packed [kv_seq, Hkv, D] (inputs K, V)
+ * y:  same shape, form and dtype as q                          (output Y)
+ *
+ * query_lengths: int32 [B+1] cumulative, starting at 0.  Required when q is
+ *   packed.  Optional when q is padded: then query_lengths[b+1] -
+ *   query_lengths[b] (<= q_seq) is the number of valid rows of batch b and
+ *   the remaining rows are left untouched; NULL means all q_seq rows.
+ * kv_lengths: packed KV: int32 [B+1] cumulative, required.  Padded KV:
+ *   int32 [B] per-batch lengths (<= kv_seq), optional (NULL = kv_seq).
+ * Rows of K/V at or beyond a sequence's length may hold any bits,
+ *   including NaN/Inf; they never reach Y.
+ *
+ * mask: optional (NULL = none), row-major, rank mask_rank <= 4 with sizes
+ *   mask_dims[0..mask_rank-1]; it is right-aligned against the logical
+ *   [B, Hq, Nq, Nkv] and each size is 1 (broadcast) or full (B, Hq, or at
+ *   least the longest query / key length of the batch).  It is indexed with
+ *   within-sequence positions (i, j).  BOOL: true = may attend.  F16, BF16,
+ *   F32: added to scale * QK^T.  TRT_Attention rejects a mask together with
+ *   a causal kind other than NONE; TRT_QuantizedAttention accepts both (a
+ *   pair must then pass both).
+ * scale: multiplies QK^T before the additive mask.  TRT_Attention itself
+ *   applies no scale (use 1.0); TRT_QuantizedAttention's default is
+ *   1/sqrt(D).
+ * nb_rank: must be 1 (single-device execution).
+ * workspace: device scratch of at least rga_attention_workspace_size(args)
+ *   bytes, 256-byte aligned, owned by the caller; its contents on entry do
+ *   not matter.  Calls that overlap on the device must not share it.
+ * device_status: one int32 on the device, owned by the caller.  A call sets
+ *   it to a non-zero rga_status when the device finds bad lengths or a wait
+ *   times out; it is never cleared by the library (clear it yourself).
+ */
+typedef struct {
+    const void *q, *k, *v;
+    void *y;
+    rga_dtype dtype;               /* of q, k, v, y: RGA_F16 or RGA_BF16 */
+    rga_form q_form, kv_form;      /* independent of each other */
+    int32_t batch, q_heads, kv_heads, head_dim;   /* q_heads % kv_heads == 0 */
+    int32_t q_seq;                 /* padded: N_q; packed: rows T_q of q */
+    int32_t kv_seq;                /* padded: N_kv; packed: rows T_kv of k, v */
+    const int32_t *query_lengths;
+    const int32_t *kv_lengths;
+    const void *mask;
+    rga_dtype mask_dtype;
+    int32_t mask_rank;
+    int64_t mask_dims[4];
+    float scale;
+    rga_causal causal;
+    rga_norm norm;
+    int32_t nb_rank;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *device_status;
+} rga_attention_args;
+
+/* Bytes of workspace that trt_attention / trt_quantized_attention need for
+ * these arguments (a bound computed from the shapes alone; the length
+ * inputs are not read).  Returns 0 when the arguments are invalid. */
+size_t rga_attention_workspace_size(const rga_attention_args *args);
+
+/* TRT_Attention ("TensorRT Custom Operator Schemas", TRT_Attention).
+ * Supported: head_dim 64 or 128; q_heads / kv_heads <= 128.
+ * Returns RGA_OK after enqueueing the work on `stream`. */
+rga_status trt_attention(const rga_attention_args *args, cudaStream_t stream);
+
+/* TRT_QuantizedAttention ("TensorRT Custom Operator Schemas",
+ * TRT_QuantizedAttention).  Same as trt_attention, plus a Q/DQ of the
+ * probabilities between normalisation and BMM2: x = p / s, q = saturate(
+ * round-half-even(x)) in E4M3FN (max 448) or int8 [-128, 127], p' = q * s.
+ * With softmax, p is the fully normalised probability.  quant_scale is a
+ * device pointer to one scalar of type quant_scale_dtype (F32, F16 or
+ * BF16), required and > 0. */
+rga_status trt_quantized_attention(const rga_attention_args *args,
+                                   rga_quant qtype, const void *quant_scale,
+                                   rga_dtype quant_scale_dtype,
+                                   cudaStream_t stream);
+
+/* Copy *device_status to *out after the work already enqueued on `stream`
+ * has finished.  This call synchronises the stream: use it in tests and
+ * debugging, not on a hot path. */
+rga_status rga_get_device_status(const int32_t *device_status,
+                                 cudaStream_t stream, int32_t *out);
+
+/* Human-readable name of a status code (static storage). */
+const char *rga_status_string(rga_status status);
+
+/* ABI version of the loaded library (RGA_ABI_VERSION). */
+int32_t rga_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RGA_H */

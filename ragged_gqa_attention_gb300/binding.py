@@ -1,0 +1,236 @@
+"""Thin ctypes binding of the C ABI in include/rga.h.
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library (librga.so).  There is no CPU or PyTorch fallback: if the library is
+not built, or the tensors are not CUDA tensors, the call raises.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import buildlib as _build
+
+c_int, c_i32, c_i64 = ctypes.c_int, ctypes.c_int32, ctypes.c_int64
+c_vp, c_size, c_float = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+
+# enums of rga.h
+RGA_OK = 0
+STATUS_NAMES = {0: "RGA_OK", 1: "RGA_ERR_INVALID_ARG", 2: "RGA_ERR_UNSUPPORTED",
+                3: "RGA_ERR_CUDA", 4: "RGA_ERR_DEVICE_LENGTHS", 5: "RGA_ERR_TIMEOUT",
+                6: "RGA_ERR_WORKSPACE"}
+FORMS = {"padded": 0, "padded_bhnd": 0, "packed": 1, "packed_nhd": 1}
+CAUSAL = {"none": 0, "upper_left": 1, "lower_right": 2}
+NORM = {"softmax": 0, "none": 1}
+QUANT = {"fp8": 0, "int8": 1}
+DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.bool: 3}
+
+EXPORTED = ("rga_attention_workspace_size", "trt_attention", "trt_quantized_attention",
+            "rga_get_device_status", "rga_status_string", "rga_abi_version")
+
+
+class Args(ctypes.Structure):
+    """Mirror of rga_attention_args."""
+    _fields_ = [
+        ("q", c_vp), ("k", c_vp), ("v", c_vp), ("y", c_vp),
+        ("dtype", c_int), ("q_form", c_int), ("kv_form", c_int),
+        ("batch", c_i32), ("q_heads", c_i32), ("kv_heads", c_i32), ("head_dim", c_i32),
+        ("q_seq", c_i32), ("kv_seq", c_i32),
+        ("query_lengths", c_vp), ("kv_lengths", c_vp),
+        ("mask", c_vp), ("mask_dtype", c_int), ("mask_rank", c_i32), ("mask_dims", c_i64 * 4),
+        ("scale", c_float), ("causal", c_int), ("norm", c_int), ("nb_rank", c_i32),
+        ("workspace", c_vp), ("workspace_bytes", c_size), ("device_status", c_vp),
+    ]
+
+
+class RgaError(RuntimeError):
+    def __init__(self, code, where=""):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load librga.so (optionally building it first)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if build_if_missing:
+                _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"the CUDA library {path} is not built; run "
+                    "ragged_gqa_attention_gb300.buildlib.build() (there is no fallback)")
+            lib = ctypes.CDLL(path)
+            P = ctypes.POINTER(Args)
+            lib.rga_attention_workspace_size.restype = c_size
+            lib.rga_attention_workspace_size.argtypes = [P]
+            lib.trt_attention.restype = c_int
+            lib.trt_attention.argtypes = [P, c_vp]
+            lib.trt_quantized_attention.restype = c_int
+            lib.trt_quantized_attention.argtypes = [P, c_int, c_vp, c_int, c_vp]
+            lib.rga_get_device_status.restype = c_int
+            lib.rga_get_device_status.argtypes = [c_vp, c_vp, ctypes.POINTER(c_i32)]
+            lib.rga_status_string.restype = ctypes.c_char_p
+            lib.rga_status_string.argtypes = [c_int]
+            lib.rga_abi_version.restype = c_i32
+            lib.rga_abi_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(name, t):
+    if t is not None and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t is not None and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_args(q, k, v, y, *, q_form="padded", kv_form="padded", query_lengths=None,
+              kv_lengths=None, mask=None, scale=1.0, causal="none", norm="softmax",
+              workspace=None, status=None, batch=None, nb_rank=1) -> Args:
+    """Fill an rga_attention_args from tensors (no device work)."""
+    qf, kf = FORMS[q_form], FORMS[kv_form]
+    for name, t in (("q", q), ("k", k), ("v", v), ("y", y), ("query_lengths", query_lengths),
+                    ("kv_lengths", kv_lengths), ("mask", mask), ("workspace", workspace),
+                    ("status", status)):
+        _need_cuda(name, t)
+    a = Args()
+    a.q, a.k, a.v, a.y = _ptr(q), _ptr(k), _ptr(v), _ptr(y)
+    a.dtype = DTYPES.get(q.dtype, 99)
+    a.q_form, a.kv_form = qf, kf
+    if batch is None:
+        if qf == 1:
+            batch = query_lengths.numel() - 1
+        elif kf == 1:
+            batch = kv_lengths.numel() - 1
+        else:
+            batch = q.shape[0]
+    a.batch = batch
+    a.q_heads = q.shape[-2] if qf == 1 else q.shape[1]
+    a.kv_heads = k.shape[-2] if kf == 1 else k.shape[1]
+    a.head_dim = q.shape[-1]
+    a.q_seq = q.shape[0] if qf == 1 else q.shape[2]
+    a.kv_seq = k.shape[0] if kf == 1 else k.shape[2]
+    a.query_lengths, a.kv_lengths = _ptr(query_lengths), _ptr(kv_lengths)
+    if mask is not None:
+        a.mask = _ptr(mask)
+        a.mask_dtype = DTYPES[mask.dtype]
+        a.mask_rank = mask.dim()
+        for i, d in enumerate(mask.shape):
+            a.mask_dims[i] = d
+    a.scale = float(scale)
+    a.causal, a.norm, a.nb_rank = CAUSAL[causal], NORM[norm], nb_rank
+    if workspace is not None:
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    a.device_status = _ptr(status)
+    return a
+
+
+def workspace_size(args: Args) -> int:
+    return load().rga_attention_workspace_size(ctypes.byref(args))
+
+
+_ws_cache = {}
+
+
+def _workspace(device, nbytes):
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _stream_handle(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _call(quant, q, k, v, out, quant_args, stream, **kw):
+    lib = load()
+    y = torch.full_like(q, float("nan")) if out is None else out
+    status = kw.pop("status", None)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    workspace = kw.pop("workspace", None)
+    a = make_args(q, k, v, y, status=status, workspace=workspace, **kw)
+    if workspace is None:
+        n = lib.rga_attention_workspace_size(ctypes.byref(a))
+        if n == 0:
+            raise RgaError(1, "rga_attention_workspace_size")
+        ws = _workspace(q.device, n)
+        a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    h = _stream_handle(stream)
+    if quant:
+        qt, qs = quant_args
+        rc = lib.trt_quantized_attention(ctypes.byref(a), QUANT[qt], qs.data_ptr(),
+                                         DTYPES[qs.dtype], h)
+        name = "trt_quantized_attention"
+    else:
+        rc = lib.trt_attention(ctypes.byref(a), h)
+        name = "trt_attention"
+    if rc != RGA_OK:
+        raise RgaError(rc, name)
+    return y, status
+
+
+def trt_attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=None,
+                  kv_lengths=None, mask=None, scale=1.0, causal="none", norm="softmax",
+                  out=None, workspace=None, status=None, stream=None, return_status=False):
+    """TRT_Attention forward.  Tensors are CUDA tensors; returns Y (and the
+    device status word when ``return_status``).  ``scale`` defaults to 1.0:
+    the operator itself does not scale Q/K/V."""
+    y, st = _call(False, q, k, v, out, None, stream, q_form=q_form, kv_form=kv_form,
+                  query_lengths=query_lengths, kv_lengths=kv_lengths, mask=mask,
+                  scale=scale, causal=causal, norm=norm, workspace=workspace, status=status)
+    return (y, st) if return_status else y
+
+
+def trt_quantized_attention(q, k, v, *, quant_scale, quant="fp8", q_form="padded",
+                            kv_form="padded", query_lengths=None, kv_lengths=None, mask=None,
+                            scale=None, causal=None, is_causal=False, norm="softmax",
+                            out=None, workspace=None, status=None, stream=None,
+                            return_status=False):
+    """TRT_QuantizedAttention forward.  ``scale`` defaults to 1/sqrt(D);
+    ``is_causal`` selects upper_left unless ``causal`` is given;
+    ``quant_scale`` is a one-element CUDA tensor (fp32, fp16 or bf16)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    if causal is None:
+        causal = "upper_left" if is_causal else "none"
+    _need_cuda("quant_scale", quant_scale)
+    y, st = _call(True, q, k, v, out, (quant, quant_scale), stream, q_form=q_form,
+                  kv_form=kv_form, query_lengths=query_lengths, kv_lengths=kv_lengths,
+                  mask=mask, scale=scale, causal=causal, norm=norm, workspace=workspace,
+                  status=status)
+    return (y, st) if return_status else y
+
+
+def device_status(status, stream=None) -> int:
+    """Read the status word (synchronises the stream)."""
+    out = c_i32(0)
+    rc = load().rga_get_device_status(ctypes.c_void_p(status.data_ptr()),
+                                      ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(out))
+    if rc != RGA_OK:
+        raise RgaError(rc, "rga_get_device_status")
+    return int(out.value)

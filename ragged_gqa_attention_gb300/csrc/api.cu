@@ -1,0 +1,276 @@
+// api.cu - the C ABI (include/rga.h): argument validation, workspace sizing,
+// TMA descriptor set-up and dispatch to the scheduler, prefill and decode
+// kernels.  No allocation, no synchronisation: everything is enqueued on
+// the caller's stream.
+#include <cmath>
+#include <cstring>
+#include <cudaTypedefs.h>
+#include "../../include/rga.h"
+#include "kernels.h"
+
+using namespace rga;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Tiled TMA descriptor over a row-major tensor whose innermost dim is D
+// (16-bit elements), 128-byte swizzle, 64-element inner box.
+bool encode(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
+            const uint32_t *box) {
+    auto fn = get_encode();
+    if (!fn) return false;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bd[5], es[5];
+    uint64_t stride = 2;
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i] < 1 ? 1 : dims[i];
+        bd[i] = box[i];
+        es[i] = 1;
+        if (i > 0) gs[i - 1] = stride;
+        stride *= gd[i];
+    }
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, rank, const_cast<void *>(base), gd, gs, bd, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_q(CUtensorMap *m, const AttnParams &p) {
+    if (p.q_packed) {
+        const uint64_t d[3] = {(uint64_t)p.D, (uint64_t)p.Hq, (uint64_t)p.q_seq};
+        const uint32_t b[3] = {64, (uint32_t)p.G, (uint32_t)p.tq};
+        return encode(m, p.q, 3, d, b);
+    }
+    const uint64_t d[4] = {(uint64_t)p.D, (uint64_t)p.q_seq, (uint64_t)p.Hq, (uint64_t)p.B};
+    const uint32_t b[4] = {64, (uint32_t)p.tq, (uint32_t)p.G, 1};
+    return encode(m, p.q, 4, d, b);
+}
+
+bool encode_kv(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t rows) {
+    if (p.kv_packed) {
+        const uint64_t d[3] = {(uint64_t)p.D, (uint64_t)p.Hkv, (uint64_t)p.kv_seq};
+        const uint32_t b[3] = {64, 1, rows};
+        return encode(m, base, 3, d, b);
+    }
+    const uint64_t d[4] = {(uint64_t)p.D, (uint64_t)p.kv_seq, (uint64_t)p.Hkv, (uint64_t)p.B};
+    const uint32_t b[4] = {64, rows, 1, 1};
+    return encode(m, base, 4, d, b);
+}
+
+// Decode (split-KV) path: short query rows per (batch, KV head), no Q/DQ.
+bool use_decode(const rga_attention_args *a, bool quant) {
+    if (quant) return false;
+    const int G = a->q_heads / a->kv_heads;
+    if (G > DEC_ROWS) return false;
+    if (a->q_form == RGA_FORM_PACKED_NHD) return a->q_seq <= a->batch;
+    return (int64_t)a->q_seq * G <= DEC_ROWS;
+}
+
+rga_status validate(const rga_attention_args *a, bool quant) {
+    if (!a) return RGA_ERR_INVALID_ARG;
+    if (a->dtype != RGA_F16 && a->dtype != RGA_BF16) {
+        return a->dtype == RGA_F32 ? RGA_ERR_UNSUPPORTED : RGA_ERR_INVALID_ARG;
+    }
+    if ((a->q_form != RGA_FORM_PADDED_BHND && a->q_form != RGA_FORM_PACKED_NHD) ||
+        (a->kv_form != RGA_FORM_PADDED_BHND && a->kv_form != RGA_FORM_PACKED_NHD))
+        return RGA_ERR_INVALID_ARG;
+    if (a->batch < 0 || a->q_heads <= 0 || a->kv_heads <= 0 || a->head_dim <= 0 ||
+        a->q_seq < 0 || a->kv_seq < 0)
+        return RGA_ERR_INVALID_ARG;
+    if (a->q_heads % a->kv_heads != 0) return RGA_ERR_INVALID_ARG;
+    if (a->causal < RGA_CAUSAL_NONE || a->causal > RGA_CAUSAL_LOWER_RIGHT) return RGA_ERR_INVALID_ARG;
+    if (a->norm != RGA_NORM_SOFTMAX && a->norm != RGA_NORM_NONE) return RGA_ERR_INVALID_ARG;
+    if (a->nb_rank != 1) return a->nb_rank < 1 ? RGA_ERR_INVALID_ARG : RGA_ERR_UNSUPPORTED;
+    if (a->head_dim != 64 && a->head_dim != 128) return RGA_ERR_UNSUPPORTED;
+    if (a->q_heads / a->kv_heads > 128) return RGA_ERR_UNSUPPORTED;
+    if (a->q_form == RGA_FORM_PACKED_NHD && !a->query_lengths) return RGA_ERR_INVALID_ARG;
+    if (a->kv_form == RGA_FORM_PACKED_NHD && !a->kv_lengths) return RGA_ERR_INVALID_ARG;
+    if (!a->device_status) return RGA_ERR_INVALID_ARG;
+    if (!std::isfinite(a->scale)) return RGA_ERR_INVALID_ARG;
+    const bool any_q = a->batch > 0 && a->q_seq > 0;
+    if (any_q && (!a->q || !a->y)) return RGA_ERR_INVALID_ARG;
+    if (any_q && a->kv_seq > 0 && (!a->k || !a->v)) return RGA_ERR_INVALID_ARG;
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->y))
+        return RGA_ERR_INVALID_ARG;
+    if (a->mask) {
+        if (!quant && a->causal != RGA_CAUSAL_NONE) return RGA_ERR_INVALID_ARG;
+        if (a->mask_dtype != RGA_BOOL && a->mask_dtype != RGA_F16 && a->mask_dtype != RGA_BF16 &&
+            a->mask_dtype != RGA_F32)
+            return RGA_ERR_INVALID_ARG;
+        if (a->mask_rank < 0 || a->mask_rank > 4) return RGA_ERR_INVALID_ARG;
+        int64_t md[4] = {1, 1, 1, 1};
+        for (int i = 0; i < a->mask_rank; ++i) {
+            if (a->mask_dims[i] < 1) return RGA_ERR_INVALID_ARG;
+            md[4 - a->mask_rank + i] = a->mask_dims[i];
+        }
+        if (md[0] != 1 && md[0] != a->batch) return RGA_ERR_INVALID_ARG;
+        if (md[1] != 1 && md[1] != a->q_heads) return RGA_ERR_INVALID_ARG;
+        if (a->q_form == RGA_FORM_PADDED_BHND && md[2] != 1 && md[2] != a->q_seq)
+            return RGA_ERR_INVALID_ARG;
+        if (a->kv_form == RGA_FORM_PADDED_BHND && md[3] != 1 && md[3] != a->kv_seq)
+            return RGA_ERR_INVALID_ARG;
+    }
+    return RGA_OK;
+}
+
+AttnParams make_params(const rga_attention_args *a, bool quant) {
+    AttnParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = a->q; p.k = a->k; p.v = a->v; p.y = a->y;
+    p.q_packed = a->q_form == RGA_FORM_PACKED_NHD;
+    p.kv_packed = a->kv_form == RGA_FORM_PACKED_NHD;
+    p.B = a->batch; p.Hq = a->q_heads; p.Hkv = a->kv_heads; p.D = a->head_dim;
+    p.G = a->q_heads / a->kv_heads;
+    p.q_seq = a->q_seq; p.kv_seq = a->kv_seq;
+    p.query_lengths = a->query_lengths;
+    p.kv_lengths = a->kv_form == RGA_FORM_PACKED_NHD || a->kv_lengths ? a->kv_lengths : nullptr;
+    p.mask = a->mask;
+    p.mask_dtype = a->mask_dtype;
+    for (int i = 0; i < 4; ++i) p.md[i] = 1;
+    if (a->mask)
+        for (int i = 0; i < a->mask_rank; ++i) p.md[4 - a->mask_rank + i] = a->mask_dims[i];
+    p.scale = a->scale;
+    p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
+    p.causal = a->causal;
+    p.quant = -1;
+    p.tq = BM / p.G;
+    if (p.q_packed)
+        p.max_items = p.Hkv * ((p.q_seq + p.tq - 1) / p.tq + p.B);
+    else
+        p.max_items = p.Hkv * p.B * ((p.q_seq + p.tq - 1) / p.tq);
+    p.max_splits = (p.kv_seq + DEC_SPLIT - 1) / DEC_SPLIT;
+    if (p.max_splits < 1) p.max_splits = 1;
+    p.status = a->device_status;
+    p.ws = static_cast<uint8_t *>(a->workspace);
+    (void)quant;
+    return p;
+}
+
+size_t workspace_bytes(const rga_attention_args *a, bool quant) {
+    AttnParams p = make_params(a, quant);
+    size_t n = align256(pf_ws_bytes(p));
+    if (use_decode(a, quant)) {
+        size_t d = align256(dec_ws_bytes(p));
+        if (d > n) n = d;
+    }
+    return n;
+}
+
+rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const void *qscale,
+               rga_dtype qscale_dtype, cudaStream_t stream) {
+    rga_status st = validate(a, quant);
+    if (st != RGA_OK) return st;
+    if (quant) {
+        if (qtype != RGA_QUANT_FP8_E4M3 && qtype != RGA_QUANT_INT8) return RGA_ERR_INVALID_ARG;
+        if (!qscale) return RGA_ERR_INVALID_ARG;
+        if (qscale_dtype != RGA_F32 && qscale_dtype != RGA_F16 && qscale_dtype != RGA_BF16)
+            return RGA_ERR_INVALID_ARG;
+    }
+    if (a->batch == 0 || a->q_seq == 0) return RGA_OK;   // no query rows: nothing to write
+    const size_t need = workspace_bytes(a, false) > workspace_bytes(a, quant)
+                            ? workspace_bytes(a, false) : workspace_bytes(a, quant);
+    if (!a->workspace || a->workspace_bytes < need ||
+        (reinterpret_cast<uintptr_t>(a->workspace) & 255))
+        return RGA_ERR_WORKSPACE;
+
+    AttnParams p = make_params(a, quant);
+    if (quant) {
+        p.quant = qtype == RGA_QUANT_FP8_E4M3 ? 0 : 1;
+        p.qscale = qscale;
+        p.qscale_dtype = qscale_dtype;
+    }
+    const int bf16 = a->dtype == RGA_BF16;
+    // Zero-extent K/V (no keys anywhere): the descriptors are never read,
+    // so they point at Y, which is a valid address.
+    const void *kp = a->kv_seq > 0 ? a->k : a->y;
+    const void *vp = a->kv_seq > 0 ? a->v : a->y;
+    const bool dec = use_decode(a, quant);
+    TensorMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if (!encode_q(&maps.q, p) || !encode_kv(&maps.k, kp, p, dec ? DEC_KEYS : BN) ||
+        !encode_kv(&maps.v, vp, p, dec ? DEC_KEYS : BN))
+        return RGA_ERR_CUDA;
+    int mode;
+    if (a->norm == RGA_NORM_SOFTMAX) mode = quant ? MODE_SOFTMAX_Q : MODE_SOFTMAX;
+    else mode = quant ? MODE_NONE_Q : MODE_NONE;
+
+    if (launch_sched(p, dec ? 1 : 0, stream) != cudaSuccess) return RGA_ERR_CUDA;
+    cudaError_t e;
+    if (dec) {
+        e = launch_decode(p, maps, mode, stream, bf16);
+    } else {
+        int grid = sm_count();
+        if (grid <= 0) return RGA_ERR_CUDA;
+        if (grid > p.max_items) grid = p.max_items;
+        if (grid < 1) grid = 1;
+        e = launch_prefill(p, maps, mode, grid, stream, bf16);
+    }
+    return e == cudaSuccess ? RGA_OK : RGA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t rga_attention_workspace_size(const rga_attention_args *args) {
+    if (validate(args, true) != RGA_OK && validate(args, false) != RGA_OK) return 0;
+    const size_t a = workspace_bytes(args, false), b = workspace_bytes(args, true);
+    return a > b ? a : b;
+}
+
+rga_status trt_attention(const rga_attention_args *args, cudaStream_t stream) {
+    return run(args, false, RGA_QUANT_FP8_E4M3, nullptr, RGA_F32, stream);
+}
+
+rga_status trt_quantized_attention(const rga_attention_args *args, rga_quant qtype,
+                                   const void *quant_scale, rga_dtype quant_scale_dtype,
+                                   cudaStream_t stream) {
+    return run(args, true, qtype, quant_scale, quant_scale_dtype, stream);
+}
+
+rga_status rga_get_device_status(const int32_t *device_status, cudaStream_t stream,
+                                 int32_t *out) {
+    if (!device_status || !out) return RGA_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(out, device_status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) !=
+        cudaSuccess)
+        return RGA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return RGA_ERR_CUDA;
+    return RGA_OK;
+}
+
+const char *rga_status_string(rga_status s) {
+    switch (s) {
+    case RGA_OK: return "RGA_OK";
+    case RGA_ERR_INVALID_ARG: return "RGA_ERR_INVALID_ARG";
+    case RGA_ERR_UNSUPPORTED: return "RGA_ERR_UNSUPPORTED";
+    case RGA_ERR_CUDA: return "RGA_ERR_CUDA";
+    case RGA_ERR_DEVICE_LENGTHS: return "RGA_ERR_DEVICE_LENGTHS";
+    case RGA_ERR_TIMEOUT: return "RGA_ERR_TIMEOUT";
+    case RGA_ERR_WORKSPACE: return "RGA_ERR_WORKSPACE";
+    }
+    return "RGA_ERR_UNKNOWN";
+}
+
+int32_t rga_abi_version(void) { return RGA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// kernels.h - internal launch parameters shared by the host dispatcher
+// (api.cu) and the device kernels.  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace rga {
+
+// Prefill tile geometry: 128 query rows (tokens x heads of one KV group)
+// against 128 keys per step.
+constexpr int BM = 128;
+constexpr int BN = 128;
+
+// Decode geometry: 16 query rows per MMA row chunk, 32 keys per warp step,
+// 4 warps per CTA, DEC_SPLIT keys per CTA.
+constexpr int DEC_ROWS = 16;
+constexpr int DEC_KEYS = 32;
+constexpr int DEC_WARPS = 4;
+constexpr int DEC_STAGES = 2;
+constexpr int DEC_SPLIT = 512;
+
+enum Mode { MODE_SOFTMAX = 0, MODE_NONE = 1, MODE_SOFTMAX_Q = 2, MODE_NONE_Q = 3 };
+
+struct AttnParams {
+    const void *q, *k, *v;
+    void *y;
+    int q_packed, kv_packed;
+    int B, Hq, Hkv, D, G;
+    int q_seq, kv_seq;
+    const int32_t *query_lengths;   // may be null for padded q
+    const int32_t *kv_lengths;      // may be null for padded kv
+    const void *mask;               // null = none
+    int mask_dtype;                 // rga_dtype
+    int64_t md[4];                  // mask dims right-aligned to rank 4
+    float scale;                    // natural units
+    float scale_log2;               // scale * log2(e)
+    int causal;                     // rga_causal
+    int quant;                      // -1 off, 0 fp8, 1 int8
+    const void *qscale;             // device scalar
+    int qscale_dtype;
+    int tq;                         // query tokens per prefill tile (BM / G)
+    int max_items;                  // capacity of the work list
+    int max_splits;                 // decode: splits per (b, kv head)
+    int32_t *status;                // device status word
+    uint8_t *ws;                    // workspace base
+};
+
+// Workspace layout (byte offsets from ws).
+constexpr size_t WS_HEADER = 256;             // int counters
+// prefill: int4 items[max_items] after the header
+// decode: after the header: int tickets[B*Hkv] (256-aligned), then
+// float partial_o[B*Hkv*max_splits][DEC_ROWS][D], float2 ml[..][DEC_ROWS]
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// prefill workspace: header + work list
+__host__ __device__ inline size_t pf_ws_bytes(const AttnParams &p) {
+    return WS_HEADER + (size_t)p.max_items * 16;
+}
+// decode workspace: header, split tickets, partial O, partial (m, l)
+__host__ __device__ inline size_t dec_part_off(const AttnParams &p) {
+    return align256(WS_HEADER + (size_t)p.B * p.Hkv * 4);
+}
+__host__ __device__ inline size_t dec_ml_off(const AttnParams &p) {
+    return dec_part_off(p) + align256((size_t)p.B * p.Hkv * p.max_splits * DEC_ROWS * p.D * 4);
+}
+__host__ __device__ inline size_t dec_ws_bytes(const AttnParams &p) {
+    return dec_ml_off(p) + (size_t)p.B * p.Hkv * p.max_splits * DEC_ROWS * 8;
+}
+
+struct TensorMaps {
+    CUtensorMap q, k, v;
+};
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_sched(const AttnParams &p, int decode, cudaStream_t s);
+cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode,
+                           int grid, cudaStream_t s, int bf16);
+cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode,
+                          cudaStream_t s, int bf16);
+
+}  // namespace rga

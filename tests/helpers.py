@@ -1,0 +1,82 @@
+"""Shared helpers for the GPU parity tests: run a Case through the C ABI with
+a guarded, NaN-prefilled output buffer, run the same Case through the CPU
+oracle, and compare."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from ragged_gqa_attention_gb300 import binding
+from ragged_gqa_attention_gb300 import workloads as W
+
+GUARD = 256                      # elements of canary on each side of Y
+SENTINEL = 0x7FDA                # a NaN bit pattern in both fp16 and bf16
+
+TOL = {None: (1e-2, 1e-3), "fp8": (3e-2, 3e-3), "int8": (3e-2, 3e-3)}
+
+
+def guarded_output(q):
+    """Y as a view into a bigger buffer prefilled with SENTINEL."""
+    n = q.numel()
+    buf = torch.full((n + 2 * GUARD,), SENTINEL, dtype=torch.int16, device=q.device)
+    y = buf[GUARD:GUARD + n].view(q.dtype).view(q.shape)
+    return buf, y
+
+
+def run_gpu(case: W.Case, *, status=None):
+    """Returns (y_gpu as float64 numpy, raw int16 buffer, status tensor)."""
+    dc = W.to_device(case, "cuda")
+    buf, y = guarded_output(dc.q)
+    kw = dict(q_form=dc.q_form, kv_form=dc.kv_form, query_lengths=dc.query_lengths,
+              kv_lengths=dc.kv_lengths, mask=dc.mask, scale=dc.scale, causal=dc.causal,
+              norm=dc.norm, out=y, status=status, return_status=True)
+    if dc.quant is None:
+        _, st = binding.trt_attention(dc.q, dc.k, dc.v, **kw)
+    else:
+        _, st = binding.trt_quantized_attention(dc.q, dc.k, dc.v, quant=dc.quant,
+                                                quant_scale=dc.quant_scale, **kw)
+    torch.cuda.synchronize()
+    return y.double().cpu().numpy(), buf.cpu().numpy(), st
+
+
+def run_oracle(case: W.Case):
+    return oracle.attention(
+        case.q, case.k, case.v, q_form=case.q_form, kv_form=case.kv_form,
+        query_lengths=case.query_lengths, kv_lengths=case.kv_lengths, mask=case.mask,
+        scale=case.scale, causal=case.causal, norm=case.norm, quant=case.quant,
+        quant_scale=case.quant_scale)
+
+
+def valid_row_mask(case: W.Case):
+    """Boolean array over Y's rows (all but the last dim): True where the
+    row belongs to a sequence and must be written."""
+    if case.q_form == W.PACKED:
+        m = np.zeros(case.q.shape[:-1], dtype=bool)
+        m[:sum(case.q_lens)] = True
+        return m
+    B, H, N = case.q.shape[:3]
+    m = np.zeros((B, H, N), dtype=bool)
+    for b, n in enumerate(case.q_lens):
+        m[b, :, :n] = True
+    return m
+
+
+def check(case: W.Case, y_gpu, raw, y_ref, tol=None):
+    """Element-wise parity on valid rows; bit-exact sentinel elsewhere."""
+    atol_max, atol_mean = tol or TOL[case.quant]
+    rows = valid_row_mask(case)
+    g, r = y_gpu[rows], y_ref[rows]
+    assert np.isfinite(g).all(), "non-finite output in a valid row"
+    err = np.abs(g - r)
+    if err.size:
+        assert err.max() <= atol_max, f"max abs err {err.max():.3e} > {atol_max}"
+        assert err.mean() <= atol_mean, f"mean abs err {err.mean():.3e} > {atol_mean}"
+    # untouched: invalid rows and the guard bands keep the sentinel bits
+    body = raw[GUARD:GUARD + case.q.numel()].reshape(case.q.shape)
+    assert (body[~rows] == np.int16(SENTINEL)).all(), "a row outside the sequences was written"
+    assert (raw[:GUARD] == np.int16(SENTINEL)).all() and \
+        (raw[GUARD + case.q.numel():] == np.int16(SENTINEL)).all(), "guard band overwritten"
+    return float(err.max()) if err.size else 0.0

@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/rga.h declares, the ctypes mirror of the argument
+struct has the C layout, and argument validation returns its codes without
+touching a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from ragged_gqa_attention_gb300 import binding
+from ragged_gqa_attention_gb300 import buildlib as B
+
+HEADER = os.path.join(B.INCLUDE, "rga.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in binding.EXPORTED:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    for n in declared_functions():
+        assert n in exported, f"{n} declared in rga.h but not exported"
+        assert hasattr(lib, n)
+
+
+def test_struct_layout_matches_c(tmp_path):
+    fields = [f[0] for f in binding.Args._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"',
+            "int main(void){",
+            'printf("%zu\\n", sizeof(rga_attention_args));']
+    for f in fields:
+        prog.append(f'printf("%zu\\n", offsetof(rga_attention_args, {f}));')
+    prog.append("return 0;}")
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(prog))
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I", "/usr/local/cuda/include", str(c), "-o", str(exe)])
+    vals = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert vals[0] == ctypes.sizeof(binding.Args)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(binding.Args, f).offset == off, f
+
+
+def test_status_strings_and_version(lib):
+    assert lib.rga_abi_version() == 1
+    for code, name in binding.STATUS_NAMES.items():
+        assert lib.rga_status_string(code).decode() == name
+
+
+def _args(**kw):
+    a = binding.Args()
+    a.q = a.k = a.v = a.y = 0x10000
+    a.dtype, a.q_form, a.kv_form = 1, 0, 0
+    a.batch, a.q_heads, a.kv_heads, a.head_dim = 2, 8, 2, 128
+    a.q_seq, a.kv_seq = 256, 256
+    a.scale, a.causal, a.norm, a.nb_rank = 1.0, 0, 0, 1
+    a.device_status = 0x20000
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q_heads=6, kv_heads=4), 1),          # heads not a multiple
+    (dict(head_dim=96), 2),                    # not implemented
+    (dict(dtype=2), 2),                        # fp32 Q/K/V not implemented
+    (dict(nb_rank=2), 2),                      # single device only
+    (dict(causal=7), 1),
+    (dict(q_form=1), 1),                       # packed Q needs query_lengths
+    (dict(kv_form=1), 1),                      # packed KV needs kv_lengths
+    (dict(q=0x10008), 1),                      # misaligned
+    (dict(device_status=None), 1),
+    (dict(mask=0x30000, mask_dtype=3, mask_rank=2, causal=1), 1),   # mask + causal
+    (dict(mask=0x30000, mask_dtype=3, mask_rank=4), 1),             # mask dims 0
+])
+def test_validation_codes_without_a_device(lib, kw, code):
+    a = _args(**kw)
+    if "mask_rank" in kw and kw["mask_rank"] == 2:
+        a.mask_dims[0], a.mask_dims[1] = 256, 256
+    rc = lib.trt_attention(ctypes.byref(a), None)
+    assert rc == code
+
+
+def test_workspace_missing_is_reported(lib):
+    a = _args()
+    assert lib.trt_attention(ctypes.byref(a), None) == 6
+    n = lib.rga_attention_workspace_size(ctypes.byref(a))
+    assert n >= 256 and n % 256 == 0
+
+
+def test_quantized_requires_scale(lib):
+    a = _args(workspace=0x100000, workspace_bytes=1 << 30)
+    assert lib.trt_quantized_attention(ctypes.byref(a), 0, None, 2, None) == 1
+    assert lib.trt_quantized_attention(ctypes.byref(a), 5, 0x40000, 2, None) == 1
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        binding.trt_attention(q, q, q)

@@ -1,0 +1,236 @@
+"""GPU parity: the CUDA library (through the C ABI) against the fp64 CPU
+oracle on the same seeded inputs, element by element.
+
+Tolerances (stated for the fused attention forward): max-abs 1e-2 and
+mean-abs 1e-3 for fp16/bf16 with unquantised P; max-abs 3e-2 when P goes
+through the fp8/int8 Q/DQ.  Rows outside the sequences and guard bands
+around Y must keep their NaN sentinel bits exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from ragged_gqa_attention_gb300 import binding
+from ragged_gqa_attention_gb300 import workloads as W
+
+from helpers import check, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    binding.load(build_if_missing=True)
+
+
+def _parity(case, tol=None):
+    y, raw, st = run_gpu(case)
+    assert binding.device_status(st) == 0
+    ref = run_oracle(case)
+    return check(case, y, raw, ref, tol)
+
+
+def test_workload1_small_padded():
+    _parity(W.workload(1))
+
+
+# --------------------------------------------------------------------------
+# option sweep on small ragged shapes that span several tiles and tails
+# --------------------------------------------------------------------------
+SWEEP = []
+for qf in ("padded", "packed"):
+    for kf in ("padded", "packed"):
+        for causal in ("none", "upper_left", "lower_right"):
+            for G in (1, 4):
+                for D in (64, 128):
+                    SWEEP.append((qf, kf, causal, G, D))
+
+
+@pytest.mark.parametrize("qf,kf,causal,G,D", SWEEP)
+def test_prefill_sweep(qf, kf, causal, G, D):
+    dtype = torch.bfloat16 if (G + D + len(causal)) % 2 else torch.float16
+    Hkv = 2
+    c = W.make_case("sweep", 100 + len(SWEEP), batch=3, q_heads=Hkv * G, kv_heads=Hkv,
+                    head_dim=D, q_lens=[1, 150, 277], kv_lens=[200, 131, 300],
+                    q_form=qf, kv_form=kf, dtype=dtype, causal=causal,
+                    pass_query_lengths=True, tail=3)
+    _parity(c)
+
+
+@pytest.mark.parametrize("G", [2, 8, 16, 32])
+def test_prefill_gqa_ratios(G):
+    c = W.make_case("gqa", 7, batch=2, q_heads=2 * G, kv_heads=2, head_dim=128,
+                    q_lens=[190, 33], kv_lens=[190, 300], q_form="packed", kv_form="packed",
+                    dtype=torch.bfloat16, causal="lower_right")
+    _parity(c)
+
+
+def test_prefill_odd_group_size():
+    # G = 3: 42 tokens x 3 heads fill 126 of the 128 tile rows
+    c = W.make_case("g3", 8, batch=2, q_heads=6, kv_heads=2, head_dim=64,
+                    q_lens=[100, 45], kv_lens=[100, 45], q_form="packed", kv_form="padded",
+                    dtype=torch.float16, causal="upper_left")
+    _parity(c)
+
+
+@pytest.mark.parametrize("mdtype", [torch.bool, torch.float16, torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", ["full", "key", "head_row"])
+def test_prefill_masks(mdtype, shape):
+    B, H, N, Nk = 2, 4, 140, 260
+    g = torch.Generator().manual_seed(5)
+
+    def mk(gen):
+        dims = {"full": (B, H, N, Nk), "key": (B, 1, 1, Nk), "head_row": (1, H, N, 1)}[shape]
+        if mdtype == torch.bool:
+            m = torch.rand(dims, generator=gen) > 0.3
+        else:
+            m = (torch.randn(dims, generator=gen) * 2).to(mdtype)
+        return m
+
+    c = W.make_case("mask", 9, batch=B, q_heads=H, kv_heads=2, head_dim=128,
+                    q_lens=[N, 77], kv_lens=[Nk, 201], q_seq=N, kv_seq=Nk,
+                    dtype=torch.float16, mask=mk, pass_query_lengths=True)
+    _parity(c)
+
+
+@pytest.mark.parametrize("causal", ["none", "upper_left"])
+def test_prefill_norm_none(causal):
+    c = W.make_case("none", 10, batch=2, q_heads=4, kv_heads=4, head_dim=64,
+                    q_lens=[130, 64], kv_lens=[130, 250], dtype=torch.float16,
+                    causal=causal, norm="none", scale=0.05, pass_query_lengths=True)
+    _parity(c)
+
+
+# --------------------------------------------------------------------------
+# quantized P (TRT_QuantizedAttention)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("quant", ["fp8", "int8"])
+@pytest.mark.parametrize("norm", ["softmax", "none"])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_quantized(quant, norm, dtype):
+    B, N = 2, 300
+
+    def suffix(gen):
+        m = torch.floor(torch.rand(B, generator=gen) * 0.25 * N).long()
+        return (torch.arange(N)[None, :] < (N - m)[:, None]).reshape(B, 1, 1, N)
+
+    c = W.make_case("quant", 11, batch=B, q_heads=4, kv_heads=4, head_dim=128,
+                    q_lens=[N, N], dtype=dtype, causal="upper_left", mask=suffix,
+                    quant=quant, norm=norm, scale=(0.02 if norm == "none" else None),
+                    pass_kv_lengths=False)
+    _parity(c)
+
+
+@pytest.mark.parametrize("sdtype", [torch.float16, torch.bfloat16])
+def test_quantized_scale_dtypes(sdtype):
+    c = W.make_case("qs", 12, batch=1, q_heads=2, kv_heads=1, head_dim=64,
+                    q_lens=[200], kv_lens=[260], q_form="packed", kv_form="packed",
+                    dtype=torch.float16, causal="lower_right", quant="int8",
+                    quant_scale=torch.tensor(1 / 127).to(sdtype))
+    _parity(c)
+
+
+# --------------------------------------------------------------------------
+# decode (split-KV) path
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("G", [1, 4, 8, 16])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_decode_packed_q(G, dtype):
+    B = 6
+    kv = [1, 31, 32, 513, 1100, 2049]
+    c = W.make_case("dec", 13, batch=B, q_heads=2 * G, kv_heads=2, head_dim=128,
+                    q_lens=[1] * B, kv_lens=kv, q_form="packed", kv_form="padded",
+                    kv_seq=2100, dtype=dtype, causal="lower_right")
+    _parity(c)
+
+
+@pytest.mark.parametrize("causal", ["none", "upper_left", "lower_right"])
+def test_decode_padded_q_packed_kv(causal):
+    c = W.make_case("dec2", 14, batch=3, q_heads=8, kv_heads=2, head_dim=64,
+                    q_lens=[1, 1, 1], kv_lens=[700, 5, 1600], q_form="padded",
+                    kv_form="packed", dtype=torch.bfloat16, causal=causal, tail=5)
+    _parity(c)
+
+
+def test_decode_multi_token_rows():
+    # two tokens x 8 heads = 16 rows per (batch, kv head); one sequence with
+    # more rows than a row block goes through the single-split loop
+    c = W.make_case("dec3", 15, batch=4, q_heads=8, kv_heads=1, head_dim=128,
+                    q_lens=[2, 0, 1, 1], kv_lens=[900, 10, 2000, 600], q_form="packed",
+                    kv_form="padded", dtype=torch.bfloat16, causal="lower_right")
+    _parity(c)
+    c = W.make_case("dec4", 16, batch=4, q_heads=8, kv_heads=1, head_dim=128,
+                    q_lens=[4, 0, 0, 0], kv_lens=[900, 10, 20, 600], q_form="packed",
+                    kv_form="padded", dtype=torch.bfloat16, causal="lower_right")
+    _parity(c)
+
+
+def test_decode_masks_and_none():
+    B, N = 3, 1000
+    c = W.make_case("decm", 17, batch=B, q_heads=8, kv_heads=2, head_dim=128,
+                    q_lens=[1] * B, kv_lens=[N, 600, 999], q_form="packed", kv_form="padded",
+                    kv_seq=N, dtype=torch.float16,
+                    mask=lambda g: torch.rand((B, 8, 1, N), generator=g) > 0.2)
+    _parity(c)
+    c = W.make_case("decn", 18, batch=B, q_heads=8, kv_heads=2, head_dim=128,
+                    q_lens=[1] * B, kv_lens=[N, 600, 999], q_form="packed", kv_form="padded",
+                    kv_seq=N, dtype=torch.float16, norm="none", scale=0.01)
+    _parity(c)
+
+
+# --------------------------------------------------------------------------
+# degenerate shapes and device-side length errors
+# --------------------------------------------------------------------------
+def test_empty_and_degenerate_rows():
+    # kv_len 0 (zero rows), q_len 0 (nothing written), lower_right with
+    # q_len > kv_len (leading rows have no key)
+    c = W.make_case("deg", 19, batch=4, q_heads=4, kv_heads=2, head_dim=64,
+                    q_lens=[5, 0, 200, 1], kv_lens=[0, 7, 150, 1], q_form="padded",
+                    kv_form="padded", q_seq=200, dtype=torch.float16, causal="lower_right",
+                    pass_query_lengths=True)
+    _parity(c)
+
+
+def test_all_keys_masked_rows_are_zero():
+    c = W.make_case("allmask", 20, batch=1, q_heads=2, kv_heads=2, head_dim=64,
+                    q_lens=[64], kv_lens=[64], dtype=torch.float16,
+                    mask=torch.zeros((1, 1, 64, 64), dtype=torch.bool))
+    y, raw, st = run_gpu(c)
+    assert (y == 0).all()
+
+
+def test_bad_lengths_set_status_and_leave_y_untouched():
+    c = W.make_case("bad", 21, batch=2, q_heads=2, kv_heads=2, head_dim=64,
+                    q_lens=[10, 20], q_form="packed", kv_form="packed", dtype=torch.float16)
+    c.query_lengths = torch.tensor([0, 25, 20], dtype=torch.int32)   # decreasing
+    y, raw, st = run_gpu(c)
+    assert binding.device_status(st) == 4
+    from helpers import SENTINEL
+    assert (raw == np.int16(SENTINEL)).all()
+
+
+def test_invalid_arguments_return_codes():
+    c = W.to_device(W.workload(1), "cuda")
+    y = torch.empty_like(c.q)
+    with pytest.raises(binding.RgaError) as e:   # mask together with causal
+        binding.trt_attention(c.q, c.k, c.v, out=y, causal="upper_left",
+                              mask=torch.ones(64, 64, dtype=torch.bool, device="cuda"))
+    assert e.value.code == 1
+    with pytest.raises(binding.RgaError) as e:   # head_dim 32 is not implemented
+        q = torch.zeros(1, 2, 8, 32, dtype=torch.float16, device="cuda")
+        binding.trt_attention(q, q, q)
+    assert e.value.code == 2
+    with pytest.raises(binding.RgaError) as e:   # 3 query heads over 2 KV heads
+        q = torch.zeros(1, 3, 8, 64, dtype=torch.float16, device="cuda")
+        kv = torch.zeros(1, 2, 8, 64, dtype=torch.float16, device="cuda")
+        binding.trt_attention(q, kv, kv)
+    assert e.value.code == 1
+
+
+def test_repeat_calls_reuse_workspace():
+    c = W.workload(1)
+    y1, _, _ = run_gpu(c)
+    y2, _, _ = run_gpu(c)
+    np.testing.assert_array_equal(y1, y2)
