@@ -85,6 +85,11 @@ def _f64(x):
     return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
 
 
+def torch_bool():
+    import torch
+    return torch.bool
+
+
 def _i32(x):
     if x is None:
         return None
@@ -138,7 +143,11 @@ def attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=None,
     madd = mbool = None
     mdims = np.ones(4, dtype=np.int64)
     if mask is not None:
-        m = mask.detach().cpu().numpy() if hasattr(mask, "detach") else np.asarray(mask)
+        if hasattr(mask, "detach"):   # torch: bool stays bool, others widen exactly
+            mask = mask.detach().cpu()
+            m = mask.numpy() if mask.dtype == torch_bool() else mask.double().numpy()
+        else:
+            m = np.asarray(mask)
         assert m.ndim <= 4
         mdims[4 - m.ndim:] = m.shape
         if m.dtype == np.bool_:
