@@ -65,7 +65,7 @@ def _load():
             lib.rga_oracle_attention.restype = i
             lib.rga_oracle_attention.argtypes = [
                 p, p, p, p, i, i, i, i, i, i, i, i, p, p, p, p, p,
-                d, i, i, i, d, i]
+                d, i, i, i, d, i, p, d]
             lib.rga_oracle_e4m3_decode.restype = d
             lib.rga_oracle_e4m3_decode.argtypes = [i]
             lib.rga_oracle_e4m3_round.restype = d
@@ -111,7 +111,7 @@ class OracleError(RuntimeError):
 def attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=None,
               kv_lengths=None, mask=None, scale=1.0, causal="none",
               norm="softmax", quant=None, quant_scale=None, y_init=None,
-              nthreads=None):
+              nthreads=None, ambiguity_eps=None):
     """Plain fp64 attention.  Returns a float64 array shaped like ``q``.
 
     q: padded [B,Hq,Nq,D] or packed [Tq,Hq,D]; k, v likewise for KV.
@@ -122,6 +122,9 @@ def attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=None,
     the scaled scores), rank <= 4, right-aligned to [B, Hq, Nq, Nkv].
     quant: None, 'fp8' or 'int8'; quant_scale the stored scale value.
     Rows that are not valid query rows keep ``y_init`` (default NaN).
+    With ``ambiguity_eps`` (quantized op), returns ``(y, amb)``: amb bounds
+    how far a quantised code within relative ``ambiguity_eps`` of a rounding
+    midpoint may move each output element if it rounds the other way.
     """
     lib = _load()
     qf = PACKED if q_form in ("packed", "packed_nhd", PACKED) else PADDED
@@ -157,14 +160,15 @@ def attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=None,
     qs = 1.0 if quant_scale is None else float(_f64(quant_scale).reshape(-1)[0])
     if nthreads is None:
         nthreads = os.cpu_count() or 1
+    amb = np.zeros(Q.shape) if ambiguity_eps is not None else None
     rc = lib.rga_oracle_attention(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(Y), qf, kf, B, Hq, Hkv, D, q_seq,
         kv_seq, _ptr(ql), _ptr(kl), _ptr(madd), _ptr(mbool), _ptr(mdims),
         float(scale), CAUSAL[causal], NORM[norm], QUANT[quant], qs,
-        int(nthreads))
+        int(nthreads), _ptr(amb), float(ambiguity_eps or 0.0))
     if rc != 0:
         raise OracleError(rc)
-    return Y
+    return Y if amb is None else (Y, amb)
 
 
 

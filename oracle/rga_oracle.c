@@ -133,12 +133,45 @@ static double qdq(double p, int quant, double s)
     return rga_oracle_int8_round(x) * s;
 }
 
+/* Where floating point decides a quantised code, a value within a relative
+ * distance eps of a rounding midpoint may round either way in any other
+ * correct evaluation order.  Returns the change of the dequantised value
+ * if such a code flipped (one quantisation step times s), or 0 when the
+ * decision is clear. */
+static double qdq_ambiguity(double p, int quant, double s, double eps)
+{
+    double x = fabs(p / s), step, t;
+    int ex;
+    if (eps <= 0.0 || x == 0.0)
+        return 0.0;
+    if (quant == ORA_Q_FP8) {
+        if (x >= 448.0)
+            return 0.0;                   /* saturated either way */
+        if (x < ldexp(1.0, -6)) {
+            step = ldexp(1.0, -9);
+        } else {
+            frexp(x, &ex);
+            step = ldexp(1.0, (ex - 1) - 3);
+        }
+    } else {
+        if (x >= 127.5)
+            return 0.0;
+        step = 1.0;
+    }
+    t = x / step - floor(x / step);      /* position inside the step */
+    if (fabs(t - 0.5) * step <= eps * (x > 1.0 ? x : 1.0))
+        return step * s;
+    return 0.0;
+}
+
 /* ---------------------------------------------------------------------------
  * Problem description shared by the worker threads.
  * ------------------------------------------------------------------------- */
 typedef struct {
     const double *q, *k, *v;
     double *y;
+    double *amb;                /* optional: per-element Q/DQ ambiguity bound */
+    double amb_eps;
     int q_form, kv_form, B, Hq, Hkv, D, q_seq, kv_seq;
     const int32_t *query_lengths, *kv_lengths;
     const double *mask_add;     /* additive mask, or NULL */
@@ -223,6 +256,9 @@ static void attend_row(const ora_problem *P, int b, int h, int64_t i,
 
     for (d = 0; d < P->D; ++d)
         yrow[d] = 0.0;
+    if (P->amb)
+        for (d = 0; d < P->D; ++d)
+            P->amb[q_index(P, b, h, i) + d] = 0.0;
     if (!any)
         return; /* no attendable key: the row is zero */
 
@@ -244,9 +280,20 @@ static void attend_row(const ora_problem *P, int b, int h, int64_t i,
     }
 
     if (P->quant != ORA_Q_OFF)
-        for (j = 0; j < L; ++j)
-            if (allowed[j])
-                s[j] = qdq(s[j], P->quant, P->quant_scale);
+        for (j = 0; j < L; ++j) {
+            if (!allowed[j])
+                continue;
+            if (P->amb) {
+                double a = qdq_ambiguity(s[j], P->quant, P->quant_scale, P->amb_eps);
+                if (a != 0.0) {
+                    const double *vrow = P->v + kv_index(P, b, g, j);
+                    double *arow = P->amb + q_index(P, b, h, i);
+                    for (d = 0; d < P->D; ++d)
+                        arow[d] += a * fabs(vrow[d]);
+                }
+            }
+            s[j] = qdq(s[j], P->quant, P->quant_scale);
+        }
 
     for (j = 0; j < L; ++j) {
         const double *vrow;
@@ -291,6 +338,10 @@ static void *worker(void *arg)
  * right-aligned to rank 4 (missing leading dims are 1).  quant is -1 (off),
  * 0 (fp8 E4M3FN) or 1 (int8).  Returns 0, 1 (bad argument) or 4 (bad
  * lengths).  Rows that are not valid query rows are left as they were.
+ * amb (optional, shaped like y): for the quantised op, the sum over the
+ * row's codes that lie within relative distance amb_eps of a rounding
+ * midpoint of (one quantisation step * s * |v|): how far another correct
+ * evaluation order may move each output element.
  * ------------------------------------------------------------------------- */
 int rga_oracle_attention(const double *q, const double *k, const double *v,
                          double *y, int q_form, int kv_form, int B, int Hq,
@@ -299,7 +350,8 @@ int rga_oracle_attention(const double *q, const double *k, const double *v,
                          const int32_t *kv_lengths, const double *mask_add,
                          const uint8_t *mask_bool, const int64_t *mask_dims,
                          double scale, int causal, int norm, int quant,
-                         double quant_scale, int nthreads)
+                         double quant_scale, int nthreads, double *amb,
+                         double amb_eps)
 {
     ora_problem P;
     pthread_t *th;
@@ -325,6 +377,7 @@ int rga_oracle_attention(const double *q, const double *k, const double *v,
         P.md[t] = (mask_add || mask_bool) ? mask_dims[t] : 1;
     P.scale = scale; P.causal = causal; P.norm = norm;
     P.quant = quant; P.quant_scale = quant_scale;
+    P.amb = amb; P.amb_eps = amb_eps;
     P.q_off = (int64_t *)calloc(B + 1, sizeof(int64_t));
     P.q_len = (int64_t *)calloc(B + 1, sizeof(int64_t));
     P.kv_off = (int64_t *)calloc(B + 1, sizeof(int64_t));

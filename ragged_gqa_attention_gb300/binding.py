@@ -176,10 +176,9 @@ def _call(quant, q, k, v, out, quant_args, stream, **kw):
     a = make_args(q, k, v, y, status=status, workspace=workspace, **kw)
     if workspace is None:
         n = lib.rga_attention_workspace_size(ctypes.byref(a))
-        if n == 0:
-            raise RgaError(1, "rga_attention_workspace_size")
-        ws = _workspace(q.device, n)
-        a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+        if n > 0:   # n == 0: invalid arguments; the call below reports which
+            ws = _workspace(q.device, n)
+            a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
     h = _stream_handle(stream)
     if quant:
         qt, qs = quant_args

@@ -17,6 +17,15 @@ SENTINEL = 0x7FDA                # a NaN bit pattern in both fp16 and bf16
 
 TOL = {None: (1e-2, 1e-3), "fp8": (3e-2, 3e-3), "int8": (3e-2, 3e-3)}
 
+# A quantised code is decided from fp32 scores on the GPU and fp64 scores in
+# the oracle; a code whose pre-quantisation value lies within
+# AMBIGUITY_EPS * max(|x|, 1) of a rounding midpoint may round either way.
+# fp32 accumulation of 128 products and exp2 put the GPU's x within a few
+# 1e-6 relative (and ~1e-4 absolute near 0) of the exact value; 2^-13 covers
+# that with margin.  Such flips are allowed on top of the tolerance, by the
+# bound the oracle computes for them.
+AMBIGUITY_EPS = 2.0 ** -13
+
 
 def guarded_output(q):
     """Y as a view into a bigger buffer prefilled with SENTINEL."""
@@ -43,11 +52,13 @@ def run_gpu(case: W.Case, *, status=None):
 
 
 def run_oracle(case: W.Case):
+    """Oracle output, or (output, ambiguity bound) for the quantized op."""
     return oracle.attention(
         case.q, case.k, case.v, q_form=case.q_form, kv_form=case.kv_form,
         query_lengths=case.query_lengths, kv_lengths=case.kv_lengths, mask=case.mask,
         scale=case.scale, causal=case.causal, norm=case.norm, quant=case.quant,
-        quant_scale=case.quant_scale)
+        quant_scale=case.quant_scale,
+        ambiguity_eps=AMBIGUITY_EPS if case.quant else None)
 
 
 def valid_row_mask(case: W.Case):
@@ -67,10 +78,15 @@ def valid_row_mask(case: W.Case):
 def check(case: W.Case, y_gpu, raw, y_ref, tol=None):
     """Element-wise parity on valid rows; bit-exact sentinel elsewhere."""
     atol_max, atol_mean = tol or TOL[case.quant]
+    amb = None
+    if isinstance(y_ref, tuple):
+        y_ref, amb = y_ref
     rows = valid_row_mask(case)
     g, r = y_gpu[rows], y_ref[rows]
     assert np.isfinite(g).all(), "non-finite output in a valid row"
     err = np.abs(g - r)
+    if amb is not None:   # allowed rounding flips of ambiguous codes
+        err = np.maximum(err - amb[rows], 0.0)
     if err.size:
         assert err.max() <= atol_max, f"max abs err {err.max():.3e} > {atol_max}"
         assert err.mean() <= atol_mean, f"mean abs err {err.mean():.3e} > {atol_mean}"

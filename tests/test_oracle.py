@@ -402,3 +402,42 @@ def test_brute_force_tiny(causal, norm, quant, maskkind):
                        v[0].double().numpy(), ql, kl, 0.6, causal, norm,
                        mask, quant, sq)
         np.testing.assert_allclose(y[0], want, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# Q/DQ ambiguity bound (quantised codes that sit on a rounding midpoint)
+# ----------------------------------------------------------------------------
+def _one_key(sval, quant, sq):
+    q = np.array([[[[1.0, 0.0]]]])
+    k = np.array([[[[sval, 0.0]]]])
+    v = np.array([[[[3.0, -2.0]]]])
+    return oracle.attention(q, k, v, scale=1.0, norm="none", quant=quant, quant_scale=sq,
+                            ambiguity_eps=1e-9)
+
+
+def test_ambiguity_marks_exact_midpoints_only():
+    y, amb = _one_key(2.5, "int8", 1.0)            # 2.5 -> 2 (even); could be 3
+    np.testing.assert_array_equal(y[0, 0, 0], [6.0, -4.0])
+    np.testing.assert_array_equal(amb[0, 0, 0], [3.0, 2.0])   # one step * s * |v|
+    y, amb = _one_key(2.3, "int8", 1.0)
+    assert (amb == 0).all()
+    y, amb = _one_key(1.0625, "fp8", 1.0)          # between 1.0 and 1.125
+    np.testing.assert_array_equal(y[0, 0, 0], [3.0, -2.0])
+    np.testing.assert_array_equal(amb[0, 0, 0], [0.375, 0.25])
+    y, amb = _one_key(1.1, "fp8", 1.0)
+    assert (amb == 0).all()
+
+
+@pytest.mark.parametrize("quant", ["fp8", "int8"])
+@pytest.mark.parametrize("norm", ["softmax", "none"])
+def test_ambiguity_bounds_perturbed_evaluation(quant, norm):
+    """Scores perturbed by a relative 1e-9 (another evaluation order) move the
+    output by no more than the bound computed with eps = 1e-8."""
+    c = _case(q_lens=[40, 30, 50], kv_lens=[60, 30, 50], causal="upper_left")
+    sq = 1 / 448 if quant == "fp8" else 1 / 127
+    sc = 0.05 if norm == "none" else c.scale
+    y0, amb = _run(c, quant=quant, quant_scale=sq, norm=norm, scale=sc, ambiguity_eps=1e-8)
+    for f in (1 + 1e-9, 1 - 1e-9):
+        y1 = _run(c, quant=quant, quant_scale=sq, norm=norm, scale=sc * f)
+        ok = ~np.isnan(y0)
+        assert (np.abs(y1[ok] - y0[ok]) <= amb[ok] + 1e-6).all()
