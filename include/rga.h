@@ -155,6 +155,31 @@ rga_status trt_quantized_attention(const rga_attention_args *args,
                                    rga_dtype quant_scale_dtype,
                                    cudaStream_t stream);
 
+/* Size of the library-owned device scratch used by
+ * trt_attention_static_scratch (40 MiB). */
+#define RGA_STATIC_SCRATCH_BYTES (40ull << 20)
+
+/* trt_attention without caller-provided scratch, for callers that cannot
+ * allocate device memory themselves (a host application that owns every
+ * allocation and hands the library only its tensors, or a caller with no
+ * allocator at hand).  The pages describe no such call: this entry point
+ * has no counterpart there.
+ *
+ * Same arguments and results as trt_attention, except that args->workspace
+ * and args->workspace_bytes are ignored: the scratch is a 40 MiB device
+ * array inside the library, held on every GPU that loads the library until
+ * the process exits.  Inputs, Y and device_status are still the caller's.
+ * Allocates nothing (no cudaMalloc, no allocating library routine).
+ *
+ * Returns RGA_ERR_WORKSPACE when rga_attention_workspace_size(args) exceeds
+ * RGA_STATIC_SCRATCH_BYTES.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call shares the
+ * one array: calls that overlap on the device race and give wrong results,
+ * so serialise them (one stream, or events).  Each call rewrites all the
+ * scratch it reads, so what a previous call left there does not matter. */
+rga_status trt_attention_static_scratch(const rga_attention_args *args, cudaStream_t stream);
+
 /* Copy *device_status to *out after the work already enqueued on `stream`
  * has finished.  This call synchronises the stream: use it in tests and
  * debugging, not on a hot path. */

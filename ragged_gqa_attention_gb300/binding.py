@@ -32,7 +32,8 @@ QUANT = {"fp8": 0, "int8": 1}
 DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.bool: 3}
 
 EXPORTED = ("rga_attention_workspace_size", "trt_attention", "trt_quantized_attention",
-            "rga_get_device_status", "rga_status_string", "rga_abi_version")
+            "rga_get_device_status", "rga_status_string", "rga_abi_version",
+            "trt_attention_static_scratch")
 
 
 class Args(ctypes.Structure):
@@ -83,6 +84,8 @@ def load(build_if_missing: bool = False):
             lib.trt_attention.argtypes = [P, c_vp]
             lib.trt_quantized_attention.restype = c_int
             lib.trt_quantized_attention.argtypes = [P, c_int, c_vp, c_int, c_vp]
+            lib.trt_attention_static_scratch.restype = c_int
+            lib.trt_attention_static_scratch.argtypes = [P, c_vp]
             lib.rga_get_device_status.restype = c_int
             lib.rga_get_device_status.argtypes = [c_vp, c_vp, ctypes.POINTER(c_i32)]
             lib.rga_status_string.restype = ctypes.c_char_p
