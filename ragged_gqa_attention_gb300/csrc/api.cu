@@ -154,10 +154,12 @@ AttnParams make_params(const rga_attention_args *a, bool quant) {
     p.causal = a->causal;
     p.quant = -1;
     p.tq = BM / p.G;
+    p.item_tokens = 2 * p.tq;
+    const int it = p.item_tokens;
     if (p.q_packed)
-        p.max_items = p.Hkv * ((p.q_seq + p.tq - 1) / p.tq + p.B);
+        p.max_items = p.Hkv * ((p.q_seq + it - 1) / it + p.B);
     else
-        p.max_items = p.Hkv * p.B * ((p.q_seq + p.tq - 1) / p.tq);
+        p.max_items = p.Hkv * p.B * ((p.q_seq + it - 1) / it);
     p.max_splits = (p.kv_seq + DEC_SPLIT - 1) / DEC_SPLIT;
     if (p.max_splits < 1) p.max_splits = 1;
     p.status = a->device_status;

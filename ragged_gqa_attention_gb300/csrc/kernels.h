@@ -40,6 +40,7 @@ struct AttnParams {
     const void *qscale;             // device scalar
     int qscale_dtype;
     int tq;                         // query tokens per prefill tile (BM / G)
+    int item_tokens;                // query tokens per prefill work item (2 tiles)
     int max_items;                  // capacity of the work list
     int max_splits;                 // decode: splits per (b, kv head)
     int32_t *status;                // device status word
@@ -75,8 +76,14 @@ struct TensorMaps {
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_sched(const AttnParams &p, int decode, cudaStream_t s);
-cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode,
-                           int grid, cudaStream_t s, int bf16);
+template <bool BF16>
+cudaError_t launch_prefill_typed(const AttnParams &p, const TensorMaps &m, int mode, int grid,
+                                 cudaStream_t s);
+inline cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode, int grid,
+                                  cudaStream_t s, int bf16) {
+    return bf16 ? launch_prefill_typed<true>(p, m, mode, grid, s)
+                : launch_prefill_typed<false>(p, m, mode, grid, s);
+}
 cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode,
                           cudaStream_t s, int bf16);
 

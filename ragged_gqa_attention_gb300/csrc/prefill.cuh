@@ -1,0 +1,784 @@
+// prefill.cuh - fused attention forward for sm_103a on the 5th-generation
+// tensor cores (tcgen05 + TMEM), with TMA-staged, 128-byte-swizzled Q/K/V
+// tiles and warp-specialised roles.
+//
+// Computes, per work item (batch b, KV head g, two query tiles):
+//   S = Q K^T (BMM1, fp32 in TMEM)  ->  scale, causal / length / mask
+//   ->  softmax (online, fp32, exp2) or 'none'  ->  optional fp8/int8 Q/DQ
+//   ->  O += P V (BMM2, fp32 in TMEM)  ->  O / l  ->  Y
+// following "TensorRT Custom Operator Schemas" (TRT_Attention,
+// TRT_QuantizedAttention) and the MHA/GQA AttentionPlugin of the "TensorRT
+// Plugins Guide".
+//
+// GQA reuse: the 128 rows of a query tile are the G = Hq/Hkv query heads of
+// one KV head times TQ = 128/G tokens, so every K/V tile is loaded once for
+// the whole group.  Row r maps to (token t, head hh) as r = t*G + hh for
+// packed Q ([T,H,D]: the G heads of a token are adjacent) and r = hh*TQ + t
+// for padded Q ([B,H,N,D]).  A work item holds two such tiles (2*TQ tokens)
+// that share every K/V tile.
+//
+// Roles (320 threads):
+//   warps 0-3  softmax warpgroup of tile 0 (thread = TMEM lane = row)
+//   warps 4-7  softmax warpgroup of tile 1
+//   warp 8     TMEM owner and single-thread MMA issuer
+//   warp 9     TMA producer (Q once per item, K and V rings)
+// Tensor-core order per key tile j:  S0(j+1) after O0 += P0(j) V(j), and
+// S1(j+1) after O1 += P1(j) V(j), so while one warpgroup turns its scores
+// into probabilities the tensor core works for the other one.
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// P (16-bit) is written over the S columns it came from and fed to BMM2 from
+// TMEM; only V is read from shared memory for BMM2.
+//
+// The grid is persistent (one CTA per SM); CTA c takes items c, c+grid, ...
+// of the work list, which the scheduler sorted longest first.
+#pragma once
+#include <cuda.h>
+#include <type_traits>
+#include "device_common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace rga {
+
+constexpr int PF_THREADS = 320;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
+constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int D>
+struct PfLayout {
+    static constexpr int KST = 3;                        // K ring stages
+    static constexpr int VST = D == 128 ? 2 : 3;         // V ring stages
+    static constexpr int BLK = 128 * 128;                // one 64-column block of 128 rows
+    static constexpr int NBLK = D / 64;
+    static constexpr int TILE = NBLK * BLK;              // 128 rows x D x 2 bytes
+    static constexpr int Q_OFF = 0;                      // two Q tiles
+    static constexpr int K_OFF = Q_OFF + 2 * TILE;
+    static constexpr int V_OFF = K_OFF + KST * TILE;
+    static constexpr int BAR_OFF = V_OFF + VST * TILE;
+    // barriers: q_full, q_empty, k_full[KST], k_empty[KST], v_full[VST],
+    // v_empty[VST], s_full[2], p_full[2], o_done[2]
+    static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 6;
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr int BYTES = MISC_OFF + 64;
+    // room to align the base to 1024; at least 120 KB so that only one CTA
+    // (and one 512-column TMEM allocation) is resident per SM
+    static constexpr int ALLOC = (BYTES + 1024) > 120 * 1024 ? (BYTES + 1024) : 120 * 1024;
+    static_assert(ALLOC <= 232448, "shared memory per CTA");
+};
+
+struct PfBars {
+    uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full,
+        *o_done;
+};
+
+template <int D>
+__device__ __forceinline__ PfBars pf_bars(uint8_t *base) {
+    using L = PfLayout<D>;
+    uint64_t *b = reinterpret_cast<uint64_t *>(base);
+    PfBars r;
+    r.q_full = b;
+    r.q_empty = b + 1;
+    r.k_full = b + 2;
+    r.k_empty = r.k_full + L::KST;
+    r.v_full = r.k_empty + L::KST;
+    r.v_empty = r.v_full + L::VST;
+    r.s_full = r.v_empty + L::VST;
+    r.p_full = r.s_full + 2;
+    r.o_done = r.p_full + 2;
+    return r;
+}
+
+// Per-item geometry, computed identically by every role.
+struct Item {
+    int b, qt, g;
+    SeqInfo s;
+    int i0;          // first query token of the item (within the sequence)
+    int ntok;        // valid tokens in the item (<= 2 * TQ)
+    int nkt;         // key tiles visited
+    int ntiles;      // BMM1 steps per tile (2 * nkt for the two-pass quantized softmax)
+};
+
+template <int MODE>
+__device__ __forceinline__ Item load_item(const AttnParams &p, int idx) {
+    const int4 it = reinterpret_cast<const int4 *>(p.ws + WS_HEADER)[idx];
+    Item m;
+    m.b = it.x;
+    m.qt = it.y;
+    m.g = it.z;
+    m.s = seq_info(p, m.b);
+    m.i0 = m.qt * p.item_tokens;
+    m.ntok = min(p.item_tokens, m.s.q_len - m.i0);
+    const int n = key_extent(p.causal, m.i0 + m.ntok - 1, m.s);
+    m.nkt = (n + BN - 1) / BN;
+    m.ntiles = (MODE == MODE_SOFTMAX_Q) ? 2 * m.nkt : m.nkt;
+    return m;
+}
+
+// Whether BMM1 step t is followed by a BMM2 (pass 1 of the two-pass
+// quantized softmax only gathers row statistics).
+template <int MODE>
+__device__ __forceinline__ bool is_pv(const Item &m, int t) {
+    return MODE != MODE_SOFTMAX_Q || t >= m.nkt;
+}
+template <int MODE>
+__device__ __forceinline__ int key_tile(const Item &m, int t) {
+    return (MODE == MODE_SOFTMAX_Q && t >= m.nkt) ? t - m.nkt : t;
+}
+
+// ------------------------------------------------------------------ loads
+// Load a partial V tile (keys j0 .. j0+127 with only `rem` < 128 valid) with
+// plain loads, zero the rows past the sequence end (they may hold NaN), and
+// publish it to the tensor core through the async proxy.
+template <int D>
+__device__ void load_v_partial(const AttnParams &p, const Item &m, int j0, int rem,
+                               uint8_t *dst, int lane) {
+    constexpr int CH = D / 8;   // 16-byte chunks per row
+    const uint16_t *v = static_cast<const uint16_t *>(p.v);
+    for (int idx = lane; idx < 128 * CH; idx += 32) {
+        const int r = idx / CH, c = idx % CH;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (r < rem) {
+            const long long j = (long long)j0 + r;
+            const long long off = p.kv_packed
+                ? ((m.s.kv_off + j) * p.Hkv + m.g) * (long long)D
+                : (((long long)m.b * p.Hkv + m.g) * p.kv_seq + j) * (long long)D;
+            val = *reinterpret_cast<const uint4 *>(v + off + c * 8);
+        }
+        const int blk = c / 8, cc = c % 8;
+        uint8_t *row = dst + blk * PfLayout<D>::BLK + r * 128;
+        *reinterpret_cast<uint4 *>(row + ((cc ^ (r & 7)) * 16)) = val;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+}
+
+// TMA box of query tile `a` of the item (per 64-column block).
+__device__ __forceinline__ void tma_q(const AttnParams &p, const CUtensorMap *map,
+                                      const Item &m, int a, void *dst, uint64_t *bar, int d0) {
+    const int tok = m.i0 + a * p.tq;
+    if (p.q_packed)   // dims (D, Hq, T): box (64, G, TQ)
+        tma_load_3d(dst, map, bar, d0, m.g * p.G, m.s.q_off + tok);
+    else              // dims (D, Nq, Hq, B): box (64, TQ, G, 1)
+        tma_load_4d(dst, map, bar, d0, tok, m.g * p.G, m.b);
+}
+__device__ __forceinline__ void tma_kv(const AttnParams &p, const CUtensorMap *map,
+                                       const Item &m, int j0, void *dst, uint64_t *bar,
+                                       int d0) {
+    if (p.kv_packed)  // dims (D, Hkv, T): box (64, 1, 128)
+        tma_load_3d(dst, map, bar, d0, m.g, m.s.kv_off + j0);
+    else              // dims (D, Nkv, Hkv, B): box (64, 128, 1, 1)
+        tma_load_4d(dst, map, bar, d0, j0, m.g, m.b);
+}
+
+// ------------------------------------------------------------------ producer
+template <int D, int MODE>
+__device__ void producer_role(const AttnParams &p, const TensorMaps &tm, uint8_t *sm,
+                              const PfBars &bar, volatile int *abort, int n_items) {
+    using L = PfLayout<D>;
+    const int lane = threadIdx.x & 31;
+    const uint32_t q_bytes = (uint32_t)(2 * L::NBLK * p.G * p.tq * 128);
+    const uint32_t kv_bytes = (uint32_t)L::TILE;
+    uint32_t kc = 0, vc = 0, qc = 0;   // running ring counters
+    for (int idx = blockIdx.x; idx < n_items && !*abort; idx += gridDim.x) {
+        const Item m = load_item<MODE>(p, idx);
+        if (m.nkt == 0) continue;
+        // both Q tiles, once per item, after the previous item's BMM1s
+        if (qc > 0 && !mbar_wait(bar.q_empty, (qc - 1) & 1, abort)) break;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar.q_full, q_bytes);
+            for (int a = 0; a < 2; ++a)
+                for (int blk = 0; blk < L::NBLK; ++blk)
+                    tma_q(p, &tm.q, m, a, sm + L::Q_OFF + a * L::TILE + blk * L::BLK, bar.q_full,
+                          blk * 64);
+        }
+        ++qc;
+        for (int t = 0; t < m.ntiles && !*abort; ++t) {
+            const int j0 = key_tile<MODE>(m, t) * BN;
+            const int ks = kc % L::KST;
+            if (kc >= L::KST && !mbar_wait(&bar.k_empty[ks], ((kc / L::KST) - 1) & 1, abort)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar.k_full[ks], kv_bytes);
+                for (int blk = 0; blk < L::NBLK; ++blk)
+                    tma_kv(p, &tm.k, m, j0, sm + L::K_OFF + ks * L::TILE + blk * L::BLK,
+                           &bar.k_full[ks], blk * 64);
+            }
+            ++kc;
+            if (!is_pv<MODE>(m, t)) continue;
+            const int vs = vc % L::VST;
+            if (vc >= L::VST && !mbar_wait(&bar.v_empty[vs], ((vc / L::VST) - 1) & 1, abort)) break;
+            uint8_t *vdst = sm + L::V_OFF + vs * L::TILE;
+            const int rem = m.s.kv_len - j0;
+            if (rem >= BN) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar.v_full[vs], kv_bytes);
+                    for (int blk = 0; blk < L::NBLK; ++blk)
+                        tma_kv(p, &tm.v, m, j0, vdst + blk * L::BLK, &bar.v_full[vs], blk * 64);
+                }
+            } else {
+                load_v_partial<D>(p, m, j0, rem, vdst, lane);
+                if (lane == 0) mbar_arrive(&bar.v_full[vs]);
+            }
+            ++vc;
+        }
+    }
+    // Before the CTA exits, let every copy this warp started land.
+    for (uint32_t c = kc > L::KST ? kc - L::KST : 0; c < kc; ++c)
+        mbar_wait_drain(&bar.k_full[c % L::KST], (c / L::KST) & 1);
+    for (uint32_t c = vc > L::VST ? vc - L::VST : 0; c < vc; ++c)
+        mbar_wait_drain(&bar.v_full[c % L::VST], (c / L::VST) & 1);
+    if (qc > 0) mbar_wait_drain(bar.q_full, (qc - 1) & 1);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+// One thread issues every tcgen05.mma, in the order
+//   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
+template <int D, int MODE, bool BF16>
+__device__ void mma_role(const AttnParams &p, uint8_t *sm, const PfBars &bar,
+                         volatile int *abort, int n_items, uint32_t tmem) {
+    using L = PfLayout<D>;
+    constexpr uint32_t ID_S = idesc_f16(BF16 ? 1 : 0, 128, BN, 0, 0);   // Q K-major, K K-major
+    constexpr uint32_t ID_O = idesc_f16(BF16 ? 1 : 0, 128, D, 0, 1);    // P from TMEM, V MN-major
+    const uint32_t q_base = smem_u32(sm + L::Q_OFF);
+    const uint32_t k_base = smem_u32(sm + L::K_OFF);
+    const uint32_t v_base = smem_u32(sm + L::V_OFF);
+    uint32_t kc = 0, vc = 0, qc = 0, tc = 0;   // tc: BMM1 steps per tile, running
+    bool ok = true;
+
+    auto bmm1 = [&](int a, uint32_t kb) {
+        const uint32_t qb = q_base + a * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::BLK + (kk & 3) * 32;
+            mma_ss(tmem + S_COL0 + a * 128, sdesc(qb + off, 16, 1024), sdesc(kb + off, 16, 1024),
+                   ID_S, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar.s_full[a]);
+    };
+    auto bmm2 = [&](int a, uint32_t vb, bool first) {
+        const uint32_t pa = tmem + S_COL0 + a * 128;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + O_COL0 + a * D, pa + kk * 8, sdesc(vb + kk * 2048, L::BLK, 1024), ID_O,
+                   (!first || kk > 0) ? 1u : 0u);
+        mma_commit(&bar.o_done[a]);
+    };
+
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const Item m = load_item<MODE>(p, idx);
+        if (m.nkt == 0) continue;
+        if (!mbar_wait(bar.q_full, qc & 1, abort)) break;
+        ++qc;
+        tc_fence_after();
+        // S0(0), S1(0)
+        {
+            const int ks = kc % L::KST;
+            if (!mbar_wait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) break;
+            tc_fence_after();
+            const uint32_t kb = k_base + ks * L::TILE;
+            bmm1(0, kb);
+            bmm1(1, kb);
+            mma_commit(&bar.k_empty[ks]);
+            ++kc;
+            if (m.ntiles == 1) mma_commit(bar.q_empty);
+        }
+        int u = 0;   // BMM2 steps of this item
+        for (int t = 0; t < m.ntiles && ok; ++t) {
+            const bool pv = is_pv<MODE>(m, t);
+            const bool more = t + 1 < m.ntiles;
+            uint32_t vb = 0;
+            if (pv) {
+                const int vs = vc % L::VST;
+                if (!mbar_wait(&bar.v_full[vs], (vc / L::VST) & 1, abort)) { ok = false; break; }
+                vb = v_base + vs * L::TILE;
+            }
+            uint32_t kb = 0;
+            int ks = 0;
+            for (int a = 0; a < 2; ++a) {
+                // P_a(t) ready (or, for a statistics step, S_a(t) consumed)
+                if (!mbar_wait(&bar.p_full[a], tc & 1, abort)) { ok = false; break; }
+                tc_fence_after();
+                if (pv) bmm2(a, vb, u == 0);
+                if (more) {
+                    if (a == 0) {
+                        ks = kc % L::KST;
+                        if (!mbar_wait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) { ok = false; break; }
+                        tc_fence_after();
+                        kb = k_base + ks * L::TILE;
+                    }
+                    bmm1(a, kb);
+                }
+            }
+            if (!ok) break;
+            if (pv) {
+                mma_commit(&bar.v_empty[vc % L::VST]);
+                ++vc;
+                ++u;
+            }
+            if (more) {
+                mma_commit(&bar.k_empty[ks]);
+                ++kc;
+                if (t + 1 == m.ntiles - 1) mma_commit(bar.q_empty);
+            }
+            ++tc;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ softmax
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Mask forms handled on the partial-tile path.
+enum MaskKind { MK_BITS = 0, MK_ADD_F16 = 1, MK_ADD_BF16 = 2, MK_ADD_F32 = 3 };
+
+template <typename T>
+__device__ __forceinline__ float ld_as_float(const void *base, long long e) {
+    if constexpr (sizeof(T) == 4) return static_cast<const float *>(base)[e];
+    else if constexpr (std::is_same<T, __half>::value)
+        return __half2float(static_cast<const __half *>(base)[e]);
+    else return __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[e]);
+}
+
+// Chunk c (keys j0 + 32c .. j0 + 32c + 31) of a partial tile, scaled and
+// masked in place.  Key kk = 32c + k is allowed when kk <= rem (causal and
+// length limits) and its bit is set: bit (kk >> 2) of word (kk & 3).
+// Writes log2-domain scores (softmax) or natural-unit scores ('none'), and
+// -inf where the pair is excluded.
+template <bool LOG2, int MK>
+__device__ __forceinline__ void mask_chunk(const AttnParams &p, float (&v)[32], int c, int rem,
+                                           const uint32_t (&bits)[4], long long mrow, int j0) {
+    const float sc = LOG2 ? p.scale_log2 : p.scale;
+    const bool keyb = p.md[3] == 1;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const int kk = c * 32 + k;
+        bool ok = kk <= rem;
+        float val = v[k] * sc;
+        if constexpr (MK == MK_BITS) {
+            ok = ok && ((bits[k & 3] >> (8 * c + (k >> 2))) & 1u);
+        } else {
+            if (ok) {
+                const long long e = keyb ? mrow : mrow + j0 + kk;
+                float add;
+                if constexpr (MK == MK_ADD_F16) add = ld_as_float<__half>(p.mask, e);
+                else if constexpr (MK == MK_ADD_BF16) add = ld_as_float<__nv_bfloat16>(p.mask, e);
+                else add = ld_as_float<float>(p.mask, e);
+                val += LOG2 ? add * LOG2E : add;
+            }
+        }
+        v[k] = ok ? val : -INFINITY;
+    }
+}
+
+template <bool LOG2>
+__device__ __forceinline__ void mask_chunk_any(const AttnParams &p, int mk, float (&v)[32], int c,
+                                               int rem, const uint32_t (&bits)[4],
+                                               long long mrow, int j0) {
+    switch (mk) {
+    case MK_ADD_F16: mask_chunk<LOG2, MK_ADD_F16>(p, v, c, rem, bits, mrow, j0); break;
+    case MK_ADD_BF16: mask_chunk<LOG2, MK_ADD_BF16>(p, v, c, rem, bits, mrow, j0); break;
+    case MK_ADD_F32: mask_chunk<LOG2, MK_ADD_F32>(p, v, c, rem, bits, mrow, j0); break;
+    default: mask_chunk<LOG2, MK_BITS>(p, v, c, rem, bits, mrow, j0); break;
+    }
+}
+
+__device__ __forceinline__ float chunk_max(const float (&v)[32]) {
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        m0 = fmax3(m0, v[k], v[k + 1]);
+        m1 = fmax3(m1, v[k + 2], v[k + 3]);
+        m2 = fmax3(m2, v[k + 4], v[k + 5]);
+        m3 = fmax3(m3, v[k + 6], v[k + 7]);
+    }
+    return fmax3(fmaxf(m0, m1), m2, m3);
+}
+
+__device__ __forceinline__ void as_float(const uint32_t (&r)[32], float (&v)[32]) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+}
+
+// Bitmap of allowed keys j0 .. j0+127 for a bool mask: bit (c >> 2) of
+// word (c & 3) is key c.  When the mask does not depend on the query row
+// (it broadcasts over heads and query positions) the warp builds it
+// together with four ballots; otherwise each thread reads its own row.
+__device__ __forceinline__ void mask_bits(const AttnParams &p, bool row_indep, long long mrow,
+                                          int j0, int kv_len, bool row_ok, uint32_t (&bits)[4]) {
+    const uint8_t *mk = static_cast<const uint8_t *>(p.mask);
+    const bool keyb = p.md[3] == 1;
+    if (row_indep) {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int j = j0 + lane * 4 + k;
+            const bool ok = j < kv_len && mk[keyb ? mrow : mrow + j] != 0;
+            bits[k] = __ballot_sync(0xffffffffu, ok);
+        }
+        return;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) bits[k] = 0;
+    if (!row_ok) return;
+#pragma unroll 1
+    for (int c = 0; c < BN; ++c) {
+        const int j = j0 + c;
+        if (j < kv_len && mk[keyb ? mrow : mrow + j] != 0) {
+            const uint32_t bit = 1u << (c >> 2);
+            switch (c & 3) {   // a switch keeps bits[] in registers
+            case 0: bits[0] |= bit; break;
+            case 1: bits[1] |= bit; break;
+            case 2: bits[2] |= bit; break;
+            default: bits[3] |= bit; break;
+            }
+        }
+    }
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void store_row(const AttnParams &p, const Item &m, int i, int h,
+                                          uint32_t o_taddr, float f, bool zero, bool write) {
+    // every lane takes part in the (warp-collective) TMEM loads; only rows
+    // that belong to the sequence are written
+    uint16_t *y = static_cast<uint16_t *>(p.y);
+    const long long off = p.q_packed
+        ? ((long long)(m.s.q_off + i) * p.Hq + h) * D
+        : (((long long)m.b * p.Hq + h) * p.q_seq + i) * D;
+    uint4 *dst = reinterpret_cast<uint4 *>(y + off);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        if (!zero) {
+            tmem_ld32(o_taddr + c * 32, r);
+            tmem_wait_ld();
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            w[k] = zero ? 0u
+                        : pack2<BF16>(__uint_as_float(r[2 * k]) * f,
+                                      __uint_as_float(r[2 * k + 1]) * f);
+        if (write) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                dst[c * 4 + k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+        }
+    }
+}
+
+template <int D, int MODE, bool BF16>
+__device__ void softmax_role(const AttnParams &p, const PfBars &bar, volatile int *abort,
+                             int n_items, uint32_t tmem, int a) {
+    constexpr bool SOFTMAX = (MODE == MODE_SOFTMAX || MODE == MODE_SOFTMAX_Q);
+    constexpr bool QUANT = (MODE == MODE_SOFTMAX_Q || MODE == MODE_NONE_Q);
+    const int r = threadIdx.x & 127;                 // row = TMEM lane
+    const uint32_t lane_base = (uint32_t)((r & ~31) << 16);
+    const uint32_t s_addr = tmem + lane_base + S_COL0 + a * 128;
+    const uint32_t o_addr = tmem + lane_base + O_COL0 + a * D;
+    const int G = p.G, TQ = p.tq;
+    const int t_row = p.q_packed ? r / G : r % TQ;
+    const int hh = p.q_packed ? r % G : r / TQ;
+    const bool in_tile = r < G * TQ;
+    const float qs = QUANT ? load_qscale(p) : 1.f;
+    const float inv_qs = 1.f / qs;
+    const float sc = SOFTMAX ? p.scale_log2 : p.scale;
+    const bool use_mask = p.mask != nullptr;
+    const bool bool_mask = use_mask && p.mask_dtype == 3;
+    const bool row_indep = bool_mask && p.md[1] == 1 && p.md[2] == 1;
+    const int mk = !use_mask || bool_mask ? MK_BITS
+                   : p.mask_dtype == 0 ? MK_ADD_F16 : p.mask_dtype == 1 ? MK_ADD_BF16 : MK_ADD_F32;
+    uint32_t tc = 0, pvw = 0;                        // steps seen, BMM2 completions waited
+    bool ok = true;
+
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const Item m = load_item<MODE>(p, idx);
+        const int tok = a * TQ + t_row;              // token within the item
+        const int i = m.i0 + tok;
+        const int h = m.g * G + hh;
+        const bool row_ok = in_tile && tok < m.ntok;
+        if (m.nkt == 0) {                            // no attendable key: the rows are zero
+            store_row<D, BF16>(p, m, i, h, 0, 0.f, true, row_ok);
+            continue;
+        }
+        const int lim = row_ok ? min(causal_limit(p.causal, i, m.s), m.s.kv_len - 1) : -1;
+        const int lim_first = min(causal_limit(p.causal, m.i0 + a * TQ, m.s), m.s.kv_len - 1);
+        const long long mrow = !use_mask ? 0
+                               : row_indep ? mask_row(p, m.b, 0, 0)
+                               : row_ok ? mask_row(p, m.b, h, i) : 0;
+        float m_ref = -INFINITY, l = 0.f, lse2 = 0.f;
+        int u = 0;
+        for (int t = 0; t < m.ntiles; ++t) {
+            if (!mbar_wait(&bar.s_full[a], tc & 1, abort)) { ok = false; break; }
+            tc_fence_after();
+            const int j0 = key_tile<MODE>(m, t) * BN;
+            const int rem = lim - j0;
+            const bool full = !use_mask && j0 + BN - 1 <= lim_first && sc > 0.f;
+            const bool stat = (MODE == MODE_SOFTMAX_Q) && t < m.nkt;
+            uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+            if (bool_mask && !full) mask_bits(p, row_indep, mrow, j0, m.s.kv_len, row_ok, bits);
+
+            // pass A: row max of the scaled, masked scores
+            float mx = -INFINITY;
+            if (MODE == MODE_SOFTMAX || stat) {
+#pragma unroll
+                for (int c2 = 0; c2 < BN / 32; c2 += 2) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(s_addr + c2 * 32, r0);
+                    tmem_ld32(s_addr + (c2 + 1) * 32, r1);
+                    tmem_wait_ld();
+                    float v0[32], v1[32];
+                    as_float(r0, v0);
+                    as_float(r1, v1);
+                    if (!full) {
+                        mask_chunk_any<SOFTMAX>(p, mk, v0, c2, rem, bits, mrow, j0);
+                        mask_chunk_any<SOFTMAX>(p, mk, v1, c2 + 1, rem, bits, mrow, j0);
+                    }
+                    mx = fmax3(mx, chunk_max(v0), chunk_max(v1));
+                }
+                if (full) mx *= sc;
+                if (!row_ok) mx = -INFINITY;
+            }
+
+            // the value subtracted inside exp2 (log2 domain)
+            float ref = 0.f, alpha = 1.f;
+            bool need = false;
+            if (stat) {
+                const float m_new = fmaxf(m_ref, mx);
+                ref = (m_new == -INFINITY) ? 0.f : m_new;
+            } else if (MODE == MODE_SOFTMAX) {
+                const float m_new = fmaxf(m_ref, mx);
+                if (m_new > m_ref + RESCALE_THRESHOLD) {
+                    alpha = ex2(m_ref - m_new);
+                    l *= alpha;
+                    m_ref = m_new;
+                    need = true;
+                }
+                ref = (m_ref == -INFINITY) ? 0.f : m_ref;
+            } else if (MODE == MODE_SOFTMAX_Q) {
+                ref = lse2;   // pass 2: p / s_q directly
+            }
+
+            // pass B: probabilities (or the row sum, for a statistics step)
+            const float mul = full ? sc : 1.f;
+            const uint64_t mul2 = f2_pack(mul, mul), neg2 = f2_pack(-ref, -ref);
+            uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+            for (int c2 = 0; c2 < BN / 32; c2 += 2) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(s_addr + c2 * 32, r0);
+                tmem_ld32(s_addr + (c2 + 1) * 32, r1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c = c2 + h2;
+                    float v[32];
+                    as_float(h2 ? r1 : r0, v);
+                    if (!full) mask_chunk_any<SOFTMAX>(p, mk, v, c, rem, bits, mrow, j0);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        float pa = v[2 * k], pb = v[2 * k + 1];
+                        if (SOFTMAX) {
+                            f2_unpack(ffma2(f2_pack(pa, pb), mul2, neg2), pa, pb);
+                            pa = ex2(pa);
+                            pb = ex2(pb);
+                            if (MODE == MODE_SOFTMAX || stat) {
+                                if (k & 1) acc1 = fadd2(acc1, f2_pack(pa, pb));
+                                else acc0 = fadd2(acc0, f2_pack(pa, pb));
+                            }
+                        } else {
+                            pa = (pa == -INFINITY) ? 0.f : pa * mul;
+                            pb = (pb == -INFINITY) ? 0.f : pb * mul;
+                            if (MODE == MODE_NONE_Q) {
+                                pa *= inv_qs;
+                                pb *= inv_qs;
+                            }
+                        }
+                        if (QUANT && !stat) {
+                            if (p.quant == 0) {
+                                const float2 e = e4m3_round2(pa, pb);
+                                pa = e.x;
+                                pb = e.y;
+                            } else {
+                                pa = int8_round(pa);
+                                pb = int8_round(pb);
+                            }
+                        }
+                        w[k] = pack2<BF16>(pa, pb);
+                    }
+                    if (!stat) tmem_st16(s_addr + c * 16, w);
+                }
+            }
+            float s0, s1, s2, s3;
+            f2_unpack(acc0, s0, s1);
+            f2_unpack(acc1, s2, s3);
+            const float psum = (s0 + s1) + (s2 + s3);
+
+            if (stat) {
+                // pass 1 of the quantized softmax: exact row max and sum
+                const float m_new = fmaxf(m_ref, mx);
+                if (m_new != -INFINITY) {
+                    l = l * ex2(m_ref - m_new) + psum;
+                    m_ref = m_new;
+                }
+                if (t == m.nkt - 1)
+                    lse2 = (l > 0.f) ? m_ref + log2f(l) + log2f(qs) : INFINITY;
+                tc_fence_before();
+                mbar_arrive(&bar.p_full[a]);
+                ++tc;
+                continue;
+            }
+            if (MODE == MODE_SOFTMAX) l += psum;
+            if (u > 0) {   // BMM2 of the previous step must be done before O is touched
+                if (!mbar_wait(&bar.o_done[a], pvw & 1, abort)) { ok = false; break; }
+                ++pvw;
+                if (MODE == MODE_SOFTMAX && __any_sync(0xffffffffu, need)) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(o_addr + c * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tmem_st32(o_addr + c * 32, o);
+                    }
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar.p_full[a]);
+            ++u;
+            ++tc;
+        }
+        if (!ok) break;
+        // epilogue: after the item's last BMM2
+        if (!mbar_wait(&bar.o_done[a], pvw & 1, abort)) { ok = false; break; }
+        ++pvw;
+        tc_fence_after();
+        float f;
+        if (MODE == MODE_SOFTMAX) f = (l > 0.f) ? 1.f / l : 0.f;
+        else f = qs;    // 'none': 1; quantized: the Q/DQ scale
+        store_row<D, BF16>(p, m, i, h, o_addr, f, false, row_ok);
+        tc_fence_before();
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, int MODE, bool BF16>
+__global__ void __launch_bounds__(PF_THREADS, 1)
+prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TensorMaps tm) {
+    using L = PfLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const PfBars bar = pf_bars<D>(sm + L::BAR_OFF);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF);
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + L::MISC_OFF + 8);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_items = *reinterpret_cast<volatile const int *>(p.ws);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar.q_full, 1);
+        mbar_init(bar.q_empty, 1);
+        for (int s = 0; s < L::KST; ++s) { mbar_init(&bar.k_full[s], 1); mbar_init(&bar.k_empty[s], 1); }
+        for (int s = 0; s < L::VST; ++s) { mbar_init(&bar.v_full[s], 1); mbar_init(&bar.v_empty[s], 1); }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar.s_full[s], 1);
+            mbar_init(&bar.p_full[s], 128);
+            mbar_init(&bar.o_done[s], 1);
+        }
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 9 && lane == 0) {
+        prefetch_tmap(&tm.q);
+        prefetch_tmap(&tm.k);
+        prefetch_tmap(&tm.v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 8) {
+        softmax_role<D, MODE, BF16>(p, bar, abort, n_items, tmem, warp >> 2);
+    } else if (warp == 8) {
+        if (lane == 0) mma_role<D, MODE, BF16>(p, sm, bar, abort, n_items, tmem);
+        __syncwarp();
+    } else {
+        producer_role<D, MODE>(p, tm, sm, bar, abort, n_items);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 8) tmem_dealloc(tmem, TMEM_COLS);
+    if (threadIdx.x == 0 && *abort) set_status(p.status, 5);
+}
+
+template <int D, int MODE, bool BF16>
+static cudaError_t launch_one(const AttnParams &p, const TensorMaps &m, int grid,
+                              cudaStream_t s) {
+    using L = PfLayout<D>;
+    static bool attr_set = false;   // per process; the attribute is per function
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MODE, BF16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             L::ALLOC);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    prefill_kernel<D, MODE, BF16><<<grid, PF_THREADS, L::ALLOC, s>>>(p, m);
+    return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+static cudaError_t launch_mode(const AttnParams &p, const TensorMaps &m, int mode, int grid,
+                               cudaStream_t s) {
+    switch (mode) {
+    case MODE_SOFTMAX: return launch_one<D, MODE_SOFTMAX, BF16>(p, m, grid, s);
+    case MODE_NONE: return launch_one<D, MODE_NONE, BF16>(p, m, grid, s);
+    case MODE_SOFTMAX_Q: return launch_one<D, MODE_SOFTMAX_Q, BF16>(p, m, grid, s);
+    default: return launch_one<D, MODE_NONE_Q, BF16>(p, m, grid, s);
+    }
+}
+
+// Launch for one element type; each type is instantiated in its own
+// translation unit (prefill_f16.cu, prefill_bf16.cu).
+template <bool BF16>
+cudaError_t launch_prefill_typed(const AttnParams &p, const TensorMaps &m, int mode, int grid,
+                                 cudaStream_t s) {
+    if (p.D == 64) return launch_mode<64, BF16>(p, m, mode, grid, s);
+    return launch_mode<128, BF16>(p, m, mode, grid, s);
+}
+
+}  // namespace rga

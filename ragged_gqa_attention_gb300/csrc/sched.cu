@@ -2,7 +2,7 @@
 //
 // Reads query_lengths / kv_lengths on the device (they never go to the
 // host), validates them, and for prefill writes the list of work items
-// (batch, query tile, KV head, cost) sorted by cost, longest first, so that
+// (batch, query block of item_tokens tokens, KV head, cost) sorted by cost, longest first, so that
 // the persistent prefill grid starts the biggest items first.  Cost is the
 // number of 128-key tiles the item visits after causal and length
 // skipping.  For decode it only validates and clears the split tickets.
@@ -17,9 +17,10 @@ namespace rga {
 
 constexpr int SCHED_THREADS = 1024;
 constexpr int COST_BUCKETS = 1024;
+static_assert(COST_BUCKETS == SCHED_THREADS, "one bucket per thread in the scan");
 
 __device__ __forceinline__ int item_cost(const AttnParams &p, const SeqInfo &s, int qt) {
-    int i_last = min((qt + 1) * p.tq, s.q_len) - 1;
+    int i_last = min((qt + 1) * p.item_tokens, s.q_len) - 1;
     int n = key_extent(p.causal, i_last, s);
     int c = (n + BN - 1) / BN;
     return c;
@@ -54,7 +55,7 @@ sched_kernel(AttnParams p, int decode) {
         }
         if (!ok) { atomicOr(&bad, 1); continue; }
         if (decode) continue;
-        const int nqt = (s.q_len + p.tq - 1) / p.tq;
+        const int nqt = (s.q_len + p.item_tokens - 1) / p.item_tokens;
         for (int qt = 0; qt < nqt; ++qt) {
             int c = min(item_cost(p, s, qt), COST_BUCKETS - 1);
             atomicAdd(&hist[c], p.Hkv);
@@ -79,23 +80,43 @@ sched_kernel(AttnParams p, int decode) {
         return;
     }
 
-    // 2. bucket starts, largest cost first (exclusive scan, serial: 1024 buckets)
-    if (tid == 0) {
-        int run = 0;
-        for (int c = COST_BUCKETS - 1; c >= 0; --c) {
-            int h = hist[c];
-            hist[c] = run;
-            run += h;
+    // 2. bucket starts, largest cost first: exclusive block scan, thread t
+    //    owning bucket COST_BUCKETS-1-t
+    {
+        __shared__ int warp_sum[SCHED_THREADS / 32];
+        const int c = COST_BUCKETS - 1 - tid, lane = tid & 31, w = tid >> 5;
+        const int h = hist[c];
+        int x = h;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
         }
-        hdr[0] = run;
-        hdr[1] = 0;
+        if (lane == 31) warp_sum[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int s = warp_sum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += y;
+            }
+            warp_sum[lane] = s;   // inclusive prefix over warps
+        }
+        __syncthreads();
+        const int before = (w > 0 ? warp_sum[w - 1] : 0) + x - h;
+        hist[c] = before;
+        if (tid == SCHED_THREADS - 1) {
+            hdr[0] = before + h;
+            hdr[1] = 0;
+        }
     }
     __syncthreads();
 
     // 3. scatter items into their sorted positions
     for (int b = tid; b < p.B; b += SCHED_THREADS) {
         SeqInfo s = seq_info(p, b);
-        const int nqt = (s.q_len + p.tq - 1) / p.tq;
+        const int nqt = (s.q_len + p.item_tokens - 1) / p.item_tokens;
         for (int qt = nqt - 1; qt >= 0; --qt) {
             int cost = item_cost(p, s, qt);
             int c = min(cost, COST_BUCKETS - 1);

@@ -118,7 +118,7 @@ def test_quantized(quant, norm, dtype):
 
     c = W.make_case("quant", 11, batch=B, q_heads=4, kv_heads=4, head_dim=128,
                     q_lens=[N, N], dtype=dtype, causal="upper_left", mask=suffix,
-                    quant=quant, norm=norm, scale=(0.02 if norm == "none" else None),
+                    quant=quant, norm=norm, scale=(0.005 if norm == "none" else None),
                     pass_kv_lengths=False)
     _parity(c)
 
