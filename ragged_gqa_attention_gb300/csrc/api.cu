@@ -232,6 +232,14 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
 
 }  // namespace
 
+namespace rga {
+cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode, int grid,
+                           cudaStream_t s, int bf16) {
+    return bf16 ? launch_prefill_typed<true>(p, m, mode, grid, s)
+                : launch_prefill_typed<false>(p, m, mode, grid, s);
+}
+}  // namespace rga
+
 extern "C" {
 
 size_t rga_attention_workspace_size(const rga_attention_args *args) {

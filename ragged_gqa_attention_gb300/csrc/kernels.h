@@ -79,11 +79,8 @@ cudaError_t launch_sched(const AttnParams &p, int decode, cudaStream_t s);
 template <bool BF16>
 cudaError_t launch_prefill_typed(const AttnParams &p, const TensorMaps &m, int mode, int grid,
                                  cudaStream_t s);
-inline cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode, int grid,
-                                  cudaStream_t s, int bf16) {
-    return bf16 ? launch_prefill_typed<true>(p, m, mode, grid, s)
-                : launch_prefill_typed<false>(p, m, mode, grid, s);
-}
+cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode, int grid,
+                           cudaStream_t s, int bf16);
 cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode,
                           cudaStream_t s, int bf16);
 

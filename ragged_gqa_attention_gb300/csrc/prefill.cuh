@@ -17,11 +17,12 @@
 // for padded Q ([B,H,N,D]).  A work item holds two such tiles (2*TQ tokens)
 // that share every K/V tile.
 //
-// Roles (320 threads):
+// Roles (384 threads, three warpgroups):
 //   warps 0-3  softmax warpgroup of tile 0 (thread = TMEM lane = row)
 //   warps 4-7  softmax warpgroup of tile 1
 //   warp 8     TMEM owner and single-thread MMA issuer
 //   warp 9     TMA producer (Q once per item, K and V rings)
+//   warps 10-11 idle (they only give up their registers)
 // Tensor-core order per key tile j:  S0(j+1) after O0 += P0(j) V(j), and
 // S1(j+1) after O1 += P1(j) V(j), so while one warpgroup turns its scores
 // into probabilities the tensor core works for the other one.
@@ -40,7 +41,18 @@
 
 namespace rga {
 
-constexpr int PF_THREADS = 320;
+constexpr int PF_THREADS = 384;
+// Register split: the CTA is launched with PF_LAUNCH_REGS registers per
+// thread (the most 384 threads can have); the MMA/TMA warpgroup then drops
+// to PF_AUX_REGS and each softmax warpgroup rises to PF_SOFTMAX_REGS.
+// 2 * 128 * PF_SOFTMAX_REGS + 128 * PF_AUX_REGS must not exceed
+// 384 * PF_LAUNCH_REGS, or the increase would wait forever; the host checks
+// the kernel's register count before it launches.
+constexpr int PF_LAUNCH_REGS = 168;
+constexpr int PF_SOFTMAX_REGS = 200;
+constexpr int PF_AUX_REGS = 104;
+static_assert(2 * 128 * PF_SOFTMAX_REGS + 128 * PF_AUX_REGS <= PF_THREADS * PF_LAUNCH_REGS,
+              "register split exceeds the launch allocation");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
@@ -174,7 +186,7 @@ __device__ __forceinline__ void tma_kv(const AttnParams &p, const CUtensorMap *m
 
 // ------------------------------------------------------------------ producer
 template <int D, int MODE>
-__device__ void producer_role(const AttnParams &p, const TensorMaps &tm, uint8_t *sm,
+__device__ __forceinline__ void producer_role(const AttnParams &p, const TensorMaps &tm, uint8_t *sm,
                               const PfBars &bar, volatile int *abort, int n_items) {
     using L = PfLayout<D>;
     const int lane = threadIdx.x & 31;
@@ -235,7 +247,7 @@ __device__ void producer_role(const AttnParams &p, const TensorMaps &tm, uint8_t
 // One thread issues every tcgen05.mma, in the order
 //   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
 template <int D, int MODE, bool BF16>
-__device__ void mma_role(const AttnParams &p, uint8_t *sm, const PfBars &bar,
+__device__ __forceinline__ void mma_role(const AttnParams &p, uint8_t *sm, const PfBars &bar,
                          volatile int *abort, int n_items, uint32_t tmem) {
     using L = PfLayout<D>;
     constexpr uint32_t ID_S = idesc_f16(BF16 ? 1 : 0, 128, BN, 0, 0);   // Q K-major, K K-major
@@ -490,7 +502,7 @@ __device__ __forceinline__ void store_row(const AttnParams &p, const Item &m, in
 }
 
 template <int D, int MODE, bool BF16>
-__device__ void softmax_role(const AttnParams &p, const PfBars &bar, volatile int *abort,
+__device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &bar, volatile int *abort,
                              int n_items, uint32_t tmem, int a) {
     constexpr bool SOFTMAX = (MODE == MODE_SOFTMAX || MODE == MODE_SOFTMAX_Q);
     constexpr bool QUANT = (MODE == MODE_SOFTMAX_Q || MODE == MODE_NONE_Q);
@@ -540,24 +552,41 @@ __device__ void softmax_role(const AttnParams &p, const PfBars &bar, volatile in
             uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
             if (bool_mask && !full) mask_bits(p, row_indep, mrow, j0, m.s.kv_len, row_ok, bits);
 
-            // pass A: row max of the scaled, masked scores
+            // this thread's score row: one TMEM round trip for a full tile;
+            // a partial tile is loaded and masked a chunk at a time, which
+            // keeps the mask reads of one chunk from piling up registers
+            float x[BN];
+            if (full) {
+                uint32_t rr[BN / 32][32];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, rr[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) x[c * 32 + k] = __uint_as_float(rr[c][k]);
+            } else {   // scale and mask in place (log2 domain for softmax)
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(s_addr + c * 32, rr);
+                    tmem_wait_ld();
+                    float v[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(rr[k]);
+                    mask_chunk_any<SOFTMAX>(p, mk, v, c, rem, bits, mrow, j0);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) x[c * 32 + k] = v[k];
+                }
+            }
+            const float mul = full ? sc : 1.f;
             float mx = -INFINITY;
             if (MODE == MODE_SOFTMAX || stat) {
+                float cm[BN / 32];
 #pragma unroll
-                for (int c2 = 0; c2 < BN / 32; c2 += 2) {
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32(s_addr + c2 * 32, r0);
-                    tmem_ld32(s_addr + (c2 + 1) * 32, r1);
-                    tmem_wait_ld();
-                    float v0[32], v1[32];
-                    as_float(r0, v0);
-                    as_float(r1, v1);
-                    if (!full) {
-                        mask_chunk_any<SOFTMAX>(p, mk, v0, c2, rem, bits, mrow, j0);
-                        mask_chunk_any<SOFTMAX>(p, mk, v1, c2 + 1, rem, bits, mrow, j0);
-                    }
-                    mx = fmax3(mx, chunk_max(v0), chunk_max(v1));
-                }
+                for (int c = 0; c < BN / 32; ++c)
+                    cm[c] = chunk_max(*reinterpret_cast<float(*)[32]>(&x[c * 32]));
+                mx = fmax3(fmaxf(cm[0], cm[1]), cm[2], cm[3]);
                 if (full) mx *= sc;
                 if (!row_ok) mx = -INFINITY;
             }
@@ -581,56 +610,44 @@ __device__ void softmax_role(const AttnParams &p, const PfBars &bar, volatile in
                 ref = lse2;   // pass 2: p / s_q directly
             }
 
-            // pass B: probabilities (or the row sum, for a statistics step)
-            const float mul = full ? sc : 1.f;
+            // probabilities (or only the row sum, for a statistics step)
             const uint64_t mul2 = f2_pack(mul, mul), neg2 = f2_pack(-ref, -ref);
             uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-            for (int c2 = 0; c2 < BN / 32; c2 += 2) {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(s_addr + c2 * 32, r0);
-                tmem_ld32(s_addr + (c2 + 1) * 32, r1);
-                tmem_wait_ld();
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t w[16];
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int c = c2 + h2;
-                    float v[32];
-                    as_float(h2 ? r1 : r0, v);
-                    if (!full) mask_chunk_any<SOFTMAX>(p, mk, v, c, rem, bits, mrow, j0);
-                    uint32_t w[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        float pa = v[2 * k], pb = v[2 * k + 1];
-                        if (SOFTMAX) {
-                            f2_unpack(ffma2(f2_pack(pa, pb), mul2, neg2), pa, pb);
-                            pa = ex2(pa);
-                            pb = ex2(pb);
-                            if (MODE == MODE_SOFTMAX || stat) {
-                                if (k & 1) acc1 = fadd2(acc1, f2_pack(pa, pb));
-                                else acc0 = fadd2(acc0, f2_pack(pa, pb));
-                            }
-                        } else {
-                            pa = (pa == -INFINITY) ? 0.f : pa * mul;
-                            pb = (pb == -INFINITY) ? 0.f : pb * mul;
-                            if (MODE == MODE_NONE_Q) {
-                                pa *= inv_qs;
-                                pb *= inv_qs;
-                            }
+                for (int k = 0; k < 16; ++k) {
+                    float pa = x[c * 32 + 2 * k], pb = x[c * 32 + 2 * k + 1];
+                    if (SOFTMAX) {
+                        f2_unpack(ffma2(f2_pack(pa, pb), mul2, neg2), pa, pb);
+                        pa = ex2(pa);
+                        pb = ex2(pb);
+                        if (MODE == MODE_SOFTMAX || stat) {
+                            if (k & 1) acc1 = fadd2(acc1, f2_pack(pa, pb));
+                            else acc0 = fadd2(acc0, f2_pack(pa, pb));
                         }
-                        if (QUANT && !stat) {
-                            if (p.quant == 0) {
-                                const float2 e = e4m3_round2(pa, pb);
-                                pa = e.x;
-                                pb = e.y;
-                            } else {
-                                pa = int8_round(pa);
-                                pb = int8_round(pb);
-                            }
+                    } else {
+                        pa = (pa == -INFINITY) ? 0.f : pa * mul;
+                        pb = (pb == -INFINITY) ? 0.f : pb * mul;
+                        if (MODE == MODE_NONE_Q) {
+                            pa *= inv_qs;
+                            pb *= inv_qs;
                         }
-                        w[k] = pack2<BF16>(pa, pb);
                     }
-                    if (!stat) tmem_st16(s_addr + c * 16, w);
+                    if (QUANT && !stat) {
+                        if (p.quant == 0) {
+                            const float2 e = e4m3_round2(pa, pb);
+                            pa = e.x;
+                            pb = e.y;
+                        } else {
+                            pa = int8_round(pa);
+                            pb = int8_round(pb);
+                        }
+                    }
+                    w[k] = pack2<BF16>(pa, pb);
                 }
+                if (!stat) tmem_st16(s_addr + c * 16, w);
             }
             float s0, s1, s2, s3;
             f2_unpack(acc0, s0, s1);
@@ -730,11 +747,16 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     const uint32_t tmem = *tmem_slot;
 
     if (warp < 8) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(PF_SOFTMAX_REGS));
         softmax_role<D, MODE, BF16>(p, bar, abort, n_items, tmem, warp >> 2);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(PF_AUX_REGS));
+    }
+    if (warp < 8) {
     } else if (warp == 8) {
         if (lane == 0) mma_role<D, MODE, BF16>(p, sm, bar, abort, n_items, tmem);
         __syncwarp();
-    } else {
+    } else if (warp == 9) {
         producer_role<D, MODE>(p, tm, sm, bar, abort, n_items);
     }
 
@@ -751,9 +773,13 @@ static cudaError_t launch_one(const AttnParams &p, const TensorMaps &m, int grid
     using L = PfLayout<D>;
     static bool attr_set = false;   // per process; the attribute is per function
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, MODE, BF16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             L::ALLOC);
+        // the register split needs exactly the launch allocation it was sized for
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MODE, BF16>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != PF_LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(prefill_kernel<D, MODE, BF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
