@@ -5,7 +5,7 @@
 #include <cmath>
 #include <cstring>
 #include <cudaTypedefs.h>
-#include "../../include/rga.h"
+#include "rga.h"
 #include "kernels.h"
 
 using namespace rga;

@@ -60,7 +60,7 @@ constexpr float LOG2E = 1.4426950408889634f;
 
 template <int D>
 struct PfLayout {
-    static constexpr int KST = 3;                        // K ring stages
+    static constexpr int KST = D == 128 ? 2 : 3;         // K ring stages
     static constexpr int VST = D == 128 ? 2 : 3;         // V ring stages
     static constexpr int BLK = 128 * 128;                // one 64-column block of 128 rows
     static constexpr int NBLK = D / 64;
@@ -68,10 +68,13 @@ struct PfLayout {
     static constexpr int Q_OFF = 0;                      // two Q tiles
     static constexpr int K_OFF = Q_OFF + 2 * TILE;
     static constexpr int V_OFF = K_OFF + KST * TILE;
-    static constexpr int BAR_OFF = V_OFF + VST * TILE;
+    // epilogue staging: 32 rows x 128 bytes per softmax warp (8 warps)
+    static constexpr int STG_OFF = V_OFF + VST * TILE;
+    static constexpr int STG_WARP = 32 * 128;
+    static constexpr int BAR_OFF = STG_OFF + 8 * STG_WARP;
     // barriers: q_full, q_empty, k_full[KST], k_empty[KST], v_full[VST],
-    // v_empty[VST], s_full[2], p_full[2], o_done[2]
-    static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 6;
+    // v_empty[VST], s_full[2], p_full[2], o_done[2], v_part
+    static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 7;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int BYTES = MISC_OFF + 64;
     // room to align the base to 1024; at least 120 KB so that only one CTA
@@ -82,7 +85,7 @@ struct PfLayout {
 
 struct PfBars {
     uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full,
-        *o_done;
+        *o_done, *v_part;
 };
 
 template <int D>
@@ -99,6 +102,7 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *base) {
     r.s_full = r.v_empty + L::VST;
     r.p_full = r.s_full + 2;
     r.o_done = r.p_full + 2;
+    r.v_part = r.o_done + 2;
     return r;
 }
 
@@ -140,27 +144,21 @@ __device__ __forceinline__ int key_tile(const Item &m, int t) {
 }
 
 // ------------------------------------------------------------------ loads
-// Load a partial V tile (keys j0 .. j0+127 with only `rem` < 128 valid) with
-// plain loads, zero the rows past the sequence end (they may hold NaN), and
-// publish it to the tensor core through the async proxy.
+// After a V tile whose keys run past the sequence end (only `rem` < 128 rows
+// valid) has landed, zero the rows from `rem` on (they may hold NaN, and
+// 0 * NaN would reach O) and publish the change to the tensor core through
+// the async proxy.  The 128-byte swizzle only permutes 16-byte chunks within
+// a row, so whole rows are cleared in place.
 template <int D>
-__device__ void load_v_partial(const AttnParams &p, const Item &m, int j0, int rem,
-                               uint8_t *dst, int lane) {
-    constexpr int CH = D / 8;   // 16-byte chunks per row
-    const uint16_t *v = static_cast<const uint16_t *>(p.v);
-    for (int idx = lane; idx < 128 * CH; idx += 32) {
-        const int r = idx / CH, c = idx % CH;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < rem) {
-            const long long j = (long long)j0 + r;
-            const long long off = p.kv_packed
-                ? ((m.s.kv_off + j) * p.Hkv + m.g) * (long long)D
-                : (((long long)m.b * p.Hkv + m.g) * p.kv_seq + j) * (long long)D;
-            val = *reinterpret_cast<const uint4 *>(v + off + c * 8);
-        }
-        const int blk = c / 8, cc = c % 8;
-        uint8_t *row = dst + blk * PfLayout<D>::BLK + r * 128;
-        *reinterpret_cast<uint4 *>(row + ((cc ^ (r & 7)) * 16)) = val;
+__device__ void zero_v_rows(uint8_t *tile, int rem, int lane) {
+    constexpr int NBLK = D / 64;
+    const int first = rem < 0 ? 0 : rem;
+    const int nchunks = (128 - first) * 8 * NBLK;   // 16-byte chunks to clear
+    for (int idx = lane; idx < nchunks; idx += 32) {
+        const int blk = idx % NBLK, rest = idx / NBLK;
+        const int r = first + rest / 8, cc = rest % 8;
+        *reinterpret_cast<uint4 *>(tile + blk * PfLayout<D>::BLK + r * 128 + cc * 16) =
+            make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -192,7 +190,7 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
     const int lane = threadIdx.x & 31;
     const uint32_t q_bytes = (uint32_t)(2 * L::NBLK * p.G * p.tq * 128);
     const uint32_t kv_bytes = (uint32_t)L::TILE;
-    uint32_t kc = 0, vc = 0, qc = 0;   // running ring counters
+    uint32_t kc = 0, vc = 0, qc = 0, vpc = 0;   // running ring / barrier counters
     for (int idx = blockIdx.x; idx < n_items && !*abort; idx += gridDim.x) {
         const Item m = load_item<MODE>(p, idx);
         if (m.nkt == 0) continue;
@@ -229,7 +227,17 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
                         tma_kv(p, &tm.v, m, j0, vdst + blk * L::BLK, &bar.v_full[vs], blk * 64);
                 }
             } else {
-                load_v_partial<D>(p, m, j0, rem, vdst, lane);
+                // the tile runs past the sequence end: land it, clear the
+                // rows past the end, then publish it
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar.v_part, kv_bytes);
+                    for (int blk = 0; blk < L::NBLK; ++blk)
+                        tma_kv(p, &tm.v, m, j0, vdst + blk * L::BLK, bar.v_part, blk * 64);
+                }
+                const bool landed = mbar_wait(bar.v_part, vpc & 1, abort);
+                ++vpc;
+                if (!landed) break;
+                zero_v_rows<D>(vdst, rem, lane);
                 if (lane == 0) mbar_arrive(&bar.v_full[vs]);
             }
             ++vc;
@@ -241,6 +249,7 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
     for (uint32_t c = vc > L::VST ? vc - L::VST : 0; c < vc; ++c)
         mbar_wait_drain(&bar.v_full[c % L::VST], (c / L::VST) & 1);
     if (qc > 0) mbar_wait_drain(bar.q_full, (qc - 1) & 1);
+    if (vpc > 0) mbar_wait_drain(bar.v_part, (vpc - 1) & 1);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -470,40 +479,101 @@ __device__ __forceinline__ void mask_bits(const AttnParams &p, bool row_indep, l
     }
 }
 
+// Output row geometry of row r of query tile a (the same mapping as the Q
+// tile): element offset of Y[token, head, 0] and whether it is written.
+struct RowOut {
+    long long off;
+    bool ok;
+};
+__device__ __forceinline__ RowOut row_out(const AttnParams &p, const Item &m, int a, int r) {
+    const int t = p.q_packed ? r / p.G : r % p.tq;
+    const int hh = p.q_packed ? r % p.G : r / p.tq;
+    const int tok = a * p.tq + t;
+    const int i = m.i0 + tok;
+    const int h = m.g * p.G + hh;
+    RowOut o;
+    o.ok = r < p.G * p.tq && tok < m.ntok;
+    o.off = p.q_packed ? ((long long)(m.s.q_off + i) * p.Hq + h) * p.D
+                       : (((long long)m.b * p.Hq + h) * p.q_seq + i) * p.D;
+    return o;
+}
+
+// Epilogue of one row per thread: O (TMEM, fp32) * f -> 16-bit -> Y.  Each
+// warp transposes its 32 rows through 4 KB of shared memory, 64 columns at a
+// time, so that every store instruction writes four whole 128-byte lines.
+// zero: write zeros (the item has no attendable key).
 template <int D, bool BF16>
-__device__ __forceinline__ void store_row(const AttnParams &p, const Item &m, int i, int h,
-                                          uint32_t o_taddr, float f, bool zero, bool write) {
-    // every lane takes part in the (warp-collective) TMEM loads; only rows
-    // that belong to the sequence are written
+__device__ __forceinline__ void store_rows(const AttnParams &p, const Item &m, int a,
+                                           uint32_t o_taddr, float f, bool zero, uint8_t *stg) {
+    const int lane = threadIdx.x & 31;
+    const int r = threadIdx.x & 127;                  // this thread's row
+    const int wr0 = r & ~31;                          // first row of this warp
     uint16_t *y = static_cast<uint16_t *>(p.y);
-    const long long off = p.q_packed
-        ? ((long long)(m.s.q_off + i) * p.Hq + h) * D
-        : (((long long)m.b * p.Hq + h) * p.q_seq + i) * D;
-    uint4 *dst = reinterpret_cast<uint4 *>(y + off);
+    uint32_t v[D / 32][32];
+    if (!zero) {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        if (!zero) {
-            tmem_ld32(o_taddr + c * 32, r);
-            tmem_wait_ld();
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-            w[k] = zero ? 0u
-                        : pack2<BF16>(__uint_as_float(r[2 * k]) * f,
-                                      __uint_as_float(r[2 * k + 1]) * f);
-        if (write) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                dst[c * 4 + k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-        }
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(o_taddr + c * 32, v[c]);
+        tmem_wait_ld();
     }
+#pragma unroll
+    for (int half = 0; half < D / 64; ++half) {
+        // this thread's row, columns [64*half, 64*half+64), as 8 x 16 bytes
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = q * 8 + 2 * e;        // within the half
+                const int c = (half * 64 + col) / 32, k = (half * 64 + col) % 32;
+                w[e] = zero ? 0u : pack2<BF16>(__uint_as_float(v[c][k]) * f,
+                                               __uint_as_float(v[c][k + 1]) * f);
+            }
+            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((q ^ (lane & 7)) * 16)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        __syncwarp();
+        // four rows per instruction: lanes 8j..8j+7 write row 4k+j
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int lr = 4 * k + (lane >> 3), q = lane & 7;
+            const RowOut o = row_out(p, m, a, wr0 + lr);
+            const uint4 val = *reinterpret_cast<const uint4 *>(stg + lr * 128 + ((q ^ (lr & 7)) * 16));
+            if (o.ok)
+                *reinterpret_cast<uint4 *>(y + o.off + half * 64 + q * 8) = val;
+        }
+        __syncwarp();
+    }
+}
+
+// One 32-column chunk of a full tile: p = 2^(s * mul - ref) packed to 16-bit
+// pairs into TMEM columns [16c, 16c+16) of the S buffer; returns the raw
+// chunk max and accumulates the sum of p.
+template <bool BF16>
+__device__ __forceinline__ float p_chunk(const uint32_t (&r)[32], uint32_t s_addr, int c,
+                                         uint64_t mul2, uint64_t neg2, uint64_t &acc0,
+                                         uint64_t &acc1) {
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+    const float mx = chunk_max(v);
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        float pa, pb;
+        f2_unpack(ffma2(f2_pack(v[2 * k], v[2 * k + 1]), mul2, neg2), pa, pb);
+        pa = ex2(pa);
+        pb = ex2(pb);
+        if (k & 1) acc1 = fadd2(acc1, f2_pack(pa, pb));
+        else acc0 = fadd2(acc0, f2_pack(pa, pb));
+        w[k] = pack2<BF16>(pa, pb);
+    }
+    tmem_st16(s_addr + c * 16, w);
+    return mx;
 }
 
 template <int D, int MODE, bool BF16>
 __device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &bar, volatile int *abort,
-                             int n_items, uint32_t tmem, int a) {
+                             int n_items, uint32_t tmem, int a, uint8_t *stg) {
     constexpr bool SOFTMAX = (MODE == MODE_SOFTMAX || MODE == MODE_SOFTMAX_Q);
     constexpr bool QUANT = (MODE == MODE_SOFTMAX_Q || MODE == MODE_NONE_Q);
     const int r = threadIdx.x & 127;                 // row = TMEM lane
@@ -532,7 +602,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &
         const int h = m.g * G + hh;
         const bool row_ok = in_tile && tok < m.ntok;
         if (m.nkt == 0) {                            // no attendable key: the rows are zero
-            store_row<D, BF16>(p, m, i, h, 0, 0.f, true, row_ok);
+            store_rows<D, BF16>(p, m, a, 0, 0.f, true, stg);
             continue;
         }
         const int lim = row_ok ? min(causal_limit(p.causal, i, m.s), m.s.kv_len - 1) : -1;
@@ -552,11 +622,78 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &
             uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
             if (bool_mask && !full) mask_bits(p, row_indep, mrow, j0, m.s.kv_len, row_ok, bits);
 
+            // Softmax, full tile, every row of the warp past its first key:
+            // start the exps against the running reference while the second
+            // half of the row is still loading; redo the step only when some
+            // row's max grows past the reference by more than the threshold.
+            if (MODE == MODE_SOFTMAX && full &&
+                __all_sync(0xffffffffu, !row_ok || m_ref != -INFINITY)) {
+                const float ref0 = row_ok ? m_ref : 0.f;
+                const uint64_t mul2 = f2_pack(sc, sc);
+                uint64_t neg2 = f2_pack(-ref0, -ref0);
+                uint32_t ra[2][32], rb[2][32];
+                tmem_ld32(s_addr, ra[0]);
+                tmem_ld32(s_addr + 32, ra[1]);
+                tmem_wait_ld();
+                tmem_ld32(s_addr + 64, rb[0]);
+                tmem_ld32(s_addr + 96, rb[1]);
+                uint64_t acc0 = 0, acc1 = 0;
+                float mraw = p_chunk<BF16>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
+                mraw = fmaxf(mraw, p_chunk<BF16>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1));
+                tmem_wait_ld();
+                mraw = fmaxf(mraw, p_chunk<BF16>(rb[0], s_addr, 2, mul2, neg2, acc0, acc1));
+                mraw = fmaxf(mraw, p_chunk<BF16>(rb[1], s_addr, 3, mul2, neg2, acc0, acc1));
+                const float mx = row_ok ? mraw * sc : -INFINITY;
+                float alpha = 1.f;
+                const bool need = mx > m_ref + RESCALE_THRESHOLD;
+                if (__any_sync(0xffffffffu, need)) {   // rare: redo with the new reference
+                    if (need) {
+                        alpha = ex2(m_ref - mx);
+                        l *= alpha;
+                        m_ref = mx;
+                    }
+                    const float ref1 = row_ok ? m_ref : 0.f;
+                    neg2 = f2_pack(-ref1, -ref1);
+                    acc0 = acc1 = 0;
+                    p_chunk<BF16>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
+                    p_chunk<BF16>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1);
+                    p_chunk<BF16>(rb[0], s_addr, 2, mul2, neg2, acc0, acc1);
+                    p_chunk<BF16>(rb[1], s_addr, 3, mul2, neg2, acc0, acc1);
+                }
+                float s0, s1, s2, s3;
+                f2_unpack(acc0, s0, s1);
+                f2_unpack(acc1, s2, s3);
+                l += (s0 + s1) + (s2 + s3);
+                if (u > 0) {   // BMM2 of the previous step must be done before O is touched
+                    if (!mbar_wait(&bar.o_done[a], pvw & 1, abort)) { ok = false; break; }
+                    ++pvw;
+                    if (__any_sync(0xffffffffu, need)) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(o_addr + c * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                            tmem_st32(o_addr + c * 32, o);
+                        }
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bar.p_full[a]);
+                ++u;
+                ++tc;
+                continue;
+            }
+
             // this thread's score row: one TMEM round trip for a full tile;
             // a partial tile is loaded and masked a chunk at a time, which
             // keeps the mask reads of one chunk from piling up registers
             float x[BN];
-            if (full) {
+            if (full || mk == MK_BITS) {
                 uint32_t rr[BN / 32][32];
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, rr[c]);
@@ -565,7 +702,12 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &
                 for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
                     for (int k = 0; k < 32; ++k) x[c * 32 + k] = __uint_as_float(rr[c][k]);
-            } else {   // scale and mask in place (log2 domain for softmax)
+                if (!full)   // causal / length / bool-mask bits: no memory reads
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+                        mask_chunk<SOFTMAX, MK_BITS>(p, *reinterpret_cast<float(*)[32]>(&x[c * 32]),
+                                                     c, rem, bits, mrow, j0);
+            } else {   // additive mask: scale and mask a chunk at a time
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t rr[32];
@@ -700,7 +842,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &
         float f;
         if (MODE == MODE_SOFTMAX) f = (l > 0.f) ? 1.f / l : 0.f;
         else f = qs;    // 'none': 1; quantized: the Q/DQ scale
-        store_row<D, BF16>(p, m, i, h, o_addr, f, false, row_ok);
+        store_rows<D, BF16>(p, m, a, o_addr, f, false, stg);
         tc_fence_before();
     }
 }
@@ -729,6 +871,7 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
             mbar_init(&bar.p_full[s], 128);
             mbar_init(&bar.o_done[s], 1);
         }
+        mbar_init(bar.v_part, 1);
         *abort = 0;
         fence_mbar_init();
     }
@@ -748,7 +891,8 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
 
     if (warp < 8) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(PF_SOFTMAX_REGS));
-        softmax_role<D, MODE, BF16>(p, bar, abort, n_items, tmem, warp >> 2);
+        softmax_role<D, MODE, BF16>(p, bar, abort, n_items, tmem, warp >> 2,
+                                    sm + L::STG_OFF + warp * L::STG_WARP);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(PF_AUX_REGS));
     }

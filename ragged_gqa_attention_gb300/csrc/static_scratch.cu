@@ -13,7 +13,7 @@
 // address is looked up with cudaGetSymbolAddress once per device, with that
 // device current, on the first call made on it.
 #include <mutex>
-#include "../../include/rga.h"
+#include "rga.h"
 
 namespace {
 
