@@ -55,15 +55,16 @@ bool encode(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_q(CUtensorMap *m, const AttnParams &p) {
+// Q (and Y, same shape): one query tile is G heads x TQ tokens per box.
+bool encode_q(CUtensorMap *m, const void *base, const AttnParams &p) {
     if (p.q_packed) {
         const uint64_t d[3] = {(uint64_t)p.D, (uint64_t)p.Hq, (uint64_t)p.q_seq};
         const uint32_t b[3] = {64, (uint32_t)p.G, (uint32_t)p.tq};
-        return encode(m, p.q, 3, d, b);
+        return encode(m, base, 3, d, b);
     }
     const uint64_t d[4] = {(uint64_t)p.D, (uint64_t)p.q_seq, (uint64_t)p.Hq, (uint64_t)p.B};
     const uint32_t b[4] = {64, (uint32_t)p.tq, (uint32_t)p.G, 1};
-    return encode(m, p.q, 4, d, b);
+    return encode(m, base, 4, d, b);
 }
 
 bool encode_kv(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t rows) {
@@ -209,7 +210,8 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
     const bool dec = use_decode(a, quant);
     TensorMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    if (!encode_q(&maps.q, p) || !encode_kv(&maps.k, kp, p, dec ? DEC_KEYS : BN) ||
+    if (!encode_q(&maps.q, p.q, p) || !encode_q(&maps.y, p.y, p) ||
+        !encode_kv(&maps.k, kp, p, dec ? DEC_KEYS : BN) ||
         !encode_kv(&maps.v, vp, p, dec ? DEC_KEYS : BN))
         return RGA_ERR_CUDA;
     int mode;

@@ -71,7 +71,7 @@ __host__ __device__ inline size_t dec_ws_bytes(const AttnParams &p) {
 }
 
 struct TensorMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, y;   // y: same geometry and box as q
 };
 
 // Launchers (return cudaError_t of the launch).

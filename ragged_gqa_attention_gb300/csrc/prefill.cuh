@@ -498,17 +498,26 @@ __device__ __forceinline__ RowOut row_out(const AttnParams &p, const Item &m, in
     return o;
 }
 
-// Epilogue of one row per thread: O (TMEM, fp32) * f -> 16-bit -> Y.  Each
-// warp transposes its 32 rows through 4 KB of shared memory, 64 columns at a
-// time, so that every store instruction writes four whole 128-byte lines.
+// Epilogue of one row per thread: O (TMEM, fp32) * f -> 16-bit -> Y, 64
+// columns at a time through the warpgroup's 16 KB staging area (row r at
+// r * 128 bytes, 16-byte chunks swizzled as TMA's 128-byte swizzle does, so
+// the four warps' buffers form one TMA box of the tile).
+//  - tile entirely inside the sequence: one thread stores the box with TMA,
+//    asynchronously; the staging is reused only after the store has read it
+//    (`pending` carries that over to the next epilogue);
+//  - tile running past the end of the sequence: each warp writes its own 32
+//    rows, four whole 128-byte lines per instruction, skipping rows outside.
 // zero: write zeros (the item has no attendable key).
 template <int D, bool BF16>
-__device__ __forceinline__ void store_rows(const AttnParams &p, const Item &m, int a,
-                                           uint32_t o_taddr, float f, bool zero, uint8_t *stg) {
+__device__ __forceinline__ void store_rows(const AttnParams &p, const TensorMaps &tm,
+                                           const Item &m, int a, uint32_t o_taddr, float f,
+                                           bool zero, uint8_t *stg_wg, bool &pending) {
     const int lane = threadIdx.x & 31;
     const int r = threadIdx.x & 127;                  // this thread's row
     const int wr0 = r & ~31;                          // first row of this warp
+    const bool whole = (a + 1) * p.tq <= m.ntok;
     uint16_t *y = static_cast<uint16_t *>(p.y);
+    uint8_t *stg = stg_wg + wr0 * 128;                // this warp's 32 rows
     uint32_t v[D / 32][32];
     if (!zero) {
 #pragma unroll
@@ -517,31 +526,48 @@ __device__ __forceinline__ void store_rows(const AttnParams &p, const Item &m, i
     }
 #pragma unroll
     for (int half = 0; half < D / 64; ++half) {
-        // this thread's row, columns [64*half, 64*half+64), as 8 x 16 bytes
+        if (pending) {   // the previous TMA store must have read the staging
+            if (r == 0) bulk_wait_read();
+            named_sync(1 + a, 128);
+            pending = false;
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int col = q * 8 + 2 * e;        // within the half
-                const int c = (half * 64 + col) / 32, k = (half * 64 + col) % 32;
-                w[e] = zero ? 0u : pack2<BF16>(__uint_as_float(v[c][k]) * f,
-                                               __uint_as_float(v[c][k + 1]) * f);
+                const int col = half * 64 + q * 8 + 2 * e;
+                w[e] = zero ? 0u : pack2<BF16>(__uint_as_float(v[col / 32][col % 32]) * f,
+                                               __uint_as_float(v[col / 32][col % 32 + 1]) * f);
             }
             *reinterpret_cast<uint4 *>(stg + lane * 128 + ((q ^ (lane & 7)) * 16)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
         }
-        __syncwarp();
-        // four rows per instruction: lanes 8j..8j+7 write row 4k+j
+        if (whole) {
+            fence_proxy_async_smem();
+            named_sync(1 + a, 128);
+            if (r == 0) {
+                const int tok = m.i0 + a * p.tq;
+                if (p.q_packed)
+                    tma_store_3d(&tm.y, stg_wg, half * 64, m.g * p.G, m.s.q_off + tok);
+                else
+                    tma_store_4d(&tm.y, stg_wg, half * 64, tok, m.g * p.G, m.b);
+                bulk_commit();
+            }
+            pending = true;
+        } else {
+            __syncwarp();
+            // four rows per instruction: lanes 8j..8j+7 write row 4k+j
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int lr = 4 * k + (lane >> 3), q = lane & 7;
-            const RowOut o = row_out(p, m, a, wr0 + lr);
-            const uint4 val = *reinterpret_cast<const uint4 *>(stg + lr * 128 + ((q ^ (lr & 7)) * 16));
-            if (o.ok)
-                *reinterpret_cast<uint4 *>(y + o.off + half * 64 + q * 8) = val;
+            for (int k = 0; k < 8; ++k) {
+                const int lr = 4 * k + (lane >> 3), q = lane & 7;
+                const RowOut o = row_out(p, m, a, wr0 + lr);
+                const uint4 val =
+                    *reinterpret_cast<const uint4 *>(stg + lr * 128 + ((q ^ (lr & 7)) * 16));
+                if (o.ok) *reinterpret_cast<uint4 *>(y + o.off + half * 64 + q * 8) = val;
+            }
+            __syncwarp();
         }
-        __syncwarp();
     }
 }
 
@@ -572,8 +598,9 @@ __device__ __forceinline__ float p_chunk(const uint32_t (&r)[32], uint32_t s_add
 }
 
 template <int D, int MODE, bool BF16>
-__device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &bar, volatile int *abort,
-                             int n_items, uint32_t tmem, int a, uint8_t *stg) {
+__device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMaps &tm,
+                                             const PfBars &bar, volatile int *abort,
+                                             int n_items, uint32_t tmem, int a, uint8_t *stg) {
     constexpr bool SOFTMAX = (MODE == MODE_SOFTMAX || MODE == MODE_SOFTMAX_Q);
     constexpr bool QUANT = (MODE == MODE_SOFTMAX_Q || MODE == MODE_NONE_Q);
     const int r = threadIdx.x & 127;                 // row = TMEM lane
@@ -593,7 +620,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &
     const int mk = !use_mask || bool_mask ? MK_BITS
                    : p.mask_dtype == 0 ? MK_ADD_F16 : p.mask_dtype == 1 ? MK_ADD_BF16 : MK_ADD_F32;
     uint32_t tc = 0, pvw = 0;                        // steps seen, BMM2 completions waited
-    bool ok = true;
+    bool ok = true, pending = false;
 
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
         const Item m = load_item<MODE>(p, idx);
@@ -602,7 +629,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &
         const int h = m.g * G + hh;
         const bool row_ok = in_tile && tok < m.ntok;
         if (m.nkt == 0) {                            // no attendable key: the rows are zero
-            store_rows<D, BF16>(p, m, a, 0, 0.f, true, stg);
+            store_rows<D, BF16>(p, tm, m, a, 0, 0.f, true, stg, pending);
             continue;
         }
         const int lim = row_ok ? min(causal_limit(p.causal, i, m.s), m.s.kv_len - 1) : -1;
@@ -842,9 +869,10 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const PfBars &
         float f;
         if (MODE == MODE_SOFTMAX) f = (l > 0.f) ? 1.f / l : 0.f;
         else f = qs;    // 'none': 1; quantized: the Q/DQ scale
-        store_rows<D, BF16>(p, m, a, o_addr, f, false, stg);
+        store_rows<D, BF16>(p, tm, m, a, o_addr, f, false, stg, pending);
         tc_fence_before();
     }
+    if (r == 0) bulk_wait_all();   // the last TMA stores complete before the CTA exits
 }
 
 // ------------------------------------------------------------------ kernel
@@ -891,8 +919,8 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
 
     if (warp < 8) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(PF_SOFTMAX_REGS));
-        softmax_role<D, MODE, BF16>(p, bar, abort, n_items, tmem, warp >> 2,
-                                    sm + L::STG_OFF + warp * L::STG_WARP);
+        softmax_role<D, MODE, BF16>(p, tm, bar, abort, n_items, tmem, warp >> 2,
+                                    sm + L::STG_OFF + (warp >> 2) * 4 * L::STG_WARP);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(PF_AUX_REGS));
     }
