@@ -221,6 +221,9 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
     if (launch_sched(p, dec ? 1 : 0, stream) != cudaSuccess) return RGA_ERR_CUDA;
     cudaError_t e;
     if (dec) {
+        const int sms = sm_count();
+        if (sms <= 0) return RGA_ERR_CUDA;
+        p.grid = sms;
         e = launch_decode(p, maps, mode, stream, bf16);
     } else {
         int grid = sm_count();

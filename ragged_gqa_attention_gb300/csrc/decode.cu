@@ -3,18 +3,20 @@
 // vanilla decoding attention) with the TRT_Attention semantics of
 // "TensorRT Custom Operator Schemas".
 //
-// Work unit: (batch b, KV head g, split of DEC_SPLIT keys).  The query rows
-// of the unit are the (token, head) pairs of the G query heads of KV head g,
-// taken 16 at a time (one MMA row block).  Each of the 4 warps streams its
-// share of 32-key K/V tiles with TMA into its own double-buffered,
-// 128-byte-swizzled ring, computes S = Q K^T and O += P V with m16n8k16
-// MMAs (K and V are read once from HBM for all G heads), and keeps an
-// online softmax in fp32 registers.  The warps' partial (m, l, O) are merged
-// in shared memory; splits are merged through the workspace by the last CTA
-// of the (b, g) pair to arrive (atomic ticket).
+// Work unit: (batch b, KV head g, split of DEC_SPLIT keys), listed by the
+// scheduler.  The grid is persistent and every warp is an independent
+// engine: it takes the next unit from an atomic counter, streams the unit's
+// 32-key K/V tiles with TMA through its own DEC_STAGES-deep, 128-byte-
+// swizzled ring, computes S = Q K^T and O += P V with m16n8k16 MMAs (K and
+// V are read once from HBM for all G query heads of the KV head) and keeps
+// an online softmax in fp32 registers.  The query rows of a unit are the
+// (token, head) pairs of the G heads, 16 at a time (one MMA row block).
+// A unit that covers its whole (b, g) pair writes Y; otherwise its partial
+// (O, m, l) goes to the workspace and the last warp to finish a pair
+// (atomic ticket) merges the splits and writes Y.
 //
-// A pair with more than 16 query rows (more than 16/G tokens) is handled by
-// a single split that loops over the row blocks.
+// A pair with more than 16 query rows (more than 16/G tokens) is one unit
+// that loops over the row blocks.
 #include <cuda.h>
 #include "device_common.cuh"
 #include "kernels.h"
@@ -31,13 +33,10 @@ struct DecLayout {
     static constexpr int STAGE = 2 * TILE;               // K + V
     static constexpr int WARP_RING = DEC_STAGES * STAGE;
     static constexpr int RING = DEC_WARPS * WARP_RING;
-    static constexpr int COMB = DEC_WARPS * DEC_ROWS * D * 4;   // fp32 partial O per warp
-    static constexpr int DATA = RING > COMB ? RING : COMB;
-    static constexpr int BAR_OFF = DATA;
-    static constexpr int ML_OFF = BAR_OFF + DEC_WARPS * DEC_STAGES * 8;
-    static constexpr int MISC_OFF = ML_OFF + DEC_WARPS * DEC_ROWS * 8;
-    static constexpr int BYTES = MISC_OFF + 64;
+    static constexpr int BAR_OFF = RING;
+    static constexpr int BYTES = BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 64;
     static constexpr int ALLOC = BYTES + 1024;
+    static_assert(ALLOC <= 232448, "shared memory per CTA");
 };
 
 template <bool BF16>
@@ -113,34 +112,115 @@ __device__ __forceinline__ DecRow dec_row(const AttnParams &p, const SeqInfo &s,
     return r;
 }
 
+// One 32-key tile for the warp's 16 query rows: S = Q K^T, scale and mask,
+// online softmax (or 'none'), O += P V.  Rows rr[0..1] are this lane's rows
+// (lane/4 and lane/4 + 8); kb/vb: the tile's K and V in shared memory.
 template <int D, bool BF16, bool SOFTMAX>
-__global__ void __launch_bounds__(DEC_THREADS)
+__device__ __forceinline__ void dec_tile(const AttnParams &p, const DecRow (&rr)[2],
+                                         const uint32_t (&qa)[D / 16][4], uint32_t kb,
+                                         uint32_t vb, int j0, float (&o)[D / 8][4],
+                                         float (&m_r)[2], float (&l_r)[2]) {
+    using L = DecLayout<D>;
+    constexpr int NT = D / 8, KS = D / 16;
+    const int lane = threadIdx.x & 31;
+    const float sc = SOFTMAX ? p.scale_log2 : p.scale;
+    float sacc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ks += 2) {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kb + swz(nt * 8 + (lane & 7), ks * 2 + (lane >> 3), L::BLK), r0, r1, r2, r3);
+            mma16816<BF16>(sacc[nt], qa[ks], r0, r1);
+            mma16816<BF16>(sacc[nt], qa[ks + 1], r2, r3);
+        }
+    }
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const DecRow &R = rr[e >> 1];
+            const int j = j0 + nt * 8 + (lane & 3) * 2 + (e & 1);
+            bool ok = j <= R.lim;
+            float add = 0.f;
+            if (ok && p.mask) ok = mask_at(p, p.md[3] == 1 ? R.mrow : R.mrow + j, add);
+            const float v = sacc[nt][e] * sc + (SOFTMAX ? add * 1.4426950408889634f : add);
+            sacc[nt][e] = ok ? v : (SOFTMAX ? -INFINITY : 0.f);
+            mx[e >> 1] = fmaxf(mx[e >> 1], sacc[nt][e]);
+        }
+    if (SOFTMAX) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+            const float m_new = fmaxf(m_r[r], mx[r]);
+            const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = ex2(m_r[r] - mu);
+            l_r[r] *= alpha;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) { o[n][2 * r] *= alpha; o[n][2 * r + 1] *= alpha; }
+            m_r[r] = m_new;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                sacc[nt][2 * r] = ex2(sacc[nt][2 * r] - mu);
+                sacc[nt][2 * r + 1] = ex2(sacc[nt][2 * r + 1] - mu);
+                l_r[r] += sacc[nt][2 * r] + sacc[nt][2 * r + 1];
+            }
+        }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a[4];
+        a[0] = pack2<BF16>(sacc[2 * kk][0], sacc[2 * kk][1]);
+        a[1] = pack2<BF16>(sacc[2 * kk][2], sacc[2 * kk][3]);
+        a[2] = pack2<BF16>(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+        a[3] = pack2<BF16>(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+#pragma unroll
+        for (int n = 0; n < NT; n += 2) {
+            uint32_t r0, r1, r2, r3;
+            const int mi = lane >> 3;
+            ldsm_x4_t(vb + swz(kk * 16 + (mi & 1) * 8 + (lane & 7), n + (mi >> 1), L::BLK),
+                      r0, r1, r2, r3);
+            mma16816<BF16>(o[n], a, r0, r1);
+            mma16816<BF16>(o[n + 1], a, r2, r3);
+        }
+    }
+}
+
+// Y row of this lane's fragment rows, scaled by f (rows outside are skipped).
+template <int D, bool BF16>
+__device__ __forceinline__ void dec_store_y(const AttnParams &p, const DecRow (&rr)[2],
+                                            const float (&o)[D / 8][4], const float (&f)[2]) {
+    const int lane = threadIdx.x & 31;
+    uint16_t *y = static_cast<uint16_t *>(p.y);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        if (!rr[r].valid) continue;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+            const int col = n * 8 + (lane & 3) * 2;
+            *reinterpret_cast<uint32_t *>(y + rr[r].qoff + col) =
+                pack2<BF16>(o[n][2 * r] * f[r], o[n][2 * r + 1] * f[r]);
+        }
+    }
+}
+
+template <int D, bool BF16, bool SOFTMAX>
+__global__ void __launch_bounds__(DEC_THREADS, 1)
 decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TensorMaps tm) {
     using L = DecLayout<D>;
-    constexpr int NT = D / 8;     // 8-column output tiles
-    constexpr int KS = D / 16;    // 16-deep k-steps over the head dimension
+    constexpr int NT = D / 8;
+    constexpr int KS = D / 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
-    float2 *mlw = reinterpret_cast<float2 *>(sm + L::ML_OFF);
-    volatile int *abort = reinterpret_cast<volatile int *>(sm + L::MISC_OFF);
-    int *ticket_s = reinterpret_cast<int *>(sm + L::MISC_OFF + 4);
-    float *comb = reinterpret_cast<float *>(sm);
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + L::BAR_OFF + DEC_WARPS * DEC_STAGES * 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (reinterpret_cast<const volatile int *>(p.ws)[0] == 0) return;   // lengths rejected
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const SeqInfo s = seq_info(p, b);
-    const int rows = s.q_len * p.G;
-    if (rows <= 0) return;
-    const int kv_hi = key_extent(p.causal, s.q_len - 1, s);
-    const int nrc = (rows + DEC_ROWS - 1) / DEC_ROWS;
-    int nsplit = (kv_hi + DEC_SPLIT - 1) / DEC_SPLIT;
-    if (nsplit < 1 || nrc > 1) nsplit = 1;
-    if (split >= nsplit) return;
-    const int k0 = split * DEC_SPLIT;
-    const int k1 = (nsplit == 1) ? kv_hi : min(kv_hi, k0 + DEC_SPLIT);
+    int *hdr = reinterpret_cast<int *>(p.ws);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < DEC_WARPS * DEC_STAGES; ++i) mbar_init(&bars[i], 1);
@@ -148,270 +228,174 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         fence_mbar_init();
     }
     __syncthreads();
+    if (reinterpret_cast<const volatile int *>(hdr)[2] == 0) return;   // lengths rejected
+    const int n_units = reinterpret_cast<const volatile int *>(hdr)[0];
+    const int4 *units = reinterpret_cast<const int4 *>(p.ws + dec_units_off(p));
+    int *tickets = reinterpret_cast<int *>(p.ws + WS_HEADER);
+    float *part = reinterpret_cast<float *>(p.ws + dec_part_off(p));
+    float2 *pml = reinterpret_cast<float2 *>(p.ws + dec_ml_off(p));
 
     uint8_t *ring = sm + warp * L::WARP_RING;
     uint64_t *wbar = bars + warp * DEC_STAGES;
-    const int ntiles = (k1 - k0 + DEC_KEYS - 1) / DEC_KEYS;
-    const int my_n = ntiles > warp ? (ntiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
     const uint32_t ring_u32 = smem_u32(ring);
     uint32_t issued = 0, consumed = 0;
-    const float sc = SOFTMAX ? p.scale_log2 : p.scale;
-    const float LOG2E_ = 1.4426950408889634f;
 
-    for (int rc = 0; rc < nrc; ++rc) {
-        // ---- this lane's two rows (lane/4 and lane/4 + 8) and Q fragments
-        DecRow rr[2];
-        rr[0] = dec_row(p, s, b, g, rc * DEC_ROWS + (lane >> 2), rows, k1);
-        rr[1] = dec_row(p, s, b, g, rc * DEC_ROWS + (lane >> 2) + 8, rows, k1);
-        uint32_t qa[KS][4];
-        const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int col = ks * 16 + (lane & 3) * 2;
-            qa[ks][0] = rr[0].valid ? q32[(rr[0].qoff + col) >> 1] : 0u;
-            qa[ks][1] = rr[1].valid ? q32[(rr[1].qoff + col) >> 1] : 0u;
-            qa[ks][2] = rr[0].valid ? q32[(rr[0].qoff + col + 8) >> 1] : 0u;
-            qa[ks][3] = rr[1].valid ? q32[(rr[1].qoff + col + 8) >> 1] : 0u;
-        }
-        float o[NT][4];
-#pragma unroll
-        for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+    for (;;) {
+        int u = 0;
+        if (lane == 0) u = atomicAdd(&hdr[1], 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (u >= n_units || *abort) break;
+        const int4 un = units[u];
+        const int b = un.x, g = un.y, split = un.z, ns = un.w;
+        const SeqInfo s = seq_info(p, b);
+        const int rows = s.q_len * p.G;
+        const int kv_hi = key_extent(p.causal, s.q_len - 1, s);
+        const int k0 = split * DEC_SPLIT;
+        const int k1 = (ns == 1) ? kv_hi : min(kv_hi, k0 + DEC_SPLIT);
+        const int ntiles = k1 > k0 ? (k1 - k0 + DEC_KEYS - 1) / DEC_KEYS : 0;
+        const int nrc = (rows + DEC_ROWS - 1) / DEC_ROWS;
+        const size_t unit_idx = ((size_t)b * p.Hkv + g) * p.max_splits + split;
+        bool unit_ok = true;
 
-        // ---- prefetch
-        if (lane == 0)
-            for (int it = 0; it < DEC_STAGES && it < my_n; ++it) {
-                const uint32_t u = issued + it;
-                dec_tma(p, tm, s, b, g, k0 + (warp + it * DEC_WARPS) * DEC_KEYS,
-                        ring + (u % DEC_STAGES) * L::STAGE, &wbar[u % DEC_STAGES], D);
+        for (int rc = 0; rc < nrc && unit_ok; ++rc) {
+            DecRow rr[2];
+            rr[0] = dec_row(p, s, b, g, rc * DEC_ROWS + (lane >> 2), rows, k1);
+            rr[1] = dec_row(p, s, b, g, rc * DEC_ROWS + (lane >> 2) + 8, rows, k1);
+            uint32_t qa[KS][4];
+            const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int col = ks * 16 + (lane & 3) * 2;
+                qa[ks][0] = rr[0].valid ? q32[(rr[0].qoff + col) >> 1] : 0u;
+                qa[ks][1] = rr[1].valid ? q32[(rr[1].qoff + col) >> 1] : 0u;
+                qa[ks][2] = rr[0].valid ? q32[(rr[0].qoff + col + 8) >> 1] : 0u;
+                qa[ks][3] = rr[1].valid ? q32[(rr[1].qoff + col + 8) >> 1] : 0u;
             }
-        issued += min(DEC_STAGES, my_n);
+            float o[NT][4];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
 
-        // ---- stream this warp's key tiles
-        for (int it = 0; it < my_n && !*abort; ++it) {
-            const uint32_t u = consumed;
-            const int st = u % DEC_STAGES;
-            if (!mbar_wait(&wbar[st], (u / DEC_STAGES) & 1, abort)) break;
-            ++consumed;
-            const int j0 = k0 + (warp + it * DEC_WARPS) * DEC_KEYS;
-            const uint32_t kb = ring_u32 + st * L::STAGE, vb = kb + L::TILE;
-            const int rem = s.kv_len - j0;
-            if (rem < DEC_KEYS) {   // rows past the sequence end may hold NaN: zero them
-                uint8_t *vp = ring + st * L::STAGE + L::TILE;
-                for (int idx = lane; idx < DEC_KEYS * (D / 8); idx += 32) {
-                    const int row = idx / (D / 8), ch = idx % (D / 8);
-                    if (row >= rem)
-                        *reinterpret_cast<uint4 *>(vp + swz(row, ch, L::BLK)) = make_uint4(0, 0, 0, 0);
+            if (lane == 0)
+                for (int it = 0; it < DEC_STAGES && it < ntiles; ++it) {
+                    const uint32_t c = issued + it;
+                    dec_tma(p, tm, s, b, g, k0 + it * DEC_KEYS, ring + (c % DEC_STAGES) * L::STAGE,
+                            &wbar[c % DEC_STAGES], D);
                 }
+            issued += min(DEC_STAGES, ntiles);
+            for (int it = 0; it < ntiles; ++it) {
+                const uint32_t c = consumed;
+                const int st = c % DEC_STAGES;
+                if (!mbar_wait(&wbar[st], (c / DEC_STAGES) & 1, abort)) { unit_ok = false; break; }
+                ++consumed;
+                const int j0 = k0 + it * DEC_KEYS;
+                const uint32_t kb = ring_u32 + st * L::STAGE, vb = kb + L::TILE;
+                const int rem = s.kv_len - j0;
+                if (rem < DEC_KEYS) {   // rows past the sequence end may hold NaN: zero them
+                    uint8_t *vp = ring + st * L::STAGE + L::TILE;
+                    for (int idx = lane; idx < DEC_KEYS * (D / 8); idx += 32) {
+                        const int row = idx / (D / 8), ch = idx % (D / 8);
+                        if (row >= rem)
+                            *reinterpret_cast<uint4 *>(vp + swz(row, ch, L::BLK)) = make_uint4(0, 0, 0, 0);
+                    }
+                    __syncwarp();
+                }
+                dec_tile<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r);
                 __syncwarp();
-            }
-            // S = Q K^T  (16 rows x 32 keys)
-            float sacc[4][4];
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < KS; ks += 2) {
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kb + swz(nt * 8 + (lane & 7), ks * 2 + (lane >> 3), L::BLK), r0, r1, r2, r3);
-                    mma16816<BF16>(sacc[nt], qa[ks], r0, r1);
-                    mma16816<BF16>(sacc[nt], qa[ks + 1], r2, r3);
+                if (it + DEC_STAGES < ntiles) {   // refill the stage just used
+                    if (lane == 0) {
+                        fence_proxy_async_smem();
+                        dec_tma(p, tm, s, b, g, k0 + (it + DEC_STAGES) * DEC_KEYS,
+                                ring + (issued % DEC_STAGES) * L::STAGE, &wbar[issued % DEC_STAGES], D);
+                    }
+                    ++issued;
                 }
             }
-            // scale, mask, online softmax
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const DecRow &R = rr[e >> 1];
-                    const int j = j0 + nt * 8 + (lane & 3) * 2 + (e & 1);
-                    bool ok = j <= R.lim;
-                    float add = 0.f;
-                    if (ok && p.mask) ok = mask_at(p, p.md[3] == 1 ? R.mrow : R.mrow + j, add);
-                    const float v = sacc[nt][e] * sc + (SOFTMAX ? add * LOG2E_ : add);
-                    sacc[nt][e] = ok ? v : (SOFTMAX ? -INFINITY : 0.f);
-                    mx[e >> 1] = fmaxf(mx[e >> 1], sacc[nt][e]);
-                }
-            if (SOFTMAX) {
+            if (!unit_ok) break;
+            if (SOFTMAX)
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                    const float m_new = fmaxf(m_r[r], mx[r]);
-                    const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-                    const float alpha = ex2(m_r[r] - mu);
-                    l_r[r] *= alpha;
+                    l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
+                    l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
+                }
+            if (ns == 1) {
+                float f[2];
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) { o[n][2 * r] *= alpha; o[n][2 * r + 1] *= alpha; }
-                    m_r[r] = m_new;
+                for (int r = 0; r < 2; ++r)
+                    f[r] = SOFTMAX ? (l_r[r] > 0.f ? 1.f / l_r[r] : 0.f) : 1.f;
+                dec_store_y<D, BF16>(p, rr, o, f);
+            } else {
+                // partial (O, m, l) of this split
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt) {
-                        sacc[nt][2 * r] = ex2(sacc[nt][2 * r] - mu);
-                        sacc[nt][2 * r + 1] = ex2(sacc[nt][2 * r + 1] - mu);
-                        l_r[r] += sacc[nt][2 * r] + sacc[nt][2 * r + 1];
+                for (int r = 0; r < 2; ++r) {
+                    const int row = (lane >> 2) + 8 * r;
+                    float *po = part + (unit_idx * DEC_ROWS + row) * D;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n)
+                        *reinterpret_cast<float2 *>(po + n * 8 + (lane & 3) * 2) =
+                            make_float2(o[n][2 * r], o[n][2 * r + 1]);
+                    if ((lane & 3) == 0) pml[unit_idx * DEC_ROWS + row] = make_float2(m_r[r], l_r[r]);
+                }
+            }
+        }
+        if (!unit_ok) break;
+        if (ns > 1) {
+            // the last split of the pair to finish merges all of them
+            __threadfence();
+            __syncwarp();
+            int t = 0;
+            if (lane == 0) t = atomicAdd(&tickets[b * p.Hkv + g], 1);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t == ns - 1) {
+                __threadfence();
+                const size_t u0 = ((size_t)b * p.Hkv + g) * p.max_splits;
+                const int row = lane >> 1, c0 = (lane & 1) * (D / 2);
+                float M = -INFINITY;
+                if (SOFTMAX)
+                    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, __ldcg(&pml[(u0 + sp) * DEC_ROWS + row].x));
+                float acc[D / 2];
+#pragma unroll
+                for (int c = 0; c < D / 2; ++c) acc[c] = 0.f;
+                float Lsum = 0.f;
+                for (int sp = 0; sp < ns; ++sp) {
+                    float wt = 1.f;
+                    if (SOFTMAX) {
+                        const float2 v = __ldcg(&pml[(u0 + sp) * DEC_ROWS + row]);
+                        wt = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
+                        Lsum += v.y * wt;
+                    }
+                    const float4 *src = reinterpret_cast<const float4 *>(part + ((u0 + sp) * DEC_ROWS + row) * D + c0);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) {
+                        const float4 x4 = __ldcg(src + c);
+                        acc[4 * c] += x4.x * wt;
+                        acc[4 * c + 1] += x4.y * wt;
+                        acc[4 * c + 2] += x4.z * wt;
+                        acc[4 * c + 3] += x4.w * wt;
                     }
                 }
-            }
-            // O += P V
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                uint32_t a[4];
-                a[0] = pack2<BF16>(sacc[2 * kk][0], sacc[2 * kk][1]);
-                a[1] = pack2<BF16>(sacc[2 * kk][2], sacc[2 * kk][3]);
-                a[2] = pack2<BF16>(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-                a[3] = pack2<BF16>(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
-#pragma unroll
-                for (int n = 0; n < NT; n += 2) {
-                    uint32_t r0, r1, r2, r3;
-                    const int mi = lane >> 3;
-                    ldsm_x4_t(vb + swz(kk * 16 + (mi & 1) * 8 + (lane & 7), n + (mi >> 1), L::BLK),
-                              r0, r1, r2, r3);
-                    mma16816<BF16>(o[n], a, r0, r1);
-                    mma16816<BF16>(o[n + 1], a, r2, r3);
-                }
-            }
-            __syncwarp();
-            // refill this stage
-            const int nxt = it + DEC_STAGES;
-            if (nxt < my_n) {
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    dec_tma(p, tm, s, b, g, k0 + (warp + nxt * DEC_WARPS) * DEC_KEYS,
-                            ring + (issued % DEC_STAGES) * L::STAGE, &wbar[issued % DEC_STAGES], D);
-                }
-                ++issued;
-            }
-        }
-        // copies still in flight (only after an abort) land before reuse
-        while (consumed < issued) {
-            mbar_wait_drain(&wbar[consumed % DEC_STAGES], (consumed / DEC_STAGES) & 1);
-            ++consumed;
-        }
-
-        // ---- merge the 4 warps' partials in shared memory (reuses the ring)
-        if (SOFTMAX)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
-                l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
-            }
-        __syncthreads();
-        {
-            float *cw = comb + warp * DEC_ROWS * D;
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int row = (lane >> 2) + (e >> 1) * 8;
-                    const int col = n * 8 + (lane & 3) * 2 + (e & 1);
-                    cw[row * D + col] = o[n][e];
-                }
-            if ((lane & 3) == 0) {
-                mlw[warp * DEC_ROWS + (lane >> 2)] = make_float2(m_r[0], l_r[0]);
-                mlw[warp * DEC_ROWS + (lane >> 2) + 8] = make_float2(m_r[1], l_r[1]);
-            }
-        }
-        __syncthreads();
-        {
-            constexpr int CPT = D / 8;                 // columns per thread (8 threads per row)
-            const int row = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * CPT;
-            float wts[DEC_WARPS];
-            float M = -INFINITY, Lsum = 0.f;
-            if (SOFTMAX) {
-#pragma unroll
-                for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, mlw[w * DEC_ROWS + row].x);
-#pragma unroll
-                for (int w = 0; w < DEC_WARPS; ++w) {
-                    const float2 v = mlw[w * DEC_ROWS + row];
-                    wts[w] = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
-                    Lsum += v.y * wts[w];
-                }
-            } else {
-#pragma unroll
-                for (int w = 0; w < DEC_WARPS; ++w) wts[w] = 1.f;
-            }
-            float acc[CPT];
-#pragma unroll
-            for (int c = 0; c < CPT; ++c) {
-                float a = 0.f;
-#pragma unroll
-                for (int w = 0; w < DEC_WARPS; ++w) a += comb[(w * DEC_ROWS + row) * D + c0 + c] * wts[w];
-                acc[c] = a;
-            }
-            const DecRow R = dec_row(p, s, b, g, rc * DEC_ROWS + row, rows, k1);
-            if (nsplit == 1) {
-                if (R.valid && !*abort) {
+                const DecRow R = dec_row(p, s, b, g, row, rows, k1);
+                if (R.valid) {
                     const float f = SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f;
-                    uint32_t w[CPT / 2];
-#pragma unroll
-                    for (int c = 0; c < CPT / 2; ++c) w[c] = pack2<BF16>(acc[2 * c] * f, acc[2 * c + 1] * f);
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff + c0);
 #pragma unroll
-                    for (int c = 0; c < CPT / 8; ++c)
-                        dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    for (int c = 0; c < D / 16; ++c)
+                        dst[c] = make_uint4(pack2<BF16>(acc[8 * c] * f, acc[8 * c + 1] * f),
+                                            pack2<BF16>(acc[8 * c + 2] * f, acc[8 * c + 3] * f),
+                                            pack2<BF16>(acc[8 * c + 4] * f, acc[8 * c + 5] * f),
+                                            pack2<BF16>(acc[8 * c + 6] * f, acc[8 * c + 7] * f));
                 }
-            } else {
-                const size_t unit = ((size_t)b * p.Hkv + g) * p.max_splits + split;
-                float *po = reinterpret_cast<float *>(p.ws + dec_part_off(p)) + (unit * DEC_ROWS + row) * D;
-#pragma unroll
-                for (int c = 0; c < CPT; ++c) po[c0 + c] = acc[c];
-                if ((threadIdx.x & 7) == 0) {
-                    float2 *pml = reinterpret_cast<float2 *>(p.ws + dec_ml_off(p));
-                    pml[unit * DEC_ROWS + row] = make_float2(M, Lsum);
-                }
+                if (lane == 0) tickets[b * p.Hkv + g] = 0;
             }
         }
-        __syncthreads();
     }
-
-    // ---- merge the splits of this (batch, KV head): the last CTA to finish does it
-    if (nsplit > 1) {
-        __threadfence();
-        __syncthreads();
-        int *tickets = reinterpret_cast<int *>(p.ws + WS_HEADER);
-        if (threadIdx.x == 0) *ticket_s = atomicAdd(&tickets[b * p.Hkv + g], 1);
-        __syncthreads();
-        if (*ticket_s != nsplit - 1) return;
-        __threadfence();
-        constexpr int CPT = D / 8;
-        const int row = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * CPT;
-        const size_t unit0 = ((size_t)b * p.Hkv + g) * p.max_splits;
-        const float *po = reinterpret_cast<const float *>(p.ws + dec_part_off(p));
-        const float2 *pml = reinterpret_cast<const float2 *>(p.ws + dec_ml_off(p));
-        float M = -INFINITY;
-        if (SOFTMAX)
-            for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(&pml[(unit0 + sp) * DEC_ROWS + row].x));
-        float acc[CPT];
-#pragma unroll
-        for (int c = 0; c < CPT; ++c) acc[c] = 0.f;
-        float Lsum = 0.f;
-        for (int sp = 0; sp < nsplit; ++sp) {
-            float wt = 1.f;
-            if (SOFTMAX) {
-                const float2 v = __ldcg(&pml[(unit0 + sp) * DEC_ROWS + row]);
-                wt = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
-                Lsum += v.y * wt;
-            }
-            const float *src = po + ((unit0 + sp) * DEC_ROWS + row) * D + c0;
-#pragma unroll
-            for (int c = 0; c < CPT; ++c) acc[c] += __ldcg(src + c) * wt;
-        }
-        const DecRow R = dec_row(p, s, b, g, row, rows, k1);
-        if (R.valid && !*abort) {
-            const float f = SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f;
-            uint32_t w[CPT / 2];
-#pragma unroll
-            for (int c = 0; c < CPT / 2; ++c) w[c] = pack2<BF16>(acc[2 * c] * f, acc[2 * c + 1] * f);
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff + c0);
-#pragma unroll
-            for (int c = 0; c < CPT / 8; ++c)
-                dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-        }
-        if (threadIdx.x == 0) tickets[b * p.Hkv + g] = 0;
+    // copies still in flight (only after an abort) land before the CTA exits
+    while (consumed < issued) {
+        mbar_wait_drain(&wbar[consumed % DEC_STAGES], (consumed / DEC_STAGES) & 1);
+        ++consumed;
     }
-    if (threadIdx.x == 0 && *abort) set_status(p.status, 5);
+    __syncwarp();
+    if (lane == 0 && *abort) set_status(p.status, 5);
 }
 
 template <int D, bool BF16, bool SOFTMAX>
@@ -424,8 +408,7 @@ static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStre
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid(p.max_splits, p.Hkv, p.B);
-    decode_kernel<D, BF16, SOFTMAX><<<grid, DEC_THREADS, L::ALLOC, s>>>(p, m);
+    decode_kernel<D, BF16, SOFTMAX><<<p.grid, DEC_THREADS, L::ALLOC, s>>>(p, m);
     return cudaGetLastError();
 }
 

@@ -12,12 +12,13 @@ namespace rga {
 constexpr int BM = 128;
 constexpr int BN = 128;
 
-// Decode geometry: 16 query rows per MMA row chunk, 32 keys per warp step,
-// 4 warps per CTA, DEC_SPLIT keys per CTA.
+// Decode geometry: 16 query rows per MMA row block, 32 keys per tile,
+// DEC_SPLIT keys per work unit, 4 independent warps per CTA with a
+// DEC_STAGES-deep TMA ring each.
 constexpr int DEC_ROWS = 16;
 constexpr int DEC_KEYS = 32;
 constexpr int DEC_WARPS = 4;
-constexpr int DEC_STAGES = 2;
+constexpr int DEC_STAGES = 3;
 constexpr int DEC_SPLIT = 512;
 
 enum Mode { MODE_SOFTMAX = 0, MODE_NONE = 1, MODE_SOFTMAX_Q = 2, MODE_NONE_Q = 3 };
@@ -43,6 +44,7 @@ struct AttnParams {
     int item_tokens;                // query tokens per prefill work item (2 tiles)
     int max_items;                  // capacity of the work list
     int max_splits;                 // decode: splits per (b, kv head)
+    int grid;                       // decode: persistent grid size
     int32_t *status;                // device status word
     uint8_t *ws;                    // workspace base
 };
@@ -59,9 +61,12 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 __host__ __device__ inline size_t pf_ws_bytes(const AttnParams &p) {
     return WS_HEADER + (size_t)p.max_items * 16;
 }
-// decode workspace: header, split tickets, partial O, partial (m, l)
-__host__ __device__ inline size_t dec_part_off(const AttnParams &p) {
+// decode workspace: header, split tickets, unit list, partial O, partial (m, l)
+__host__ __device__ inline size_t dec_units_off(const AttnParams &p) {
     return align256(WS_HEADER + (size_t)p.B * p.Hkv * 4);
+}
+__host__ __device__ inline size_t dec_part_off(const AttnParams &p) {
+    return align256(dec_units_off(p) + (size_t)p.B * p.Hkv * p.max_splits * 16);
 }
 __host__ __device__ inline size_t dec_ml_off(const AttnParams &p) {
     return dec_part_off(p) + align256((size_t)p.B * p.Hkv * p.max_splits * DEC_ROWS * p.D * 4);

@@ -68,15 +68,33 @@ sched_kernel(AttnParams p, int decode) {
             set_status(p.status, 4);
             hdr[0] = 0;
             hdr[1] = 0;
+            hdr[2] = 0;
         }
         return;
     }
 
     if (decode) {
-        // clear the per-(batch, kv head) split tickets
+        // clear the per-(batch, kv head) split tickets and list the decode
+        // units (batch, KV head, split, splits of the pair)
         int *tickets = reinterpret_cast<int *>(p.ws + WS_HEADER);
         for (int i = tid; i < p.B * p.Hkv; i += SCHED_THREADS) tickets[i] = 0;
-        if (tid == 0) hdr[0] = 1;   // lengths accepted
+        int4 *units = reinterpret_cast<int4 *>(p.ws + dec_units_off(p));
+        for (int b = tid; b < p.B; b += SCHED_THREADS) {
+            const SeqInfo s = seq_info(p, b);
+            const int rows = s.q_len * p.G;
+            if (rows <= 0) continue;
+            const int ns = dec_splits(p, s);
+            const int pos = atomicAdd(&total, ns * p.Hkv);
+            for (int sp = 0; sp < ns; ++sp)
+                for (int g = 0; g < p.Hkv; ++g)
+                    units[pos + sp * p.Hkv + g] = make_int4(b, g, sp, ns);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            hdr[0] = total;   // units listed (0 also when nothing to do)
+            hdr[1] = 0;       // next unit to take
+            hdr[2] = 1;       // lengths accepted
+        }
         return;
     }
 
