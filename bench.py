@@ -48,6 +48,32 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+PROFILES = {   # headline kernel source and the ncu summary of it
+    "prefill": ("ragged_gqa_attention_gb300/csrc/prefill.cuh",
+                "profiles/prefill_kernel_packed_ragged_prefill_gqa32x8_d128_bf16.md"),
+    "decode": ("ragged_gqa_attention_gb300/csrc/decode.cu",
+               "profiles/decode_kernel_decode_b64_gqa64x8_kv4096_d128_bf16.md"),
+}
+
+
+def profile_traffic(kind):
+    """DRAM bytes per launch (read + write) from the committed ncu summary, or
+    None when the kernel source has changed since that capture."""
+    import hashlib
+    import re
+    src, md = (os.path.join(ROOT, x) for x in PROFILES[kind])
+    try:
+        text = open(md).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m_sha = re.search(r"sha256 ([0-9a-f]{64})", text)
+    m_tr = re.search(r"traffic \(read \+ write\) \| ([0-9.]+) MB", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1)) * 1e6
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during a region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -366,7 +392,9 @@ def main():
             "roofline": {"bound": head["bound"], "achieved": round(head["value"], 3),
                          "peak": head["peak"], "unit": head["unit"],
                          "frac": round(head["value"] / head["peak"], 4),
-                         "traffic": None, "peak_source": peak_src,
+                         "traffic": profile_traffic("decode" if metrics.is_decode(case)
+                                                    else "prefill"),
+                         "peak_source": peak_src,
                          "note": "achieved = algorithmic work / CUDA-event time of the whole "
                                  "call (scheduler + attention kernel)"},
             "e2e": {"value": round(e2e_val * world, 3), "unit": head["unit"],

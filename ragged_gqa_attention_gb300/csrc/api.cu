@@ -80,7 +80,7 @@ bool encode_kv(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t r
 
 // Decode (split-KV) path: short query rows per (batch, KV head), no Q/DQ.
 bool use_decode(const rga_attention_args *a, bool quant) {
-    if (quant) return false;
+    if (quant || a->batch > DEC_MAX_B) return false;
     const int G = a->q_heads / a->kv_heads;
     if (G > DEC_ROWS) return false;
     if (a->q_form == RGA_FORM_PACKED_NHD) return a->q_seq <= a->batch;
@@ -218,8 +218,8 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
     if (a->norm == RGA_NORM_SOFTMAX) mode = quant ? MODE_SOFTMAX_Q : MODE_SOFTMAX;
     else mode = quant ? MODE_NONE_Q : MODE_NONE;
 
-    if (launch_sched(p, dec ? 1 : 0, stream) != cudaSuccess) return RGA_ERR_CUDA;
     cudaError_t e;
+    if (!dec && launch_sched(p, 0, stream) != cudaSuccess) return RGA_ERR_CUDA;
     if (dec) {
         const int sms = sm_count();
         if (sms <= 0) return RGA_ERR_CUDA;

@@ -3,9 +3,10 @@
 // vanilla decoding attention) with the TRT_Attention semantics of
 // "TensorRT Custom Operator Schemas".
 //
-// Work unit: (batch b, KV head g, split of DEC_SPLIT keys), listed by the
-// scheduler.  The grid is persistent and every warp is an independent
-// engine: it takes the next unit from an atomic counter, streams the unit's
+// Work unit: (batch b, KV head g, split of DEC_SPLIT keys).  The grid is
+// persistent; each CTA validates the lengths and lists the units itself
+// (no scheduler launch), and every warp is an independent engine: it takes
+// the next unit from an atomic counter, streams the unit's
 // 32-key K/V tiles with TMA through its own DEC_STAGES-deep, 128-byte-
 // swizzled ring, computes S = Q K^T and O += P V with m16n8k16 MMAs (K and
 // V are read once from HBM for all G query heads of the KV head) and keeps
@@ -34,7 +35,8 @@ struct DecLayout {
     static constexpr int WARP_RING = DEC_STAGES * STAGE;
     static constexpr int RING = DEC_WARPS * WARP_RING;
     static constexpr int BAR_OFF = RING;
-    static constexpr int BYTES = BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 64;
+    static constexpr int BOFF_OFF = BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 64;
+    static constexpr int BYTES = BOFF_OFF + (DEC_MAX_B + 1) * 4 + 64;
     static constexpr int ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory per CTA");
 };
@@ -220,18 +222,47 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
     volatile int *abort = reinterpret_cast<volatile int *>(sm + L::BAR_OFF + DEC_WARPS * DEC_STAGES * 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int *hdr = reinterpret_cast<int *>(p.ws);
 
+    int *boff = reinterpret_cast<int *>(sm + L::BOFF_OFF);    // first unit of each batch
+    int *flags = reinterpret_cast<int *>(sm + L::BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 4);
     if (threadIdx.x == 0) {
         for (int i = 0; i < DEC_WARPS * DEC_STAGES; ++i) mbar_init(&bars[i], 1);
         *abort = 0;
+        flags[0] = 0;   // bad lengths
         fence_mbar_init();
     }
     __syncthreads();
-    if (reinterpret_cast<const volatile int *>(hdr)[2] == 0) return;   // lengths rejected
-    const int n_units = reinterpret_cast<const volatile int *>(hdr)[0];
-    const int4 *units = reinterpret_cast<const int4 *>(p.ws + dec_units_off(p));
-    int *tickets = reinterpret_cast<int *>(p.ws + WS_HEADER);
+    // Every CTA validates the lengths and lists the units itself: unit u of
+    // batch b is (split, KV head) = ((u - boff[b]) / Hkv, (u - boff[b]) % Hkv).
+    for (int b = threadIdx.x; b < p.B; b += DEC_THREADS) {
+        const int32_t *ql = p.query_lengths, *kl = p.kv_lengths;
+        const SeqInfo s = seq_info(p, b);
+        bool ok = s.q_len >= 0 && s.kv_len >= 0;
+        if (ql) ok = ok && ql[0] == 0;
+        if (p.q_packed) ok = ok && ql[b + 1] <= p.q_seq;
+        else ok = ok && s.q_len <= p.q_seq;
+        if (p.kv_packed) ok = ok && kl[0] == 0 && kl[b + 1] <= p.kv_seq;
+        else ok = ok && s.kv_len <= p.kv_seq;
+        if (p.mask) {
+            if (p.md[2] != 1 && p.md[2] < s.q_len) ok = false;
+            if (p.md[3] != 1 && p.md[3] < s.kv_len) ok = false;
+        }
+        if (!ok) atomicOr(&flags[0], 1);
+        boff[b + 1] = (ok && s.q_len > 0) ? dec_splits(p, s) * p.Hkv : 0;
+    }
+    __syncthreads();
+    if (flags[0]) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_status(p.status, 4);
+        return;
+    }
+    if (threadIdx.x == 0) {   // prefix over batches (serial: B is at most DEC_MAX_B)
+        boff[0] = 0;
+        for (int b = 0; b < p.B; ++b) boff[b + 1] += boff[b];
+    }
+    __syncthreads();
+    const int n_units = boff[p.B];
+    pdl_wait();   // the tickets and the unit counter have been cleared
+    int *tickets = reinterpret_cast<int *>(p.ws + dec_tickets_off(p));
     float *part = reinterpret_cast<float *>(p.ws + dec_part_off(p));
     float2 *pml = reinterpret_cast<float2 *>(p.ws + dec_ml_off(p));
 
@@ -240,13 +271,20 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     const uint32_t ring_u32 = smem_u32(ring);
     uint32_t issued = 0, consumed = 0;
 
+    int *next_unit = tickets + p.B * p.Hkv;    // cleared with the tickets
     for (;;) {
         int u = 0;
-        if (lane == 0) u = atomicAdd(&hdr[1], 1);
+        if (lane == 0) u = atomicAdd(next_unit, 1);
         u = __shfl_sync(0xffffffffu, u, 0);
         if (u >= n_units || *abort) break;
-        const int4 un = units[u];
-        const int b = un.x, g = un.y, split = un.z, ns = un.w;
+        int lo = 0, hi = p.B;   // boff[lo] <= u < boff[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (boff[mid] <= u) lo = mid; else hi = mid;
+        }
+        const int b = lo;
+        const int g = (u - boff[b]) % p.Hkv, split = (u - boff[b]) / p.Hkv;
+        const int ns = (boff[b + 1] - boff[b]) / p.Hkv;
         const SeqInfo s = seq_info(p, b);
         const int rows = s.q_len * p.G;
         const int kv_hi = key_extent(p.causal, s.q_len - 1, s);
@@ -398,6 +436,14 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     if (lane == 0 && *abort) set_status(p.status, 5);
 }
 
+// Clears the split tickets and the next-unit counter of a decode call; the
+// decode kernel follows it as a programmatic dependent.
+__global__ void decode_prep_kernel(int *tickets, int n) {
+    pdl_launch_dependents();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        tickets[i] = 0;
+}
+
 template <int D, bool BF16, bool SOFTMAX>
 static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStream_t s) {
     using L = DecLayout<D>;
@@ -408,8 +454,12 @@ static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStre
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    decode_kernel<D, BF16, SOFTMAX><<<p.grid, DEC_THREADS, L::ALLOC, s>>>(p, m);
-    return cudaGetLastError();
+    const int n = p.B * p.Hkv + 1;
+    decode_prep_kernel<<<(n + 255) / 256 < 64 ? (n + 255) / 256 : 64, 256, 0, s>>>(
+        reinterpret_cast<int *>(p.ws + dec_tickets_off(p)), n);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_dependent(decode_kernel<D, BF16, SOFTMAX>, p.grid, DEC_THREADS, L::ALLOC, s, p, m);
 }
 
 cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode, cudaStream_t s,

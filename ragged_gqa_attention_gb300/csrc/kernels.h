@@ -61,12 +61,13 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 __host__ __device__ inline size_t pf_ws_bytes(const AttnParams &p) {
     return WS_HEADER + (size_t)p.max_items * 16;
 }
-// decode workspace: header, split tickets, unit list, partial O, partial (m, l)
-__host__ __device__ inline size_t dec_units_off(const AttnParams &p) {
-    return align256(WS_HEADER + (size_t)p.B * p.Hkv * 4);
+// decode workspace, after the prefill region: split tickets and the next-unit
+// counter (cleared before each decode launch), partial O, partial (m, l)
+__host__ __device__ inline size_t dec_tickets_off(const AttnParams &p) {
+    return align256(pf_ws_bytes(p));
 }
 __host__ __device__ inline size_t dec_part_off(const AttnParams &p) {
-    return align256(dec_units_off(p) + (size_t)p.B * p.Hkv * p.max_splits * 16);
+    return align256(dec_tickets_off(p) + ((size_t)p.B * p.Hkv + 1) * 4);
 }
 __host__ __device__ inline size_t dec_ml_off(const AttnParams &p) {
     return dec_part_off(p) + align256((size_t)p.B * p.Hkv * p.max_splits * DEC_ROWS * p.D * 4);
@@ -74,10 +75,31 @@ __host__ __device__ inline size_t dec_ml_off(const AttnParams &p) {
 __host__ __device__ inline size_t dec_ws_bytes(const AttnParams &p) {
     return dec_ml_off(p) + (size_t)p.B * p.Hkv * p.max_splits * DEC_ROWS * 8;
 }
+// Largest batch the decode kernel lists in shared memory.
+constexpr int DEC_MAX_B = 4096;
 
 struct TensorMaps {
     CUtensorMap q, k, v, y;   // y: same geometry and box as q
 };
+
+// Launch a kernel that follows the scheduler on the same stream as a
+// programmatic dependent: it may start (and run its prologue) while the
+// scheduler finishes, and waits for it with griddepcontrol.wait.
+template <typename Kernel>
+inline cudaError_t launch_dependent(Kernel kernel, int grid, int block, int smem,
+                                    cudaStream_t s, const AttnParams &p, const TensorMaps &m) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p, m);
+}
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_sched(const AttnParams &p, int decode, cudaStream_t s);

@@ -887,7 +887,6 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF);
     volatile int *abort = reinterpret_cast<volatile int *>(sm + L::MISC_OFF + 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = *reinterpret_cast<volatile const int *>(p.ws);
 
     if (threadIdx.x == 0) {
         mbar_init(bar.q_full, 1);
@@ -916,6 +915,8 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();   // the scheduler's work list is complete and visible
+    const int n_items = *reinterpret_cast<volatile const int *>(p.ws);
 
     if (warp < 8) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(PF_SOFTMAX_REGS));
@@ -955,8 +956,7 @@ static cudaError_t launch_one(const AttnParams &p, const TensorMaps &m, int grid
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    prefill_kernel<D, MODE, BF16><<<grid, PF_THREADS, L::ALLOC, s>>>(p, m);
-    return cudaGetLastError();
+    return launch_dependent(prefill_kernel<D, MODE, BF16>, grid, PF_THREADS, L::ALLOC, s, p, m);
 }
 
 template <int D, bool BF16>

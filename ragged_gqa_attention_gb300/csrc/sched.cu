@@ -5,18 +5,20 @@
 // (batch, query block of item_tokens tokens, KV head, cost) sorted by cost, longest first, so that
 // the persistent prefill grid starts the biggest items first.  Cost is the
 // number of 128-key tiles the item visits after causal and length
-// skipping.  For decode it only validates and clears the split tickets.
+// skipping.  (The decode kernel validates and lists its own work.)
 //
 // Work-list layout in the workspace: int n_items at byte 0, int4 items from
 // byte WS_HEADER.  On bad lengths it writes RGA_ERR_DEVICE_LENGTHS (4) to
 // the status word and an empty list, so no attention work runs.
 #include "device_common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace rga {
 
 constexpr int SCHED_THREADS = 1024;
 constexpr int COST_BUCKETS = 1024;
+constexpr int SCHED_MAX_B = 4096;   // per-batch prefix in shared memory up to this batch
 static_assert(COST_BUCKETS == SCHED_THREADS, "one bucket per thread in the scan");
 
 __device__ __forceinline__ int item_cost(const AttnParams &p, const SeqInfo &s, int qt) {
@@ -26,23 +28,55 @@ __device__ __forceinline__ int item_cost(const AttnParams &p, const SeqInfo &s, 
     return c;
 }
 
+// Block-wide exclusive scan of one int per thread (all SCHED_THREADS threads
+// call it); returns this thread's prefix and sets *total to the block sum.
+__device__ __forceinline__ int block_excl_scan(int x, int *warp_sum, int *total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int v = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    if (lane == 31) warp_sum[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int t = warp_sum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        warp_sum[lane] = t;
+    }
+    __syncthreads();
+    const int before = (w > 0 ? warp_sum[w - 1] : 0) + v - x;
+    *total = warp_sum[SCHED_THREADS / 32 - 1];   // every thread: the block total
+    __syncthreads();
+    return before;
+}
+
 __global__ void __launch_bounds__(SCHED_THREADS)
 sched_kernel(AttnParams p, int decode) {
     __shared__ int hist[COST_BUCKETS];
+    __shared__ int qoff[SCHED_MAX_B + 1];    // per-batch first query block
+    __shared__ int warp_sum[32];
     __shared__ int bad;
     __shared__ int total;
+    __shared__ int nblocks;
     int *hdr = reinterpret_cast<int *>(p.ws);
     int4 *items = reinterpret_cast<int4 *>(p.ws + WS_HEADER);
     const int tid = threadIdx.x;
 
-    if (tid == 0) { bad = 0; total = 0; }
+    pdl_launch_dependents();   // the attention kernel may start its prologue
+    if (tid == 0) { bad = 0; total = 0; nblocks = 0; }
     for (int c = tid; c < COST_BUCKETS; c += SCHED_THREADS) hist[c] = 0;
     __syncthreads();
 
-    // 1. validate lengths, count items per cost bucket
+    // 1. validate lengths
     for (int b = tid; b < p.B; b += SCHED_THREADS) {
         const int32_t *ql = p.query_lengths, *kl = p.kv_lengths;
-        SeqInfo s = seq_info(p, b);
+        const SeqInfo s = seq_info(p, b);
         bool ok = s.q_len >= 0 && s.kv_len >= 0;
         if (ql) ok = ok && ql[0] == 0;
         if (p.q_packed) ok = ok && ql[b + 1] <= p.q_seq;
@@ -53,17 +87,10 @@ sched_kernel(AttnParams p, int decode) {
             if (p.md[2] != 1 && p.md[2] < s.q_len) ok = false;
             if (p.md[3] != 1 && p.md[3] < s.kv_len) ok = false;
         }
-        if (!ok) { atomicOr(&bad, 1); continue; }
-        if (decode) continue;
-        const int nqt = (s.q_len + p.item_tokens - 1) / p.item_tokens;
-        for (int qt = 0; qt < nqt; ++qt) {
-            int c = min(item_cost(p, s, qt), COST_BUCKETS - 1);
-            atomicAdd(&hist[c], p.Hkv);
-            atomicAdd(&total, p.Hkv);
-        }
+        if (!ok) atomicOr(&bad, 1);
     }
     __syncthreads();
-    if (bad || total > p.max_items) {
+    if (bad) {
         if (tid == 0) {
             set_status(p.status, 4);
             hdr[0] = 0;
@@ -73,73 +100,100 @@ sched_kernel(AttnParams p, int decode) {
         return;
     }
 
-    if (decode) {
-        // clear the per-(batch, kv head) split tickets and list the decode
-        // units (batch, KV head, split, splits of the pair)
-        int *tickets = reinterpret_cast<int *>(p.ws + WS_HEADER);
-        for (int i = tid; i < p.B * p.Hkv; i += SCHED_THREADS) tickets[i] = 0;
-        int4 *units = reinterpret_cast<int4 *>(p.ws + dec_units_off(p));
+    // 2. query blocks per batch and their prefix (batch-parallel)
+    const bool par = p.B <= SCHED_MAX_B;
+    if (par) {
+        for (int base = 0; base < p.B; base += SCHED_THREADS) {
+            const int b = base + tid;
+            int n = 0;
+            if (b < p.B) {
+                const SeqInfo s = seq_info(p, b);
+                n = (s.q_len + p.item_tokens - 1) / p.item_tokens;
+            }
+            int chunk_total;
+            const int before = block_excl_scan(n, warp_sum, &chunk_total);
+            if (b < p.B) qoff[b] = nblocks + before;
+            __syncthreads();
+            if (tid == 0) nblocks += chunk_total;
+            __syncthreads();
+        }
+        if (tid == 0) qoff[p.B] = nblocks;
+        __syncthreads();
+    }
+
+    // (batch, query block) of flat block index i
+    auto locate = [&](int i, int &b, int &qt) {
+        int lo = 0, hi = p.B;                 // qoff[lo] <= i < qoff[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (qoff[mid] <= i) lo = mid; else hi = mid;
+        }
+        b = lo;
+        qt = i - qoff[lo];
+    };
+
+    // 3. cost histogram
+    if (par) {
+        for (int i = tid; i < nblocks; i += SCHED_THREADS) {
+            int b, qt;
+            locate(i, b, qt);
+            const SeqInfo s = seq_info(p, b);
+            atomicAdd(&hist[min(item_cost(p, s, qt), COST_BUCKETS - 1)], p.Hkv);
+        }
+        if (tid == 0) total = nblocks * p.Hkv;
+    } else {
         for (int b = tid; b < p.B; b += SCHED_THREADS) {
             const SeqInfo s = seq_info(p, b);
-            const int rows = s.q_len * p.G;
-            if (rows <= 0) continue;
-            const int ns = dec_splits(p, s);
-            const int pos = atomicAdd(&total, ns * p.Hkv);
-            for (int sp = 0; sp < ns; ++sp)
-                for (int g = 0; g < p.Hkv; ++g)
-                    units[pos + sp * p.Hkv + g] = make_int4(b, g, sp, ns);
+            const int nqt = (s.q_len + p.item_tokens - 1) / p.item_tokens;
+            for (int qt = 0; qt < nqt; ++qt) {
+                atomicAdd(&hist[min(item_cost(p, s, qt), COST_BUCKETS - 1)], p.Hkv);
+                atomicAdd(&total, p.Hkv);
+            }
         }
-        __syncthreads();
+    }
+    __syncthreads();
+    if (total > p.max_items) {
         if (tid == 0) {
-            hdr[0] = total;   // units listed (0 also when nothing to do)
-            hdr[1] = 0;       // next unit to take
-            hdr[2] = 1;       // lengths accepted
+            set_status(p.status, 4);
+            hdr[0] = 0;
+            hdr[1] = 0;
         }
         return;
     }
 
-    // 2. bucket starts, largest cost first: exclusive block scan, thread t
-    //    owning bucket COST_BUCKETS-1-t
+    // 4. bucket starts, largest cost first: thread t owns bucket COST_BUCKETS-1-t
     {
-        __shared__ int warp_sum[SCHED_THREADS / 32];
-        const int c = COST_BUCKETS - 1 - tid, lane = tid & 31, w = tid >> 5;
+        const int c = COST_BUCKETS - 1 - tid;
         const int h = hist[c];
-        int x = h;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) warp_sum[w] = x;
-        __syncthreads();
-        if (w == 0) {
-            int s = warp_sum[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += y;
-            }
-            warp_sum[lane] = s;   // inclusive prefix over warps
-        }
-        __syncthreads();
-        const int before = (w > 0 ? warp_sum[w - 1] : 0) + x - h;
+        int all;
+        const int before = block_excl_scan(h, warp_sum, &all);
         hist[c] = before;
-        if (tid == SCHED_THREADS - 1) {
-            hdr[0] = before + h;
+        if (tid == 0) {
+            hdr[0] = all;
             hdr[1] = 0;
         }
     }
     __syncthreads();
 
-    // 3. scatter items into their sorted positions
-    for (int b = tid; b < p.B; b += SCHED_THREADS) {
-        SeqInfo s = seq_info(p, b);
-        const int nqt = (s.q_len + p.item_tokens - 1) / p.item_tokens;
-        for (int qt = nqt - 1; qt >= 0; --qt) {
-            int cost = item_cost(p, s, qt);
-            int c = min(cost, COST_BUCKETS - 1);
-            int pos = atomicAdd(&hist[c], p.Hkv);
+    // 5. scatter items into their sorted positions
+    if (par) {
+        for (int i = tid; i < nblocks; i += SCHED_THREADS) {
+            int b, qt;
+            locate(i, b, qt);
+            const SeqInfo s = seq_info(p, b);
+            const int cost = item_cost(p, s, qt);
+            const int pos = atomicAdd(&hist[min(cost, COST_BUCKETS - 1)], p.Hkv);
             for (int g = 0; g < p.Hkv; ++g) items[pos + g] = make_int4(b, qt, g, cost);
+        }
+    } else {
+        for (int b = tid; b < p.B; b += SCHED_THREADS) {
+            const SeqInfo s = seq_info(p, b);
+            const int nqt = (s.q_len + p.item_tokens - 1) / p.item_tokens;
+            for (int qt = nqt - 1; qt >= 0; --qt) {
+                const int cost = item_cost(p, s, qt);
+                const int pos = atomicAdd(&hist[min(cost, COST_BUCKETS - 1)], p.Hkv);
+                for (int g = 0; g < p.Hkv; ++g) items[pos + g] = make_int4(b, qt, g, cost);
+            }
         }
     }
 }
