@@ -58,6 +58,15 @@ constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
 constexpr float LOG2E = 1.4426950408889634f;
 
+// Work items are handed out dynamically: a CTA's first item is its block
+// index, every later one comes from a global counter (the work list's
+// second header word, cleared by the scheduler), so that a CTA that drew
+// short items takes more of them.  The producer warp draws the index and
+// passes it to the other roles through a ring of IRING slots in shared
+// memory.
+constexpr int IRING = 4;
+constexpr int ITEM_CONSUMERS = 1 + 8;   // the MMA thread and the 8 softmax warps
+
 template <int D>
 struct PfLayout {
     static constexpr int KST = D == 128 ? 2 : 3;         // K ring stages
@@ -73,8 +82,9 @@ struct PfLayout {
     static constexpr int STG_WARP = 32 * 128;
     static constexpr int BAR_OFF = STG_OFF + 8 * STG_WARP;
     // barriers: q_full, q_empty, k_full[KST], k_empty[KST], v_full[VST],
-    // v_empty[VST], s_full[2], p_full[2], o_done[2], v_part
-    static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 7;
+    // v_empty[VST], s_full[2], p_full[2], o_done[2], v_part,
+    // item_full[IRING], item_empty[IRING]
+    static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 7 + 2 * IRING;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int BYTES = MISC_OFF + 64;
     // room to align the base to 1024; at least 120 KB so that only one CTA
@@ -85,7 +95,8 @@ struct PfLayout {
 
 struct PfBars {
     uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full,
-        *o_done, *v_part;
+        *o_done, *v_part, *item_full, *item_empty;
+    volatile int *ring;   // IRING item indices
 };
 
 template <int D>
@@ -103,7 +114,27 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *base) {
     r.p_full = r.s_full + 2;
     r.o_done = r.p_full + 2;
     r.v_part = r.o_done + 2;
+    r.item_full = r.v_part + 1;
+    r.item_empty = r.item_full + IRING;
+    r.ring = reinterpret_cast<volatile int *>(base + (L::MISC_OFF - L::BAR_OFF) + 16);
     return r;
+}
+
+// Consumer side of the item ring: the index of this role's n-th item, or
+// -1 when a wait gave up.  One arrival per consumer (a whole softmax warp
+// arrives once, from lane 0).
+__device__ __forceinline__ int next_item(const PfBars &bar, uint32_t n, volatile int *abort,
+                                         bool warp_consumer) {
+    const int slot = n % IRING;
+    if (!mbar_wait(&bar.item_full[slot], (n / IRING) & 1, abort)) return -1;
+    const int idx = bar.ring[slot];
+    if (warp_consumer) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&bar.item_empty[slot]);
+    } else {
+        mbar_arrive(&bar.item_empty[slot]);
+    }
+    return idx;
 }
 
 // Per-item geometry, computed identically by every role.
@@ -191,7 +222,19 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
     const uint32_t q_bytes = (uint32_t)(2 * L::NBLK * p.G * p.tq * 128);
     const uint32_t kv_bytes = (uint32_t)L::TILE;
     uint32_t kc = 0, vc = 0, qc = 0, vpc = 0;   // running ring / barrier counters
-    for (int idx = blockIdx.x; idx < n_items && !*abort; idx += gridDim.x) {
+    int *counter = reinterpret_cast<int *>(p.ws) + 1;
+    int next = blockIdx.x;                      // lane 0: the next item to hand out
+    for (uint32_t n = 0; !*abort; ++n) {
+        const int slot = n % IRING;
+        if (n >= IRING && !mbar_wait(&bar.item_empty[slot], ((n / IRING) - 1) & 1, abort)) break;
+        const int idx = __shfl_sync(0xffffffffu, next, 0);
+        if (lane == 0) {
+            bar.ring[slot] = idx;
+            mbar_arrive(&bar.item_full[slot]);
+            // draw the following item now; the index is read one item later
+            if (idx < n_items) next = (int)gridDim.x + atomicAdd(counter, 1);
+        }
+        if (idx >= n_items) break;
         const Item m = load_item<MODE>(p, idx);
         if (m.nkt == 0) continue;
         // both Q tiles, once per item, after the previous item's BMM1s
@@ -286,7 +329,9 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint8_t *sm, const
         mma_commit(&bar.o_done[a]);
     };
 
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    for (uint32_t n = 0; ok; ++n) {
+        const int idx = next_item(bar, n, abort, false);
+        if (idx < 0 || idx >= n_items) break;
         const Item m = load_item<MODE>(p, idx);
         if (m.nkt == 0) continue;
         if (!mbar_wait(bar.q_full, qc & 1, abort)) break;
@@ -622,7 +667,9 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
     uint32_t tc = 0, pvw = 0;                        // steps seen, BMM2 completions waited
     bool ok = true, pending = false;
 
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    for (uint32_t n = 0; ok; ++n) {
+        const int idx = next_item(bar, n, abort, true);
+        if (idx < 0 || idx >= n_items) break;
         const Item m = load_item<MODE>(p, idx);
         const int tok = a * TQ + t_row;              // token within the item
         const int i = m.i0 + tok;
@@ -899,6 +946,10 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
             mbar_init(&bar.o_done[s], 1);
         }
         mbar_init(bar.v_part, 1);
+        for (int s = 0; s < IRING; ++s) {
+            mbar_init(&bar.item_full[s], 1);
+            mbar_init(&bar.item_empty[s], ITEM_CONSUMERS);
+        }
         *abort = 0;
         fence_mbar_init();
     }

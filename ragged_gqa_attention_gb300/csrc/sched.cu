@@ -7,7 +7,8 @@
 // number of 128-key tiles the item visits after causal and length
 // skipping.  (The decode kernel validates and lists its own work.)
 //
-// Work-list layout in the workspace: int n_items at byte 0, int4 items from
+// Work-list layout in the workspace: int n_items at byte 0, the attention
+// kernel's next-item counter (cleared here) at byte 4, int4 items from
 // byte WS_HEADER.  On bad lengths it writes RGA_ERR_DEVICE_LENGTHS (4) to
 // the status word and an empty list, so no attention work runs.
 #include "device_common.cuh"
