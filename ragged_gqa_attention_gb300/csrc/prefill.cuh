@@ -58,12 +58,24 @@ constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
 constexpr float LOG2E = 1.4426950408889634f;
 
+// Per-item geometry, computed identically by every role.
+struct Item {
+    int b, qt, g;
+    SeqInfo s;
+    int i0;          // first query token of the item (within the sequence)
+    int ntok;        // valid tokens in the item (<= 2 * TQ)
+    int nkt;         // key tiles visited
+    int ntiles;      // BMM1 steps per tile (2 * nkt for the two-pass quantized softmax)
+};
+
 // Work items are handed out dynamically: a CTA's first item is its block
 // index, every later one comes from a global counter (the work list's
 // second header word, cleared by the scheduler), so that a CTA that drew
 // short items takes more of them.  The producer warp draws the index and
 // passes it to the other roles through a ring of IRING slots in shared
-// memory.
+// memory, each slot holding the whole Item (the producer reads the work
+// list and the sequence lengths; the other roles make no global loads to
+// start an item).
 constexpr int IRING = 4;
 constexpr int ITEM_CONSUMERS = 1 + 8;   // the MMA thread and the 8 softmax warps
 
@@ -86,7 +98,9 @@ struct PfLayout {
     // item_full[IRING], item_empty[IRING]
     static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 7 + 2 * IRING;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int BYTES = MISC_OFF + 64;
+    // misc: TMEM address (+0), abort flag (+8), item ring (+64)
+    static constexpr int RING_OFF = 64;
+    static constexpr int BYTES = MISC_OFF + 256;
     // room to align the base to 1024; at least 120 KB so that only one CTA
     // (and one 512-column TMEM allocation) is resident per SM
     static constexpr int ALLOC = (BYTES + 1024) > 120 * 1024 ? (BYTES + 1024) : 120 * 1024;
@@ -96,7 +110,7 @@ struct PfLayout {
 struct PfBars {
     uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full,
         *o_done, *v_part, *item_full, *item_empty;
-    volatile int *ring;   // IRING item indices
+    Item *ring;   // IRING items
 };
 
 template <int D>
@@ -116,36 +130,27 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *base) {
     r.v_part = r.o_done + 2;
     r.item_full = r.v_part + 1;
     r.item_empty = r.item_full + IRING;
-    r.ring = reinterpret_cast<volatile int *>(base + (L::MISC_OFF - L::BAR_OFF) + 16);
+    static_assert(L::RING_OFF + IRING * sizeof(Item) <= 256, "item ring fits the misc area");
+    r.ring = reinterpret_cast<Item *>(base + (L::MISC_OFF - L::BAR_OFF) + L::RING_OFF);
     return r;
 }
 
-// Consumer side of the item ring: the index of this role's n-th item, or
-// -1 when a wait gave up.  One arrival per consumer (a whole softmax warp
-// arrives once, from lane 0).
-__device__ __forceinline__ int next_item(const PfBars &bar, uint32_t n, volatile int *abort,
-                                         bool warp_consumer) {
+// Consumer side of the item ring: this role's n-th item; false at the end
+// of the work (an item with b < 0) or when a wait gave up.  One arrival per
+// consumer (a whole softmax warp arrives once, from lane 0).
+__device__ __forceinline__ bool next_item(const PfBars &bar, uint32_t n, volatile int *abort,
+                                          bool warp_consumer, Item &m) {
     const int slot = n % IRING;
-    if (!mbar_wait(&bar.item_full[slot], (n / IRING) & 1, abort)) return -1;
-    const int idx = bar.ring[slot];
+    if (!mbar_wait(&bar.item_full[slot], (n / IRING) & 1, abort)) return false;
+    m = bar.ring[slot];
     if (warp_consumer) {
         __syncwarp();
         if ((threadIdx.x & 31) == 0) mbar_arrive(&bar.item_empty[slot]);
     } else {
         mbar_arrive(&bar.item_empty[slot]);
     }
-    return idx;
+    return m.b >= 0;
 }
-
-// Per-item geometry, computed identically by every role.
-struct Item {
-    int b, qt, g;
-    SeqInfo s;
-    int i0;          // first query token of the item (within the sequence)
-    int ntok;        // valid tokens in the item (<= 2 * TQ)
-    int nkt;         // key tiles visited
-    int ntiles;      // BMM1 steps per tile (2 * nkt for the two-pass quantized softmax)
-};
 
 template <int MODE>
 __device__ __forceinline__ Item load_item(const AttnParams &p, int idx) {
@@ -228,14 +233,16 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
         const int slot = n % IRING;
         if (n >= IRING && !mbar_wait(&bar.item_empty[slot], ((n / IRING) - 1) & 1, abort)) break;
         const int idx = __shfl_sync(0xffffffffu, next, 0);
+        Item m;
+        if (idx < n_items) m = load_item<MODE>(p, idx);
+        else m.b = -1;                          // end of the work
         if (lane == 0) {
-            bar.ring[slot] = idx;
+            bar.ring[slot] = m;
             mbar_arrive(&bar.item_full[slot]);
             // draw the following item now; the index is read one item later
             if (idx < n_items) next = (int)gridDim.x + atomicAdd(counter, 1);
         }
         if (idx >= n_items) break;
-        const Item m = load_item<MODE>(p, idx);
         if (m.nkt == 0) continue;
         // both Q tiles, once per item, after the previous item's BMM1s
         if (qc > 0 && !mbar_wait(bar.q_empty, (qc - 1) & 1, abort)) break;
@@ -298,96 +305,120 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
 // ------------------------------------------------------------------ MMA issuer
 // One thread issues every tcgen05.mma, in the order
 //   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
+// An MMA issue returns only once the tensor pipe can take it (about one
+// MMA ahead of execution), and this thread shares its SMSP with busy
+// softmax warps, so each instruction it runs between two GEMMs can leave
+// the pipe idle.  The loop keeps that hand-over short: descriptors and
+// TMEM addresses are plain additions of constants, and the barriers the
+// next step starts with (P_0 and the V tile) are tested before the last
+// MMA of S_1, while the queued MMAs still keep the pipe busy.
 template <int D, int MODE, bool BF16>
 __device__ __forceinline__ void mma_role(const AttnParams &p, uint8_t *sm, const PfBars &bar,
-                         volatile int *abort, int n_items, uint32_t tmem) {
+                         volatile int *abort, uint32_t tmem) {
     using L = PfLayout<D>;
     constexpr uint32_t ID_S = idesc_f16(BF16 ? 1 : 0, 128, BN, 0, 0);   // Q K-major, K K-major
     constexpr uint32_t ID_O = idesc_f16(BF16 ? 1 : 0, 128, D, 0, 1);    // P from TMEM, V MN-major
-    const uint32_t q_base = smem_u32(sm + L::Q_OFF);
-    const uint32_t k_base = smem_u32(sm + L::K_OFF);
-    const uint32_t v_base = smem_u32(sm + L::V_OFF);
-    uint32_t kc = 0, vc = 0, qc = 0, tc = 0;   // tc: BMM1 steps per tile, running
+    constexpr int NS = D / 16;      // MMAs of one BMM1 (16 of the head dimension each)
+    constexpr int NO = BN / 16;     // MMAs of one BMM2 (16 keys each)
+    // A descriptor's start-address field holds addr >> 4, so a byte offset
+    // o moves a descriptor by o >> 4 (every address stays below 256 KB).
+    constexpr uint64_t TILE16 = L::TILE >> 4;
+    const uint64_t dq0 = sdesc(smem_u32(sm + L::Q_OFF), 16, 1024);
+    const uint64_t dk0 = sdesc(smem_u32(sm + L::K_OFF), 16, 1024);
+    const uint64_t dv0 = sdesc(smem_u32(sm + L::V_OFF), L::BLK, 1024);
+    uint32_t kc = 0, vc = 0, qc = 0, tc = 0;   // ring counters; tc: BMM1 steps per tile, running
     bool ok = true;
 
-    auto bmm1 = [&](int a, uint32_t kb) {
-        const uint32_t qb = q_base + a * L::TILE;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::BLK + (kk & 3) * 32;
-            mma_ss(tmem + S_COL0 + a * 128, sdesc(qb + off, 16, 1024), sdesc(kb + off, 16, 1024),
-                   ID_S, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar.s_full[a]);
+    // k-step kk of S_a = Q_a K^T: 16 columns of the 128-byte swizzled rows,
+    // four k-steps per 64-column block
+    auto s_mma = [&](int a, uint64_t dk, int kk) {
+        const uint64_t off = (uint64_t)(((kk >> 2) * L::BLK + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + S_COL0 + a * 128, dq0 + a * TILE16 + off, dk + off, ID_S, kk > 0 ? 1u : 0u);
     };
-    auto bmm2 = [&](int a, uint32_t vb, bool first) {
-        const uint32_t pa = tmem + S_COL0 + a * 128;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + O_COL0 + a * D, pa + kk * 8, sdesc(vb + kk * 2048, L::BLK, 1024), ID_O,
-                   (!first || kk > 0) ? 1u : 0u);
-        mma_commit(&bar.o_done[a]);
+    // k-step kk of O_a (+)= P_a V: 16 keys, i.e. 8 packed TMEM columns of
+    // P_a and 16 rows (2 KB) of the MN-major V tile
+    auto o_mma = [&](int a, uint64_t dv, int kk, bool acc) {
+        mma_ts(tmem + O_COL0 + a * D, tmem + S_COL0 + a * 128 + kk * 8,
+               dv + (uint64_t)((kk * 2048) >> 4), ID_O, acc ? 1u : 0u);
     };
 
     for (uint32_t n = 0; ok; ++n) {
-        const int idx = next_item(bar, n, abort, false);
-        if (idx < 0 || idx >= n_items) break;
-        const Item m = load_item<MODE>(p, idx);
+        Item m;
+        if (!next_item(bar, n, abort, false, m)) break;
         if (m.nkt == 0) continue;
         if (!mbar_wait(bar.q_full, qc & 1, abort)) break;
         ++qc;
-        tc_fence_after();
         // S0(0), S1(0)
+        int ks = kc % L::KST;
+        if (!mbar_wait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) break;
+        tc_fence_after();
         {
-            const int ks = kc % L::KST;
-            if (!mbar_wait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) break;
-            tc_fence_after();
-            const uint32_t kb = k_base + ks * L::TILE;
-            bmm1(0, kb);
-            bmm1(1, kb);
+            const uint64_t dk = dk0 + ks * TILE16;
+#pragma unroll
+            for (int kk = 0; kk < NS; ++kk) s_mma(0, dk, kk);
+            mma_commit(&bar.s_full[0]);
+#pragma unroll
+            for (int kk = 0; kk < NS; ++kk) s_mma(1, dk, kk);
+            mma_commit(&bar.s_full[1]);
             mma_commit(&bar.k_empty[ks]);
             ++kc;
             if (m.ntiles == 1) mma_commit(bar.q_empty);
         }
-        int u = 0;   // BMM2 steps of this item
-        for (int t = 0; t < m.ntiles && ok; ++t) {
+        int u = 0;                                // BMM2 steps of this item
+        bool p0_ready = false, v_ready = false;   // found complete ahead of time
+        for (int t = 0; t < m.ntiles; ++t) {
             const bool pv = is_pv<MODE>(m, t);
             const bool more = t + 1 < m.ntiles;
-            uint32_t vb = 0;
-            if (pv) {
-                const int vs = vc % L::VST;
-                if (!mbar_wait(&bar.v_full[vs], (vc / L::VST) & 1, abort)) { ok = false; break; }
-                vb = v_base + vs * L::TILE;
+            const int vs = vc % L::VST;
+            const uint64_t dv = dv0 + vs * TILE16;
+            if (pv && !v_ready && !mbar_wait(&bar.v_full[vs], (vc / L::VST) & 1, abort)) { ok = false; break; }
+            // P_0(t) ready (or, for a statistics step, S_0(t) consumed)
+            if (!p0_ready && !mbar_wait(&bar.p_full[0], tc & 1, abort)) { ok = false; break; }
+            tc_fence_after();
+            if (pv) {                             // PV0(t)
+#pragma unroll
+                for (int kk = 0; kk < NO; ++kk) o_mma(0, dv, kk, u > 0 || kk > 0);
+                mma_commit(&bar.o_done[0]);
             }
-            uint32_t kb = 0;
-            int ks = 0;
-            for (int a = 0; a < 2; ++a) {
-                // P_a(t) ready (or, for a statistics step, S_a(t) consumed)
-                if (!mbar_wait(&bar.p_full[a], tc & 1, abort)) { ok = false; break; }
+            ks = kc % L::KST;
+            const uint64_t dk = dk0 + ks * TILE16;
+            if (more) {                           // S0(t+1)
+                if (!mbar_wait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) { ok = false; break; }
                 tc_fence_after();
-                if (pv) bmm2(a, vb, u == 0);
-                if (more) {
-                    if (a == 0) {
-                        ks = kc % L::KST;
-                        if (!mbar_wait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) { ok = false; break; }
-                        tc_fence_after();
-                        kb = k_base + ks * L::TILE;
-                    }
-                    bmm1(a, kb);
-                }
+#pragma unroll
+                for (int kk = 0; kk < NS; ++kk) s_mma(0, dk, kk);
+                mma_commit(&bar.s_full[0]);
             }
-            if (!ok) break;
-            if (pv) {
-                mma_commit(&bar.v_empty[vc % L::VST]);
+            if (!mbar_wait(&bar.p_full[1], tc & 1, abort)) { ok = false; break; }
+            tc_fence_after();
+            if (pv) {                             // PV1(t); V(t) is free once it completes
+#pragma unroll
+                for (int kk = 0; kk < NO; ++kk) o_mma(1, dv, kk, u > 0 || kk > 0);
+                mma_commit(&bar.o_done[1]);
+                mma_commit(&bar.v_empty[vs]);
                 ++vc;
                 ++u;
             }
-            if (more) {
+            ++tc;
+            p0_ready = v_ready = false;
+            if (more) {                           // S1(t+1)
+#pragma unroll
+                for (int kk = 0; kk < NS; ++kk) {
+                    if (kk == NS - 1) {
+                        // neither barrier can run a phase past these tests:
+                        // their next phases need S_0(t+2) and the release
+                        // of V(t+1), both still to come from this thread
+                        p0_ready = mbar_test(smem_u32(&bar.p_full[0]), tc & 1);
+                        v_ready = !is_pv<MODE>(m, t + 1) ||
+                                  mbar_test(smem_u32(&bar.v_full[vc % L::VST]), (vc / L::VST) & 1);
+                    }
+                    s_mma(1, dk, kk);
+                }
+                mma_commit(&bar.s_full[1]);
                 mma_commit(&bar.k_empty[ks]);
                 ++kc;
                 if (t + 1 == m.ntiles - 1) mma_commit(bar.q_empty);
             }
-            ++tc;
         }
     }
 }
@@ -668,9 +699,8 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
     bool ok = true, pending = false;
 
     for (uint32_t n = 0; ok; ++n) {
-        const int idx = next_item(bar, n, abort, true);
-        if (idx < 0 || idx >= n_items) break;
-        const Item m = load_item<MODE>(p, idx);
+        Item m;
+        if (!next_item(bar, n, abort, true, m)) break;
         const int tok = a * TQ + t_row;              // token within the item
         const int i = m.i0 + tok;
         const int h = m.g * G + hh;
@@ -978,7 +1008,7 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     }
     if (warp < 8) {
     } else if (warp == 8) {
-        if (lane == 0) mma_role<D, MODE, BF16>(p, sm, bar, abort, n_items, tmem);
+        if (lane == 0) mma_role<D, MODE, BF16>(p, sm, bar, abort, tmem);
         __syncwarp();
     } else if (warp == 9) {
         producer_role<D, MODE>(p, tm, sm, bar, abort, n_items);
