@@ -77,7 +77,7 @@ struct Item {
 // list and the sequence lengths; the other roles make no global loads to
 // start an item).
 constexpr int IRING = 4;
-constexpr int ITEM_CONSUMERS = 1 + 8;   // the MMA thread and the 8 softmax warps
+constexpr int ITEM_CONSUMERS = 1 + 8;   // the MMA warp and the 8 softmax warps
 
 template <int D>
 struct PfLayout {
@@ -303,15 +303,17 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
 }
 
 // ------------------------------------------------------------------ MMA issuer
-// One thread issues every tcgen05.mma, in the order
+// One warp issues every tcgen05.mma, in the order
 //   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
-// An MMA issue returns only once the tensor pipe can take it (about one
-// MMA ahead of execution), and this thread shares its SMSP with busy
-// softmax warps, so each instruction it runs between two GEMMs can leave
-// the pipe idle.  The loop keeps that hand-over short: descriptors and
-// TMEM addresses are plain additions of constants, and the barriers the
-// next step starts with (P_0 and the V tile) are tested before the last
-// MMA of S_1, while the queued MMAs still keep the pipe busy.
+// The whole warp runs this code, converged, and one elected lane issues
+// each MMA and commit: issuing from a single diverged lane instead costs
+// about a third more time per MMA, and more again while the softmax warps
+// sharing this warp's scheduler are busy.  Every wait result is taken from
+// lane 0 so that all branches stay warp-uniform.  The hand-over from one
+// GEMM to the next is kept short: descriptors and TMEM addresses are plain
+// additions of constants, and the barriers the next step starts with (P_0
+// and the V tile) are tested before the last MMA of S_1, while the queued
+// MMAs still keep the pipe busy.
 template <int D, int MODE, bool BF16>
 __device__ __forceinline__ void mma_role(const AttnParams &p, uint8_t *sm, const PfBars &bar,
                          volatile int *abort, uint32_t tmem) {
@@ -328,41 +330,47 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint8_t *sm, const
     const uint64_t dv0 = sdesc(smem_u32(sm + L::V_OFF), L::BLK, 1024);
     uint32_t kc = 0, vc = 0, qc = 0, tc = 0;   // ring counters; tc: BMM1 steps per tile, running
     bool ok = true;
+    auto wwait = [&](uint64_t *b, uint32_t parity, volatile int *ab) -> bool {
+        return __shfl_sync(0xffffffffu, mbar_wait(b, parity, ab) ? 1 : 0, 0) != 0;
+    };
+    auto wtest = [&](uint32_t b, uint32_t parity) -> bool {
+        return __shfl_sync(0xffffffffu, mbar_test(b, parity) ? 1 : 0, 0) != 0;
+    };
 
     // k-step kk of S_a = Q_a K^T: 16 columns of the 128-byte swizzled rows,
     // four k-steps per 64-column block
     auto s_mma = [&](int a, uint64_t dk, int kk) {
         const uint64_t off = (uint64_t)(((kk >> 2) * L::BLK + (kk & 3) * 32) >> 4);
-        mma_ss(tmem + S_COL0 + a * 128, dq0 + a * TILE16 + off, dk + off, ID_S, kk > 0 ? 1u : 0u);
+        mma_ss_w(tmem + S_COL0 + a * 128, dq0 + a * TILE16 + off, dk + off, ID_S, kk > 0 ? 1u : 0u);
     };
     // k-step kk of O_a (+)= P_a V: 16 keys, i.e. 8 packed TMEM columns of
     // P_a and 16 rows (2 KB) of the MN-major V tile
     auto o_mma = [&](int a, uint64_t dv, int kk, bool acc) {
-        mma_ts(tmem + O_COL0 + a * D, tmem + S_COL0 + a * 128 + kk * 8,
+        mma_ts_w(tmem + O_COL0 + a * D, tmem + S_COL0 + a * 128 + kk * 8,
                dv + (uint64_t)((kk * 2048) >> 4), ID_O, acc ? 1u : 0u);
     };
 
     for (uint32_t n = 0; ok; ++n) {
         Item m;
-        if (!next_item(bar, n, abort, false, m)) break;
+        if (!next_item(bar, n, abort, true, m)) break;
         if (m.nkt == 0) continue;
-        if (!mbar_wait(bar.q_full, qc & 1, abort)) break;
+        if (!wwait(bar.q_full, qc & 1, abort)) break;
         ++qc;
         // S0(0), S1(0)
         int ks = kc % L::KST;
-        if (!mbar_wait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) break;
+        if (!wwait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) break;
         tc_fence_after();
         {
             const uint64_t dk = dk0 + ks * TILE16;
 #pragma unroll
             for (int kk = 0; kk < NS; ++kk) s_mma(0, dk, kk);
-            mma_commit(&bar.s_full[0]);
+            mma_commit_w(&bar.s_full[0]);
 #pragma unroll
             for (int kk = 0; kk < NS; ++kk) s_mma(1, dk, kk);
-            mma_commit(&bar.s_full[1]);
-            mma_commit(&bar.k_empty[ks]);
+            mma_commit_w(&bar.s_full[1]);
+            mma_commit_w(&bar.k_empty[ks]);
             ++kc;
-            if (m.ntiles == 1) mma_commit(bar.q_empty);
+            if (m.ntiles == 1) mma_commit_w(bar.q_empty);
         }
         int u = 0;                                // BMM2 steps of this item
         bool p0_ready = false, v_ready = false;   // found complete ahead of time
@@ -371,31 +379,31 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint8_t *sm, const
             const bool more = t + 1 < m.ntiles;
             const int vs = vc % L::VST;
             const uint64_t dv = dv0 + vs * TILE16;
-            if (pv && !v_ready && !mbar_wait(&bar.v_full[vs], (vc / L::VST) & 1, abort)) { ok = false; break; }
+            if (pv && !v_ready && !wwait(&bar.v_full[vs], (vc / L::VST) & 1, abort)) { ok = false; break; }
             // P_0(t) ready (or, for a statistics step, S_0(t) consumed)
-            if (!p0_ready && !mbar_wait(&bar.p_full[0], tc & 1, abort)) { ok = false; break; }
+            if (!p0_ready && !wwait(&bar.p_full[0], tc & 1, abort)) { ok = false; break; }
             tc_fence_after();
             if (pv) {                             // PV0(t)
 #pragma unroll
                 for (int kk = 0; kk < NO; ++kk) o_mma(0, dv, kk, u > 0 || kk > 0);
-                mma_commit(&bar.o_done[0]);
+                mma_commit_w(&bar.o_done[0]);
             }
             ks = kc % L::KST;
             const uint64_t dk = dk0 + ks * TILE16;
             if (more) {                           // S0(t+1)
-                if (!mbar_wait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) { ok = false; break; }
+                if (!wwait(&bar.k_full[ks], (kc / L::KST) & 1, abort)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < NS; ++kk) s_mma(0, dk, kk);
-                mma_commit(&bar.s_full[0]);
+                mma_commit_w(&bar.s_full[0]);
             }
-            if (!mbar_wait(&bar.p_full[1], tc & 1, abort)) { ok = false; break; }
+            if (!wwait(&bar.p_full[1], tc & 1, abort)) { ok = false; break; }
             tc_fence_after();
             if (pv) {                             // PV1(t); V(t) is free once it completes
 #pragma unroll
                 for (int kk = 0; kk < NO; ++kk) o_mma(1, dv, kk, u > 0 || kk > 0);
-                mma_commit(&bar.o_done[1]);
-                mma_commit(&bar.v_empty[vs]);
+                mma_commit_w(&bar.o_done[1]);
+                mma_commit_w(&bar.v_empty[vs]);
                 ++vc;
                 ++u;
             }
@@ -408,16 +416,16 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint8_t *sm, const
                         // neither barrier can run a phase past these tests:
                         // their next phases need S_0(t+2) and the release
                         // of V(t+1), both still to come from this thread
-                        p0_ready = mbar_test(smem_u32(&bar.p_full[0]), tc & 1);
+                        p0_ready = wtest(smem_u32(&bar.p_full[0]), tc & 1);
                         v_ready = !is_pv<MODE>(m, t + 1) ||
-                                  mbar_test(smem_u32(&bar.v_full[vc % L::VST]), (vc / L::VST) & 1);
+                                  wtest(smem_u32(&bar.v_full[vc % L::VST]), (vc / L::VST) & 1);
                     }
                     s_mma(1, dk, kk);
                 }
-                mma_commit(&bar.s_full[1]);
-                mma_commit(&bar.k_empty[ks]);
+                mma_commit_w(&bar.s_full[1]);
+                mma_commit_w(&bar.k_empty[ks]);
                 ++kc;
-                if (t + 1 == m.ntiles - 1) mma_commit(bar.q_empty);
+                if (t + 1 == m.ntiles - 1) mma_commit_w(bar.q_empty);
             }
         }
     }
@@ -1008,8 +1016,7 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     }
     if (warp < 8) {
     } else if (warp == 8) {
-        if (lane == 0) mma_role<D, MODE, BF16>(p, sm, bar, abort, tmem);
-        __syncwarp();
+        mma_role<D, MODE, BF16>(p, sm, bar, abort, tmem);
     } else if (warp == 9) {
         producer_role<D, MODE>(p, tm, sm, bar, abort, n_items);
     }
