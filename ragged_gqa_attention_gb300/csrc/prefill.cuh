@@ -56,6 +56,7 @@ static_assert(2 * 128 * PF_SOFTMAX_REGS + 128 * PF_AUX_REGS <= PF_THREADS * PF_L
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t S_COL0 = 0, O_COL0 = 256;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
+constexpr float RESCALE_SUM = 256.0f;       // 2^RESCALE_THRESHOLD
 constexpr float LOG2E = 1.4426950408889634f;
 
 // Per-item geometry, computed identically by every role.
@@ -655,17 +656,24 @@ __device__ __forceinline__ void store_rows(const AttnParams &p, const TensorMaps
     }
 }
 
-// One 32-column chunk of a full tile: p = 2^(s * mul - ref) packed to 16-bit
-// pairs into TMEM columns [16c, 16c+16) of the S buffer; returns the raw
-// chunk max and accumulates the sum of p.
-template <bool BF16>
-__device__ __forceinline__ float p_chunk(const uint32_t (&r)[32], uint32_t s_addr, int c,
-                                         uint64_t mul2, uint64_t neg2, uint64_t &acc0,
-                                         uint64_t &acc1) {
+// Largest of 32 scores held as raw bits.
+__device__ __forceinline__ float reg_max(const uint32_t (&r)[32]) {
     float v[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
-    const float mx = chunk_max(v);
+    return chunk_max(v);
+}
+
+// One 32-column chunk of a full tile: p = 2^(s * mul - ref) packed to 16-bit
+// pairs into TMEM columns [16c, 16c+16) of the S buffer; accumulates the
+// sum of p.
+template <bool BF16>
+__device__ __forceinline__ void p_chunk(const uint32_t (&r)[32], uint32_t s_addr, int c,
+                                        uint64_t mul2, uint64_t neg2, uint64_t &acc0,
+                                        uint64_t &acc1) {
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
     uint32_t w[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
@@ -678,7 +686,6 @@ __device__ __forceinline__ float p_chunk(const uint32_t (&r)[32], uint32_t s_add
         w[k] = pack2<BF16>(pa, pb);
     }
     tmem_st16(s_addr + c * 16, w);
-    return mx;
 }
 
 template <int D, int MODE, bool BF16>
@@ -750,14 +757,28 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                 tmem_ld32(s_addr + 64, rb[0]);
                 tmem_ld32(s_addr + 96, rb[1]);
                 uint64_t acc0 = 0, acc1 = 0;
-                float mraw = p_chunk<BF16>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
-                mraw = fmaxf(mraw, p_chunk<BF16>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1));
+                p_chunk<BF16>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
+                p_chunk<BF16>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1);
                 tmem_wait_ld();
-                mraw = fmaxf(mraw, p_chunk<BF16>(rb[0], s_addr, 2, mul2, neg2, acc0, acc1));
-                mraw = fmaxf(mraw, p_chunk<BF16>(rb[1], s_addr, 3, mul2, neg2, acc0, acc1));
-                const float mx = row_ok ? mraw * sc : -INFINITY;
-                float alpha = 1.f;
-                const bool need = mx > m_ref + RESCALE_THRESHOLD;
+                p_chunk<BF16>(rb[0], s_addr, 2, mul2, neg2, acc0, acc1);
+                p_chunk<BF16>(rb[1], s_addr, 3, mul2, neg2, acc0, acc1);
+                // No probability can pass 2^threshold while their sum stays
+                // below it, so the row max is only needed (to decide on a
+                // new reference) when the sum is that large.
+                float alpha = 1.f, mx = -INFINITY;
+                bool need = false;
+                {
+                    float s0, s1, s2, s3;
+                    f2_unpack(acc0, s0, s1);
+                    f2_unpack(acc1, s2, s3);
+                    const bool big = row_ok && !((s0 + s1) + (s2 + s3) <= RESCALE_SUM);
+                    if (__any_sync(0xffffffffu, big)) {
+                        const float mraw = fmaxf(fmaxf(reg_max(ra[0]), reg_max(ra[1])),
+                                                 fmaxf(reg_max(rb[0]), reg_max(rb[1])));
+                        mx = row_ok ? mraw * sc : -INFINITY;
+                        need = mx > m_ref + RESCALE_THRESHOLD;
+                    }
+                }
                 if (__any_sync(0xffffffffu, need)) {   // rare: redo with the new reference
                     if (need) {
                         alpha = ex2(m_ref - mx);
