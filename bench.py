@@ -13,7 +13,8 @@ decode in KV GB/s, quantized P) are reported under "workloads".
 Prints one JSON line (rank 0).  Inputs are synthetic (seeded) and resident
 in HBM for ``value``; ``e2e`` times the same call from pinned host buffers
 with the host<->device copies inside the timed region.  L2 is flushed
-(a 256 MiB write) between timed iterations.
+between timed iterations (a 256 MiB write, then a 256 MiB read that leaves
+no dirty lines behind).
 """
 from __future__ import annotations
 
@@ -184,11 +185,22 @@ def max_over_ranks(x, dist_on):
 
 
 def device_timed(run, stream, steps, warmup, dist_on, sampler_index=None):
-    """Per-step CUDA-event durations (ms) with an L2 flush between steps."""
+    """Per-step CUDA-event durations (ms) with an L2 flush between steps.
+
+    The flush writes a 256 MiB buffer (twice L2) and then reads another one,
+    so that each timed call starts with none of its inputs in L2 and without
+    the flush's dirty lines, whose write-back would otherwise be charged to
+    the call."""
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")   # 256 MiB
+    clean = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device="cuda")   # 256 MiB
+    sink = torch.empty(1, dtype=torch.float32, device="cuda")
+
+    def l2_flush():
+        flush.zero_()
+        torch.sum(clean, dim=0, out=sink)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            flush.zero_()
+            l2_flush()
             run()
     barrier(dist_on)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -198,7 +210,7 @@ def device_timed(run, stream, steps, warmup, dist_on, sampler_index=None):
         sampler.__enter__()
     with torch.cuda.stream(stream):
         for s, e in ev:
-            flush.zero_()
+            l2_flush()
             s.record(stream)
             run()
             e.record(stream)
@@ -387,7 +399,7 @@ def main():
             "config": {"workload": case.name, "batch": case.batch, "q_heads": case.q_heads,
                        "kv_heads": case.kv_heads, "head_dim": case.head_dim,
                        "q_tokens": sum(case.q_lens), "kv_tokens": sum(case.kv_lens),
-                       "causal": case.causal, "l2": "flushed (256 MiB write) between steps",
+                       "causal": case.causal, "l2": "flushed between steps (256 MiB written, then 256 MiB read)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": head["bound"], "achieved": round(head["value"], 3),
                          "peak": head["peak"], "unit": head["unit"],
