@@ -78,13 +78,25 @@ bool encode_kv(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t r
     return encode(m, base, 4, d, b);
 }
 
-// Decode (split-KV) path: short query rows per (batch, KV head), no Q/DQ.
+// Bound on the decode work pairs (batch, KV head, chunk of DEC_ROWS query
+// rows): one chunk per batch for padded Q (at most DEC_ROWS rows), and at
+// most B + q_seq*G/DEC_ROWS chunks over all batches for packed Q.
+static int64_t dec_max_pairs(int64_t B, int64_t Hkv, int64_t G, int64_t q_seq, bool packed) {
+    const int64_t chunks = packed ? B + (q_seq * G + DEC_ROWS - 1) / DEC_ROWS : B;
+    return Hkv * chunks;
+}
+
+// Decode (split-KV) path: short query rows per (batch, KV head), no Q/DQ,
+// and every key tile of the work countable in 32 bits.
 bool use_decode(const rga_attention_args *a, bool quant) {
     if (quant || a->batch > DEC_MAX_B) return false;
     const int G = a->q_heads / a->kv_heads;
     if (G > DEC_ROWS) return false;
-    if (a->q_form == RGA_FORM_PACKED_NHD) return a->q_seq <= a->batch;
-    return (int64_t)a->q_seq * G <= DEC_ROWS;
+    const bool packed = a->q_form == RGA_FORM_PACKED_NHD;
+    if (packed ? a->q_seq > a->batch : (int64_t)a->q_seq * G > DEC_ROWS) return false;
+    const int64_t tiles = dec_max_pairs(a->batch, a->kv_heads, G, a->q_seq, packed) *
+                          (((int64_t)a->kv_seq + DEC_KEYS - 1) / DEC_KEYS);
+    return tiles < (int64_t(1) << 31);
 }
 
 rga_status validate(const rga_attention_args *a, bool quant) {
@@ -161,8 +173,8 @@ AttnParams make_params(const rga_attention_args *a, bool quant) {
         p.max_items = p.Hkv * ((p.q_seq + it - 1) / it + p.B);
     else
         p.max_items = p.Hkv * p.B * ((p.q_seq + it - 1) / it);
-    p.max_splits = (p.kv_seq + DEC_SPLIT - 1) / DEC_SPLIT;
-    if (p.max_splits < 1) p.max_splits = 1;
+    p.max_pairs = (int)dec_max_pairs(p.B, p.Hkv, p.G, p.q_seq, p.q_packed != 0);
+    p.dec_slots = 2 * DEC_WARPS * (sm_count() > 0 ? sm_count() : 1);
     p.status = a->device_status;
     p.ws = static_cast<uint8_t *>(a->workspace);
     (void)quant;

@@ -3,21 +3,21 @@
 // vanilla decoding attention) with the TRT_Attention semantics of
 // "TensorRT Custom Operator Schemas".
 //
-// Work unit: (batch b, KV head g, split of DEC_SPLIT keys).  The grid is
-// persistent; each CTA validates the lengths and lists the units itself
-// (no scheduler launch), and every warp is an independent engine: it takes
-// the next unit from an atomic counter, streams the unit's
-// 32-key K/V tiles with TMA through its own DEC_STAGES-deep, 128-byte-
-// swizzled ring, computes S = Q K^T and O += P V with m16n8k16 MMAs (K and
-// V are read once from HBM for all G query heads of the KV head) and keeps
-// an online softmax in fp32 registers.  The query rows of a unit are the
-// (token, head) pairs of the G heads, 16 at a time (one MMA row block).
-// A unit that covers its whole (b, g) pair writes Y; otherwise its partial
-// (O, m, l) goes to the workspace and the last warp to finish a pair
-// (atomic ticket) merges the splits and writes Y.
-//
-// A pair with more than 16 query rows (more than 16/G tokens) is one unit
-// that loops over the row blocks.
+// Work: pairs (batch b, KV head g, chunk of 16 query rows), each with the
+// 32-key tiles of the batch's key extent.  The query rows of a pair are the
+// (token, head) pairs of the G heads of g, 16 at a time (one MMA row block).
+// All tiles of all pairs form one batch-major line that is cut into equal
+// contiguous ranges, one per warp of the persistent grid, so that every
+// warp streams the same number of tiles and none is left finishing a long
+// unit alone at the end.  Each CTA validates the lengths and lays out the
+// line itself (no scheduler launch).  A warp streams its range's K/V tiles
+// with TMA through its own DEC_STAGES-deep, 128-byte-swizzled ring, straight
+// across pair boundaries, computes S = Q K^T and O += P V with m16n8k16 MMAs
+// (K and V are read once from HBM for all G query heads of the KV head) and
+// keeps an online softmax in fp32 registers.  A pair inside one range is
+// written to Y by its warp; a pair cut by range ends leaves a partial
+// (O, m, l) per warp, and the last of its warps to finish (atomic ticket)
+// merges them in warp order and writes Y.
 #include <cuda.h>
 #include "device_common.cuh"
 #include "kernels.h"
@@ -35,8 +35,10 @@ struct DecLayout {
     static constexpr int WARP_RING = DEC_STAGES * STAGE;
     static constexpr int RING = DEC_WARPS * WARP_RING;
     static constexpr int BAR_OFF = RING;
-    static constexpr int BOFF_OFF = BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 64;
-    static constexpr int BYTES = BOFF_OFF + (DEC_MAX_B + 1) * 4 + 64;
+    static constexpr int SCR_OFF = BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 64;   // prefix scratch
+    static constexpr int TPRE_OFF = SCR_OFF + (DEC_THREADS + 1) * 4 + 12;
+    static constexpr int PPRE_OFF = TPRE_OFF + (DEC_MAX_B + 1) * 4;
+    static constexpr int BYTES = PPRE_OFF + (DEC_MAX_B + 1) * 4 + 64;
     static constexpr int ALLOC = BYTES + 1024;
     static_assert(ALLOC <= 232448, "shared memory per CTA");
 };
@@ -210,6 +212,54 @@ __device__ __forceinline__ void dec_store_y(const AttnParams &p, const DecRow (&
     }
 }
 
+// One lane's view of the pair being computed or loaded: a pair is
+// (batch b, KV head g, row chunk rc of DEC_ROWS query rows); its key tiles
+// are the 32-key tiles of [0, key extent of the batch).
+struct DecCur {
+    int b, pib;          // batch, pair within the batch (g * nrc + rc)
+    int tile;            // tile within the pair
+    int nt, nrc;         // tiles per pair, row chunks of the batch
+    SeqInfo s;
+};
+
+// Batch b's row chunks and key tiles per pair (0 chunks: no query rows).
+__device__ __forceinline__ void dec_batch_shape(const AttnParams &p, const SeqInfo &s, int &nrc,
+                                                int &nt) {
+    const int rows = s.q_len * p.G;
+    nrc = (rows + DEC_ROWS - 1) / DEC_ROWS;
+    const int kv_hi = rows > 0 ? key_extent(p.causal, s.q_len - 1, s) : 0;
+    nt = (kv_hi + DEC_KEYS - 1) / DEC_KEYS;
+}
+
+// Block-wide exclusive prefix of v[0..n) in place (n <= DEC_MAX_B), with
+// v[n] set to the total; every thread of the block calls it.
+__device__ __forceinline__ void dec_prefix(int *v, int n, int *scratch) {
+    const int per = (n + DEC_THREADS - 1) / DEC_THREADS;
+    const int lo = threadIdx.x * per, hi = min(n, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += v[i];
+    scratch[threadIdx.x] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int t = 0; t < DEC_THREADS; ++t) {
+            const int x = scratch[t];
+            scratch[t] = run;
+            run += x;
+        }
+        scratch[DEC_THREADS] = run;
+    }
+    __syncthreads();
+    int run = scratch[threadIdx.x];
+    for (int i = lo; i < hi; ++i) {
+        const int x = v[i];
+        v[i] = run;
+        run += x;
+    }
+    if (threadIdx.x == 0) v[n] = scratch[DEC_THREADS];
+    __syncthreads();
+}
+
 template <int D, bool BF16, bool SOFTMAX>
 __global__ void __launch_bounds__(DEC_THREADS, 1)
 decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TensorMaps tm) {
@@ -221,10 +271,12 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
     volatile int *abort = reinterpret_cast<volatile int *>(sm + L::BAR_OFF + DEC_WARPS * DEC_STAGES * 8);
+    int *flags = reinterpret_cast<int *>(sm + L::BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 4);
+    int *scratch = reinterpret_cast<int *>(sm + L::SCR_OFF);
+    int *tpre = reinterpret_cast<int *>(sm + L::TPRE_OFF);   // key tiles before batch b
+    int *ppre = reinterpret_cast<int *>(sm + L::PPRE_OFF);   // pairs before batch b
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    int *boff = reinterpret_cast<int *>(sm + L::BOFF_OFF);    // first unit of each batch
-    int *flags = reinterpret_cast<int *>(sm + L::BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 4);
     if (threadIdx.x == 0) {
         for (int i = 0; i < DEC_WARPS * DEC_STAGES; ++i) mbar_init(&bars[i], 1);
         *abort = 0;
@@ -232,8 +284,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         fence_mbar_init();
     }
     __syncthreads();
-    // Every CTA validates the lengths and lists the units itself: unit u of
-    // batch b is (split, KV head) = ((u - boff[b]) / Hkv, (u - boff[b]) % Hkv).
+    // Every CTA validates the lengths and lays out the work itself.
     for (int b = threadIdx.x; b < p.B; b += DEC_THREADS) {
         const int32_t *ql = p.query_lengths, *kl = p.kv_lengths;
         const SeqInfo s = seq_info(p, b);
@@ -248,58 +299,112 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             if (p.md[3] != 1 && p.md[3] < s.kv_len) ok = false;
         }
         if (!ok) atomicOr(&flags[0], 1);
-        boff[b + 1] = (ok && s.q_len > 0) ? dec_splits(p, s) * p.Hkv : 0;
+        int nrc = 0, nt = 0;
+        if (ok) dec_batch_shape(p, s, nrc, nt);
+        tpre[b] = p.Hkv * nrc * nt;
+        ppre[b] = p.Hkv * nrc;
     }
     __syncthreads();
     if (flags[0]) {
         if (blockIdx.x == 0 && threadIdx.x == 0) set_status(p.status, 4);
         return;
     }
-    if (threadIdx.x == 0) {   // prefix over batches (serial: B is at most DEC_MAX_B)
-        boff[0] = 0;
-        for (int b = 0; b < p.B; ++b) boff[b + 1] += boff[b];
-    }
-    __syncthreads();
-    const int n_units = boff[p.B];
-    pdl_wait();   // the tickets and the unit counter have been cleared
+    dec_prefix(tpre, p.B, scratch);
+    dec_prefix(ppre, p.B, scratch);
+    pdl_wait();   // the tickets have been cleared
+
+    // Stream-K split of the work: all key tiles of all pairs, batch-major,
+    // in one line of T tiles, cut into equal contiguous ranges, one per warp
+    // of the grid.  A pair inside one range is finished by its warp; a pair
+    // cut by range ends is finished by the last of its warps to arrive
+    // (atomic ticket), which merges the others' partials in warp order.
+    const int T = tpre[p.B];
+    const int wg = blockIdx.x * DEC_WARPS + warp;
+    // at most one warp per tile, so that every range holds at least one
+    // (the merge counts a pair's warps from the range ends); later warps idle
+    const int Wn = max(1, min((int)gridDim.x * DEC_WARPS, T));
+    auto range_start = [&](int w) { return (int)((long long)w * T / Wn); };
+    auto warp_of = [&](int x) { return (int)(((long long)(x + 1) * Wn - 1) / T); };
     int *tickets = reinterpret_cast<int *>(p.ws + dec_tickets_off(p));
     float *part = reinterpret_cast<float *>(p.ws + dec_part_off(p));
     float2 *pml = reinterpret_cast<float2 *>(p.ws + dec_ml_off(p));
+
+    // batches with query rows but no key tile: their rows are zero
+    for (int b = wg; b < p.B; b += gridDim.x * DEC_WARPS) {
+        const SeqInfo s = seq_info(p, b);
+        int nrc, nt;
+        dec_batch_shape(p, s, nrc, nt);
+        if (nrc == 0 || nt > 0) continue;
+        const int rows = s.q_len * p.G;
+        for (int r = lane; r < p.Hkv * rows; r += 32) {
+            const DecRow R = dec_row(p, s, b, r / rows, r % rows, rows, 0);
+            uint4 *y = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff);
+            for (int c = 0; c < D / 8; ++c) y[c] = make_uint4(0, 0, 0, 0);
+        }
+    }
 
     uint8_t *ring = sm + warp * L::WARP_RING;
     uint64_t *wbar = bars + warp * DEC_STAGES;
     const uint32_t ring_u32 = smem_u32(ring);
     uint32_t issued = 0, consumed = 0;
+    const int t_begin = wg < Wn ? range_start(wg) : T, t_end = wg < Wn ? range_start(wg + 1) : T;
 
-    int *next_unit = tickets + p.B * p.Hkv;    // cleared with the tickets
-    for (;;) {
-        int u = 0;
-        if (lane == 0) u = atomicAdd(next_unit, 1);
-        u = __shfl_sync(0xffffffffu, u, 0);
-        if (u >= n_units || *abort) break;
-        int lo = 0, hi = p.B;   // boff[lo] <= u < boff[hi]
+    auto locate = [&](int t, DecCur &c) {
+        int lo = 0, hi = p.B;   // tpre[lo] <= t < tpre[lo + 1]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (boff[mid] <= u) lo = mid; else hi = mid;
+            if (tpre[mid] <= t) lo = mid; else hi = mid;
         }
-        const int b = lo;
-        const int g = (u - boff[b]) % p.Hkv, split = (u - boff[b]) / p.Hkv;
-        const int ns = (boff[b + 1] - boff[b]) / p.Hkv;
-        const SeqInfo s = seq_info(p, b);
-        const int rows = s.q_len * p.G;
-        const int kv_hi = key_extent(p.causal, s.q_len - 1, s);
-        const int k0 = split * DEC_SPLIT;
-        const int k1 = (ns == 1) ? kv_hi : min(kv_hi, k0 + DEC_SPLIT);
-        const int ntiles = k1 > k0 ? (k1 - k0 + DEC_KEYS - 1) / DEC_KEYS : 0;
-        const int nrc = (rows + DEC_ROWS - 1) / DEC_ROWS;
-        const size_t unit_idx = ((size_t)b * p.Hkv + g) * p.max_splits + split;
-        bool unit_ok = true;
+        c.b = lo;
+        c.s = seq_info(p, lo);
+        dec_batch_shape(p, c.s, c.nrc, c.nt);
+        const int r = t - tpre[lo];
+        c.pib = r / c.nt;
+        c.tile = r % c.nt;
+    };
+    auto advance = [&](DecCur &c) {   // the next tile of the line
+        if (++c.tile < c.nt) return;
+        c.tile = 0;
+        if (++c.pib < p.Hkv * c.nrc) return;
+        int b = c.b + 1;
+        while (b < p.B && tpre[b + 1] == tpre[b]) ++b;   // batches without tiles
+        if (b >= p.B) return;                              // past the end: never used
+        c.b = b;
+        c.pib = 0;
+        c.s = seq_info(p, b);
+        dec_batch_shape(p, c.s, c.nrc, c.nt);
+    };
+    auto issue = [&](const DecCur &c) {
+        if (lane == 0) {
+            fence_proxy_async_smem();   // the stage's previous tile was read by ldmatrix
+            dec_tma(p, tm, c.s, c.b, c.pib / c.nrc, c.tile * DEC_KEYS,
+                    ring + (issued % DEC_STAGES) * L::STAGE, &wbar[issued % DEC_STAGES], D);
+        }
+        ++issued;
+    };
 
-        for (int rc = 0; rc < nrc && unit_ok; ++rc) {
-            DecRow rr[2];
-            rr[0] = dec_row(p, s, b, g, rc * DEC_ROWS + (lane >> 2), rows, k1);
-            rr[1] = dec_row(p, s, b, g, rc * DEC_ROWS + (lane >> 2) + 8, rows, k1);
-            uint32_t qa[KS][4];
+    bool ok = true;
+    if (t_begin < t_end) {
+        DecCur lc, cc;
+        locate(t_begin, lc);
+        cc = lc;
+        int next_issue = t_begin;
+        for (; next_issue < t_end && next_issue < t_begin + DEC_STAGES; ++next_issue) {
+            issue(lc);
+            advance(lc);
+        }
+        DecRow rr[2];
+        uint32_t qa[KS][4];
+        float o[NT][4];
+        float m_r[2], l_r[2];
+        int seg0 = t_begin;    // first tile of the current pair in this range
+        int kv_hi = 0, rows = 0;
+        auto start_pair = [&]() {
+            const int g = cc.pib / cc.nrc, rc = cc.pib % cc.nrc;
+            rows = cc.s.q_len * p.G;
+            kv_hi = key_extent(p.causal, cc.s.q_len - 1, cc.s);
+            rr[0] = dec_row(p, cc.s, cc.b, g, rc * DEC_ROWS + (lane >> 2), rows, kv_hi);
+            rr[1] = dec_row(p, cc.s, cc.b, g, rc * DEC_ROWS + (lane >> 2) + 8, rows, kv_hi);
             const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
@@ -309,121 +414,128 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                 qa[ks][2] = rr[0].valid ? q32[(rr[0].qoff + col + 8) >> 1] : 0u;
                 qa[ks][3] = rr[1].valid ? q32[(rr[1].qoff + col + 8) >> 1] : 0u;
             }
-            float o[NT][4];
 #pragma unroll
             for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-            float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+            m_r[0] = m_r[1] = -INFINITY;
+            l_r[0] = l_r[1] = 0.f;
+        };
+        start_pair();
 
-            if (lane == 0)
-                for (int it = 0; it < DEC_STAGES && it < ntiles; ++it) {
-                    const uint32_t c = issued + it;
-                    dec_tma(p, tm, s, b, g, k0 + it * DEC_KEYS, ring + (c % DEC_STAGES) * L::STAGE,
-                            &wbar[c % DEC_STAGES], D);
+        for (int t = t_begin; t < t_end; ++t) {
+            const uint32_t c = consumed;
+            const int st = c % DEC_STAGES;
+            if (!mbar_wait(&wbar[st], (c / DEC_STAGES) & 1, abort)) { ok = false; break; }
+            ++consumed;
+            const int j0 = cc.tile * DEC_KEYS;
+            const uint32_t kb = ring_u32 + st * L::STAGE, vb = kb + L::TILE;
+            const int rem = cc.s.kv_len - j0;
+            if (rem < DEC_KEYS) {   // rows past the sequence end may hold NaN: zero them
+                uint8_t *vp = ring + st * L::STAGE + L::TILE;
+                for (int idx = lane; idx < DEC_KEYS * (D / 8); idx += 32) {
+                    const int row = idx / (D / 8), ch = idx % (D / 8);
+                    if (row >= rem)
+                        *reinterpret_cast<uint4 *>(vp + swz(row, ch, L::BLK)) = make_uint4(0, 0, 0, 0);
                 }
-            issued += min(DEC_STAGES, ntiles);
-            for (int it = 0; it < ntiles; ++it) {
-                const uint32_t c = consumed;
-                const int st = c % DEC_STAGES;
-                if (!mbar_wait(&wbar[st], (c / DEC_STAGES) & 1, abort)) { unit_ok = false; break; }
-                ++consumed;
-                const int j0 = k0 + it * DEC_KEYS;
-                const uint32_t kb = ring_u32 + st * L::STAGE, vb = kb + L::TILE;
-                const int rem = s.kv_len - j0;
-                if (rem < DEC_KEYS) {   // rows past the sequence end may hold NaN: zero them
-                    uint8_t *vp = ring + st * L::STAGE + L::TILE;
-                    for (int idx = lane; idx < DEC_KEYS * (D / 8); idx += 32) {
-                        const int row = idx / (D / 8), ch = idx % (D / 8);
-                        if (row >= rem)
-                            *reinterpret_cast<uint4 *>(vp + swz(row, ch, L::BLK)) = make_uint4(0, 0, 0, 0);
-                    }
-                    __syncwarp();
-                }
-                dec_tile<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r);
                 __syncwarp();
-                if (it + DEC_STAGES < ntiles) {   // refill the stage just used
-                    if (lane == 0) {
-                        fence_proxy_async_smem();
-                        dec_tma(p, tm, s, b, g, k0 + (it + DEC_STAGES) * DEC_KEYS,
-                                ring + (issued % DEC_STAGES) * L::STAGE, &wbar[issued % DEC_STAGES], D);
-                    }
-                    ++issued;
-                }
             }
-            if (!unit_ok) break;
-            if (SOFTMAX)
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
-                    l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
-                }
-            if (ns == 1) {
-                float f[2];
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-                    f[r] = SOFTMAX ? (l_r[r] > 0.f ? 1.f / l_r[r] : 0.f) : 1.f;
-                dec_store_y<D, BF16>(p, rr, o, f);
-            } else {
-                // partial (O, m, l) of this split
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const int row = (lane >> 2) + 8 * r;
-                    float *po = part + (unit_idx * DEC_ROWS + row) * D;
-#pragma unroll
-                    for (int n = 0; n < NT; ++n)
-                        *reinterpret_cast<float2 *>(po + n * 8 + (lane & 3) * 2) =
-                            make_float2(o[n][2 * r], o[n][2 * r + 1]);
-                    if ((lane & 3) == 0) pml[unit_idx * DEC_ROWS + row] = make_float2(m_r[r], l_r[r]);
-                }
-            }
-        }
-        if (!unit_ok) break;
-        if (ns > 1) {
-            // the last split of the pair to finish merges all of them
-            __threadfence();
+            dec_tile<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r);
             __syncwarp();
-            int t = 0;
-            if (lane == 0) t = atomicAdd(&tickets[b * p.Hkv + g], 1);
-            t = __shfl_sync(0xffffffffu, t, 0);
-            if (t == ns - 1) {
-                __threadfence();
-                const size_t u0 = ((size_t)b * p.Hkv + g) * p.max_splits;
-                const int row = lane >> 1, c0 = (lane & 1) * (D / 2);
-                float M = -INFINITY;
+            if (next_issue < t_end) {   // refill the stage just used
+                issue(lc);
+                advance(lc);
+                ++next_issue;
+            }
+            const bool pair_end = cc.tile + 1 == cc.nt;
+            if (pair_end || t + 1 == t_end) {
+                // this range's share of the pair is done
                 if (SOFTMAX)
-                    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, __ldcg(&pml[(u0 + sp) * DEC_ROWS + row].x));
-                float acc[D / 2];
 #pragma unroll
-                for (int c = 0; c < D / 2; ++c) acc[c] = 0.f;
-                float Lsum = 0.f;
-                for (int sp = 0; sp < ns; ++sp) {
-                    float wt = 1.f;
-                    if (SOFTMAX) {
-                        const float2 v = __ldcg(&pml[(u0 + sp) * DEC_ROWS + row]);
-                        wt = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
-                        Lsum += v.y * wt;
+                    for (int r = 0; r < 2; ++r) {
+                        l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
+                        l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
                     }
-                    const float4 *src = reinterpret_cast<const float4 *>(part + ((u0 + sp) * DEC_ROWS + row) * D + c0);
+                const int b = cc.b, g = cc.pib / cc.nrc, rc = cc.pib % cc.nrc;
+                const int ps = tpre[b] + cc.pib * cc.nt, pe = ps + cc.nt;
+                if (seg0 == ps && t + 1 == pe) {   // the whole pair: write Y
+                    float f[2];
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
-                        const float4 x4 = __ldcg(src + c);
-                        acc[4 * c] += x4.x * wt;
-                        acc[4 * c + 1] += x4.y * wt;
-                        acc[4 * c + 2] += x4.z * wt;
-                        acc[4 * c + 3] += x4.w * wt;
+                    for (int r = 0; r < 2; ++r)
+                        f[r] = SOFTMAX ? (l_r[r] > 0.f ? 1.f / l_r[r] : 0.f) : 1.f;
+                    dec_store_y<D, BF16>(p, rr, o, f);
+                } else {
+                    // partial (O, m, l): slot 0 for the first pair of the
+                    // range, slot 1 for the last
+                    const size_t slot = (size_t)wg * 2 + (seg0 == t_begin ? 0 : 1);
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int row = (lane >> 2) + 8 * r;
+                        float *po = part + (slot * DEC_ROWS + row) * D;
+#pragma unroll
+                        for (int n = 0; n < NT; ++n)
+                            *reinterpret_cast<float2 *>(po + n * 8 + (lane & 3) * 2) =
+                                make_float2(o[n][2 * r], o[n][2 * r + 1]);
+                        if ((lane & 3) == 0) pml[slot * DEC_ROWS + row] = make_float2(m_r[r], l_r[r]);
+                    }
+                    __threadfence();
+                    __syncwarp();
+                    const int w_lo = warp_of(ps), w_hi = warp_of(pe - 1);
+                    const int pidx = ppre[b] + cc.pib;
+                    int tk = 0;
+                    if (lane == 0) tk = atomicAdd(&tickets[pidx], 1);
+                    tk = __shfl_sync(0xffffffffu, tk, 0);
+                    if (tk == w_hi - w_lo) {   // the last of the pair's warps: merge
+                        __threadfence();
+                        const int row = lane >> 1, c0 = (lane & 1) * (D / 2);
+                        // the first warp's share is its slot 1 unless the pair
+                        // starts its range; every later warp's share is its slot 0
+                        auto slot_of = [&](int w) -> size_t {
+                            return (size_t)w * 2 + ((w == w_lo && range_start(w) != ps) ? 1 : 0);
+                        };
+                        float M = -INFINITY;
+                        if (SOFTMAX)
+                            for (int w = w_lo; w <= w_hi; ++w)
+                                M = fmaxf(M, __ldcg(&pml[slot_of(w) * DEC_ROWS + row].x));
+                        float acc[D / 2];
+#pragma unroll
+                        for (int k = 0; k < D / 2; ++k) acc[k] = 0.f;
+                        float Lsum = 0.f;
+                        for (int w = w_lo; w <= w_hi; ++w) {
+                            const size_t sl = slot_of(w);
+                            float wt = 1.f;
+                            if (SOFTMAX) {
+                                const float2 v = __ldcg(&pml[sl * DEC_ROWS + row]);
+                                wt = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
+                                Lsum += v.y * wt;
+                            }
+                            const float4 *src = reinterpret_cast<const float4 *>(part + (sl * DEC_ROWS + row) * D + c0);
+#pragma unroll
+                            for (int k = 0; k < D / 8; ++k) {
+                                const float4 x4 = __ldcg(src + k);
+                                acc[4 * k] += x4.x * wt;
+                                acc[4 * k + 1] += x4.y * wt;
+                                acc[4 * k + 2] += x4.z * wt;
+                                acc[4 * k + 3] += x4.w * wt;
+                            }
+                        }
+                        const DecRow R = dec_row(p, cc.s, b, g, rc * DEC_ROWS + row, rows, kv_hi);
+                        if (R.valid) {
+                            const float f = SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f;
+                            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff + c0);
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k)
+                                dst[k] = make_uint4(pack2<BF16>(acc[8 * k] * f, acc[8 * k + 1] * f),
+                                                    pack2<BF16>(acc[8 * k + 2] * f, acc[8 * k + 3] * f),
+                                                    pack2<BF16>(acc[8 * k + 4] * f, acc[8 * k + 5] * f),
+                                                    pack2<BF16>(acc[8 * k + 6] * f, acc[8 * k + 7] * f));
+                        }
+                        if (lane == 0) tickets[pidx] = 0;   // ready for the next call
                     }
                 }
-                const DecRow R = dec_row(p, s, b, g, row, rows, k1);
-                if (R.valid) {
-                    const float f = SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f;
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff + c0);
-#pragma unroll
-                    for (int c = 0; c < D / 16; ++c)
-                        dst[c] = make_uint4(pack2<BF16>(acc[8 * c] * f, acc[8 * c + 1] * f),
-                                            pack2<BF16>(acc[8 * c + 2] * f, acc[8 * c + 3] * f),
-                                            pack2<BF16>(acc[8 * c + 4] * f, acc[8 * c + 5] * f),
-                                            pack2<BF16>(acc[8 * c + 6] * f, acc[8 * c + 7] * f));
-                }
-                if (lane == 0) tickets[b * p.Hkv + g] = 0;
+            }
+            advance(cc);
+            if (pair_end && t + 1 < t_end) {
+                start_pair();
+                seg0 = t + 1;
             }
         }
     }
@@ -433,11 +545,11 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         ++consumed;
     }
     __syncwarp();
-    if (lane == 0 && *abort) set_status(p.status, 5);
+    if (lane == 0 && (!ok || *abort)) set_status(p.status, 5);
 }
 
-// Clears the split tickets and the next-unit counter of a decode call; the
-// decode kernel follows it as a programmatic dependent.
+// Clears the merge tickets of a decode call; the decode kernel follows it as
+// a programmatic dependent.
 __global__ void decode_prep_kernel(int *tickets, int n) {
     pdl_launch_dependents();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
@@ -454,7 +566,7 @@ static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStre
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int n = p.B * p.Hkv + 1;
+    const int n = p.max_pairs + 1;
     decode_prep_kernel<<<(n + 255) / 256 < 64 ? (n + 255) / 256 : 64, 256, 0, s>>>(
         reinterpret_cast<int *>(p.ws + dec_tickets_off(p)), n);
     cudaError_t e = cudaGetLastError();

@@ -80,15 +80,6 @@ __device__ __forceinline__ bool mask_at(const AttnParams &p, long long e, float 
     }
 }
 
-// Splits of the key range of one sequence in the decode path (one split when
-// the sequence's query rows exceed one 16-row MMA block).
-__device__ __forceinline__ int dec_splits(const AttnParams &p, const SeqInfo &s) {
-    const int rows = s.q_len * p.G;
-    const int kv_hi = key_extent(p.causal, s.q_len - 1, s);
-    int ns = (kv_hi + DEC_SPLIT - 1) / DEC_SPLIT;
-    if (ns < 1 || rows > DEC_ROWS) ns = 1;
-    return ns;
-}
 
 __device__ __forceinline__ float load_qscale(const AttnParams &p) {
     if (p.qscale_dtype == 0) return __half2float(*static_cast<const __half *>(p.qscale));

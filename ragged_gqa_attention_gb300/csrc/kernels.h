@@ -13,13 +13,12 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 
 // Decode geometry: 16 query rows per MMA row block, 32 keys per tile,
-// DEC_SPLIT keys per work unit, 4 independent warps per CTA with a
-// DEC_STAGES-deep TMA ring each.
+// 4 independent warps per CTA with a DEC_STAGES-deep TMA ring each; the key
+// tiles of all work are split into equal contiguous ranges, one per warp.
 constexpr int DEC_ROWS = 16;
 constexpr int DEC_KEYS = 32;
 constexpr int DEC_WARPS = 4;
 constexpr int DEC_STAGES = 3;
-constexpr int DEC_SPLIT = 512;
 
 enum Mode { MODE_SOFTMAX = 0, MODE_NONE = 1, MODE_SOFTMAX_Q = 2, MODE_NONE_Q = 3 };
 
@@ -43,7 +42,8 @@ struct AttnParams {
     int tq;                         // query tokens per prefill tile (BM / G)
     int item_tokens;                // query tokens per prefill work item (2 tiles)
     int max_items;                  // capacity of the work list
-    int max_splits;                 // decode: splits per (b, kv head)
+    int max_pairs;                  // decode: bound on (batch, KV head, row chunk) pairs
+    int dec_slots;                  // decode: partial slots (2 per warp of the grid)
     int grid;                       // decode: persistent grid size
     int32_t *status;                // device status word
     uint8_t *ws;                    // workspace base
@@ -52,8 +52,8 @@ struct AttnParams {
 // Workspace layout (byte offsets from ws).
 constexpr size_t WS_HEADER = 256;             // int counters
 // prefill: int4 items[max_items] after the header
-// decode: after the header: int tickets[B*Hkv] (256-aligned), then
-// float partial_o[B*Hkv*max_splits][DEC_ROWS][D], float2 ml[..][DEC_ROWS]
+// decode: after the prefill region: int tickets[max_pairs] (256-aligned),
+// then float partial_o[dec_slots][DEC_ROWS][D], float2 ml[dec_slots][DEC_ROWS]
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -61,19 +61,19 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 __host__ __device__ inline size_t pf_ws_bytes(const AttnParams &p) {
     return WS_HEADER + (size_t)p.max_items * 16;
 }
-// decode workspace, after the prefill region: split tickets and the next-unit
-// counter (cleared before each decode launch), partial O, partial (m, l)
+// decode workspace, after the prefill region: merge tickets (cleared before
+// each decode launch), partial O, partial (m, l)
 __host__ __device__ inline size_t dec_tickets_off(const AttnParams &p) {
     return align256(pf_ws_bytes(p));
 }
 __host__ __device__ inline size_t dec_part_off(const AttnParams &p) {
-    return align256(dec_tickets_off(p) + ((size_t)p.B * p.Hkv + 1) * 4);
+    return align256(dec_tickets_off(p) + ((size_t)p.max_pairs + 1) * 4);
 }
 __host__ __device__ inline size_t dec_ml_off(const AttnParams &p) {
-    return dec_part_off(p) + align256((size_t)p.B * p.Hkv * p.max_splits * DEC_ROWS * p.D * 4);
+    return dec_part_off(p) + align256((size_t)p.dec_slots * DEC_ROWS * p.D * 4);
 }
 __host__ __device__ inline size_t dec_ws_bytes(const AttnParams &p) {
-    return dec_ml_off(p) + (size_t)p.B * p.Hkv * p.max_splits * DEC_ROWS * 8;
+    return dec_ml_off(p) + (size_t)p.dec_slots * DEC_ROWS * 8;
 }
 // Largest batch the decode kernel lists in shared memory.
 constexpr int DEC_MAX_B = 4096;

@@ -167,6 +167,22 @@ def test_decode_multi_token_rows():
     _parity(c)
 
 
+def test_decode_zero_keys_and_range_edges():
+    # sequences without keys (their rows are zero and no warp's range holds
+    # them), and many short sequences whose pairs are cut by the ends of the
+    # warps' tile ranges
+    c = W.make_case("dec5", 21, batch=5, q_heads=16, kv_heads=2, head_dim=128,
+                    q_lens=[1] * 5, kv_lens=[0, 1, 0, 700, 3000], q_form="packed",
+                    kv_form="padded", kv_seq=3000, dtype=torch.bfloat16, causal="lower_right")
+    _parity(c)
+    g = torch.Generator().manual_seed(22)
+    kv = torch.randint(1, 300, (257,), generator=g).tolist()
+    c = W.make_case("dec6", 23, batch=257, q_heads=16, kv_heads=2, head_dim=64,
+                    q_lens=[1] * 257, kv_lens=kv, q_form="packed", kv_form="padded",
+                    kv_seq=300, dtype=torch.float16, causal="lower_right")
+    _parity(c)
+
+
 def test_decode_masks_and_none():
     B, N = 3, 1000
     c = W.make_case("decm", 17, batch=B, q_heads=8, kv_heads=2, head_dim=128,

@@ -55,16 +55,17 @@ def test_static_scratch_matches_trt_attention(name):
 
 def test_static_scratch_rejects_oversized_problems():
     lib = binding.load(build_if_missing=True)
-    # decode over 1024 sequences x 8 KV heads needs 1024*8*16*128*4 bytes
-    # (64 MiB) of split partials: more than the 40 MiB scratch
-    B, Hq, Hkv, D = 1024, 64, 8, 128
-    q = torch.zeros(B, Hq, D, dtype=torch.bfloat16, device="cuda")
-    kv = torch.zeros(B, Hkv, 1, D, dtype=torch.bfloat16, device="cuda")
+    # prefill over 50000 packed sequences x 64 KV heads: the work list has room
+    # for 64 * (1 + 50000) items of 16 bytes (51 MB), more than the 40 MiB
+    # scratch; the sequences are empty, so the tensors stay tiny
+    B, H, D = 50000, 64, 64
+    q = torch.zeros(64, H, D, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(1, H, D, dtype=torch.bfloat16, device="cuda")
     y = torch.full_like(q, float("nan"))
-    ql = torch.arange(B + 1, dtype=torch.int32, device="cuda")
+    lens = torch.zeros(B + 1, dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    a = binding.make_args(q, kv, kv, y, q_form="packed", kv_form="padded",
-                          query_lengths=ql, status=status)
+    a = binding.make_args(q, kv, kv, y, q_form="packed", kv_form="packed",
+                          query_lengths=lens, kv_lengths=lens, status=status)
     assert lib.rga_attention_workspace_size(ctypes.byref(a)) > (40 << 20)
     rc = lib.trt_attention_static_scratch(ctypes.byref(a), None)
     assert rc == 6
