@@ -656,6 +656,13 @@ __device__ __forceinline__ void store_rows(const AttnParams &p, const TensorMaps
     }
 }
 
+// Scores of a chunk past key `last` (chunk-relative) become -inf.
+__device__ __forceinline__ void mask_after(uint32_t (&r)[32], int last) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+        if (k > last) r[k] = 0xff800000u;
+}
+
 // Largest of 32 scores held as raw bits.
 __device__ __forceinline__ float reg_max(const uint32_t (&r)[32]) {
     float v[32];
@@ -741,25 +748,40 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
             uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
             if (bool_mask && !full) mask_bits(p, row_indep, mrow, j0, m.s.kv_len, row_ok, bits);
 
-            // Softmax, full tile, every row of the warp past its first key:
-            // start the exps against the running reference while the second
-            // half of the row is still loading; redo the step only when some
-            // row's max grows past the reference by more than the threshold.
-            if (MODE == MODE_SOFTMAX && full &&
-                __all_sync(0xffffffffu, !row_ok || m_ref != -INFINITY)) {
-                const float ref0 = row_ok ? m_ref : 0.f;
+            // Softmax without an explicit mask: take the exps against the
+            // running reference while the second half of the row is still
+            // loading; redo the step only when some row's max grows past the
+            // reference by more than the threshold.  Keys past a row's
+            // causal or length limit (a prefix of the tile stays visible)
+            // become -inf in registers.  A row without a reference yet takes
+            // the max of its first 64 visible scores (none visible: the row
+            // sees no key of the tile and all its p are 0).
+            if (MODE == MODE_SOFTMAX && !use_mask && sc > 0.f) {
                 const uint64_t mul2 = f2_pack(sc, sc);
-                uint64_t neg2 = f2_pack(-ref0, -ref0);
                 uint32_t ra[2][32], rb[2][32];
                 tmem_ld32(s_addr, ra[0]);
                 tmem_ld32(s_addr + 32, ra[1]);
                 tmem_wait_ld();
                 tmem_ld32(s_addr + 64, rb[0]);
                 tmem_ld32(s_addr + 96, rb[1]);
+                if (!full) {
+                    mask_after(ra[0], rem);
+                    mask_after(ra[1], rem - 32);
+                }
+                if (__any_sync(0xffffffffu, row_ok && m_ref == -INFINITY)) {
+                    const float m01 = fmaxf(reg_max(ra[0]), reg_max(ra[1])) * sc;
+                    if (row_ok && m_ref == -INFINITY) m_ref = m01;
+                }
+                const float ref0 = (row_ok && m_ref != -INFINITY) ? m_ref : 0.f;
+                uint64_t neg2 = f2_pack(-ref0, -ref0);
                 uint64_t acc0 = 0, acc1 = 0;
                 p_chunk<BF16>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
                 p_chunk<BF16>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1);
                 tmem_wait_ld();
+                if (!full) {
+                    mask_after(rb[0], rem - 64);
+                    mask_after(rb[1], rem - 96);
+                }
                 p_chunk<BF16>(rb[0], s_addr, 2, mul2, neg2, acc0, acc1);
                 p_chunk<BF16>(rb[1], s_addr, 3, mul2, neg2, acc0, acc1);
                 // No probability can pass 2^threshold while their sum stays
