@@ -186,3 +186,7 @@ def e4m3_encode(x: float) -> int:
 
 def int8_round(x: float) -> float:
     return _load().rga_oracle_int8_round(float(x))
+
+
+# TRT_KVCacheUpdate (a plain scatter; see kv_update.py)
+from .kv_update import kv_cache_update  # noqa: E402,F401
