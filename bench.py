@@ -331,6 +331,42 @@ def measure(index, quant, stream, steps, warmup, dist_on, peaks, rank, clocks=Fa
                 clocks=clk, launches_per_step=2, times=times)
 
 
+def measure_kv_update(stream, steps, warmup, dist_on, peaks):
+    """TRT_KVCacheUpdate in place: the chunked-prefill workload's new K rows
+    (packed, one chunk per sequence) written into its padded 8192-key cache
+    at the chunk's positions.  GB/s of the update rows read and written."""
+    import ctypes
+    c = W.workload(3, kv_pad=0.0)
+    g = torch.Generator().manual_seed(3)
+    cache = c.k.to("cuda")                                   # [16, 8, 8192, 128]
+    upd = torch.randn(sum(c.q_lens), c.kv_heads, c.head_dim, generator=g).to(c.k.dtype).cuda()
+    cu = torch.zeros(c.batch + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(c.q_lens), 0)
+    wi = torch.tensor([kl - ql for ql, kl in zip(c.q_lens, c.kv_lens)], dtype=torch.int32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib = binding.load()
+    wi_d, cu_d = wi.cuda(), cu.cuda()      # referenced for as long as `a` is used
+    a = binding.make_kv_args(cache, upd, cache, update_form="packed", write_indices=wi_d,
+                             update_lengths=cu_d, status=status)
+    h = ctypes.c_void_p(stream.cuda_stream)
+
+    def run():
+        rc = lib.trt_kv_cache_update(ctypes.byref(a), h)
+        if rc != 0:
+            raise binding.RgaError(rc, "bench kv update")
+
+    times, _ = device_timed(run, stream, steps, warmup, dist_on)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"kv update device status {int(status.item())}")
+    ms = max_over_ranks(statistics.mean(times), dist_on)
+    work = 2 * upd.numel() * upd.element_size()
+    value = work / (ms * 1e-3) / 1e9
+    name = f"kv_cache_update_packed{upd.shape[0]}_into_b16_h8_n8192_d128_bf16"
+    return name, dict(value=value, unit="GB/s", ms=ms, bound="hbm", peak=peaks["hbm_gbs"],
+                      work=work)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -380,6 +416,13 @@ def main():
                 "frac_of_peak": round(r["value"] / r["peak"], 4),
                 "peak": r["peak"], "peak_source": peak_src}
             del r
+        torch.cuda.empty_cache()
+        name, r = measure_kv_update(stream, max(5, args.steps // 2), 3, dist_on, peaks)
+        secondary[name] = {
+            "value": round(r["value"] * world, 3), "unit": r["unit"],
+            "ms_per_step": round(r["ms"], 4), "bound": r["bound"],
+            "frac_of_peak": round(r["value"] / r["peak"], 4),
+            "peak": r["peak"], "peak_source": peak_src}
 
     cpu = None
     if rank == 0:

@@ -180,6 +180,48 @@ rga_status trt_quantized_attention(const rga_attention_args *args,
  * scratch it reads, so what a previous call left there does not matter. */
 rga_status trt_attention_static_scratch(const rga_attention_args *args, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * TRT_KVCacheUpdate ("TensorRT Custom Operator Schemas", TRT_KVCacheUpdate):
+ * the TensorScatter update of a KV cache in "linear" mode along axis -2, the
+ * step in front of decode attention.  For every batch b, every head h and
+ * every update token t < len_b:
+ *     Y[b, h, w_b + t, :] = update token t of batch b, head h
+ * and every other element of Y equals past_cache.
+ *   w_b   = write_indices[b] (device int32 [B]); 0 for every batch when NULL.
+ *   len_b = update_lengths[b+1] - update_lengths[b] (device int32 [B+1],
+ *           cumulative from 0); required for the packed form, where batch
+ *           b's tokens are rows update_lengths[b] .. update_lengths[b+1]-1
+ *           of the update; for the padded form, NULL means update_seq
+ *           tokens for every batch.
+ * past_cache, y: [B, H, N, D] (row-major, N = cache_seq); update: padded
+ * [B, H, update_seq, D] or packed [update_seq, H, D].  All device pointers,
+ * owned by the caller.  y == past_cache updates the cache in place (only the
+ * written rows move); otherwise the whole cache is copied to y with the
+ * update applied, and y must not overlap past_cache or update otherwise.
+ * The op moves element bits without arithmetic: dtype only sets the element
+ * size (RGA_F16, RGA_BF16 or RGA_F32).
+ * Errors: RGA_ERR_INVALID_ARG for bad pointers, shapes or enums (nothing is
+ * enqueued); batch > 8192 gives RGA_ERR_UNSUPPORTED.  On the device, a
+ * window [w_b, w_b + len_b) outside [0, N), negative or non-cumulative
+ * lengths, or lengths past the update tensor set *device_status to
+ * RGA_ERR_DEVICE_LENGTHS and nothing is written.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    const void *past_cache;
+    const void *update;
+    void *y;
+    rga_dtype dtype;               /* element size only: F16, BF16 or F32 */
+    rga_form update_form;
+    int32_t batch, heads, cache_seq, head_dim;
+    int32_t update_seq;            /* padded: N_u of the update; packed: rows T */
+    const int32_t *write_indices;  /* [B] or NULL */
+    const int32_t *update_lengths; /* [B+1] cumulative, or NULL (padded only) */
+    int32_t *device_status;
+} rga_kv_update_args;
+
+/* Enqueue TRT_KVCacheUpdate on `stream`; returns RGA_OK once enqueued. */
+rga_status trt_kv_cache_update(const rga_kv_update_args *args, cudaStream_t stream);
+
 /* Copy *device_status to *out after the work already enqueued on `stream`
  * has finished.  This call synchronises the stream: use it in tests and
  * debugging, not on a hot path. */

@@ -33,7 +33,7 @@ DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.bool: 3}
 
 EXPORTED = ("rga_attention_workspace_size", "trt_attention", "trt_quantized_attention",
             "rga_get_device_status", "rga_status_string", "rga_abi_version",
-            "trt_attention_static_scratch")
+            "trt_attention_static_scratch", "trt_kv_cache_update")
 
 
 class Args(ctypes.Structure):
@@ -47,6 +47,17 @@ class Args(ctypes.Structure):
         ("mask", c_vp), ("mask_dtype", c_int), ("mask_rank", c_i32), ("mask_dims", c_i64 * 4),
         ("scale", c_float), ("causal", c_int), ("norm", c_int), ("nb_rank", c_i32),
         ("workspace", c_vp), ("workspace_bytes", c_size), ("device_status", c_vp),
+    ]
+
+
+class KvArgs(ctypes.Structure):
+    """Mirror of rga_kv_update_args."""
+    _fields_ = [
+        ("past_cache", c_vp), ("update", c_vp), ("y", c_vp),
+        ("dtype", c_int), ("update_form", c_int),
+        ("batch", c_i32), ("heads", c_i32), ("cache_seq", c_i32), ("head_dim", c_i32),
+        ("update_seq", c_i32),
+        ("write_indices", c_vp), ("update_lengths", c_vp), ("device_status", c_vp),
     ]
 
 
@@ -92,6 +103,8 @@ def load(build_if_missing: bool = False):
             lib.rga_status_string.argtypes = [c_int]
             lib.rga_abi_version.restype = c_i32
             lib.rga_abi_version.argtypes = []
+            lib.trt_kv_cache_update.restype = c_int
+            lib.trt_kv_cache_update.argtypes = [ctypes.POINTER(KvArgs), c_vp]
             _lib = lib
     return _lib
 
@@ -236,3 +249,43 @@ def device_status(status, stream=None) -> int:
     if rc != RGA_OK:
         raise RgaError(rc, "rga_get_device_status")
     return int(out.value)
+
+
+def make_kv_args(past_cache, update, y, *, update_form="padded", write_indices=None,
+                 update_lengths=None, status=None) -> KvArgs:
+    """rga_kv_update_args for device tensors (see include/rga.h)."""
+    for name, t in (("past_cache", past_cache), ("update", update), ("y", y),
+                    ("write_indices", write_indices), ("update_lengths", update_lengths),
+                    ("status", status)):
+        _need_cuda(name, t)
+    if past_cache.dim() != 4:
+        raise ValueError("past_cache must be [B, H, N, D]")
+    if update.dtype != past_cache.dtype or y.dtype != past_cache.dtype:
+        raise ValueError("past_cache, update and y must share one dtype")
+    a = KvArgs()
+    a.past_cache, a.update, a.y = _ptr(past_cache), _ptr(update), _ptr(y)
+    a.dtype = DTYPES.get(past_cache.dtype, -1)
+    a.update_form = FORMS[update_form]
+    B, H, N, D = past_cache.shape
+    a.batch, a.heads, a.cache_seq, a.head_dim = B, H, N, D
+    a.update_seq = update.shape[2] if a.update_form == 0 else update.shape[0]
+    a.write_indices, a.update_lengths = _ptr(write_indices), _ptr(update_lengths)
+    a.device_status = _ptr(status)
+    return a
+
+
+def trt_kv_cache_update(past_cache, update, *, update_form="padded", write_indices=None,
+                        update_lengths=None, out=None, status=None, stream=None,
+                        return_status=False):
+    """TRT_KVCacheUpdate: returns Y ([B, H, N, D]).  With out=None the cache
+    is updated in place and returned; otherwise Y is written to `out`."""
+    lib = load()
+    y = past_cache if out is None else out
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=past_cache.device)
+    a = make_kv_args(past_cache, update, y, update_form=update_form, write_indices=write_indices,
+                     update_lengths=update_lengths, status=status)
+    rc = lib.trt_kv_cache_update(ctypes.byref(a), c_vp(_stream_handle(stream)))
+    if rc != RGA_OK:
+        raise RgaError(rc, "trt_kv_cache_update")
+    return (y, status) if return_status else y

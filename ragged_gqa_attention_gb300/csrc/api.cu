@@ -10,6 +10,16 @@
 
 using namespace rga;
 
+namespace rga {
+// SMs of the current device (0 when it cannot be read).
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+}  // namespace rga
+
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -23,13 +33,6 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
     }
     return fn;
-}
-
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }

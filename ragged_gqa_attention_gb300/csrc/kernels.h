@@ -101,6 +101,9 @@ inline cudaError_t launch_dependent(Kernel kernel, int grid, int block, int smem
     return cudaLaunchKernelEx(&cfg, kernel, p, m);
 }
 
+// SMs of the current device (0 when it cannot be read); api.cu.
+int sm_count();
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_sched(const AttnParams &p, int decode, cudaStream_t s);
 template <bool BF16>

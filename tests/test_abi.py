@@ -43,22 +43,30 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n)
 
 
-def test_struct_layout_matches_c(tmp_path):
-    fields = [f[0] for f in binding.Args._fields_]
+def _layout_matches_c(tmp_path, struct, cname):
+    fields = [f[0] for f in struct._fields_]
     prog = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"',
             "int main(void){",
-            'printf("%zu\\n", sizeof(rga_attention_args));']
+            f'printf("%zu\\n", sizeof({cname}));']
     for f in fields:
-        prog.append(f'printf("%zu\\n", offsetof(rga_attention_args, {f}));')
+        prog.append(f'printf("%zu\\n", offsetof({cname}, {f}));')
     prog.append("return 0;}")
-    c = tmp_path / "layout.c"
+    c = tmp_path / f"layout_{cname}.c"
     c.write_text("\n".join(prog))
-    exe = tmp_path / "layout"
+    exe = tmp_path / f"layout_{cname}"
     subprocess.check_call(["gcc", "-I", "/usr/local/cuda/include", str(c), "-o", str(exe)])
     vals = [int(x) for x in subprocess.check_output([str(exe)]).split()]
-    assert vals[0] == ctypes.sizeof(binding.Args)
+    assert vals[0] == ctypes.sizeof(struct)
     for f, off in zip(fields, vals[1:]):
-        assert getattr(binding.Args, f).offset == off, f
+        assert getattr(struct, f).offset == off, f
+
+
+def test_struct_layout_matches_c(tmp_path):
+    _layout_matches_c(tmp_path, binding.Args, "rga_attention_args")
+
+
+def test_kv_update_struct_layout_matches_c(tmp_path):
+    _layout_matches_c(tmp_path, binding.KvArgs, "rga_kv_update_args")
 
 
 def test_status_strings_and_version(lib):
@@ -119,3 +127,31 @@ def test_python_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 2, 8, 64, dtype=torch.float16)
     with pytest.raises(ValueError):
         binding.trt_attention(q, q, q)
+
+
+def _kv_args(**kw):
+    a = binding.KvArgs()
+    a.past_cache = a.update = a.y = 0x10000
+    a.dtype, a.update_form = 1, 0
+    a.batch, a.heads, a.cache_seq, a.head_dim, a.update_seq = 2, 8, 64, 128, 4
+    a.device_status = 0x20000
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(past_cache=None), 1),
+    (dict(update=None), 1),
+    (dict(y=None), 1),
+    (dict(device_status=None), 1),
+    (dict(dtype=3), 1),                  # element type outside F16/BF16/F32
+    (dict(update_form=5), 1),
+    (dict(batch=-1), 1),
+    (dict(head_dim=0), 1),
+    (dict(update_form=1), 1),            # packed update needs update_lengths
+    (dict(batch=9000), 2),               # more batches than the kernel lists
+])
+def test_kv_update_validation_codes_without_a_device(lib, kw, code):
+    a = _kv_args(**kw)
+    assert lib.trt_kv_cache_update(ctypes.byref(a), None) == code
