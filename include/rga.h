@@ -228,6 +228,17 @@ rga_status trt_kv_cache_update(const rga_kv_update_args *args, cudaStream_t stre
 rga_status rga_get_device_status(const int32_t *device_status,
                                  cudaStream_t stream, int32_t *out);
 
+/* Failure-path self-test: enqueue one CTA whose single wait (on an mbarrier
+ * that nothing arrives on) gives up after `wait_cycles` SM clock cycles
+ * (1 .. 2^32) and sets *device_status to RGA_ERR_TIMEOUT, exactly as a
+ * timed-out wait in the attention kernels does.  Nothing faults or hangs and
+ * the context stays usable; the attention kernels bound every wait at about
+ * 2 s of clock cycles the same way.  device_status: one device int32 owned
+ * by the caller.  Returns RGA_ERR_INVALID_ARG for a null pointer or a limit
+ * out of range. */
+rga_status rga_selftest_wait_timeout(int32_t *device_status, int64_t wait_cycles,
+                                     cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *rga_status_string(rga_status status);
 

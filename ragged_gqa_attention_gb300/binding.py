@@ -33,7 +33,7 @@ DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.bool: 3}
 
 EXPORTED = ("rga_attention_workspace_size", "trt_attention", "trt_quantized_attention",
             "rga_get_device_status", "rga_status_string", "rga_abi_version",
-            "trt_attention_static_scratch", "trt_kv_cache_update")
+            "trt_attention_static_scratch", "trt_kv_cache_update", "rga_selftest_wait_timeout")
 
 
 class Args(ctypes.Structure):
@@ -103,6 +103,8 @@ def load(build_if_missing: bool = False):
             lib.rga_status_string.argtypes = [c_int]
             lib.rga_abi_version.restype = c_i32
             lib.rga_abi_version.argtypes = []
+            lib.rga_selftest_wait_timeout.restype = c_int
+            lib.rga_selftest_wait_timeout.argtypes = [c_vp, c_i64, c_vp]
             lib.trt_kv_cache_update.restype = c_int
             lib.trt_kv_cache_update.argtypes = [ctypes.POINTER(KvArgs), c_vp]
             _lib = lib

@@ -60,17 +60,24 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false if
-// the wait ran out of time or *abort became non-zero meanwhile.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort) {
+// the wait ran out of time (after `limit` clock cycles; it then sets *abort)
+// or *abort became non-zero meanwhile.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity,
+                                                volatile int *abort,
+                                                unsigned long long limit) {
     const uint32_t a = smem_u32(bar);
     if (mbar_test(a, parity)) return true;
     const unsigned long long t0 = clock64();
     for (;;) {
         if (mbar_test(a, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > RGA_WAIT_CYCLES) { *abort = 1; return false; }
+        if (clock64() - t0 > limit) { *abort = 1; return false; }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort) {
+    return mbar_wait_limit(bar, parity, abort, RGA_WAIT_CYCLES);
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight copies

@@ -155,3 +155,9 @@ def _kv_args(**kw):
 def test_kv_update_validation_codes_without_a_device(lib, kw, code):
     a = _kv_args(**kw)
     assert lib.trt_kv_cache_update(ctypes.byref(a), None) == code
+
+
+def test_selftest_validates_its_arguments(lib):
+    assert lib.rga_selftest_wait_timeout(None, 1000, None) == 1
+    assert lib.rga_selftest_wait_timeout(0x20000, 0, None) == 1
+    assert lib.rga_selftest_wait_timeout(0x20000, (1 << 32) + 1, None) == 1
