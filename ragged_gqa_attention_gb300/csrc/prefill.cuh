@@ -608,6 +608,8 @@ __device__ __forceinline__ void store_rows(const AttnParams &p, const TensorMaps
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) tmem_ld32(o_taddr + c * 32, v[c]);
         tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_regs_ready(v[c]);
     }
 #pragma unroll
     for (int half = 0; half < D / 64; ++half) {
@@ -661,6 +663,62 @@ __device__ __forceinline__ void mask_after(uint32_t (&r)[32], int last) {
 #pragma unroll
     for (int k = 0; k < 32; ++k)
         if (k > last) r[k] = 0xff800000u;
+}
+
+// Scores of chunk c whose key is excluded by a row-independent bool mask
+// become -inf.  bits[k] bit L is key 4L + k of the tile (mask_bits, ballot).
+__device__ __forceinline__ void mask_keys(uint32_t (&r)[32], const uint32_t (&bits)[4], int c) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (!((bits[i & 3] >> (8 * c + (i >> 2))) & 1u)) r[i] = 0xff800000u;
+}
+
+// Sum of 2^(s * mul - ref) over one 32-score chunk (statistics pass).
+__device__ __forceinline__ void sum_chunk(const uint32_t (&r)[32], uint64_t mul2, uint64_t neg2,
+                                          uint64_t &acc0, uint64_t &acc1) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        float pa, pb;
+        f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])), mul2, neg2),
+                  pa, pb);
+        pa = ex2(pa);
+        pb = ex2(pb);
+        if (k & 1) acc1 = fadd2(acc1, f2_pack(pa, pb));
+        else acc0 = fadd2(acc0, f2_pack(pa, pb));
+    }
+}
+
+// One 32-column chunk of the quantized pass: x = 2^(s * mul - ref) (with
+// ref = log2 of l * s_q, x is p / s_q), rounded to the fp8 E4M3 (quant 0)
+// or int8 (quant 1) grid, stored as 16-bit pairs into TMEM columns
+// [16c, 16c+16) of the S buffer (every code is exact in f16 and bf16).
+template <bool BF16>
+__device__ __forceinline__ void p_chunk_q(const uint32_t (&r)[32], uint32_t s_addr, int c,
+                                          uint64_t mul2, uint64_t neg2, int quant) {
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        float pa, pb;
+        f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])), mul2, neg2),
+                  pa, pb);
+        pa = ex2(pa);
+        pb = ex2(pb);
+        if (quant == 0) {
+            uint16_t q;
+            uint32_t h;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(pb), "f"(pa));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(q));
+            if constexpr (BF16) {
+                const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&h));
+                w[k] = pack2<true>(f.x, f.y);
+            } else {
+                w[k] = h;
+            }
+        } else {
+            w[k] = pack2<BF16>(int8_round(pa), int8_round(pb));
+        }
+    }
+    tmem_st16(s_addr + c * 16, w);
 }
 
 // Largest of 32 scores held as raw bits.
@@ -748,27 +806,101 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
             uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
             if (bool_mask && !full) mask_bits(p, row_indep, mrow, j0, m.s.kv_len, row_ok, bits);
 
-            // Softmax without an explicit mask: take the exps against the
+            // Softmax without an explicit mask (and the quantized op's
+            // statistics and quantized passes, also under a bool mask that
+            // depends on the key only): take the exps against the
             // running reference while the second half of the row is still
             // loading; redo the step only when some row's max grows past the
             // reference by more than the threshold.  Keys past a row's
-            // causal or length limit (a prefix of the tile stays visible)
-            // become -inf in registers.  A row without a reference yet takes
-            // the max of its first 64 visible scores (none visible: the row
-            // sees no key of the tile and all its p are 0).
-            if (MODE == MODE_SOFTMAX && !use_mask && sc > 0.f) {
+            // causal or length limit (a prefix of the tile stays visible) and
+            // keys the bool mask excludes become -inf in registers.  A row
+            // without a reference yet takes the max of its first 64 visible
+            // scores (none visible: all its p are 0).
+            if (((MODE == MODE_SOFTMAX && !use_mask) ||
+                 (MODE == MODE_SOFTMAX_Q && (!use_mask || row_indep))) && sc > 0.f) {
+                const bool lim_full = j0 + BN - 1 <= lim_first;   // no causal/length limit in the tile
                 const uint64_t mul2 = f2_pack(sc, sc);
                 uint32_t ra[2][32], rb[2][32];
                 tmem_ld32(s_addr, ra[0]);
                 tmem_ld32(s_addr + 32, ra[1]);
                 tmem_wait_ld();
+                if (MODE == MODE_SOFTMAX_Q) {
+                    tmem_regs_ready(ra[0]);
+                    tmem_regs_ready(ra[1]);
+                }
                 tmem_ld32(s_addr + 64, rb[0]);
                 tmem_ld32(s_addr + 96, rb[1]);
-                if (!full) {
+                if (!lim_full) {
                     mask_after(ra[0], rem);
                     mask_after(ra[1], rem - 32);
                 }
+                if (MODE == MODE_SOFTMAX_Q && use_mask) {
+                    mask_keys(ra[0], bits, 0);
+                    mask_keys(ra[1], bits, 1);
+                }
+                if (MODE == MODE_SOFTMAX_Q) {
+                    tmem_wait_ld();
+                    tmem_regs_ready(rb[0]);
+                    tmem_regs_ready(rb[1]);
+                    if (!lim_full) {
+                        mask_after(rb[0], rem - 64);
+                        mask_after(rb[1], rem - 96);
+                    }
+                    if (use_mask) {
+                        mask_keys(rb[0], bits, 2);
+                        mask_keys(rb[1], bits, 3);
+                    }
+                    if (stat) {
+                        // pass 1: S is in registers, so the tensor core may
+                        // already write the next S over it; exact max and sum
+                        tc_fence_before();
+                        mbar_arrive(&bar.p_full[a]);
+                        const float mraw = fmaxf(fmaxf(reg_max(ra[0]), reg_max(ra[1])),
+                                                 fmaxf(reg_max(rb[0]), reg_max(rb[1])));
+                        const float mx = row_ok ? mraw * sc : -INFINITY;
+                        const float m_new = fmaxf(m_ref, mx);
+                        if (m_new != -INFINITY) {
+                            const uint64_t neg2 = f2_pack(-m_new, -m_new);
+                            uint64_t acc0 = 0, acc1 = 0;
+                            sum_chunk(ra[0], mul2, neg2, acc0, acc1);
+                            sum_chunk(ra[1], mul2, neg2, acc0, acc1);
+                            sum_chunk(rb[0], mul2, neg2, acc0, acc1);
+                            sum_chunk(rb[1], mul2, neg2, acc0, acc1);
+                            float s0, s1, s2, s3;
+                            f2_unpack(acc0, s0, s1);
+                            f2_unpack(acc1, s2, s3);
+                            l = l * ex2(m_ref - m_new) + ((s0 + s1) + (s2 + s3));
+                            m_ref = m_new;
+                        }
+                        if (t == m.nkt - 1)
+                            lse2 = (l > 0.f) ? m_ref + log2f(l) + log2f(qs) : INFINITY;
+                        ++tc;
+                        continue;
+                    }
+                    // pass 2: p / s_q = 2^(s sc - lse2), quantized (0 for an
+                    // excluded key or a row with no key: lse2 is +inf there).
+                    // Take the previous BMM2's completion in turn (it is done:
+                    // S(t) follows it), so that the epilogue's parity wait
+                    // finds exactly the last one outstanding.
+                    if (u > 0) {
+                        if (!mbar_wait(&bar.o_done[a], pvw & 1, abort)) { ok = false; break; }
+                        ++pvw;
+                    }
+                    const uint64_t neg2 = f2_pack(-lse2, -lse2);
+                    p_chunk_q<BF16>(ra[0], s_addr, 0, mul2, neg2, p.quant);
+                    p_chunk_q<BF16>(ra[1], s_addr, 1, mul2, neg2, p.quant);
+                    p_chunk_q<BF16>(rb[0], s_addr, 2, mul2, neg2, p.quant);
+                    p_chunk_q<BF16>(rb[1], s_addr, 3, mul2, neg2, p.quant);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bar.p_full[a]);
+                    ++u;
+                    ++tc;
+                    continue;
+                }
                 if (__any_sync(0xffffffffu, row_ok && m_ref == -INFINITY)) {
+                    // first reference: the max of the first 64 scores
+                    // (visible keys form a prefix here: no explicit mask)
                     const float m01 = fmaxf(reg_max(ra[0]), reg_max(ra[1])) * sc;
                     if (row_ok && m_ref == -INFINITY) m_ref = m01;
                 }
@@ -778,7 +910,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                 p_chunk<BF16>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
                 p_chunk<BF16>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1);
                 tmem_wait_ld();
-                if (!full) {
+                if (!lim_full) {
                     mask_after(rb[0], rem - 64);
                     mask_after(rb[1], rem - 96);
                 }
@@ -829,6 +961,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                             uint32_t o[32];
                             tmem_ld32(o_addr + c * 32, o);
                             tmem_wait_ld();
+                            tmem_regs_ready(o);
 #pragma unroll
                             for (int k = 0; k < 32; ++k)
                                 o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
@@ -854,6 +987,8 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                 for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, rr[c]);
                 tmem_wait_ld();
 #pragma unroll
+                for (int c = 0; c < BN / 32; ++c) tmem_regs_ready(rr[c]);
+#pragma unroll
                 for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
                     for (int k = 0; k < 32; ++k) x[c * 32 + k] = __uint_as_float(rr[c][k]);
@@ -868,6 +1003,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                     uint32_t rr[32];
                     tmem_ld32(s_addr + c * 32, rr);
                     tmem_wait_ld();
+                    tmem_regs_ready(rr);
                     float v[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(rr[k]);
@@ -976,6 +1112,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                         uint32_t o[32];
                         tmem_ld32(o_addr + c * 32, o);
                         tmem_wait_ld();
+                        tmem_regs_ready(o);
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
                             o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);

@@ -243,6 +243,16 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// tcgen05.ld fills its registers asynchronously, until tcgen05.wait::ld,
+// but the compiler sees them written by the load itself and may move their
+// uses above the wait.  Calling this right after the wait redefines each
+// register in an ordered (volatile) statement, so every later use follows
+// the wait.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) asm volatile("" : "+r"(r[k]));
+}
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }

@@ -95,6 +95,25 @@ def test_prefill_masks(mdtype, shape):
     _parity(c)
 
 
+@pytest.mark.parametrize("quant", [None, "fp8"])
+def test_key_mask_hiding_the_start_of_a_tile(quant):
+    # a key-only bool mask that excludes the first 64 keys of the first tile
+    # (and scattered keys later): the rows' first reference must come from
+    # keys past the first half of the tile
+    B, N = 2, 300
+
+    def mk(gen):
+        keep = torch.rand((B, 1, 1, N), generator=gen) > 0.2
+        keep[..., :64] = False
+        keep[1, ..., 128:200] = False
+        return keep
+
+    c = W.make_case("latekeys", 24, batch=B, q_heads=4, kv_heads=2, head_dim=128,
+                    q_lens=[N, 131], kv_lens=[N, N], q_seq=N, kv_seq=N,
+                    dtype=torch.bfloat16, mask=mk, quant=quant, pass_query_lengths=True)
+    _parity(c)
+
+
 @pytest.mark.parametrize("causal", ["none", "upper_left"])
 def test_prefill_norm_none(causal):
     c = W.make_case("none", 10, batch=2, q_heads=4, kv_heads=4, head_dim=64,
