@@ -405,7 +405,7 @@ def main():
 
     secondary = {}
     if not args.no_secondary:
-        for idx, q in ((3, "fp8"), (4, "fp8"), (5, "fp8"), (5, "int8")):
+        for idx, q in ((3, "fp8"), (4, "fp8"), (5, "fp8"), (5, "int8"), (6, "fp8")):
             if idx == args.workload:
                 continue
             torch.cuda.empty_cache()

@@ -89,14 +89,17 @@ static int64_t dec_max_pairs(int64_t B, int64_t Hkv, int64_t G, int64_t q_seq, b
     return Hkv * chunks;
 }
 
-// Decode (split-KV) path: short query rows per (batch, KV head), no Q/DQ,
-// and every key tile of the work countable in 32 bits.
+// Decode (split-KV) path: short query rows per (batch, KV head) -- one
+// token each in vanilla decoding, a few draft tokens in tree decoding (at
+// most 8 per sequence on average for packed Q; the decode kernel streams the
+// keys once per 16-row chunk) -- no Q/DQ, and every key tile of the work
+// countable in 32 bits.
 bool use_decode(const rga_attention_args *a, bool quant) {
     if (quant || a->batch > DEC_MAX_B) return false;
     const int G = a->q_heads / a->kv_heads;
     if (G > DEC_ROWS) return false;
     const bool packed = a->q_form == RGA_FORM_PACKED_NHD;
-    if (packed ? a->q_seq > a->batch : (int64_t)a->q_seq * G > DEC_ROWS) return false;
+    if (packed ? a->q_seq > 8 * (int64_t)a->batch : (int64_t)a->q_seq * G > DEC_ROWS) return false;
     const int64_t tiles = dec_max_pairs(a->batch, a->kv_heads, G, a->q_seq, packed) *
                           (((int64_t)a->kv_seq + DEC_KEYS - 1) / DEC_KEYS);
     return tiles < (int64_t(1) << 31);

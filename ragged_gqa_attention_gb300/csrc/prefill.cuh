@@ -549,6 +549,22 @@ __device__ __forceinline__ void mask_bits(const AttnParams &p, bool row_indep, l
 #pragma unroll
     for (int k = 0; k < 4; ++k) bits[k] = 0;
     if (!row_ok) return;
+    const uint8_t *src = mk + (keyb ? mrow : mrow + j0);
+    if (!keyb && j0 + BN <= kv_len && j0 + BN <= p.md[3] &&
+        (reinterpret_cast<uintptr_t>(src) & 7) == 0) {
+        // the tile lies inside the mask row and the sequence: 16 loads of 8
+        // key bytes each; key 8q + e lands in bits[e & 3], bit 2q + (e >> 2)
+#pragma unroll
+        for (int q = 0; q < BN / 8; ++q) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(src + 8 * q);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t byte = ((e < 4 ? w.x : w.y) >> (8 * (e & 3))) & 0xffu;
+                if (byte) bits[e & 3] |= 1u << (2 * q + (e >> 2));
+            }
+        }
+        return;
+    }
 #pragma unroll 1
     for (int c = 0; c < BN; ++c) {
         const int j = j0 + c;

@@ -73,4 +73,7 @@ def input_bytes(case: Case):
 
 
 def is_decode(case: Case) -> bool:
-    return case.q_form == PACKED and case.q.shape[0] <= case.batch
+    """Short query rows per sequence (at most 16 tokens on average, as in
+    vanilla and tree decoding): the work is bound by reading K and V, and
+    is reported in GB/s of decode_bytes."""
+    return case.q_form == PACKED and case.q.shape[0] <= 16 * case.batch

@@ -139,7 +139,7 @@ def _uniform_int(g, lo, hi, n):
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
 
 
-# The five named workloads.  Each entry: (name, description).
+# The named workloads.  Each entry: (name, description).
 WORKLOADS = {
     1: ("padded_selfattn_b2_h4_n64_d64_fp16",
         "padded_bhnd B=2 Hq=Hkv=4 N=64 D=64 fp16, scale 1/8, no causal"),
@@ -155,11 +155,16 @@ WORKLOADS = {
     5: ("quantized_padded_b4_h16_n4096_d128_fp16",
         "padded B=4 Hq=Hkv=16 N=4096 D=128 fp16, upper_left, bool key-suffix "
         "mask [B,1,1,N] of 0-25%, P Q/DQ to fp8 (s=1/448) or int8 (s=1/127)"),
+    6: ("tree_decode_b16_draft8_gqa64x8_kv4096_d128_bf16",
+        "tree (speculative) decoding: packed Q of 8 draft tokens per sequence, "
+        "padded KV N=4104 holding the cache (U[256,4096] keys) then the 8 drafts, "
+        "bool mask [B,1,8,N]: every cached key, and of the drafts the token's "
+        "ancestors in a seeded random tree and itself; B=16, Hq=64 Hkv=8 D=128 bf16"),
 }
 
 
 def workload(index, *, quant="fp8", kv_pad=math.nan, seed=None):
-    """The named workload ``index`` (1..5) as a Case on host memory.
+    """The named workload ``index`` (1..6) as a Case on host memory.
 
     ``quant`` selects the fp8 or int8 variant of workload 5.
     """
@@ -190,6 +195,26 @@ def workload(index, *, quant="fp8", kv_pad=math.nan, seed=None):
                          head_dim=128, q_lens=[1] * 64, kv_lens=kvls,
                          q_form=PACKED, kv_form=PADDED, kv_seq=4096,
                          dtype=torch.bfloat16, causal="lower_right",
+                         kv_pad=kv_pad, g=g)
+    if index == 6:
+        B, T, N = 16, 8, 4096 + 8
+        cache = _uniform_int(g, 256, 4096, B)
+
+        def tree_mask(gen):
+            keep = torch.zeros(B, 1, T, N, dtype=torch.bool)
+            for b in range(B):
+                parent = [-1] + [int(torch.randint(0, i, (1,), generator=gen)) for i in range(1, T)]
+                keep[b, 0, :, :cache[b]] = True
+                for i in range(T):
+                    j = i
+                    while j >= 0:   # the token and its ancestors
+                        keep[b, 0, i, cache[b] + j] = True
+                        j = parent[j]
+            return keep
+
+        return make_case(name, seed, batch=B, q_heads=64, kv_heads=8, head_dim=128,
+                         q_lens=[T] * B, kv_lens=[c + T for c in cache], q_form=PACKED,
+                         kv_form=PADDED, kv_seq=N, dtype=torch.bfloat16, mask=tree_mask,
                          kv_pad=kv_pad, g=g)
     if index == 5:
         N, B = 4096, 4

@@ -67,7 +67,7 @@ def ref_rows(c: W.Case, yref, b):
     return yref[:, :, :c.q_lens[b]]
 
 
-CASES = [(2, None), (3, None), (4, None), (5, "fp8"), (5, "int8")]
+CASES = [(2, None), (3, None), (4, None), (5, "fp8"), (5, "int8"), (6, None)]
 
 
 @pytest.mark.parametrize("index,quant", CASES, ids=[f"w{i}-{q}" for i, q in CASES])
