@@ -173,13 +173,16 @@ class Runner:
 def barrier(dist_on):
     if dist_on:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(x, dist_on):
+    """Largest x over the ranks (a time: the slowest rank sets the step)."""
     if not dist_on:
         return x
-    t = torch.tensor([x], dtype=torch.float64)
+    nccl = torch.distributed.get_backend() == "nccl"   # NCCL reduces device tensors only
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if nccl else "cpu")
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 
