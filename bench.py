@@ -6,7 +6,8 @@ the workload (device-side scheduler + the attention kernel).  The headline is
 the ragged packed GQA prefill workload (8 sequences of 128-2048 tokens,
 Hq=32, Hkv=8, D=128, bf16, upper_left causal) in TFLOP/s, with FLOPs = 4 * D
 * attendable pairs counted exactly.  The other workloads (chunked context,
-decode in KV GB/s, quantized P) are reported under "workloads".
+decode in KV GB/s over a 16-bit and an fp8 KV cache, tree decoding,
+quantized P, the KV cache update) are reported under "workloads".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -153,10 +154,15 @@ class Runner:
             self.qt = binding.QUANT[dc.quant]
             self.qs = ctypes.c_void_p(dc.quant_scale.data_ptr())
             self.qsd = binding.DTYPES[dc.quant_scale.dtype]
+        if dc.kv_scales is not None:
+            self.ks = ctypes.c_void_p(dc.kv_scales[0].data_ptr())
+            self.vs = ctypes.c_void_p(dc.kv_scales[1].data_ptr())
 
     def __call__(self):
         b = self.ctypes.byref(self.args)
-        if self.dc.quant is None:
+        if self.dc.kv_scales is not None:
+            rc = self.lib.trt_attention_fp8_kv(b, self.ks, self.vs, self.h)
+        elif self.dc.quant is None:
             rc = self.lib.trt_attention(b, self.h)
         else:
             rc = self.lib.trt_quantized_attention(b, self.qt, self.qs, self.qsd, self.h)
@@ -231,7 +237,14 @@ def e2e_timed(case: W.Case, stream, steps, warmup, dist_on):
         t = getattr(case, name)
         host[name] = None if t is None else t.pin_memory()
     dev = {n: (None if t is None else torch.empty_like(t, device="cuda")) for n, t in host.items()}
-    dc = W.Case(**{**case.__dict__, **dev})
+    if case.kv_scales is not None:   # fp8 KV cache: the two dequantisation scales
+        for i, t in enumerate(case.kv_scales):
+            host[f"kv_scale{i}"] = t.pin_memory()
+            dev[f"kv_scale{i}"] = torch.empty_like(t, device="cuda")
+    fields = {n: t for n, t in dev.items() if not n.startswith("kv_scale")}
+    if case.kv_scales is not None:
+        fields["kv_scales"] = (dev["kv_scale0"], dev["kv_scale1"])
+    dc = W.Case(**{**case.__dict__, **fields})
     run = Runner(dc, stream)
     y_host = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
 
@@ -263,21 +276,23 @@ def e2e_timed(case: W.Case, stream, steps, warmup, dist_on):
 def oracle_sample(case: W.Case, budget_s: float, max_units=None):
     """Time the CPU oracle, as it stands, on whole sequences of the workload
     (all heads), shortest first, until ``budget_s`` seconds have been spent.
-    Returns (flops done, seconds, threads, description)."""
+    Returns (work done, seconds, threads, description); work is FLOPs, or
+    decode bytes for a decode workload."""
     import oracle   # the CPU baseline leg is one of the oracle's permitted users
     order = sorted(range(case.batch), key=lambda b: (case.q_lens[b] * case.kv_lens[b], b))
     threads = os.cpu_count() or 1
     done_flops, spent, seqs = 0.0, 0.0, []
     for b in order:
         sub = single_sequence(case, b)
-        f = metrics.flops(sub)
-        if f == 0:
+        if metrics.flops(sub) == 0:
             continue
+        f = metrics.decode_bytes(sub) if metrics.is_decode(case) else metrics.flops(sub)
         t0 = time.perf_counter()
         oracle.attention(sub.q, sub.k, sub.v, q_form=sub.q_form, kv_form=sub.kv_form,
                          query_lengths=sub.query_lengths, kv_lengths=sub.kv_lengths,
                          mask=sub.mask, scale=sub.scale, causal=sub.causal, norm=sub.norm,
-                         quant=sub.quant, quant_scale=sub.quant_scale, nthreads=threads)
+                         quant=sub.quant, quant_scale=sub.quant_scale, nthreads=threads,
+                         kv_fp8_scales=sub.kv_scales)
         spent += time.perf_counter() - t0
         done_flops += f
         seqs.append(b)
@@ -408,7 +423,7 @@ def main():
 
     secondary = {}
     if not args.no_secondary:
-        for idx, q in ((3, "fp8"), (4, "fp8"), (5, "fp8"), (5, "int8"), (6, "fp8")):
+        for idx, q in ((3, "fp8"), (4, "fp8"), (5, "fp8"), (5, "int8"), (6, "fp8"), (7, "fp8")):
             if idx == args.workload:
                 continue
             torch.cuda.empty_cache()
@@ -483,10 +498,8 @@ def reference_arm(args, rank, world):
         f, s, thr, desc = oracle_sample(case, 0.0, max_units=1)
         flops += f
         secs += s
-    unit = "TFLOP/s"
-    if metrics.is_decode(case):
-        unit = "GB/s"
-    val = flops / secs / 1e12 if secs > 0 else None
+    unit, div = ("GB/s", 1e9) if metrics.is_decode(case) else ("TFLOP/s", 1e12)
+    val = flops / secs / div if secs > 0 else None
     line = {"impl": "reference", "metric": "attention TFLOP/s (prefill) / KV-read GB/s (decode) "
             "and % of roofline, 1 GB300", "value": val, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,

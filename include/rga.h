@@ -67,9 +67,13 @@ typedef enum {
 /* TRT_normalization_op. */
 typedef enum { RGA_NORM_SOFTMAX = 0, RGA_NORM_NONE = 1 } rga_norm;
 
-/* Element types.  Q, K, V and Y share one of F16 / BF16.  A mask is BOOL
- * (one byte per element, non-zero = may attend) or additive F16/BF16/F32. */
-typedef enum { RGA_F16 = 0, RGA_BF16 = 1, RGA_F32 = 2, RGA_BOOL = 3 } rga_dtype;
+/* Element types.  Q, K, V and Y share one of F16 / BF16 (K and V are
+ * E4M3 codes for trt_attention_fp8_kv).  A mask is BOOL (one byte per
+ * element, non-zero = may attend) or additive F16/BF16/F32.  FP8_E4M3: OCP
+ * E4M3FN codes, one byte each (an fp8 KV cache). */
+typedef enum {
+    RGA_F16 = 0, RGA_BF16 = 1, RGA_F32 = 2, RGA_BOOL = 3, RGA_FP8_E4M3 = 4
+} rga_dtype;
 
 /* normalization_quantize_to_type (TRT_QuantizedAttention). */
 typedef enum { RGA_QUANT_FP8_E4M3 = 0, RGA_QUANT_INT8 = 1 } rga_quant;
@@ -155,6 +159,24 @@ rga_status trt_quantized_attention(const rga_attention_args *args,
                                    rga_dtype quant_scale_dtype,
                                    cudaStream_t stream);
 
+/* Attention over an FP8 KV cache ("TensorRT Plugins Guide",
+ * AttentionPlugin: kv_cache_type FP8, vanilla and tree decoding).  Same as
+ * trt_attention, except that args->k and args->v hold OCP E4M3FN codes (one
+ * byte per element, same shapes and forms as there) and the keys and values
+ * attended are
+ *     K[..] = e4m3(code) * (*k_scale),   V[..] = e4m3(code) * (*v_scale)
+ * (per-tensor dequantisation; k_scale, v_scale: device pointers to one
+ * float each, required).  args->dtype is the type of q and y (F16 or BF16);
+ * k and v must be 16-byte aligned.  The codes past a sequence's kv length
+ * may hold any bits, NaN codes included.
+ * Supported for decode shapes: q_heads / kv_heads <= 16 and either padded q
+ * with q_seq * (q_heads / kv_heads) <= 16 or packed q with q_seq <= 8 *
+ * batch (one token per sequence, or a few draft tokens for tree decoding
+ * with a bool mask).  Other shapes return RGA_ERR_UNSUPPORTED.  Workspace:
+ * rga_attention_workspace_size(args) bytes. */
+rga_status trt_attention_fp8_kv(const rga_attention_args *args, const float *k_scale,
+                                const float *v_scale, cudaStream_t stream);
+
 /* Size of the library-owned device scratch used by
  * trt_attention_static_scratch (40 MiB). */
 #define RGA_STATIC_SCRATCH_BYTES (40ull << 20)
@@ -199,7 +221,8 @@ rga_status trt_attention_static_scratch(const rga_attention_args *args, cudaStre
  * written rows move); otherwise the whole cache is copied to y with the
  * update applied, and y must not overlap past_cache or update otherwise.
  * The op moves element bits without arithmetic: dtype only sets the element
- * size (RGA_F16, RGA_BF16 or RGA_F32).
+ * size (RGA_F16, RGA_BF16, RGA_F32, or RGA_FP8_E4M3 for an fp8 cache whose
+ * update arrives already encoded).
  * Errors: RGA_ERR_INVALID_ARG for bad pointers, shapes or enums (nothing is
  * enqueued); batch > 8192 gives RGA_ERR_UNSUPPORTED.  On the device, a
  * window [w_b, w_b + len_b) outside [0, N), negative or non-cumulative
@@ -210,7 +233,7 @@ typedef struct {
     const void *past_cache;
     const void *update;
     void *y;
-    rga_dtype dtype;               /* element size only: F16, BF16 or F32 */
+    rga_dtype dtype;               /* element size only: F16, BF16, F32 or FP8_E4M3 */
     rga_form update_form;
     int32_t batch, heads, cache_seq, head_dim;
     int32_t update_seq;            /* padded: N_u of the update; packed: rows T */
@@ -238,6 +261,13 @@ rga_status rga_get_device_status(const int32_t *device_status,
  * out of range. */
 rga_status rga_selftest_wait_timeout(int32_t *device_status, int64_t wait_cycles,
                                      cudaStream_t stream);
+
+/* Conversion self-test of the fp8 KV cache path: enqueue one CTA that
+ * decodes all 256 E4M3 codes with the in-register conversion of the decode
+ * kernel and writes the f16 bits of code c to out_f16[c] and the bf16 bits
+ * to out_bf16[c] (device arrays of 256 uint16 each, owned by the caller).
+ * Returns RGA_ERR_INVALID_ARG for a null pointer. */
+rga_status rga_selftest_e4m3_decode(uint16_t *out_f16, uint16_t *out_bf16, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *rga_status_string(rga_status status);

@@ -15,7 +15,10 @@ TRT_QuantizedAttention sections), for every query row:
     p     = s_q * Q(p / s_q)            (quantized op only; fp8 E4M3FN or int8)
     y_i   = sum_{j in A} p_j v_j
 
-in double precision from the stored fp16/bf16 input values.  The arithmetic
+in double precision from the stored fp16/bf16 input values.  For an FP8 KV
+cache ("TensorRT Plugins Guide", AttentionPlugin: kv_cache_type FP8) the
+keys and values are first dequantised: decoded E4M3FN code times the
+tensor's scale (``dequant_e4m3``, ``attention(..., kv_fp8_scales=...)``).  The arithmetic
 lives in ``rga_oracle.c`` (compiled with gcc on first use); this module only
 marshals arrays.
 
@@ -72,6 +75,8 @@ def _load():
             lib.rga_oracle_e4m3_round.argtypes = [d]
             lib.rga_oracle_e4m3_encode.restype = i
             lib.rga_oracle_e4m3_encode.argtypes = [d]
+            lib.rga_oracle_e4m3_dequant.restype = None
+            lib.rga_oracle_e4m3_dequant.argtypes = [p, ctypes.c_long, d, p]
             lib.rga_oracle_int8_round.restype = d
             lib.rga_oracle_int8_round.argtypes = [d]
             _lib = lib
@@ -111,7 +116,7 @@ class OracleError(RuntimeError):
 def attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=None,
               kv_lengths=None, mask=None, scale=1.0, causal="none",
               norm="softmax", quant=None, quant_scale=None, y_init=None,
-              nthreads=None, ambiguity_eps=None):
+              nthreads=None, ambiguity_eps=None, kv_fp8_scales=None):
     """Plain fp64 attention.  Returns a float64 array shaped like ``q``.
 
     q: padded [B,Hq,Nq,D] or packed [Tq,Hq,D]; k, v likewise for KV.
@@ -122,6 +127,8 @@ def attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=None,
     the scaled scores), rank <= 4, right-aligned to [B, Hq, Nq, Nkv].
     quant: None, 'fp8' or 'int8'; quant_scale the stored scale value.
     Rows that are not valid query rows keep ``y_init`` (default NaN).
+    kv_fp8_scales: (k_scale, v_scale) when k and v hold E4M3FN codes (uint8
+    or float8_e4m3fn tensors / uint8 arrays): they are dequantised first.
     With ``ambiguity_eps`` (quantized op), returns ``(y, amb)``: amb bounds
     how far a quantised code within relative ``ambiguity_eps`` of a rounding
     midpoint may move each output element if it rounds the other way.
@@ -129,7 +136,11 @@ def attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=None,
     lib = _load()
     qf = PACKED if q_form in ("packed", "packed_nhd", PACKED) else PADDED
     kf = PACKED if kv_form in ("packed", "packed_nhd", PACKED) else PADDED
-    Q, K, V = _f64(q), _f64(k), _f64(v)
+    if kv_fp8_scales is not None:
+        K, V = dequant_e4m3(k, kv_fp8_scales[0]), dequant_e4m3(v, kv_fp8_scales[1])
+    else:
+        K, V = _f64(k), _f64(v)
+    Q = _f64(q)
     D = Q.shape[-1]
     Hq = Q.shape[-2] if qf == PACKED else Q.shape[1]
     Hkv = K.shape[-2] if kf == PACKED else K.shape[1]
@@ -170,6 +181,28 @@ def attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=None,
         raise OracleError(rc)
     return Y if amb is None else (Y, amb)
 
+
+
+def _codes(x):
+    """uint8 numpy copy of E4M3 codes (uint8 / float8_e4m3fn tensor or array)."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().cpu()
+        if x.dtype != torch.uint8:
+            x = x.view(torch.uint8)
+        x = x.numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.uint8))
+
+
+def dequant_e4m3(codes, scale):
+    """fp64 values of an FP8 KV cache tensor: decoded code times ``scale``
+    (a float or a one-element tensor holding the stored fp32 scale)."""
+    c = _codes(codes)
+    s = float(_f64(scale).reshape(-1)[0]) if hasattr(scale, "detach") or isinstance(
+        scale, np.ndarray) else float(scale)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().rga_oracle_e4m3_dequant(_ptr(c), c.size, s, _ptr(out))
+    return out
 
 
 def e4m3_decode(code: int) -> float:

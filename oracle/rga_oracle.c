@@ -110,6 +110,16 @@ int rga_oracle_e4m3_encode(double x)
     return -1;
 }
 
+/* FP8 KV cache ("TensorRT Plugins Guide", AttentionPlugin: kv_cache_type
+ * FP8): the cache holds E4M3FN codes and one scale per tensor; the key or
+ * value element is the decoded code times the scale.  out[i] for i < n. */
+void rga_oracle_e4m3_dequant(const unsigned char *codes, long n, double scale, double *out)
+{
+    long i;
+    for (i = 0; i < n; ++i)
+        out[i] = rga_oracle_e4m3_decode(codes[i]) * scale;
+}
+
 /* int8 QuantizeLinear with zero-point 0: round half to even, clamp. */
 double rga_oracle_int8_round(double x)
 {

@@ -29,11 +29,15 @@ FORMS = {"padded": 0, "padded_bhnd": 0, "packed": 1, "packed_nhd": 1}
 CAUSAL = {"none": 0, "upper_left": 1, "lower_right": 2}
 NORM = {"softmax": 0, "none": 1}
 QUANT = {"fp8": 0, "int8": 1}
-DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.bool: 3}
+DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.bool: 3,
+          torch.float8_e4m3fn: 4}
+# tensors that may carry E4M3 codes (an fp8 KV cache)
+FP8_CODE_DTYPES = (torch.float8_e4m3fn, torch.uint8)
 
 EXPORTED = ("rga_attention_workspace_size", "trt_attention", "trt_quantized_attention",
             "rga_get_device_status", "rga_status_string", "rga_abi_version",
-            "trt_attention_static_scratch", "trt_kv_cache_update", "rga_selftest_wait_timeout")
+            "trt_attention_static_scratch", "trt_kv_cache_update", "rga_selftest_wait_timeout",
+            "trt_attention_fp8_kv", "rga_selftest_e4m3_decode")
 
 
 class Args(ctypes.Structure):
@@ -105,6 +109,10 @@ def load(build_if_missing: bool = False):
             lib.rga_abi_version.argtypes = []
             lib.rga_selftest_wait_timeout.restype = c_int
             lib.rga_selftest_wait_timeout.argtypes = [c_vp, c_i64, c_vp]
+            lib.trt_attention_fp8_kv.restype = c_int
+            lib.trt_attention_fp8_kv.argtypes = [P, c_vp, c_vp, c_vp]
+            lib.rga_selftest_e4m3_decode.restype = c_int
+            lib.rga_selftest_e4m3_decode.argtypes = [c_vp, c_vp, c_vp]
             lib.trt_kv_cache_update.restype = c_int
             lib.trt_kv_cache_update.argtypes = [ctypes.POINTER(KvArgs), c_vp]
             _lib = lib
@@ -184,7 +192,9 @@ def _stream_handle(stream):
     return s.cuda_stream
 
 
-def _call(quant, q, k, v, out, quant_args, stream, **kw):
+def _call(kind, q, k, v, out, extra, stream, **kw):
+    """kind: 'plain' (trt_attention), 'quant' (extra = (qtype, quant_scale))
+    or 'fp8kv' (extra = (k_scale, v_scale))."""
     lib = load()
     y = torch.full_like(q, float("nan")) if out is None else out
     status = kw.pop("status", None)
@@ -198,11 +208,15 @@ def _call(quant, q, k, v, out, quant_args, stream, **kw):
             ws = _workspace(q.device, n)
             a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
     h = _stream_handle(stream)
-    if quant:
-        qt, qs = quant_args
+    if kind == "quant":
+        qt, qs = extra
         rc = lib.trt_quantized_attention(ctypes.byref(a), QUANT[qt], qs.data_ptr(),
                                          DTYPES[qs.dtype], h)
         name = "trt_quantized_attention"
+    elif kind == "fp8kv":
+        ks, vs = extra
+        rc = lib.trt_attention_fp8_kv(ctypes.byref(a), ks.data_ptr(), vs.data_ptr(), h)
+        name = "trt_attention_fp8_kv"
     else:
         rc = lib.trt_attention(ctypes.byref(a), h)
         name = "trt_attention"
@@ -217,7 +231,7 @@ def trt_attention(q, k, v, *, q_form="padded", kv_form="padded", query_lengths=N
     """TRT_Attention forward.  Tensors are CUDA tensors; returns Y (and the
     device status word when ``return_status``).  ``scale`` defaults to 1.0:
     the operator itself does not scale Q/K/V."""
-    y, st = _call(False, q, k, v, out, None, stream, q_form=q_form, kv_form=kv_form,
+    y, st = _call("plain", q, k, v, out, None, stream, q_form=q_form, kv_form=kv_form,
                   query_lengths=query_lengths, kv_lengths=kv_lengths, mask=mask,
                   scale=scale, causal=causal, norm=norm, workspace=workspace, status=status)
     return (y, st) if return_status else y
@@ -236,11 +250,46 @@ def trt_quantized_attention(q, k, v, *, quant_scale, quant="fp8", q_form="padded
     if causal is None:
         causal = "upper_left" if is_causal else "none"
     _need_cuda("quant_scale", quant_scale)
-    y, st = _call(True, q, k, v, out, (quant, quant_scale), stream, q_form=q_form,
+    y, st = _call("quant", q, k, v, out, (quant, quant_scale), stream, q_form=q_form,
                   kv_form=kv_form, query_lengths=query_lengths, kv_lengths=kv_lengths,
                   mask=mask, scale=scale, causal=causal, norm=norm, workspace=workspace,
                   status=status)
     return (y, st) if return_status else y
+
+
+def trt_attention_fp8_kv(q, k, v, *, k_scale, v_scale, q_form="padded", kv_form="padded",
+                         query_lengths=None, kv_lengths=None, mask=None, scale=1.0,
+                         causal="none", norm="softmax", out=None, workspace=None, status=None,
+                         stream=None, return_status=False):
+    """Attention over an FP8 KV cache: ``k`` and ``v`` hold E4M3 codes
+    (torch.float8_e4m3fn, or uint8 holding the codes), dequantised with the
+    one-element fp32 CUDA tensors ``k_scale`` and ``v_scale``; ``q`` and the
+    returned Y are f16 or bf16.  Decode shapes only (see include/rga.h)."""
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype not in FP8_CODE_DTYPES:
+            raise ValueError(f"{name} must hold E4M3 codes (float8_e4m3fn or uint8)")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _need_cuda(name, t)
+        if t.dtype != torch.float32 or t.numel() != 1:
+            raise ValueError(f"{name} must be a one-element fp32 CUDA tensor")
+    y, st = _call("fp8kv", q, k, v, out, (k_scale, v_scale), stream, q_form=q_form,
+                  kv_form=kv_form, query_lengths=query_lengths, kv_lengths=kv_lengths,
+                  mask=mask, scale=scale, causal=causal, norm=norm, workspace=workspace,
+                  status=status)
+    return (y, st) if return_status else y
+
+
+def selftest_e4m3_decode(device=None):
+    """(f16 bits, bf16 bits) of all 256 E4M3 codes through the decode
+    kernel's in-register conversion, as int16 CUDA tensors."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    f16 = torch.zeros(256, dtype=torch.int16, device=dev)
+    bf16 = torch.zeros(256, dtype=torch.int16, device=dev)
+    rc = load().rga_selftest_e4m3_decode(f16.data_ptr(), bf16.data_ptr(),
+                                         c_vp(_stream_handle(None)))
+    if rc != RGA_OK:
+        raise RgaError(rc, "rga_selftest_e4m3_decode")
+    return f16, bf16
 
 
 def device_status(status, stream=None) -> int:
@@ -266,7 +315,7 @@ def make_kv_args(past_cache, update, y, *, update_form="padded", write_indices=N
         raise ValueError("past_cache, update and y must share one dtype")
     a = KvArgs()
     a.past_cache, a.update, a.y = _ptr(past_cache), _ptr(update), _ptr(y)
-    a.dtype = DTYPES.get(past_cache.dtype, -1)
+    a.dtype = 4 if past_cache.dtype == torch.uint8 else DTYPES.get(past_cache.dtype, -1)
     a.update_form = FORMS[update_form]
     B, H, N, D = past_cache.shape
     a.batch, a.heads, a.cache_seq, a.head_dim = B, H, N, D

@@ -37,15 +37,18 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Tiled TMA descriptor over a row-major tensor whose innermost dim is D
-// (16-bit elements), 128-byte swizzle, 64-element inner box.
+// Tiled TMA descriptor over a row-major tensor whose innermost dim is D:
+// 16-bit elements with a 64-element inner box by default, or bytes (esize
+// 1, fp8 codes) with a D-byte inner box; `swizzle` as the box's row size
+// allows (128-byte rows: 128B, 64-byte rows: 64B).
 bool encode(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
-            const uint32_t *box) {
+            const uint32_t *box, int esize = 2,
+            CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = get_encode();
     if (!fn) return false;
     cuuint64_t gd[5], gs[4];
     cuuint32_t bd[5], es[5];
-    uint64_t stride = 2;
+    uint64_t stride = (uint64_t)esize;
     for (int i = 0; i < rank; ++i) {
         gd[i] = dims[i] < 1 ? 1 : dims[i];
         bd[i] = box[i];
@@ -53,8 +56,8 @@ bool encode(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
         if (i > 0) gs[i - 1] = stride;
         stride *= gd[i];
     }
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, rank, const_cast<void *>(base), gd, gs, bd, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return fn(m, esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+              rank, const_cast<void *>(base), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -79,6 +82,19 @@ bool encode_kv(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t r
     const uint64_t d[4] = {(uint64_t)p.D, (uint64_t)p.kv_seq, (uint64_t)p.Hkv, (uint64_t)p.B};
     const uint32_t b[4] = {64, rows, 1, 1};
     return encode(m, base, 4, d, b);
+}
+
+// fp8 K or V (one byte per element): a box is `rows` whole D-byte rows.
+bool encode_kv8(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t rows) {
+    const CUtensorMapSwizzle sw = p.D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (p.kv_packed) {
+        const uint64_t d[3] = {(uint64_t)p.D, (uint64_t)p.Hkv, (uint64_t)p.kv_seq};
+        const uint32_t b[3] = {(uint32_t)p.D, 1, rows};
+        return encode(m, base, 3, d, b, 1, sw);
+    }
+    const uint64_t d[4] = {(uint64_t)p.D, (uint64_t)p.kv_seq, (uint64_t)p.Hkv, (uint64_t)p.B};
+    const uint32_t b[4] = {(uint32_t)p.D, rows, 1, 1};
+    return encode(m, base, 4, d, b, 1, sw);
 }
 
 // Bound on the decode work pairs (batch, KV head, chunk of DEC_ROWS query
@@ -180,7 +196,7 @@ AttnParams make_params(const rga_attention_args *a, bool quant) {
     else
         p.max_items = p.Hkv * p.B * ((p.q_seq + it - 1) / it);
     p.max_pairs = (int)dec_max_pairs(p.B, p.Hkv, p.G, p.q_seq, p.q_packed != 0);
-    p.dec_slots = 2 * DEC_WARPS * (sm_count() > 0 ? sm_count() : 1);
+    p.dec_slots = 2 * DEC_WARPS_MAX * (sm_count() > 0 ? sm_count() : 1);
     p.status = a->device_status;
     p.ws = static_cast<uint8_t *>(a->workspace);
     (void)quant;
@@ -197,10 +213,17 @@ size_t workspace_bytes(const rga_attention_args *a, bool quant) {
     return n;
 }
 
+// kv8: K and V are E4M3 codes dequantised with *k_scale / *v_scale (the
+// fp8 KV cache; decode shapes only).
 rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const void *qscale,
-               rga_dtype qscale_dtype, cudaStream_t stream) {
+               rga_dtype qscale_dtype, cudaStream_t stream, bool kv8 = false,
+               const float *k_scale = nullptr, const float *v_scale = nullptr) {
     rga_status st = validate(a, quant);
     if (st != RGA_OK) return st;
+    if (kv8) {
+        if (!k_scale || !v_scale) return RGA_ERR_INVALID_ARG;
+        if (!use_decode(a, false)) return RGA_ERR_UNSUPPORTED;
+    }
     if (quant) {
         if (qtype != RGA_QUANT_FP8_E4M3 && qtype != RGA_QUANT_INT8) return RGA_ERR_INVALID_ARG;
         if (!qscale) return RGA_ERR_INVALID_ARG;
@@ -220,6 +243,9 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
         p.qscale = qscale;
         p.qscale_dtype = qscale_dtype;
     }
+    p.kv8 = kv8;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     const int bf16 = a->dtype == RGA_BF16;
     // Zero-extent K/V (no keys anywhere): the descriptors are never read,
     // so they point at Y, which is a valid address.
@@ -228,9 +254,11 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
     const bool dec = use_decode(a, quant);
     TensorMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    if (!encode_q(&maps.q, p.q, p) || !encode_q(&maps.y, p.y, p) ||
-        !encode_kv(&maps.k, kp, p, dec ? DEC_KEYS : BN) ||
-        !encode_kv(&maps.v, vp, p, dec ? DEC_KEYS : BN))
+    if (!encode_q(&maps.q, p.q, p) || !encode_q(&maps.y, p.y, p))
+        return RGA_ERR_CUDA;
+    if (kv8 ? !encode_kv8(&maps.k, kp, p, DEC_KEYS) || !encode_kv8(&maps.v, vp, p, DEC_KEYS)
+            : !encode_kv(&maps.k, kp, p, dec ? DEC_KEYS : BN) ||
+                  !encode_kv(&maps.v, vp, p, dec ? DEC_KEYS : BN))
         return RGA_ERR_CUDA;
     int mode;
     if (a->norm == RGA_NORM_SOFTMAX) mode = quant ? MODE_SOFTMAX_Q : MODE_SOFTMAX;
@@ -242,7 +270,7 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
         const int sms = sm_count();
         if (sms <= 0) return RGA_ERR_CUDA;
         p.grid = sms;
-        e = launch_decode(p, maps, mode, stream, bf16);
+        e = launch_decode(p, maps, mode, stream, bf16, kv8);
     } else {
         int grid = sm_count();
         if (grid <= 0) return RGA_ERR_CUDA;
@@ -279,6 +307,11 @@ rga_status trt_quantized_attention(const rga_attention_args *args, rga_quant qty
                                    const void *quant_scale, rga_dtype quant_scale_dtype,
                                    cudaStream_t stream) {
     return run(args, true, qtype, quant_scale, quant_scale_dtype, stream);
+}
+
+rga_status trt_attention_fp8_kv(const rga_attention_args *args, const float *k_scale,
+                                const float *v_scale, cudaStream_t stream) {
+    return run(args, false, RGA_QUANT_FP8_E4M3, nullptr, RGA_F32, stream, true, k_scale, v_scale);
 }
 
 rga_status rga_get_device_status(const int32_t *device_status, cudaStream_t stream,

@@ -18,6 +18,14 @@
 // written to Y by its warp; a pair cut by range ends leaves a partial
 // (O, m, l) per warp, and the last of its warps to finish (atomic ticket)
 // merges them in warp order and writes Y.
+//
+// FP8 KV cache ("TensorRT Plugins Guide", AttentionPlugin: kv_cache_type
+// FP8): K and V hold OCP E4M3FN codes with one dequantisation scale each.
+// The tiles arrive as bytes (half the HBM traffic), each thread converts its
+// MMA operand fragments to f16/bf16 in registers (exactly: every E4M3 value
+// is an f16 and a bf16 value), the K scale is folded into the softmax scale
+// and the V scale into the final 1/l.  An fp8 CTA runs 8 warps, since a
+// tile carries half the bytes and more arithmetic per byte.
 #include <cuda.h>
 #include "device_common.cuh"
 #include "kernels.h"
@@ -25,18 +33,19 @@
 
 namespace rga {
 
-constexpr int DEC_THREADS = DEC_WARPS * 32;
-
-template <int D>
+// KV8: K and V are E4M3 codes (one byte per element).
+template <int D, bool KV8>
 struct DecLayout {
-    static constexpr int BLK = DEC_KEYS * 128;          // 32 rows x 64 columns x 2 bytes
-    static constexpr int TILE = (D / 64) * BLK;          // one K or V tile
+    static constexpr int NW = KV8 ? DEC_WARPS_KV8 : DEC_WARPS;   // warps per CTA
+    static constexpr int THREADS = NW * 32;
+    static constexpr int BLK = DEC_KEYS * 128;          // 16-bit: 32 rows x 64 columns x 2 bytes
+    static constexpr int TILE = KV8 ? DEC_KEYS * D : (D / 64) * BLK;   // one K or V tile
     static constexpr int STAGE = 2 * TILE;               // K + V
     static constexpr int WARP_RING = DEC_STAGES * STAGE;
-    static constexpr int RING = DEC_WARPS * WARP_RING;
+    static constexpr int RING = NW * WARP_RING;
     static constexpr int BAR_OFF = RING;
-    static constexpr int SCR_OFF = BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 64;   // prefix scratch
-    static constexpr int TPRE_OFF = SCR_OFF + (DEC_THREADS + 1) * 4 + 12;
+    static constexpr int SCR_OFF = BAR_OFF + NW * DEC_STAGES * 8 + 64;   // prefix scratch
+    static constexpr int TPRE_OFF = SCR_OFF + (THREADS + 1) * 4 + 12;
     static constexpr int PPRE_OFF = TPRE_OFF + (DEC_MAX_B + 1) * 4;
     static constexpr int BYTES = PPRE_OFF + (DEC_MAX_B + 1) * 4 + 64;
     static constexpr int ALLOC = BYTES + 1024;
@@ -77,9 +86,22 @@ __device__ __forceinline__ uint32_t swz(int row, int ch, int blk) {
     return (ch >> 3) * blk + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
 }
 
+template <bool KV8>
 __device__ __forceinline__ void dec_tma(const AttnParams &p, const TensorMaps &tm,
                                         const SeqInfo &s, int b, int g, int j0, uint8_t *dst,
                                         uint64_t *bar, int D) {
+    if constexpr (KV8) {   // one box of DEC_KEYS rows x D bytes per tensor
+        const int tile = DEC_KEYS * D;
+        mbar_arrive_expect_tx(bar, 2 * tile);
+        if (p.kv_packed) {
+            tma_load_3d(dst, &tm.k, bar, 0, g, s.kv_off + j0);
+            tma_load_3d(dst + tile, &tm.v, bar, 0, g, s.kv_off + j0);
+        } else {
+            tma_load_4d(dst, &tm.k, bar, 0, j0, g, b);
+            tma_load_4d(dst + tile, &tm.v, bar, 0, j0, g, b);
+        }
+        return;
+    }
     const int tile = (D / 64) * DEC_KEYS * 128;
     mbar_arrive_expect_tx(bar, 2 * tile);
     for (int blk = 0; blk < D / 64; ++blk) {
@@ -116,31 +138,17 @@ __device__ __forceinline__ DecRow dec_row(const AttnParams &p, const SeqInfo &s,
     return r;
 }
 
-// One 32-key tile for the warp's 16 query rows: S = Q K^T, scale and mask,
-// online softmax (or 'none'), O += P V.  Rows rr[0..1] are this lane's rows
-// (lane/4 and lane/4 + 8); kb/vb: the tile's K and V in shared memory.
-template <int D, bool BF16, bool SOFTMAX>
-__device__ __forceinline__ void dec_tile(const AttnParams &p, const DecRow (&rr)[2],
-                                         const uint32_t (&qa)[D / 16][4], uint32_t kb,
-                                         uint32_t vb, int j0, float (&o)[D / 8][4],
-                                         float (&m_r)[2], float (&l_r)[2]) {
-    using L = DecLayout<D>;
-    constexpr int NT = D / 8, KS = D / 16;
+// Scale, mask and online softmax ('none': scale and mask only) of one
+// 32-key score tile held as four m16n8 accumulators: column n * 8 + 2 (lane
+// % 4) + e % 2 is key j0 + that column; rows rr[0..1] are this lane's rows
+// (lane / 4 and lane / 4 + 8).  sc: the score scale (times log2 e for
+// softmax).  Leaves P in sacc and rescales O and l.
+template <int D, bool SOFTMAX>
+__device__ __forceinline__ void dec_normalize(const AttnParams &p, const DecRow (&rr)[2],
+                                              float (&sacc)[4][4], int j0, float (&o)[D / 8][4],
+                                              float (&m_r)[2], float (&l_r)[2], float sc) {
+    constexpr int NT = D / 8;
     const int lane = threadIdx.x & 31;
-    const float sc = SOFTMAX ? p.scale_log2 : p.scale;
-    float sacc[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ks += 2) {
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(kb + swz(nt * 8 + (lane & 7), ks * 2 + (lane >> 3), L::BLK), r0, r1, r2, r3);
-            mma16816<BF16>(sacc[nt], qa[ks], r0, r1);
-            mma16816<BF16>(sacc[nt], qa[ks + 1], r2, r3);
-        }
-    }
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -175,13 +183,46 @@ __device__ __forceinline__ void dec_tile(const AttnParams &p, const DecRow (&rr)
             }
         }
     }
+}
+
+// P of keys kk * 16 .. kk * 16 + 15 as the A fragment of an m16n8k16 MMA.
+template <bool BF16>
+__device__ __forceinline__ void dec_p_frag(const float (&sacc)[4][4], int kk, uint32_t (&a)[4]) {
+    a[0] = pack2<BF16>(sacc[2 * kk][0], sacc[2 * kk][1]);
+    a[1] = pack2<BF16>(sacc[2 * kk][2], sacc[2 * kk][3]);
+    a[2] = pack2<BF16>(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+    a[3] = pack2<BF16>(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+}
+
+// One 32-key tile for the warp's 16 query rows: S = Q K^T, scale and mask,
+// online softmax (or 'none'), O += P V.  kb/vb: the tile's K and V in
+// shared memory (16-bit elements).
+template <int D, bool BF16, bool SOFTMAX>
+__device__ __forceinline__ void dec_tile(const AttnParams &p, const DecRow (&rr)[2],
+                                         const uint32_t (&qa)[D / 16][4], uint32_t kb,
+                                         uint32_t vb, int j0, float (&o)[D / 8][4],
+                                         float (&m_r)[2], float (&l_r)[2], float sc) {
+    using L = DecLayout<D, false>;
+    constexpr int NT = D / 8, KS = D / 16;
+    const int lane = threadIdx.x & 31;
+    float sacc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ks += 2) {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kb + swz(nt * 8 + (lane & 7), ks * 2 + (lane >> 3), L::BLK), r0, r1, r2, r3);
+            mma16816<BF16>(sacc[nt], qa[ks], r0, r1);
+            mma16816<BF16>(sacc[nt], qa[ks + 1], r2, r3);
+        }
+    }
+    dec_normalize<D, SOFTMAX>(p, rr, sacc, j0, o, m_r, l_r, sc);
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
         uint32_t a[4];
-        a[0] = pack2<BF16>(sacc[2 * kk][0], sacc[2 * kk][1]);
-        a[1] = pack2<BF16>(sacc[2 * kk][2], sacc[2 * kk][3]);
-        a[2] = pack2<BF16>(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-        a[3] = pack2<BF16>(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+        dec_p_frag<BF16>(sacc, kk, a);
 #pragma unroll
         for (int n = 0; n < NT; n += 2) {
             uint32_t r0, r1, r2, r3;
@@ -194,20 +235,166 @@ __device__ __forceinline__ void dec_tile(const AttnParams &p, const DecRow (&rr)
     }
 }
 
-// Y row of this lane's fragment rows, scaled by f (rows outside are skipped).
-template <int D, bool BF16>
+// Byte offset of 16-byte chunk `ch` of key row `row` in an fp8 tile of
+// D-byte rows as the TMA writes it: 128-byte swizzle for D = 128 (chunk
+// XOR row % 8), 64-byte swizzle for D = 64 (chunk XOR (row / 2) % 4).
+template <int D>
+__device__ __forceinline__ uint32_t off8(int row, int ch) {
+    if constexpr (D == 128) return row * 128 + ((ch ^ (row & 7)) << 4);
+    else return row * 64 + ((ch ^ ((row >> 1) & 3)) << 4);
+}
+
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&w)[4]) {
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+}
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t &w0, uint32_t &w1) {
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(addr));
+}
+
+// dec_tile for an fp8 KV cache: kb/vb hold E4M3 codes, converted in
+// registers.  Two fragment layouts differ from the 16-bit tile, each a
+// permutation that a dot product does not see:
+//  - S = Q K^T: thread t takes dims [c D/4, (c+1) D/4) of its key row
+//    (c = t % 4), four per k-step (k positions 2c, 2c+1, 2c+8, 2c+9 hold
+//    dims c D/4 + 4s + 0..3); Q was loaded with the same order;
+//  - O += P V: n-tile j, column n stands for dim n D/8 + j, so that a
+//    thread reads D/8 contiguous codes of each of its four key rows and
+//    pairs keys with byte permutes; accumulator o[j][e] therefore holds dim
+//    (2c + e % 2) D/8 + j of row lane/4 + 8 (e / 2).
+template <int D, bool BF16, bool SOFTMAX>
+__device__ __forceinline__ void dec_tile8(const AttnParams &p, const DecRow (&rr)[2],
+                                          const uint32_t (&qa)[D / 16][4], uint32_t kb,
+                                          uint32_t vb, int j0, float (&o)[D / 8][4],
+                                          float (&m_r)[2], float (&l_r)[2], float sc) {
+    constexpr int NT = D / 8, KS = D / 16, CH = D / 64;
+    const int lane = threadIdx.x & 31, c = lane & 3, r = lane >> 2;
+    float sacc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+        uint32_t kw[KS];
+#pragma unroll
+        for (int h = 0; h < CH; ++h) {
+            uint32_t w[4];
+            lds128(kb + off8<D>(nt * 8 + r, c * CH + h), w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) kw[4 * h + i] = w[i];
+        }
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t b0, b1;
+            e4m3x4_to_x2<BF16>(kw[ks], b0, b1);
+            mma16816<BF16>(sacc[nt], qa[ks], b0, b1);
+        }
+    }
+    dec_normalize<D, SOFTMAX>(p, rr, sacc, j0, o, m_r, l_r, sc);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a[4];
+        dec_p_frag<BF16>(sacc, kk, a);
+        // key rows k0, k0 + 1 (b0) and k0 + 8, k0 + 9 (b1); codes [r NT, r NT + NT)
+        const int k0 = kk * 16 + 2 * c;
+        uint32_t v0[NT / 4], v1[NT / 4], v8[NT / 4], v9[NT / 4];
+        if constexpr (D == 128) {
+            uint32_t w[4];
+            lds128(vb + off8<D>(k0, r), w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v0[i] = w[i];
+            lds128(vb + off8<D>(k0 + 1, r), w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v1[i] = w[i];
+            lds128(vb + off8<D>(k0 + 8, r), w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v8[i] = w[i];
+            lds128(vb + off8<D>(k0 + 9, r), w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v9[i] = w[i];
+        } else {
+            const int ch = r >> 1, half = (r & 1) * 8;
+            lds64(vb + off8<D>(k0, ch) + half, v0[0], v0[1]);
+            lds64(vb + off8<D>(k0 + 1, ch) + half, v1[0], v1[1]);
+            lds64(vb + off8<D>(k0 + 8, ch) + half, v8[0], v8[1]);
+            lds64(vb + off8<D>(k0 + 9, ch) + half, v9[0], v9[1]);
+        }
+#pragma unroll
+        for (int w = 0; w < NT / 4; ++w) {
+            uint32_t b0[4], b1[4];
+            e4m3x4_to_x2<BF16>(__byte_perm(v0[w], v1[w], 0x5140), b0[0], b0[1]);
+            e4m3x4_to_x2<BF16>(__byte_perm(v0[w], v1[w], 0x7362), b0[2], b0[3]);
+            e4m3x4_to_x2<BF16>(__byte_perm(v8[w], v9[w], 0x5140), b1[0], b1[1]);
+            e4m3x4_to_x2<BF16>(__byte_perm(v8[w], v9[w], 0x7362), b1[2], b1[3]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mma16816<BF16>(o[4 * w + i], a, b0[i], b1[i]);
+        }
+    }
+}
+
+// Dim of accumulator o[j][e] (e = 0..3) of this lane: the 16-bit tile keeps
+// the MMA's natural column order, the fp8 tile the permuted one above.
+template <int D, bool KV8>
+__device__ __forceinline__ int dec_dim(int j, int e) {
+    const int c = threadIdx.x & 3;
+    if constexpr (KV8) return (2 * c + (e & 1)) * (D / 8) + j;
+    else return j * 8 + 2 * c + (e & 1);
+}
+
+// Y rows of this lane's fragment rows, scaled by f (rows outside are skipped).
+template <int D, bool BF16, bool KV8>
 __device__ __forceinline__ void dec_store_y(const AttnParams &p, const DecRow (&rr)[2],
                                             const float (&o)[D / 8][4], const float (&f)[2]) {
+    constexpr int NT = D / 8;
     const int lane = threadIdx.x & 31;
     uint16_t *y = static_cast<uint16_t *>(p.y);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         if (!rr[r].valid) continue;
+        if constexpr (KV8) {
+            // this lane holds dims [2c NT, 2c NT + 2 NT) of the row, in order
+            uint4 *dst = reinterpret_cast<uint4 *>(y + rr[r].qoff + dec_dim<D, true>(0, 0));
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            const int col = n * 8 + (lane & 3) * 2;
-            *reinterpret_cast<uint32_t *>(y + rr[r].qoff + col) =
-                pack2<BF16>(o[n][2 * r] * f[r], o[n][2 * r + 1] * f[r]);
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int i = 0; i < NT / 8; ++i) {
+                    const int e2 = 2 * r + e;
+                    dst[e * (NT / 8) + i] = make_uint4(
+                        pack2<BF16>(o[8 * i][e2] * f[r], o[8 * i + 1][e2] * f[r]),
+                        pack2<BF16>(o[8 * i + 2][e2] * f[r], o[8 * i + 3][e2] * f[r]),
+                        pack2<BF16>(o[8 * i + 4][e2] * f[r], o[8 * i + 5][e2] * f[r]),
+                        pack2<BF16>(o[8 * i + 6][e2] * f[r], o[8 * i + 7][e2] * f[r]));
+                }
+        } else {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int col = n * 8 + (lane & 3) * 2;
+                *reinterpret_cast<uint32_t *>(y + rr[r].qoff + col) =
+                    pack2<BF16>(o[n][2 * r] * f[r], o[n][2 * r + 1] * f[r]);
+            }
+        }
+    }
+}
+
+// This lane's partial O rows (unnormalised) into one partial slot row pair.
+template <int D, bool KV8>
+__device__ __forceinline__ void dec_store_part(float *slot_rows, const float (&o)[D / 8][4]) {
+    constexpr int NT = D / 8;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        float *po = slot_rows + ((lane >> 2) + 8 * r) * D;
+        if constexpr (KV8) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int i = 0; i < NT / 4; ++i)
+                    *reinterpret_cast<float4 *>(po + dec_dim<D, true>(4 * i, e)) =
+                        make_float4(o[4 * i][2 * r + e], o[4 * i + 1][2 * r + e],
+                                    o[4 * i + 2][2 * r + e], o[4 * i + 3][2 * r + e]);
+        } else {
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                *reinterpret_cast<float2 *>(po + n * 8 + (lane & 3) * 2) =
+                    make_float2(o[n][2 * r], o[n][2 * r + 1]);
         }
     }
 }
@@ -232,9 +419,10 @@ __device__ __forceinline__ void dec_batch_shape(const AttnParams &p, const SeqIn
 }
 
 // Block-wide exclusive prefix of v[0..n) in place (n <= DEC_MAX_B), with
-// v[n] set to the total; every thread of the block calls it.
+// v[n] set to the total; every thread of the block (THREADS) calls it.
+template <int THREADS>
 __device__ __forceinline__ void dec_prefix(int *v, int n, int *scratch) {
-    const int per = (n + DEC_THREADS - 1) / DEC_THREADS;
+    const int per = (n + THREADS - 1) / THREADS;
     const int lo = threadIdx.x * per, hi = min(n, lo + per);
     int sum = 0;
     for (int i = lo; i < hi; ++i) sum += v[i];
@@ -242,12 +430,12 @@ __device__ __forceinline__ void dec_prefix(int *v, int n, int *scratch) {
     __syncthreads();
     if (threadIdx.x == 0) {
         int run = 0;
-        for (int t = 0; t < DEC_THREADS; ++t) {
+        for (int t = 0; t < THREADS; ++t) {
             const int x = scratch[t];
             scratch[t] = run;
             run += x;
         }
-        scratch[DEC_THREADS] = run;
+        scratch[THREADS] = run;
     }
     __syncthreads();
     int run = scratch[threadIdx.x];
@@ -256,36 +444,37 @@ __device__ __forceinline__ void dec_prefix(int *v, int n, int *scratch) {
         v[i] = run;
         run += x;
     }
-    if (threadIdx.x == 0) v[n] = scratch[DEC_THREADS];
+    if (threadIdx.x == 0) v[n] = scratch[THREADS];
     __syncthreads();
 }
 
-template <int D, bool BF16, bool SOFTMAX>
-__global__ void __launch_bounds__(DEC_THREADS, 1)
+template <int D, bool BF16, bool SOFTMAX, bool KV8>
+__global__ void __launch_bounds__(DecLayout<D, KV8>::THREADS, 1)
 decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TensorMaps tm) {
-    using L = DecLayout<D>;
+    using L = DecLayout<D, KV8>;
+    constexpr int NW = L::NW;
     constexpr int NT = D / 8;
     constexpr int KS = D / 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
-    volatile int *abort = reinterpret_cast<volatile int *>(sm + L::BAR_OFF + DEC_WARPS * DEC_STAGES * 8);
-    int *flags = reinterpret_cast<int *>(sm + L::BAR_OFF + DEC_WARPS * DEC_STAGES * 8 + 4);
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + L::BAR_OFF + NW * DEC_STAGES * 8);
+    int *flags = reinterpret_cast<int *>(sm + L::BAR_OFF + NW * DEC_STAGES * 8 + 4);
     int *scratch = reinterpret_cast<int *>(sm + L::SCR_OFF);
     int *tpre = reinterpret_cast<int *>(sm + L::TPRE_OFF);   // key tiles before batch b
     int *ppre = reinterpret_cast<int *>(sm + L::PPRE_OFF);   // pairs before batch b
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < DEC_WARPS * DEC_STAGES; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NW * DEC_STAGES; ++i) mbar_init(&bars[i], 1);
         *abort = 0;
         flags[0] = 0;   // bad lengths
         fence_mbar_init();
     }
     __syncthreads();
     // Every CTA validates the lengths and lays out the work itself.
-    for (int b = threadIdx.x; b < p.B; b += DEC_THREADS) {
+    for (int b = threadIdx.x; b < p.B; b += L::THREADS) {
         const int32_t *ql = p.query_lengths, *kl = p.kv_lengths;
         const SeqInfo s = seq_info(p, b);
         bool ok = s.q_len >= 0 && s.kv_len >= 0;
@@ -309,8 +498,8 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         if (blockIdx.x == 0 && threadIdx.x == 0) set_status(p.status, 4);
         return;
     }
-    dec_prefix(tpre, p.B, scratch);
-    dec_prefix(ppre, p.B, scratch);
+    dec_prefix<L::THREADS>(tpre, p.B, scratch);
+    dec_prefix<L::THREADS>(ppre, p.B, scratch);
     pdl_wait();   // the tickets have been cleared
 
     // Stream-K split of the work: all key tiles of all pairs, batch-major,
@@ -319,10 +508,10 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     // cut by range ends is finished by the last of its warps to arrive
     // (atomic ticket), which merges the others' partials in warp order.
     const int T = tpre[p.B];
-    const int wg = blockIdx.x * DEC_WARPS + warp;
+    const int wg = blockIdx.x * NW + warp;
     // at most one warp per tile, so that every range holds at least one
     // (the merge counts a pair's warps from the range ends); later warps idle
-    const int Wn = max(1, min((int)gridDim.x * DEC_WARPS, T));
+    const int Wn = max(1, min((int)gridDim.x * NW, T));
     auto range_start = [&](int w) { return (int)((long long)w * T / Wn); };
     auto warp_of = [&](int x) { return (int)(((long long)(x + 1) * Wn - 1) / T); };
     int *tickets = reinterpret_cast<int *>(p.ws + dec_tickets_off(p));
@@ -330,7 +519,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     float2 *pml = reinterpret_cast<float2 *>(p.ws + dec_ml_off(p));
 
     // batches with query rows but no key tile: their rows are zero
-    for (int b = wg; b < p.B; b += gridDim.x * DEC_WARPS) {
+    for (int b = wg; b < p.B; b += gridDim.x * NW) {
         const SeqInfo s = seq_info(p, b);
         int nrc, nt;
         dec_batch_shape(p, s, nrc, nt);
@@ -377,12 +566,16 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     auto issue = [&](const DecCur &c) {
         if (lane == 0) {
             fence_proxy_async_smem();   // the stage's previous tile was read by ldmatrix
-            dec_tma(p, tm, c.s, c.b, c.pib / c.nrc, c.tile * DEC_KEYS,
+            dec_tma<KV8>(p, tm, c.s, c.b, c.pib / c.nrc, c.tile * DEC_KEYS,
                     ring + (issued % DEC_STAGES) * L::STAGE, &wbar[issued % DEC_STAGES], D);
         }
         ++issued;
     };
 
+    // score scale (the K dequantisation scale folded in) and output factor
+    // (the V dequantisation scale)
+    const float sc = (SOFTMAX ? p.scale_log2 : p.scale) * (KV8 ? __ldg(p.k_scale) : 1.f);
+    const float sv = KV8 ? __ldg(p.v_scale) : 1.f;
     bool ok = true;
     if (t_begin < t_end) {
         DecCur lc, cc;
@@ -406,13 +599,34 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             rr[0] = dec_row(p, cc.s, cc.b, g, rc * DEC_ROWS + (lane >> 2), rows, kv_hi);
             rr[1] = dec_row(p, cc.s, cc.b, g, rc * DEC_ROWS + (lane >> 2) + 8, rows, kv_hi);
             const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
+            if constexpr (KV8) {
+                // dims [c D/4, (c+1) D/4) of each row, four per k-step (the
+                // contraction order of dec_tile8)
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int col = ks * 16 + (lane & 3) * 2;
-                qa[ks][0] = rr[0].valid ? q32[(rr[0].qoff + col) >> 1] : 0u;
-                qa[ks][1] = rr[1].valid ? q32[(rr[1].qoff + col) >> 1] : 0u;
-                qa[ks][2] = rr[0].valid ? q32[(rr[0].qoff + col + 8) >> 1] : 0u;
-                qa[ks][3] = rr[1].valid ? q32[(rr[1].qoff + col + 8) >> 1] : 0u;
+                for (int i = 0; i < 2; ++i) {
+                    uint32_t w[D / 8];
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        static_cast<const uint16_t *>(p.q) + rr[i].qoff + (lane & 3) * (D / 4));
+#pragma unroll
+                    for (int k = 0; k < D / 32; ++k) {
+                        const uint4 x = rr[i].valid ? src[k] : make_uint4(0, 0, 0, 0);
+                        w[4 * k] = x.x; w[4 * k + 1] = x.y; w[4 * k + 2] = x.z; w[4 * k + 3] = x.w;
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        qa[ks][i] = w[2 * ks];
+                        qa[ks][2 + i] = w[2 * ks + 1];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int col = ks * 16 + (lane & 3) * 2;
+                    qa[ks][0] = rr[0].valid ? q32[(rr[0].qoff + col) >> 1] : 0u;
+                    qa[ks][1] = rr[1].valid ? q32[(rr[1].qoff + col) >> 1] : 0u;
+                    qa[ks][2] = rr[0].valid ? q32[(rr[0].qoff + col + 8) >> 1] : 0u;
+                    qa[ks][3] = rr[1].valid ? q32[(rr[1].qoff + col + 8) >> 1] : 0u;
+                }
             }
 #pragma unroll
             for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -431,14 +645,17 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             const int rem = cc.s.kv_len - j0;
             if (rem < DEC_KEYS) {   // rows past the sequence end may hold NaN: zero them
                 uint8_t *vp = ring + st * L::STAGE + L::TILE;
-                for (int idx = lane; idx < DEC_KEYS * (D / 8); idx += 32) {
-                    const int row = idx / (D / 8), ch = idx % (D / 8);
+                constexpr int CPR = KV8 ? D / 16 : D / 8;   // 16-byte chunks per row
+                for (int idx = lane; idx < DEC_KEYS * CPR; idx += 32) {
+                    const int row = idx / CPR, ch = idx % CPR;
                     if (row >= rem)
-                        *reinterpret_cast<uint4 *>(vp + swz(row, ch, L::BLK)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vp + (KV8 ? off8<D>(row, ch) : swz(row, ch, L::BLK))) =
+                            make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
             }
-            dec_tile<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r);
+            if constexpr (KV8) dec_tile8<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc);
+            else dec_tile<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc);
             __syncwarp();
             if (next_issue < t_end) {   // refill the stage just used
                 issue(lc);
@@ -460,20 +677,16 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                     float f[2];
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
-                        f[r] = SOFTMAX ? (l_r[r] > 0.f ? 1.f / l_r[r] : 0.f) : 1.f;
-                    dec_store_y<D, BF16>(p, rr, o, f);
+                        f[r] = (SOFTMAX ? (l_r[r] > 0.f ? 1.f / l_r[r] : 0.f) : 1.f) * sv;
+                    dec_store_y<D, BF16, KV8>(p, rr, o, f);
                 } else {
                     // partial (O, m, l): slot 0 for the first pair of the
                     // range, slot 1 for the last
                     const size_t slot = (size_t)wg * 2 + (seg0 == t_begin ? 0 : 1);
+                    dec_store_part<D, KV8>(part + slot * DEC_ROWS * D, o);
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         const int row = (lane >> 2) + 8 * r;
-                        float *po = part + (slot * DEC_ROWS + row) * D;
-#pragma unroll
-                        for (int n = 0; n < NT; ++n)
-                            *reinterpret_cast<float2 *>(po + n * 8 + (lane & 3) * 2) =
-                                make_float2(o[n][2 * r], o[n][2 * r + 1]);
                         if ((lane & 3) == 0) pml[slot * DEC_ROWS + row] = make_float2(m_r[r], l_r[r]);
                     }
                     __threadfence();
@@ -519,7 +732,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                         }
                         const DecRow R = dec_row(p, cc.s, b, g, rc * DEC_ROWS + row, rows, kv_hi);
                         if (R.valid) {
-                            const float f = SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f;
+                            const float f = (SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f) * sv;
                             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff + c0);
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k)
@@ -556,12 +769,12 @@ __global__ void decode_prep_kernel(int *tickets, int n) {
         tickets[i] = 0;
 }
 
-template <int D, bool BF16, bool SOFTMAX>
+template <int D, bool BF16, bool SOFTMAX, bool KV8>
 static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStream_t s) {
-    using L = DecLayout<D>;
+    using L = DecLayout<D, KV8>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, SOFTMAX>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, SOFTMAX, KV8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -571,18 +784,25 @@ static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStre
         reinterpret_cast<int *>(p.ws + dec_tickets_off(p)), n);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_dependent(decode_kernel<D, BF16, SOFTMAX>, p.grid, DEC_THREADS, L::ALLOC, s, p, m);
+    return launch_dependent(decode_kernel<D, BF16, SOFTMAX, KV8>, p.grid, L::THREADS, L::ALLOC, s,
+                            p, m);
+}
+
+template <bool KV8>
+static cudaError_t dec_launch_kv(const AttnParams &p, const TensorMaps &m, bool sm,
+                                 cudaStream_t s, int bf16) {
+    if (p.D == 64) {
+        if (bf16) return sm ? dec_launch<64, true, true, KV8>(p, m, s) : dec_launch<64, true, false, KV8>(p, m, s);
+        return sm ? dec_launch<64, false, true, KV8>(p, m, s) : dec_launch<64, false, false, KV8>(p, m, s);
+    }
+    if (bf16) return sm ? dec_launch<128, true, true, KV8>(p, m, s) : dec_launch<128, true, false, KV8>(p, m, s);
+    return sm ? dec_launch<128, false, true, KV8>(p, m, s) : dec_launch<128, false, false, KV8>(p, m, s);
 }
 
 cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode, cudaStream_t s,
-                          int bf16) {
+                          int bf16, int kv8) {
     const bool sm = (mode == MODE_SOFTMAX);
-    if (p.D == 64) {
-        if (bf16) return sm ? dec_launch<64, true, true>(p, m, s) : dec_launch<64, true, false>(p, m, s);
-        return sm ? dec_launch<64, false, true>(p, m, s) : dec_launch<64, false, false>(p, m, s);
-    }
-    if (bf16) return sm ? dec_launch<128, true, true>(p, m, s) : dec_launch<128, true, false>(p, m, s);
-    return sm ? dec_launch<128, false, true>(p, m, s) : dec_launch<128, false, false>(p, m, s);
+    return kv8 ? dec_launch_kv<true>(p, m, sm, s, bf16) : dec_launch_kv<false>(p, m, sm, s, bf16);
 }
 
 }  // namespace rga

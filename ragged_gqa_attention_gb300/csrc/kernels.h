@@ -13,11 +13,15 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 
 // Decode geometry: 16 query rows per MMA row block, 32 keys per tile,
-// 4 independent warps per CTA with a DEC_STAGES-deep TMA ring each; the key
-// tiles of all work are split into equal contiguous ranges, one per warp.
+// independent warps (4 per CTA for a 16-bit KV cache, 8 for an fp8 one,
+// whose tiles take half the bytes and more arithmetic per byte) with a
+// DEC_STAGES-deep TMA ring each; the key tiles of all work are split into
+// equal contiguous ranges, one per warp.
 constexpr int DEC_ROWS = 16;
 constexpr int DEC_KEYS = 32;
 constexpr int DEC_WARPS = 4;
+constexpr int DEC_WARPS_KV8 = 8;
+constexpr int DEC_WARPS_MAX = 8;
 constexpr int DEC_STAGES = 3;
 
 enum Mode { MODE_SOFTMAX = 0, MODE_NONE = 1, MODE_SOFTMAX_Q = 2, MODE_NONE_Q = 3 };
@@ -44,6 +48,8 @@ struct AttnParams {
     int max_items;                  // capacity of the work list
     int max_pairs;                  // decode: bound on (batch, KV head, row chunk) pairs
     int dec_slots;                  // decode: partial slots (2 per warp of the grid)
+    int kv8;                        // K, V hold E4M3 codes (fp8 KV cache)
+    const float *k_scale, *v_scale; // fp8 KV cache: dequantisation scales (device scalars)
     int grid;                       // decode: persistent grid size
     int32_t *status;                // device status word
     uint8_t *ws;                    // workspace base
@@ -112,6 +118,6 @@ cudaError_t launch_prefill_typed(const AttnParams &p, const TensorMaps &m, int m
 cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode, int grid,
                            cudaStream_t s, int bf16);
 cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode,
-                          cudaStream_t s, int bf16);
+                          cudaStream_t s, int bf16, int kv8);
 
 }  // namespace rga

@@ -12,7 +12,7 @@
 //   - otherwise: every cache row, taken from the update inside the window
 //     and from past_cache outside it (one pass, no separate copy).
 // Rows move in 16-byte vectors when the row size and every base address
-// allow it, else in 4- or 2-byte units.
+// allow it, else in 4-, 2- or (fp8 codes) 1-byte units.
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cstdint>
@@ -73,7 +73,8 @@ kv_update_kernel(const __grid_constant__ KvuParams p) {
     auto copy = [&](const uint8_t *src, uint8_t *dst) {
         if constexpr (V == 16) *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
         else if constexpr (V == 4) *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(src);
-        else *reinterpret_cast<uint16_t *>(dst) = *reinterpret_cast<const uint16_t *>(src);
+        else if constexpr (V == 2) *reinterpret_cast<uint16_t *>(dst) = *reinterpret_cast<const uint16_t *>(src);
+        else *dst = *src;
     };
     // byte offset of update token t of batch b, head h
     auto upd_row = [&](int b, int h, int t) -> int64_t {
@@ -158,6 +159,7 @@ extern "C" rga_status trt_kv_cache_update(const rga_kv_update_args *a, cudaStrea
     switch (a->dtype) {
     case RGA_F16: case RGA_BF16: esize = 2; break;
     case RGA_F32: esize = 4; break;
+    case RGA_FP8_E4M3: esize = 1; break;
     default: return RGA_ERR_INVALID_ARG;
     }
     if (a->update_form != RGA_FORM_PADDED_BHND && a->update_form != RGA_FORM_PACKED_NHD)
@@ -202,6 +204,7 @@ extern "C" rga_status trt_kv_cache_update(const rga_kv_update_args *a, cudaStrea
     if (aligned(16)) e = kvu_launch<16>(p, grid, stream);
     else if (aligned(4)) e = kvu_launch<4>(p, grid, stream);
     else if (aligned(2)) e = kvu_launch<2>(p, grid, stream);
-    else return RGA_ERR_INVALID_ARG;   // element storage not even 2-byte aligned
+    else if (esize == 1) e = kvu_launch<1>(p, grid, stream);
+    else return RGA_ERR_INVALID_ARG;   // 16-bit element storage not 2-byte aligned
     return e == cudaSuccess ? RGA_OK : RGA_ERR_CUDA;
 }

@@ -334,4 +334,27 @@ __device__ __forceinline__ float int8_round(float x) {
     return fminf(fmaxf(r, -128.f), 127.f);
 }
 
+// Four E4M3 codes (bytes 0..3 of w) as two words of 16-bit values: lo holds
+// codes 0 and 1, hi codes 2 and 3, the lower-numbered code in the lower
+// half.  Exact: every E4M3 value is an f16 and a bf16 value.  (A NaN code
+// gives NaN as f16 and a finite value as bf16; callers never use either.)
+template <bool BF16>
+__device__ __forceinline__ void e4m3x4_to_x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    if constexpr (!BF16) {
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+            : "=r"(lo), "=r"(hi) : "r"(w));
+    } else {
+        // Code s.eeee.mmm becomes the bf16 bits s.0000eeee.mmm0000: the
+        // code's value times 2^-120 (a bf16 subnormal exactly when the code
+        // is subnormal), then one exact multiply by 2^120.
+        const uint32_t lo8 = (w << 4) & 0xf0f0f0f0u;                       // bf16 bits 0..7
+        const uint32_t hi8 = ((w >> 4) & 0x07070707u) | (w & 0x80808080u);  // bf16 bits 8..15
+        const uint32_t l = __byte_perm(lo8, hi8, 0x5140), h = __byte_perm(lo8, hi8, 0x7362);
+        const uint32_t two120 = 0x7b807b80u;   // 2^120 in both halves
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(two120));
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(two120));
+    }
+}
+
 }  // namespace rga

@@ -55,10 +55,10 @@ def flops(case: Case) -> float:
 
 
 def decode_bytes(case: Case) -> float:
-    """K and V bytes over the valid key rows, plus Q and Y."""
-    e = case.q.element_size()
-    kv = 2 * sum(case.kv_lens) * case.kv_heads * case.head_dim * e
-    rows = sum(case.q_lens) * case.q_heads * case.head_dim * e
+    """K and V bytes over the valid key rows (one byte per element for an
+    fp8 KV cache), plus Q and Y."""
+    kv = 2 * sum(case.kv_lens) * case.kv_heads * case.head_dim * case.k.element_size()
+    rows = sum(case.q_lens) * case.q_heads * case.head_dim * case.q.element_size()
     return float(kv + 2 * rows)
 
 
@@ -66,7 +66,7 @@ def input_bytes(case: Case):
     """Host->device bytes of one call's inputs (Q, K, V, lengths, mask, scale)."""
     n = 0
     for t in (case.q, case.k, case.v, case.query_lengths, case.kv_lengths, case.mask,
-              case.quant_scale):
+              case.quant_scale, *(case.kv_scales or ())):
         if t is not None:
             n += t.numel() * t.element_size()
     return n

@@ -12,6 +12,12 @@ with inclusive bounds.  Rows of padded KV at or beyond a sequence's kv length
 hold ``kv_pad`` (NaN by default, so that any read of them shows in the
 output); packed tensors may carry ``tail`` extra rows past the last sequence,
 filled the same way.
+
+FP8 KV cache workloads draw K and V the same way, divide them by the
+tensor's scale (s_k, s_v), clamp to +-448 and store them as E4M3FN codes
+with PyTorch's round-to-nearest-even cast to float8_e4m3fn (uint8 tensors);
+padding rows then hold the code of ``kv_pad`` (0x7F, a NaN code, by
+default).
 """
 from __future__ import annotations
 
@@ -45,6 +51,7 @@ class Case:
     mask: Optional[torch.Tensor] = None
     quant: Optional[str] = None
     quant_scale: Optional[torch.Tensor] = None
+    kv_scales: Optional[tuple] = None       # fp8 KV cache: (s_k, s_v) fp32 [1] tensors
     meta: dict = field(default_factory=dict)
 
     @property
@@ -76,7 +83,7 @@ def make_case(name, seed, *, batch, q_heads, kv_heads, head_dim, q_lens,
               kv_seq=None, dtype=torch.float16, scale=None, causal="none",
               norm="softmax", mask=None, quant=None, quant_scale=None,
               pass_query_lengths=None, pass_kv_lengths=True, kv_pad=math.nan,
-              tail=0, g=None):
+              tail=0, g=None, kv_fp8=None):
     """Build a Case from explicit per-batch lengths.
 
     q_lens / kv_lens: per-batch valid lengths (python ints).  For padded forms
@@ -85,7 +92,8 @@ def make_case(name, seed, *, batch, q_heads, kv_heads, head_dim, q_lens,
     query_lengths; ``pass_kv_lengths`` (padded KV) passes the optional [B]
     kv_lengths.  ``mask`` is either a ready tensor or a callable
     ``mask(g) -> tensor`` drawn after V.  ``g`` continues an existing
-    generator (used when the lengths were drawn from it).
+    generator (used when the lengths were drawn from it).  ``kv_fp8 = (s_k,
+    s_v)`` stores K and V as E4M3FN codes of K / s_k and V / s_v.
     """
     if g is None:
         g = torch.Generator("cpu").manual_seed(seed)
@@ -120,6 +128,10 @@ def make_case(name, seed, *, batch, q_heads, kv_heads, head_dim, q_lens,
             v[b, :, n:] = kv_pad
         kv_lengths = (torch.tensor(kv_lens, dtype=torch.int32)
                       if pass_kv_lengths else None)
+    kv_scales = None
+    if kv_fp8 is not None:
+        k, v = _to_e4m3_codes(k, kv_fp8[0], kv_pad), _to_e4m3_codes(v, kv_fp8[1], kv_pad)
+        kv_scales = tuple(torch.tensor([float(x)], dtype=torch.float32) for x in kv_fp8)
     if callable(mask):
         mask = mask(g)
     if scale is None:
@@ -131,7 +143,17 @@ def make_case(name, seed, *, batch, q_heads, kv_heads, head_dim, q_lens,
                 batch=batch, query_lengths=query_lengths,
                 kv_lengths=kv_lengths, q_lens=q_lens, kv_lens=kv_lens,
                 scale=scale, causal=causal, norm=norm, mask=mask, quant=quant,
-                quant_scale=quant_scale)
+                quant_scale=quant_scale, kv_scales=kv_scales)
+
+
+def _to_e4m3_codes(x, s, pad):
+    """E4M3FN codes (uint8) of x / s; elements that hold ``pad`` (the
+    padding fill) get the code of ``pad`` itself."""
+    pad_t = torch.tensor(pad, dtype=torch.float32)
+    is_pad = torch.isnan(x) if math.isnan(pad) else (x == pad_t)
+    codes = (x.float() / s).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    codes[is_pad] = pad_t.to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes
 
 
 def _uniform_int(g, lo, hi, n):
@@ -160,11 +182,20 @@ WORKLOADS = {
         "padded KV N=4104 holding the cache (U[256,4096] keys) then the 8 drafts, "
         "bool mask [B,1,8,N]: every cached key, and of the drafts the token's "
         "ancestors in a seeded random tree and itself; B=16, Hq=64 Hkv=8 D=128 bf16"),
+    7: ("decode_fp8kv_b64_gqa64x8_kv4096_d128_bf16",
+        "decode over an FP8 (E4M3) KV cache: packed Q (one token each), padded KV "
+        "N=4096 with kv_len U[256,4096], B=64, Hq=64 Hkv=8 D=128, bf16 Q/Y, "
+        "lower_right; K, V stored as E4M3FN codes with per-tensor scales "
+        "s_k = 1/56, s_v = 1/48"),
 }
+
+# per-tensor scales of the fp8 KV cache workload (K, V ~ N(0, 1) land near
+# code magnitude 56 and 48, far inside the E4M3 range)
+FP8_KV_SCALES = (1.0 / 56.0, 1.0 / 48.0)
 
 
 def workload(index, *, quant="fp8", kv_pad=math.nan, seed=None):
-    """The named workload ``index`` (1..6) as a Case on host memory.
+    """The named workload ``index`` (1..7) as a Case on host memory.
 
     ``quant`` selects the fp8 or int8 variant of workload 5.
     """
@@ -196,6 +227,13 @@ def workload(index, *, quant="fp8", kv_pad=math.nan, seed=None):
                          q_form=PACKED, kv_form=PADDED, kv_seq=4096,
                          dtype=torch.bfloat16, causal="lower_right",
                          kv_pad=kv_pad, g=g)
+    if index == 7:
+        kvls = _uniform_int(g, 256, 4096, 64)
+        return make_case(name, seed, batch=64, q_heads=64, kv_heads=8,
+                         head_dim=128, q_lens=[1] * 64, kv_lens=kvls,
+                         q_form=PACKED, kv_form=PADDED, kv_seq=4096,
+                         dtype=torch.bfloat16, causal="lower_right",
+                         kv_pad=kv_pad, g=g, kv_fp8=FP8_KV_SCALES)
     if index == 6:
         B, T, N = 16, 8, 4096 + 8
         cache = _uniform_int(g, 256, 4096, B)
@@ -242,4 +280,6 @@ def to_device(case: Case, device, non_blocking=False) -> Case:
     return replace(case, q=mv(case.q), k=mv(case.k), v=mv(case.v),
                    query_lengths=mv(case.query_lengths),
                    kv_lengths=mv(case.kv_lengths), mask=mv(case.mask),
-                   quant_scale=mv(case.quant_scale))
+                   quant_scale=mv(case.quant_scale),
+                   kv_scales=None if case.kv_scales is None else tuple(
+                       mv(t) for t in case.kv_scales))

@@ -42,7 +42,10 @@ def run_gpu(case: W.Case, *, status=None):
     kw = dict(q_form=dc.q_form, kv_form=dc.kv_form, query_lengths=dc.query_lengths,
               kv_lengths=dc.kv_lengths, mask=dc.mask, scale=dc.scale, causal=dc.causal,
               norm=dc.norm, out=y, status=status, return_status=True)
-    if dc.quant is None:
+    if dc.kv_scales is not None:
+        _, st = binding.trt_attention_fp8_kv(dc.q, dc.k, dc.v, k_scale=dc.kv_scales[0],
+                                             v_scale=dc.kv_scales[1], **kw)
+    elif dc.quant is None:
         _, st = binding.trt_attention(dc.q, dc.k, dc.v, **kw)
     else:
         _, st = binding.trt_quantized_attention(dc.q, dc.k, dc.v, quant=dc.quant,
@@ -58,7 +61,7 @@ def run_oracle(case: W.Case):
         query_lengths=case.query_lengths, kv_lengths=case.kv_lengths, mask=case.mask,
         scale=case.scale, causal=case.causal, norm=case.norm, quant=case.quant,
         quant_scale=case.quant_scale,
-        ambiguity_eps=AMBIGUITY_EPS if case.quant else None)
+        ambiguity_eps=AMBIGUITY_EPS if case.quant else None, kv_fp8_scales=case.kv_scales)
 
 
 def valid_row_mask(case: W.Case):

@@ -161,3 +161,27 @@ def test_selftest_validates_its_arguments(lib):
     assert lib.rga_selftest_wait_timeout(None, 1000, None) == 1
     assert lib.rga_selftest_wait_timeout(0x20000, 0, None) == 1
     assert lib.rga_selftest_wait_timeout(0x20000, (1 << 32) + 1, None) == 1
+
+
+def test_fp8_kv_validation_without_a_device(lib):
+    a = _args(workspace=0x100000, workspace_bytes=1 << 30)
+    assert lib.trt_attention_fp8_kv(ctypes.byref(a), None, 0x40000, None) == 1   # k_scale
+    assert lib.trt_attention_fp8_kv(ctypes.byref(a), 0x40000, None, None) == 1   # v_scale
+    # prefill shapes (256 query rows per sequence) are not on the fp8 path
+    assert lib.trt_attention_fp8_kv(ctypes.byref(a), 0x40000, 0x40010, None) == 2
+    # argument errors come first, as for trt_attention
+    a = _args(q_heads=6, kv_heads=4)
+    assert lib.trt_attention_fp8_kv(ctypes.byref(a), 0x40000, 0x40010, None) == 1
+
+
+def test_fp8_codes_are_a_kv_update_element_type(lib):
+    # E4M3 codes move as bytes: an odd head dim is valid (1-byte moves)
+    a = _kv_args(dtype=4, head_dim=3)
+    a.batch = 0            # nothing to move: validation only, no launch
+    assert lib.trt_kv_cache_update(ctypes.byref(a), None) == 0
+
+
+
+def test_e4m3_selftest_validates_its_arguments(lib):
+    assert lib.rga_selftest_e4m3_decode(None, 0x20000, None) == 1
+    assert lib.rga_selftest_e4m3_decode(0x20000, None, None) == 1

@@ -1,4 +1,4 @@
-"""The five named workloads at full size, run on the GPU exactly as the
+"""The named workloads (2 to 7) at full size, run on the GPU exactly as the
 benchmark launches them; the oracle checks sampled (batch, KV head) pairs
 (each one a complete sub-problem it can finish in seconds), and every row
 outside the sequences is checked for its sentinel bits."""
@@ -48,7 +48,8 @@ def sub_problem(c: W.Case, b: int, g: int):
     return oracle.attention(q, k, v, q_form=c.q_form, kv_form=c.kv_form, query_lengths=qlen,
                             kv_lengths=klen, mask=mask, scale=c.scale, causal=c.causal,
                             norm=c.norm, quant=c.quant, quant_scale=c.quant_scale,
-                            ambiguity_eps=AMBIGUITY_EPS if c.quant else None)
+                            ambiguity_eps=AMBIGUITY_EPS if c.quant else None,
+                            kv_fp8_scales=c.kv_scales)
 
 
 def gpu_rows(c: W.Case, y, b, g):
@@ -67,7 +68,7 @@ def ref_rows(c: W.Case, yref, b):
     return yref[:, :, :c.q_lens[b]]
 
 
-CASES = [(2, None), (3, None), (4, None), (5, "fp8"), (5, "int8"), (6, None)]
+CASES = [(2, None), (3, None), (4, None), (5, "fp8"), (5, "int8"), (6, None), (7, None)]
 
 
 @pytest.mark.parametrize("index,quant", CASES, ids=[f"w{i}-{q}" for i, q in CASES])

@@ -441,3 +441,62 @@ def test_ambiguity_bounds_perturbed_evaluation(quant, norm):
         y1 = _run(c, quant=quant, quant_scale=sq, norm=norm, scale=sc * f)
         ok = ~np.isnan(y0)
         assert (np.abs(y1[ok] - y0[ok]) <= amb[ok] + 1e-6).all()
+
+
+# ----------------------------------------------------------------------------
+# FP8 KV cache ("TensorRT Plugins Guide", AttentionPlugin: kv_cache_type FP8):
+# dequantisation against PyTorch's float8_e4m3fn decoding, the attention on
+# dequantised keys and values against SDPA, and closed forms that tell the K
+# scale from the V scale.
+# ----------------------------------------------------------------------------
+def test_e4m3_dequant_matches_torch_for_all_codes():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    for s in (1.0, 1.0 / 56.0, 3.0):
+        got = oracle.dequant_e4m3(codes, s)
+        ref = codes.view(torch.float8_e4m3fn).double().numpy() * s
+        nan = np.isnan(ref)
+        assert (np.isnan(got) == nan).all()
+        np.testing.assert_array_equal(got[~nan], ref[~nan])
+        assert (np.signbit(got[~nan]) == np.signbit(ref[~nan])).all()
+
+
+def _codes(shape, seed, s):
+    return (_rand(shape, seed, torch.float32) / s).clamp(-448, 448).to(
+        torch.float8_e4m3fn).view(torch.uint8)
+
+
+@pytest.mark.parametrize("causal", ["none", "upper_left"])
+def test_fp8_kv_matches_torch_sdpa_on_decoded_cache(causal):
+    B, H, N, D = 2, 3, 29, 16
+    sk, sv = 1.0 / 56.0, 1.0 / 20.0
+    q = _rand((B, H, N, D), 11)
+    kc, vc = _codes((B, H, N, D), 12, sk), _codes((B, H, N, D), 13, sv)
+    y = oracle.attention(q, kc, vc, scale=0.4, causal=causal, kv_fp8_scales=(sk, sv))
+    kd = kc.view(torch.float8_e4m3fn).double() * sk
+    vd = vc.view(torch.float8_e4m3fn).double() * sv
+    ref = F.scaled_dot_product_attention(q.double(), kd, vd, is_causal=(causal == "upper_left"),
+                                         scale=0.4)
+    np.testing.assert_allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_kv_constant_value_code_returns_its_value():
+    # every value code 0x3A (1.25): softmax rows average to 1.25 * s_v, for
+    # any keys and any K scale
+    B, H, N, D = 1, 2, 17, 8
+    q = _rand((B, H, N, D), 14)
+    kc = _codes((B, H, N, D), 15, 0.05)
+    vc = torch.full((B, H, N, D), 0x3A, dtype=torch.uint8)
+    y = oracle.attention(q, kc, vc, scale=1.0, kv_fp8_scales=(0.05, 0.375))
+    np.testing.assert_allclose(y, 1.25 * 0.375, rtol=1e-13)
+
+
+def test_fp8_kv_zero_key_codes_give_uniform_weights():
+    # all key codes zero: every score is 0 whatever s_k, so each row is the
+    # plain mean of the dequantised values (V scale applied, K scale not)
+    B, H, N, D = 1, 1, 9, 4
+    q = _rand((B, H, N, D), 16)
+    kc = torch.zeros((B, H, N, D), dtype=torch.uint8)
+    vc = _codes((B, H, N, D), 17, 0.1)
+    y = oracle.attention(q, kc, vc, kv_fp8_scales=(123.0, 0.1))
+    vd = np.array([[oracle.e4m3_decode(int(c)) for c in row] for row in vc[0, 0]]) * 0.1
+    np.testing.assert_allclose(y[0, 0], np.tile(vd.mean(axis=0), (N, 1)), rtol=1e-13)
