@@ -97,11 +97,13 @@ bool encode_kv8(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t 
     return encode(m, base, 4, d, b, 1, sw);
 }
 
-// Bound on the decode work pairs (batch, KV head, chunk of DEC_ROWS query
-// rows): one chunk per batch for padded Q (at most DEC_ROWS rows), and at
-// most B + q_seq*G/DEC_ROWS chunks over all batches for packed Q.
-static int64_t dec_max_pairs(int64_t B, int64_t Hkv, int64_t G, int64_t q_seq, bool packed) {
-    const int64_t chunks = packed ? B + (q_seq * G + DEC_ROWS - 1) / DEC_ROWS : B;
+// Bound on the decode work pairs (batch, KV head, chunk of `rows` query
+// rows): ceil(q_seq*G/rows) chunks per batch for padded Q, and at most
+// B + q_seq*G/rows chunks over all batches for packed Q.
+static int64_t dec_max_pairs(int64_t B, int64_t Hkv, int64_t G, int64_t q_seq, bool packed,
+                             int64_t rows) {
+    const int64_t per = (q_seq * G + rows - 1) / rows;
+    const int64_t chunks = packed ? B + per : B * per;
     return Hkv * chunks;
 }
 
@@ -116,7 +118,7 @@ bool use_decode(const rga_attention_args *a, bool quant) {
     if (G > DEC_ROWS) return false;
     const bool packed = a->q_form == RGA_FORM_PACKED_NHD;
     if (packed ? a->q_seq > 8 * (int64_t)a->batch : (int64_t)a->q_seq * G > DEC_ROWS) return false;
-    const int64_t tiles = dec_max_pairs(a->batch, a->kv_heads, G, a->q_seq, packed) *
+    const int64_t tiles = dec_max_pairs(a->batch, a->kv_heads, G, a->q_seq, packed, DEC_ROWS_KV8) *
                           (((int64_t)a->kv_seq + DEC_KEYS - 1) / DEC_KEYS);
     return tiles < (int64_t(1) << 31);
 }
@@ -168,7 +170,8 @@ rga_status validate(const rga_attention_args *a, bool quant) {
     return RGA_OK;
 }
 
-AttnParams make_params(const rga_attention_args *a, bool quant) {
+// kv8: the fp8 KV cache decode layout (DEC_ROWS_KV8 rows per pair).
+AttnParams make_params(const rga_attention_args *a, bool quant, bool kv8 = false) {
     AttnParams p;
     std::memset(&p, 0, sizeof(p));
     p.q = a->q; p.k = a->k; p.v = a->v; p.y = a->y;
@@ -195,7 +198,8 @@ AttnParams make_params(const rga_attention_args *a, bool quant) {
         p.max_items = p.Hkv * ((p.q_seq + it - 1) / it + p.B);
     else
         p.max_items = p.Hkv * p.B * ((p.q_seq + it - 1) / it);
-    p.max_pairs = (int)dec_max_pairs(p.B, p.Hkv, p.G, p.q_seq, p.q_packed != 0);
+    p.dec_rows = kv8 ? DEC_ROWS_KV8 : DEC_ROWS;
+    p.max_pairs = (int)dec_max_pairs(p.B, p.Hkv, p.G, p.q_seq, p.q_packed != 0, p.dec_rows);
     p.dec_slots = 2 * DEC_WARPS_MAX * (sm_count() > 0 ? sm_count() : 1);
     p.status = a->device_status;
     p.ws = static_cast<uint8_t *>(a->workspace);
@@ -203,12 +207,15 @@ AttnParams make_params(const rga_attention_args *a, bool quant) {
     return p;
 }
 
+// (covers both decode layouts: 16-bit and fp8 KV caches)
 size_t workspace_bytes(const rga_attention_args *a, bool quant) {
     AttnParams p = make_params(a, quant);
     size_t n = align256(pf_ws_bytes(p));
     if (use_decode(a, quant)) {
-        size_t d = align256(dec_ws_bytes(p));
-        if (d > n) n = d;
+        for (int kv8 = 0; kv8 < 2; ++kv8) {
+            const size_t d = align256(dec_ws_bytes(make_params(a, quant, kv8 != 0)));
+            if (d > n) n = d;
+        }
     }
     return n;
 }
@@ -237,7 +244,7 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
         (reinterpret_cast<uintptr_t>(a->workspace) & 255))
         return RGA_ERR_WORKSPACE;
 
-    AttnParams p = make_params(a, quant);
+    AttnParams p = make_params(a, quant, kv8);
     if (quant) {
         p.quant = qtype == RGA_QUANT_FP8_E4M3 ? 0 : 1;
         p.qscale = qscale;

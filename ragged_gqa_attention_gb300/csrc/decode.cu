@@ -11,7 +11,7 @@
 // warp streams the same number of tiles and none is left finishing a long
 // unit alone at the end.  Each CTA validates the lengths and lays out the
 // line itself (no scheduler launch).  A warp streams its range's K/V tiles
-// with TMA through its own DEC_STAGES-deep, 128-byte-swizzled ring, straight
+// with TMA through its own ring of a few stages (128-byte swizzle), straight
 // across pair boundaries, computes S = Q K^T and O += P V with m16n8k16 MMAs
 // (K and V are read once from HBM for all G query heads of the KV head) and
 // keeps an online softmax in fp32 registers.  A pair inside one range is
@@ -38,13 +38,15 @@ template <int D, bool KV8>
 struct DecLayout {
     static constexpr int NW = KV8 ? DEC_WARPS_KV8 : DEC_WARPS;   // warps per CTA
     static constexpr int THREADS = NW * 32;
+    static constexpr int ROWS = KV8 ? DEC_ROWS_KV8 : DEC_ROWS;     // query rows per pair
+    static constexpr int STAGES = KV8 ? DEC_STAGES_KV8 : DEC_STAGES;
     static constexpr int BLK = DEC_KEYS * 128;          // 16-bit: 32 rows x 64 columns x 2 bytes
     static constexpr int TILE = KV8 ? DEC_KEYS * D : (D / 64) * BLK;   // one K or V tile
     static constexpr int STAGE = 2 * TILE;               // K + V
-    static constexpr int WARP_RING = DEC_STAGES * STAGE;
+    static constexpr int WARP_RING = STAGES * STAGE;
     static constexpr int RING = NW * WARP_RING;
     static constexpr int BAR_OFF = RING;
-    static constexpr int SCR_OFF = BAR_OFF + NW * DEC_STAGES * 8 + 64;   // prefix scratch
+    static constexpr int SCR_OFF = BAR_OFF + NW * STAGES * 8 + 64;   // prefix scratch
     static constexpr int TPRE_OFF = SCR_OFF + (THREADS + 1) * 4 + 12;
     static constexpr int PPRE_OFF = TPRE_OFF + (DEC_MAX_B + 1) * 4;
     static constexpr int BYTES = PPRE_OFF + (DEC_MAX_B + 1) * 4 + 64;
@@ -168,13 +170,27 @@ __device__ __forceinline__ void dec_normalize(const AttnParams &p, const DecRow 
         for (int r = 0; r < 2; ++r) {
             mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
             mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-            const float m_new = fmaxf(m_r[r], mx[r]);
-            const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m_r[r] - mu);
-            l_r[r] *= alpha;
+        }
+        // O and l need rescaling only when a row's running max grew (alpha
+        // is exactly 1 otherwise); the test is warp-uniform, so a warp whose
+        // maxima are settled skips the multiplies
+        const float mn0 = fmaxf(m_r[0], mx[0]), mn1 = fmaxf(m_r[1], mx[1]);
+        if (__any_sync(0xffffffffu, mn0 > m_r[0] || mn1 > m_r[1])) {
 #pragma unroll
-            for (int n = 0; n < NT; ++n) { o[n][2 * r] *= alpha; o[n][2 * r + 1] *= alpha; }
-            m_r[r] = m_new;
+            for (int r = 0; r < 2; ++r) {
+                const float m_new = r ? mn1 : mn0;
+                const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+                const float alpha = ex2(m_r[r] - mu);
+                l_r[r] *= alpha;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) { o[n][2 * r] *= alpha; o[n][2 * r + 1] *= alpha; }
+            }
+        }
+        m_r[0] = mn0;
+        m_r[1] = mn1;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float mu = (m_r[r] == -INFINITY) ? 0.f : m_r[r];
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 sacc[nt][2 * r] = ex2(sacc[nt][2 * r] - mu);
@@ -252,50 +268,117 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t &w0, uint32_t &w1)
     asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(addr));
 }
 
-// dec_tile for an fp8 KV cache: kb/vb hold E4M3 codes, converted in
-// registers.  Two fragment layouts differ from the 16-bit tile, each a
-// permutation that a dot product does not see:
-//  - S = Q K^T: thread t takes dims [c D/4, (c+1) D/4) of its key row
-//    (c = t % 4), four per k-step (k positions 2c, 2c+1, 2c+8, 2c+9 hold
-//    dims c D/4 + 4s + 0..3); Q was loaded with the same order;
-//  - O += P V: n-tile j, column n stands for dim n D/8 + j, so that a
-//    thread reads D/8 contiguous codes of each of its four key rows and
-//    pairs keys with byte permutes; accumulator o[j][e] therefore holds dim
-//    (2c + e % 2) D/8 + j of row lane/4 + 8 (e / 2).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// dec_tile for an fp8 KV cache, kb/vb holding E4M3 codes that each thread
+// converts in registers.  Both products are transposed so that the MMA's
+// 8-wide N dimension holds the pair's 8 query rows and nothing is wasted:
+//   S^T = K Q^T:  M = keys (two blocks of 16), N = rows, K = head dims;
+//   O^T = V^T P^T: M = head dims (D/16 blocks), N = rows, K = keys.
+// S^T is an f16 product whatever the input type: qb holds Q as f16 (bf16
+// queries were scaled by a power of two into f16 range when the pair
+// started) and a single cvt converts two key codes exactly.  The head dims
+// of the S^T contraction are permuted (lane c = lane % 4 takes dims
+// [c D/4, (c+1) D/4) of its key rows, four per k-step; Q was loaded the
+// same way) so that a thread's K codes are contiguous.  P^T reaches the B
+// fragment layout by an 8x8 transpose (movmatrix) of the S^T accumulator.
+// V^T's M rows are permuted too: in dim block m, M-row r stands for dim
+// (D/8) r + 2m and M-row r + 8 for dim (D/8) r + 2m + 1, so a thread reads
+// D/8 contiguous codes from each of four key rows and pairs keys with byte
+// permutes.  Accumulator o[m][e] therefore holds row 2c + e % 2, dim
+// (D/8) (lane / 4) + 2m + e / 2.  Rows rr[0..1] are rows 2c and 2c + 1.
+// With softmax, P (in [0, 1]) and V enter the P V product as f16 whatever
+// the input type (every E4M3 value is an f16; f16 holds P more finely than
+// bf16; P below 2^-24 flushes to zero, far inside the tolerance); 'none'
+// leaves P unbounded and keeps the input type.
 template <int D, bool BF16, bool SOFTMAX>
 __device__ __forceinline__ void dec_tile8(const AttnParams &p, const DecRow (&rr)[2],
-                                          const uint32_t (&qa)[D / 16][4], uint32_t kb,
-                                          uint32_t vb, int j0, float (&o)[D / 8][4],
+                                          const uint32_t (&qb)[D / 16][2], uint32_t kb,
+                                          uint32_t vb, int j0, float (&o)[D / 16][4],
                                           float (&m_r)[2], float (&l_r)[2], float sc) {
-    constexpr int NT = D / 8, KS = D / 16, CH = D / 64;
+    constexpr int KS = D / 16, CH = D / 64, NO = D / 16, VW = D / 8;
+    constexpr bool PV_BF16 = BF16 && !SOFTMAX;   // type of P and V in the P V product
     const int lane = threadIdx.x & 31, c = lane & 3, r = lane >> 2;
-    float sacc[4][4];
+    float sacc[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-        sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-        uint32_t kw[KS];
+    for (int mb = 0; mb < 2; ++mb) {
+        sacc[mb][0] = sacc[mb][1] = sacc[mb][2] = sacc[mb][3] = 0.f;
+        uint32_t k0[KS], k8[KS];   // key rows 16 mb + r and 16 mb + r + 8
 #pragma unroll
         for (int h = 0; h < CH; ++h) {
             uint32_t w[4];
-            lds128(kb + off8<D>(nt * 8 + r, c * CH + h), w);
+            lds128(kb + off8<D>(16 * mb + r, c * CH + h), w);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) kw[4 * h + i] = w[i];
+            for (int i = 0; i < 4; ++i) k0[4 * h + i] = w[i];
+            lds128(kb + off8<D>(16 * mb + r + 8, c * CH + h), w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) k8[4 * h + i] = w[i];
         }
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            uint32_t b0, b1;
-            e4m3x4_to_x2<BF16>(kw[ks], b0, b1);
-            mma16816<BF16>(sacc[nt], qa[ks], b0, b1);
+            uint32_t a[4];
+            e4m3x4_to_x2<false>(k0[ks], a[0], a[2]);
+            e4m3x4_to_x2<false>(k8[ks], a[1], a[3]);
+            mma16816<false>(sacc[mb], a, qb[ks][0], qb[ks][1]);
         }
     }
-    dec_normalize<D, SOFTMAX>(p, rr, sacc, j0, o, m_r, l_r, sc);
+    // scale and mask: element (mb, e) is key j0 + 16 mb + r + 8 (e / 2) of row rr[e % 2]
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const DecRow &R = rr[e & 1];
+            const int j = j0 + 16 * mb + r + 8 * (e >> 1);
+            bool ok = j <= R.lim;
+            float add = 0.f;
+            if (ok && p.mask) ok = mask_at(p, p.md[3] == 1 ? R.mrow : R.mrow + j, add);
+            const float v = sacc[mb][e] * sc + (SOFTMAX ? add * 1.4426950408889634f : add);
+            sacc[mb][e] = ok ? v : (SOFTMAX ? -INFINITY : 0.f);
+            mx[e & 1] = fmaxf(mx[e & 1], sacc[mb][e]);
+        }
+    if (SOFTMAX) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int m = 4; m < 32; m <<= 1) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], m));
+        // O and l need rescaling only when a row's running max grew (alpha
+        // is exactly 1 otherwise); the test is warp-uniform
+        const float mn0 = fmaxf(m_r[0], mx[0]), mn1 = fmaxf(m_r[1], mx[1]);
+        if (__any_sync(0xffffffffu, mn0 > m_r[0] || mn1 > m_r[1])) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float m_new = i ? mn1 : mn0;
+                const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+                const float alpha = ex2(m_r[i] - mu);
+                l_r[i] *= alpha;
+#pragma unroll
+                for (int m = 0; m < NO; ++m) { o[m][i] *= alpha; o[m][i + 2] *= alpha; }
+            }
+        }
+        m_r[0] = mn0;
+        m_r[1] = mn1;
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sacc[mb][e] = ex2(sacc[mb][e] - ((e & 1) ? mu1 : mu0));
+                l_r[e & 1] += sacc[mb][e];
+            }
+    }
+    // O^T += V^T P^T over the tile's two 16-key halves
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
-        uint32_t a[4];
-        dec_p_frag<BF16>(sacc, kk, a);
-        // key rows k0, k0 + 1 (b0) and k0 + 8, k0 + 9 (b1); codes [r NT, r NT + NT)
+        const uint32_t b0 = movmatrix_trans(pack2<PV_BF16>(sacc[kk][0], sacc[kk][1]));
+        const uint32_t b1 = movmatrix_trans(pack2<PV_BF16>(sacc[kk][2], sacc[kk][3]));
+        // key rows k0, k0 + 1 (a0, a1) and k0 + 8, k0 + 9 (a2, a3); codes [VW r, VW r + VW)
         const int k0 = kk * 16 + 2 * c;
-        uint32_t v0[NT / 4], v1[NT / 4], v8[NT / 4], v9[NT / 4];
+        uint32_t v0[VW / 4], v1[VW / 4], v8[VW / 4], v9[VW / 4];
         if constexpr (D == 128) {
             uint32_t w[4];
             lds128(vb + off8<D>(k0, r), w);
@@ -318,54 +401,44 @@ __device__ __forceinline__ void dec_tile8(const AttnParams &p, const DecRow (&rr
             lds64(vb + off8<D>(k0 + 9, ch) + half, v9[0], v9[1]);
         }
 #pragma unroll
-        for (int w = 0; w < NT / 4; ++w) {
-            uint32_t b0[4], b1[4];
-            e4m3x4_to_x2<BF16>(__byte_perm(v0[w], v1[w], 0x5140), b0[0], b0[1]);
-            e4m3x4_to_x2<BF16>(__byte_perm(v0[w], v1[w], 0x7362), b0[2], b0[3]);
-            e4m3x4_to_x2<BF16>(__byte_perm(v8[w], v9[w], 0x5140), b1[0], b1[1]);
-            e4m3x4_to_x2<BF16>(__byte_perm(v8[w], v9[w], 0x7362), b1[2], b1[3]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) mma16816<BF16>(o[4 * w + i], a, b0[i], b1[i]);
+        for (int w = 0; w < VW / 4; ++w) {
+            uint32_t x[4], y[4];   // dims VW r + 4w .. + 3: keys (k0, k0 + 1) in x, (k0 + 8, k0 + 9) in y
+            e4m3x4_to_x2<PV_BF16>(__byte_perm(v0[w], v1[w], 0x5140), x[0], x[1]);
+            e4m3x4_to_x2<PV_BF16>(__byte_perm(v0[w], v1[w], 0x7362), x[2], x[3]);
+            e4m3x4_to_x2<PV_BF16>(__byte_perm(v8[w], v9[w], 0x5140), y[0], y[1]);
+            e4m3x4_to_x2<PV_BF16>(__byte_perm(v8[w], v9[w], 0x7362), y[2], y[3]);
+            const uint32_t a0[4] = {x[0], x[1], y[0], y[1]};   // dim block 2w
+            const uint32_t a1[4] = {x[2], x[3], y[2], y[3]};   // dim block 2w + 1
+            mma16816<PV_BF16>(o[2 * w], a0, b0, b1);
+            mma16816<PV_BF16>(o[2 * w + 1], a1, b0, b1);
         }
     }
 }
 
-// Dim of accumulator o[j][e] (e = 0..3) of this lane: the 16-bit tile keeps
-// the MMA's natural column order, the fp8 tile the permuted one above.
-template <int D, bool KV8>
-__device__ __forceinline__ int dec_dim(int j, int e) {
-    const int c = threadIdx.x & 3;
-    if constexpr (KV8) return (2 * c + (e & 1)) * (D / 8) + j;
-    else return j * 8 + 2 * c + (e & 1);
-}
-
-// Y rows of this lane's fragment rows, scaled by f (rows outside are skipped).
+// Y rows of this lane's output rows, scaled by f (rows outside are skipped):
+// the 16-bit tile's rows lane/4 and lane/4 + 8 in the MMA's column order;
+// the fp8 tile's rows 2c and 2c + 1, dims [(D/8) (lane/4), +D/8).
 template <int D, bool BF16, bool KV8>
 __device__ __forceinline__ void dec_store_y(const AttnParams &p, const DecRow (&rr)[2],
-                                            const float (&o)[D / 8][4], const float (&f)[2]) {
-    constexpr int NT = D / 8;
+                                            const float (&o)[KV8 ? D / 16 : D / 8][4],
+                                            const float (&f)[2]) {
     const int lane = threadIdx.x & 31;
     uint16_t *y = static_cast<uint16_t *>(p.y);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         if (!rr[r].valid) continue;
         if constexpr (KV8) {
-            // this lane holds dims [2c NT, 2c NT + 2 NT) of the row, in order
-            uint4 *dst = reinterpret_cast<uint4 *>(y + rr[r].qoff + dec_dim<D, true>(0, 0));
+            constexpr int NO = D / 16;
+            uint4 *dst = reinterpret_cast<uint4 *>(y + rr[r].qoff + (D / 8) * (lane >> 2));
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-                for (int i = 0; i < NT / 8; ++i) {
-                    const int e2 = 2 * r + e;
-                    dst[e * (NT / 8) + i] = make_uint4(
-                        pack2<BF16>(o[8 * i][e2] * f[r], o[8 * i + 1][e2] * f[r]),
-                        pack2<BF16>(o[8 * i + 2][e2] * f[r], o[8 * i + 3][e2] * f[r]),
-                        pack2<BF16>(o[8 * i + 4][e2] * f[r], o[8 * i + 5][e2] * f[r]),
-                        pack2<BF16>(o[8 * i + 6][e2] * f[r], o[8 * i + 7][e2] * f[r]));
-                }
+            for (int i = 0; i < NO / 4; ++i)
+                dst[i] = make_uint4(pack2<BF16>(o[4 * i][r] * f[r], o[4 * i][r + 2] * f[r]),
+                                    pack2<BF16>(o[4 * i + 1][r] * f[r], o[4 * i + 1][r + 2] * f[r]),
+                                    pack2<BF16>(o[4 * i + 2][r] * f[r], o[4 * i + 2][r + 2] * f[r]),
+                                    pack2<BF16>(o[4 * i + 3][r] * f[r], o[4 * i + 3][r + 2] * f[r]));
         } else {
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
+            for (int n = 0; n < D / 8; ++n) {
                 const int col = n * 8 + (lane & 3) * 2;
                 *reinterpret_cast<uint32_t *>(y + rr[r].qoff + col) =
                     pack2<BF16>(o[n][2 * r] * f[r], o[n][2 * r + 1] * f[r]);
@@ -374,25 +447,23 @@ __device__ __forceinline__ void dec_store_y(const AttnParams &p, const DecRow (&
     }
 }
 
-// This lane's partial O rows (unnormalised) into one partial slot row pair.
+// This lane's partial O rows (unnormalised) into one partial slot.
 template <int D, bool KV8>
-__device__ __forceinline__ void dec_store_part(float *slot_rows, const float (&o)[D / 8][4]) {
-    constexpr int NT = D / 8;
+__device__ __forceinline__ void dec_store_part(float *slot_rows,
+                                               const float (&o)[KV8 ? D / 16 : D / 8][4]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-        float *po = slot_rows + ((lane >> 2) + 8 * r) * D;
         if constexpr (KV8) {
+            float *po = slot_rows + (2 * (lane & 3) + r) * D + (D / 8) * (lane >> 2);
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-                for (int i = 0; i < NT / 4; ++i)
-                    *reinterpret_cast<float4 *>(po + dec_dim<D, true>(4 * i, e)) =
-                        make_float4(o[4 * i][2 * r + e], o[4 * i + 1][2 * r + e],
-                                    o[4 * i + 2][2 * r + e], o[4 * i + 3][2 * r + e]);
+            for (int i = 0; i < D / 32; ++i)
+                *reinterpret_cast<float4 *>(po + 4 * i) =
+                    make_float4(o[2 * i][r], o[2 * i][r + 2], o[2 * i + 1][r], o[2 * i + 1][r + 2]);
         } else {
+            float *po = slot_rows + ((lane >> 2) + 8 * r) * D;
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
+            for (int n = 0; n < D / 8; ++n)
                 *reinterpret_cast<float2 *>(po + n * 8 + (lane & 3) * 2) =
                     make_float2(o[n][2 * r], o[n][2 * r + 1]);
         }
@@ -400,7 +471,7 @@ __device__ __forceinline__ void dec_store_part(float *slot_rows, const float (&o
 }
 
 // One lane's view of the pair being computed or loaded: a pair is
-// (batch b, KV head g, row chunk rc of DEC_ROWS query rows); its key tiles
+// (batch b, KV head g, row chunk rc of DR query rows); its key tiles
 // are the 32-key tiles of [0, key extent of the batch).
 struct DecCur {
     int b, pib;          // batch, pair within the batch (g * nrc + rc)
@@ -409,11 +480,13 @@ struct DecCur {
     SeqInfo s;
 };
 
-// Batch b's row chunks and key tiles per pair (0 chunks: no query rows).
+// Batch b's row chunks of DR rows and key tiles per pair (0 chunks: no
+// query rows).
+template <int DR>
 __device__ __forceinline__ void dec_batch_shape(const AttnParams &p, const SeqInfo &s, int &nrc,
                                                 int &nt) {
     const int rows = s.q_len * p.G;
-    nrc = (rows + DEC_ROWS - 1) / DEC_ROWS;
+    nrc = (rows + DR - 1) / DR;
     const int kv_hi = rows > 0 ? key_extent(p.causal, s.q_len - 1, s) : 0;
     nt = (kv_hi + DEC_KEYS - 1) / DEC_KEYS;
 }
@@ -453,21 +526,24 @@ __global__ void __launch_bounds__(DecLayout<D, KV8>::THREADS, 1)
 decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TensorMaps tm) {
     using L = DecLayout<D, KV8>;
     constexpr int NW = L::NW;
-    constexpr int NT = D / 8;
+    constexpr int DR = L::ROWS;                    // query rows per pair
+    constexpr int NS = L::STAGES;
+    constexpr int NO = KV8 ? D / 16 : D / 8;       // O accumulator blocks
+    constexpr int QW = KV8 ? 2 : 4;                // Q fragment words per k-step
     constexpr int KS = D / 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
-    volatile int *abort = reinterpret_cast<volatile int *>(sm + L::BAR_OFF + NW * DEC_STAGES * 8);
-    int *flags = reinterpret_cast<int *>(sm + L::BAR_OFF + NW * DEC_STAGES * 8 + 4);
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + L::BAR_OFF + NW * NS * 8);
+    int *flags = reinterpret_cast<int *>(sm + L::BAR_OFF + NW * NS * 8 + 4);
     int *scratch = reinterpret_cast<int *>(sm + L::SCR_OFF);
     int *tpre = reinterpret_cast<int *>(sm + L::TPRE_OFF);   // key tiles before batch b
     int *ppre = reinterpret_cast<int *>(sm + L::PPRE_OFF);   // pairs before batch b
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NW * DEC_STAGES; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NW * NS; ++i) mbar_init(&bars[i], 1);
         *abort = 0;
         flags[0] = 0;   // bad lengths
         fence_mbar_init();
@@ -489,7 +565,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         }
         if (!ok) atomicOr(&flags[0], 1);
         int nrc = 0, nt = 0;
-        if (ok) dec_batch_shape(p, s, nrc, nt);
+        if (ok) dec_batch_shape<DR>(p, s, nrc, nt);
         tpre[b] = p.Hkv * nrc * nt;
         ppre[b] = p.Hkv * nrc;
     }
@@ -522,7 +598,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     for (int b = wg; b < p.B; b += gridDim.x * NW) {
         const SeqInfo s = seq_info(p, b);
         int nrc, nt;
-        dec_batch_shape(p, s, nrc, nt);
+        dec_batch_shape<DR>(p, s, nrc, nt);
         if (nrc == 0 || nt > 0) continue;
         const int rows = s.q_len * p.G;
         for (int r = lane; r < p.Hkv * rows; r += 32) {
@@ -533,7 +609,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     }
 
     uint8_t *ring = sm + warp * L::WARP_RING;
-    uint64_t *wbar = bars + warp * DEC_STAGES;
+    uint64_t *wbar = bars + warp * NS;
     const uint32_t ring_u32 = smem_u32(ring);
     uint32_t issued = 0, consumed = 0;
     const int t_begin = wg < Wn ? range_start(wg) : T, t_end = wg < Wn ? range_start(wg + 1) : T;
@@ -546,7 +622,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         }
         c.b = lo;
         c.s = seq_info(p, lo);
-        dec_batch_shape(p, c.s, c.nrc, c.nt);
+        dec_batch_shape<DR>(p, c.s, c.nrc, c.nt);
         const int r = t - tpre[lo];
         c.pib = r / c.nt;
         c.tile = r % c.nt;
@@ -561,13 +637,13 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         c.b = b;
         c.pib = 0;
         c.s = seq_info(p, b);
-        dec_batch_shape(p, c.s, c.nrc, c.nt);
+        dec_batch_shape<DR>(p, c.s, c.nrc, c.nt);
     };
     auto issue = [&](const DecCur &c) {
         if (lane == 0) {
             fence_proxy_async_smem();   // the stage's previous tile was read by ldmatrix
             dec_tma<KV8>(p, tm, c.s, c.b, c.pib / c.nrc, c.tile * DEC_KEYS,
-                    ring + (issued % DEC_STAGES) * L::STAGE, &wbar[issued % DEC_STAGES], D);
+                    ring + (issued % NS) * L::STAGE, &wbar[issued % NS], D);
         }
         ++issued;
     };
@@ -575,6 +651,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     // score scale (the K dequantisation scale folded in) and output factor
     // (the V dequantisation scale)
     const float sc = (SOFTMAX ? p.scale_log2 : p.scale) * (KV8 ? __ldg(p.k_scale) : 1.f);
+    float sc_pair = sc;   // sc times the power of two taken out of Q (fp8 KV, bf16 Q)
     const float sv = KV8 ? __ldg(p.v_scale) : 1.f;
     bool ok = true;
     if (t_begin < t_end) {
@@ -582,13 +659,13 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         locate(t_begin, lc);
         cc = lc;
         int next_issue = t_begin;
-        for (; next_issue < t_end && next_issue < t_begin + DEC_STAGES; ++next_issue) {
+        for (; next_issue < t_end && next_issue < t_begin + NS; ++next_issue) {
             issue(lc);
             advance(lc);
         }
-        DecRow rr[2];
-        uint32_t qa[KS][4];
-        float o[NT][4];
+        DecRow rr[2];       // this lane's two output rows
+        uint32_t qa[KS][QW];
+        float o[NO][4];
         float m_r[2], l_r[2];
         int seg0 = t_begin;    // first tile of the current pair in this range
         int kv_hi = 0, rows = 0;
@@ -596,29 +673,59 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             const int g = cc.pib / cc.nrc, rc = cc.pib % cc.nrc;
             rows = cc.s.q_len * p.G;
             kv_hi = key_extent(p.causal, cc.s.q_len - 1, cc.s);
-            rr[0] = dec_row(p, cc.s, cc.b, g, rc * DEC_ROWS + (lane >> 2), rows, kv_hi);
-            rr[1] = dec_row(p, cc.s, cc.b, g, rc * DEC_ROWS + (lane >> 2) + 8, rows, kv_hi);
             const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
             if constexpr (KV8) {
-                // dims [c D/4, (c+1) D/4) of each row, four per k-step (the
+                // output rows 2c, 2c + 1; Q row lane / 4 (the B operand of
+                // S^T), dims [c D/4, (c+1) D/4), four per k-step (the
                 // contraction order of dec_tile8)
+                rr[0] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3), rows, kv_hi);
+                rr[1] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3) + 1, rows, kv_hi);
+                const DecRow rq = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2), rows, kv_hi);
+                uint32_t w[D / 8];
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    static_cast<const uint16_t *>(p.q) + rq.qoff + (lane & 3) * (D / 4));
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    uint32_t w[D / 8];
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        static_cast<const uint16_t *>(p.q) + rr[i].qoff + (lane & 3) * (D / 4));
+                for (int k = 0; k < D / 32; ++k) {
+                    const uint4 x = rq.valid ? src[k] : make_uint4(0, 0, 0, 0);
+                    w[4 * k] = x.x; w[4 * k + 1] = x.y; w[4 * k + 2] = x.z; w[4 * k + 3] = x.w;
+                }
 #pragma unroll
-                    for (int k = 0; k < D / 32; ++k) {
-                        const uint4 x = rr[i].valid ? src[k] : make_uint4(0, 0, 0, 0);
-                        w[4 * k] = x.x; w[4 * k + 1] = x.y; w[4 * k + 2] = x.z; w[4 * k + 3] = x.w;
-                    }
+                for (int ks = 0; ks < KS; ++ks) {
+                    qa[ks][0] = w[2 * ks];
+                    qa[ks][1] = w[2 * ks + 1];
+                }
+                if constexpr (BF16) {
+                    // bf16 -> f16 for the f16 S product: scale the warp's
+                    // 8 rows by 2^-e so that their largest magnitude lies
+                    // in [2^14, 2^15).  Every bf16 value (8 significant
+                    // bits) at or above 2^-14 after scaling is then an exact
+                    // f16; smaller ones (below 2^-28 of the largest) round
+                    // to the f16 spacing 2^-24, a change far below the
+                    // fp32 rounding of the dot product.  2^e goes back into
+                    // the score scale.
+                    float mx = 0.f;
 #pragma unroll
-                    for (int ks = 0; ks < KS; ++ks) {
-                        qa[ks][i] = w[2 * ks];
-                        qa[ks][2 + i] = w[2 * ks + 1];
-                    }
+                    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                        for (int i = 0; i < QW; ++i)
+                            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(qa[ks][i] << 16)),
+                                                 fabsf(__uint_as_float(qa[ks][i] & 0xffff0000u))));
+#pragma unroll
+                    for (int m = 1; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+                    int e = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xff) - 127 - 14 : 0;
+                    e = min(max(e, -100), 100);
+                    const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+                    sc_pair = sc * __uint_as_float((uint32_t)(127 + e) << 23);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                        for (int i = 0; i < QW; ++i)
+                            qa[ks][i] = pack2<false>(__uint_as_float(qa[ks][i] << 16) * down,
+                                                     __uint_as_float(qa[ks][i] & 0xffff0000u) * down);
                 }
             } else {
+                rr[0] = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2), rows, kv_hi);
+                rr[1] = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2) + 8, rows, kv_hi);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     const int col = ks * 16 + (lane & 3) * 2;
@@ -629,7 +736,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                 }
             }
 #pragma unroll
-            for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
             m_r[0] = m_r[1] = -INFINITY;
             l_r[0] = l_r[1] = 0.f;
         };
@@ -637,8 +744,8 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
 
         for (int t = t_begin; t < t_end; ++t) {
             const uint32_t c = consumed;
-            const int st = c % DEC_STAGES;
-            if (!mbar_wait(&wbar[st], (c / DEC_STAGES) & 1, abort)) { ok = false; break; }
+            const int st = c % NS;
+            if (!mbar_wait(&wbar[st], (c / NS) & 1, abort)) { ok = false; break; }
             ++consumed;
             const int j0 = cc.tile * DEC_KEYS;
             const uint32_t kb = ring_u32 + st * L::STAGE, vb = kb + L::TILE;
@@ -654,7 +761,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                 }
                 __syncwarp();
             }
-            if constexpr (KV8) dec_tile8<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc);
+            if constexpr (KV8) dec_tile8<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc_pair);
             else dec_tile<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc);
             __syncwarp();
             if (next_issue < t_end) {   // refill the stage just used
@@ -665,11 +772,19 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             const bool pair_end = cc.tile + 1 == cc.nt;
             if (pair_end || t + 1 == t_end) {
                 // this range's share of the pair is done
+                // (the lanes sharing a row: lane % 4 for the 16-bit tile,
+                // lane / 4 for the fp8 one)
                 if (SOFTMAX)
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
-                        l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
+                        if constexpr (KV8) {
+#pragma unroll
+                            for (int m = 4; m < 32; m <<= 1)
+                                l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], m);
+                        } else {
+                            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
+                            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
+                        }
                     }
                 const int b = cc.b, g = cc.pib / cc.nrc, rc = cc.pib % cc.nrc;
                 const int ps = tpre[b] + cc.pib * cc.nt, pe = ps + cc.nt;
@@ -683,11 +798,15 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                     // partial (O, m, l): slot 0 for the first pair of the
                     // range, slot 1 for the last
                     const size_t slot = (size_t)wg * 2 + (seg0 == t_begin ? 0 : 1);
-                    dec_store_part<D, KV8>(part + slot * DEC_ROWS * D, o);
+                    dec_store_part<D, KV8>(part + slot * DR * D, o);
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const int row = (lane >> 2) + 8 * r;
-                        if ((lane & 3) == 0) pml[slot * DEC_ROWS + row] = make_float2(m_r[r], l_r[r]);
+                        if constexpr (KV8) {
+                            if (lane < 4) pml[slot * DR + 2 * lane + r] = make_float2(m_r[r], l_r[r]);
+                        } else {
+                            const int row = (lane >> 2) + 8 * r;
+                            if ((lane & 3) == 0) pml[slot * DR + row] = make_float2(m_r[r], l_r[r]);
+                        }
                     }
                     __threadfence();
                     __syncwarp();
@@ -698,7 +817,9 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                     tk = __shfl_sync(0xffffffffu, tk, 0);
                     if (tk == w_hi - w_lo) {   // the last of the pair's warps: merge
                         __threadfence();
-                        const int row = lane >> 1, c0 = (lane & 1) * (D / 2);
+                        // LPR lanes per row, each with D / LPR dims
+                        constexpr int LPR = 32 / DR, DL = D / LPR;
+                        const int row = lane / LPR, c0 = (lane % LPR) * DL;
                         // the first warp's share is its slot 1 unless the pair
                         // starts its range; every later warp's share is its slot 0
                         auto slot_of = [&](int w) -> size_t {
@@ -707,22 +828,22 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                         float M = -INFINITY;
                         if (SOFTMAX)
                             for (int w = w_lo; w <= w_hi; ++w)
-                                M = fmaxf(M, __ldcg(&pml[slot_of(w) * DEC_ROWS + row].x));
-                        float acc[D / 2];
+                                M = fmaxf(M, __ldcg(&pml[slot_of(w) * DR + row].x));
+                        float acc[DL];
 #pragma unroll
-                        for (int k = 0; k < D / 2; ++k) acc[k] = 0.f;
+                        for (int k = 0; k < DL; ++k) acc[k] = 0.f;
                         float Lsum = 0.f;
                         for (int w = w_lo; w <= w_hi; ++w) {
                             const size_t sl = slot_of(w);
                             float wt = 1.f;
                             if (SOFTMAX) {
-                                const float2 v = __ldcg(&pml[sl * DEC_ROWS + row]);
+                                const float2 v = __ldcg(&pml[sl * DR + row]);
                                 wt = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
                                 Lsum += v.y * wt;
                             }
-                            const float4 *src = reinterpret_cast<const float4 *>(part + (sl * DEC_ROWS + row) * D + c0);
+                            const float4 *src = reinterpret_cast<const float4 *>(part + (sl * DR + row) * D + c0);
 #pragma unroll
-                            for (int k = 0; k < D / 8; ++k) {
+                            for (int k = 0; k < DL / 4; ++k) {
                                 const float4 x4 = __ldcg(src + k);
                                 acc[4 * k] += x4.x * wt;
                                 acc[4 * k + 1] += x4.y * wt;
@@ -730,12 +851,12 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                                 acc[4 * k + 3] += x4.w * wt;
                             }
                         }
-                        const DecRow R = dec_row(p, cc.s, b, g, rc * DEC_ROWS + row, rows, kv_hi);
+                        const DecRow R = dec_row(p, cc.s, b, g, rc * DR + row, rows, kv_hi);
                         if (R.valid) {
                             const float f = (SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f) * sv;
                             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff + c0);
 #pragma unroll
-                            for (int k = 0; k < D / 16; ++k)
+                            for (int k = 0; k < DL / 8; ++k)
                                 dst[k] = make_uint4(pack2<BF16>(acc[8 * k] * f, acc[8 * k + 1] * f),
                                                     pack2<BF16>(acc[8 * k + 2] * f, acc[8 * k + 3] * f),
                                                     pack2<BF16>(acc[8 * k + 4] * f, acc[8 * k + 5] * f),
@@ -754,7 +875,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     }
     // copies still in flight (only after an abort) land before the CTA exits
     while (consumed < issued) {
-        mbar_wait_drain(&wbar[consumed % DEC_STAGES], (consumed / DEC_STAGES) & 1);
+        mbar_wait_drain(&wbar[consumed % NS], (consumed / NS) & 1);
         ++consumed;
     }
     __syncwarp();

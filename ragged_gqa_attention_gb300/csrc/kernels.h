@@ -18,11 +18,13 @@ constexpr int BN = 128;
 // DEC_STAGES-deep TMA ring each; the key tiles of all work are split into
 // equal contiguous ranges, one per warp.
 constexpr int DEC_ROWS = 16;
+constexpr int DEC_ROWS_KV8 = 8;     // fp8 tiles: the 8 query rows are the MMA's N
 constexpr int DEC_KEYS = 32;
 constexpr int DEC_WARPS = 4;
 constexpr int DEC_WARPS_KV8 = 8;
 constexpr int DEC_WARPS_MAX = 8;
 constexpr int DEC_STAGES = 3;
+constexpr int DEC_STAGES_KV8 = 3;
 
 enum Mode { MODE_SOFTMAX = 0, MODE_NONE = 1, MODE_SOFTMAX_Q = 2, MODE_NONE_Q = 3 };
 
@@ -48,6 +50,7 @@ struct AttnParams {
     int max_items;                  // capacity of the work list
     int max_pairs;                  // decode: bound on (batch, KV head, row chunk) pairs
     int dec_slots;                  // decode: partial slots (2 per warp of the grid)
+    int dec_rows;                   // decode: query rows per pair (DEC_ROWS or DEC_ROWS_KV8)
     int kv8;                        // K, V hold E4M3 codes (fp8 KV cache)
     const float *k_scale, *v_scale; // fp8 KV cache: dequantisation scales (device scalars)
     int grid;                       // decode: persistent grid size
@@ -59,7 +62,7 @@ struct AttnParams {
 constexpr size_t WS_HEADER = 256;             // int counters
 // prefill: int4 items[max_items] after the header
 // decode: after the prefill region: int tickets[max_pairs] (256-aligned),
-// then float partial_o[dec_slots][DEC_ROWS][D], float2 ml[dec_slots][DEC_ROWS]
+// then float partial_o[dec_slots][dec_rows][D], float2 ml[dec_slots][dec_rows]
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -76,10 +79,10 @@ __host__ __device__ inline size_t dec_part_off(const AttnParams &p) {
     return align256(dec_tickets_off(p) + ((size_t)p.max_pairs + 1) * 4);
 }
 __host__ __device__ inline size_t dec_ml_off(const AttnParams &p) {
-    return dec_part_off(p) + align256((size_t)p.dec_slots * DEC_ROWS * p.D * 4);
+    return dec_part_off(p) + align256((size_t)p.dec_slots * p.dec_rows * p.D * 4);
 }
 __host__ __device__ inline size_t dec_ws_bytes(const AttnParams &p) {
-    return dec_ml_off(p) + (size_t)p.dec_slots * DEC_ROWS * 8;
+    return dec_ml_off(p) + (size_t)p.dec_slots * p.dec_rows * 8;
 }
 // Largest batch the decode kernel lists in shared memory.
 constexpr int DEC_MAX_B = 4096;

@@ -347,10 +347,16 @@ __device__ __forceinline__ void e4m3x4_to_x2(uint32_t w, uint32_t &lo, uint32_t 
     } else {
         // Code s.eeee.mmm becomes the bf16 bits s.0000eeee.mmm0000: the
         // code's value times 2^-120 (a bf16 subnormal exactly when the code
-        // is subnormal), then one exact multiply by 2^120.
-        const uint32_t lo8 = (w << 4) & 0xf0f0f0f0u;                       // bf16 bits 0..7
-        const uint32_t hi8 = ((w >> 4) & 0x07070707u) | (w & 0x80808080u);  // bf16 bits 8..15
-        const uint32_t l = __byte_perm(lo8, hi8, 0x5140), h = __byte_perm(lo8, hi8, 0x7362);
+        // is subnormal), then one exact multiply by 2^120.  Each code is
+        // first sign-extended to 16 bits by prmt (in its default mode a
+        // selector nibble with bit 3 set replicates the sign bit of the
+        // byte it selects; __byte_perm ignores that bit); shifted left by
+        // 4, the code's low 7 bits sit in bits 4..10 and a sign copy in 15.
+        uint32_t l, h;
+        asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(l) : "r"(w));
+        asm("prmt.b32 %0, %1, 0, 0xb3a2;" : "=r"(h) : "r"(w));
+        l = (l << 4) & 0x87f087f0u;
+        h = (h << 4) & 0x87f087f0u;
         const uint32_t two120 = 0x7b807b80u;   // 2^120 in both halves
         asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(two120));
         asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(two120));
