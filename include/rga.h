@@ -171,8 +171,9 @@ rga_status trt_quantized_attention(const rga_attention_args *args,
  * may hold any bits, NaN codes included.
  * Supported for decode shapes: q_heads / kv_heads <= 16 and either padded q
  * with q_seq * (q_heads / kv_heads) <= 16 or packed q with q_seq <= 8 *
- * batch (one token per sequence, or a few draft tokens for tree decoding
- * with a bool mask).  Other shapes return RGA_ERR_UNSUPPORTED.  Workspace:
+ * batch (one token per sequence, or up to 8 draft tokens per sequence on
+ * average for tree decoding with a bool mask).  Other shapes return
+ * RGA_ERR_UNSUPPORTED.  Workspace:
  * rga_attention_workspace_size(args) bytes. */
 rga_status trt_attention_fp8_kv(const rga_attention_args *args, const float *k_scale,
                                 const float *v_scale, cudaStream_t stream);

@@ -110,9 +110,12 @@ static int64_t dec_max_pairs(int64_t B, int64_t Hkv, int64_t G, int64_t q_seq, b
 // Decode (split-KV) path: short query rows per (batch, KV head) -- one
 // token each in vanilla decoding, a few draft tokens in tree decoding (at
 // most 8 per sequence on average for packed Q; the decode kernel streams the
-// keys once per 16-row chunk) -- no Q/DQ, and every key tile of the work
-// countable in 32 bits.
-bool use_decode(const rga_attention_args *a, bool quant) {
+// keys once per chunk of 16 query rows, 8 for an fp8 cache) -- no Q/DQ, and
+// every key tile of the work countable in 32 bits.  (Tree decoding with 64
+// rows per (batch, KV head) measured slower on the prefill kernel: it has no
+// split over the keys, so the longest cache sets its time.)
+bool use_decode(const rga_attention_args *a, bool quant, bool kv8 = false) {
+    (void)kv8;   // both caches take the same shapes
     if (quant || a->batch > DEC_MAX_B) return false;
     const int G = a->q_heads / a->kv_heads;
     if (G > DEC_ROWS) return false;
@@ -211,11 +214,10 @@ AttnParams make_params(const rga_attention_args *a, bool quant, bool kv8 = false
 size_t workspace_bytes(const rga_attention_args *a, bool quant) {
     AttnParams p = make_params(a, quant);
     size_t n = align256(pf_ws_bytes(p));
-    if (use_decode(a, quant)) {
-        for (int kv8 = 0; kv8 < 2; ++kv8) {
-            const size_t d = align256(dec_ws_bytes(make_params(a, quant, kv8 != 0)));
-            if (d > n) n = d;
-        }
+    for (int kv8 = 0; kv8 < 2; ++kv8) {
+        if (!use_decode(a, quant, kv8 != 0)) continue;
+        const size_t d = align256(dec_ws_bytes(make_params(a, quant, kv8 != 0)));
+        if (d > n) n = d;
     }
     return n;
 }
@@ -229,7 +231,7 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
     if (st != RGA_OK) return st;
     if (kv8) {
         if (!k_scale || !v_scale) return RGA_ERR_INVALID_ARG;
-        if (!use_decode(a, false)) return RGA_ERR_UNSUPPORTED;
+        if (!use_decode(a, false, true)) return RGA_ERR_UNSUPPORTED;
     }
     if (quant) {
         if (qtype != RGA_QUANT_FP8_E4M3 && qtype != RGA_QUANT_INT8) return RGA_ERR_INVALID_ARG;
@@ -258,7 +260,7 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
     // so they point at Y, which is a valid address.
     const void *kp = a->kv_seq > 0 ? a->k : a->y;
     const void *vp = a->kv_seq > 0 ? a->v : a->y;
-    const bool dec = use_decode(a, quant);
+    const bool dec = use_decode(a, quant, kv8);
     TensorMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     if (!encode_q(&maps.q, p.q, p) || !encode_q(&maps.y, p.y, p))

@@ -99,3 +99,23 @@ def check(case: W.Case, y_gpu, raw, y_ref, tol=None):
     assert (raw[:GUARD] == np.int16(SENTINEL)).all() and \
         (raw[GUARD + case.q.numel():] == np.int16(SENTINEL)).all(), "guard band overwritten"
     return float(err.max()) if err.size else 0.0
+
+
+def tree_mask(B, T, N, cache):
+    """A mask(gen) callable for W.make_case: speculative-decoding tree masks
+    [B, 1, T, N] where draft token i of sequence b sees every cached key
+    (cache[b] of them) and, of the T drafts stored right after them, itself
+    and its ancestors in a seeded random tree."""
+    def draw(gen):
+        keep = torch.zeros(B, 1, T, N, dtype=torch.bool)
+        for b in range(B):
+            parent = [-1] + [int(torch.randint(0, i, (1,), generator=gen)) for i in range(1, T)]
+            keep[b, 0, :, :cache[b]] = True
+            for i in range(T):
+                j = i
+                while j >= 0:
+                    keep[b, 0, i, cache[b] + j] = True
+                    j = parent[j]
+        return keep
+    return draw
+

@@ -92,26 +92,14 @@ def test_long_ranges_split_across_warps(D):
 
 
 def test_tree_decoding_mask():
+    from helpers import tree_mask
     B, T = 3, 8
     cache = [40, 257, 100]
     N = max(cache) + T + 3
-
-    def tree_mask(gen):
-        keep = torch.zeros(B, 1, T, N, dtype=torch.bool)
-        for b in range(B):
-            parent = [-1] + [int(torch.randint(0, i, (1,), generator=gen)) for i in range(1, T)]
-            keep[b, 0, :, :cache[b]] = True
-            for i in range(T):
-                j = i
-                while j >= 0:
-                    keep[b, 0, i, cache[b] + j] = True
-                    j = parent[j]
-        return keep
-
     for dtype in (torch.float16, torch.bfloat16):
         c = W.make_case("fp8kv_tree", 150, batch=B, q_heads=16, kv_heads=2, head_dim=128,
                         q_lens=[T] * B, kv_lens=[x + T for x in cache], q_form="packed",
-                        kv_form="padded", kv_seq=N, dtype=dtype, mask=tree_mask,
+                        kv_form="padded", kv_seq=N, dtype=dtype, mask=tree_mask(B, T, N, cache),
                         kv_fp8=W.FP8_KV_SCALES)
         _parity(c)
 

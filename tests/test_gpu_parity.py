@@ -215,6 +215,22 @@ def test_decode_masks_and_none():
     _parity(c)
 
 
+@pytest.mark.parametrize("G", [2, 8])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_tree_decoding(G, dtype):
+    # 8 draft tokens per sequence under a tree mask on the split-KV decode
+    # kernel: 16 rows per (batch, KV head) with G = 2 (one row chunk), 64
+    # rows with G = 8 (four chunks)
+    from helpers import tree_mask
+    B, T = 3, 8
+    cache = [40, 700, 129]
+    N = max(cache) + T + 5
+    c = W.make_case("tree", 24 + G, batch=B, q_heads=2 * G, kv_heads=2, head_dim=128,
+                    q_lens=[T] * B, kv_lens=[x + T for x in cache], q_form="packed",
+                    kv_form="padded", kv_seq=N, dtype=dtype, mask=tree_mask(B, T, N, cache))
+    _parity(c)
+
+
 # --------------------------------------------------------------------------
 # degenerate shapes and device-side length errors
 # --------------------------------------------------------------------------
