@@ -141,10 +141,17 @@ class Runner:
         self.stream = stream
         self.y = torch.empty_like(dc.q)
         self.status = torch.zeros(1, dtype=torch.int32, device=dc.q.device)
-        a = binding.make_args(dc.q, dc.k, dc.v, self.y, q_form=dc.q_form, kv_form=dc.kv_form,
+        paged = dc.kv_form == W.PAGED
+        a = binding.make_args(dc.q, dc.k, dc.v, self.y, q_form=dc.q_form,
+                              kv_form="padded" if paged else dc.kv_form,
                               query_lengths=dc.query_lengths, kv_lengths=dc.kv_lengths,
                               mask=dc.mask, scale=dc.scale, causal=dc.causal, norm=dc.norm,
-                              status=self.status)
+                              status=self.status, batch=dc.batch)
+        self.pk = None
+        if paged:
+            ks, vs = dc.kv_scales if dc.kv_scales is not None else (None, None)
+            self.pk = binding.make_paged(dc.k, dc.v, dc.page_table, k_scale=ks, v_scale=vs)
+            a.kv_seq = self.pk.max_pages_per_seq * self.pk.page_size
         n = self.lib.rga_attention_workspace_size(ctypes.byref(a))
         self.ws = torch.empty(n, dtype=torch.uint8, device=dc.q.device)
         a.workspace, a.workspace_bytes = self.ws.data_ptr(), n
@@ -160,7 +167,9 @@ class Runner:
 
     def __call__(self):
         b = self.ctypes.byref(self.args)
-        if self.dc.kv_scales is not None:
+        if self.pk is not None:
+            rc = self.lib.trt_attention_paged_kv(b, self.ctypes.byref(self.pk), self.h)
+        elif self.dc.kv_scales is not None:
             rc = self.lib.trt_attention_fp8_kv(b, self.ks, self.vs, self.h)
         elif self.dc.quant is None:
             rc = self.lib.trt_attention(b, self.h)
@@ -233,7 +242,8 @@ def device_timed(run, stream, steps, warmup, dist_on, sampler_index=None):
 def e2e_timed(case: W.Case, stream, steps, warmup, dist_on):
     """The public call from pinned host buffers: H2D inputs, attention, D2H Y."""
     host = {}
-    for name in ("q", "k", "v", "query_lengths", "kv_lengths", "mask", "quant_scale"):
+    for name in ("q", "k", "v", "query_lengths", "kv_lengths", "mask", "quant_scale",
+                 "page_table"):
         t = getattr(case, name)
         host[name] = None if t is None else t.pin_memory()
     dev = {n: (None if t is None else torch.empty_like(t, device="cuda")) for n, t in host.items()}
@@ -279,6 +289,10 @@ def oracle_sample(case: W.Case, budget_s: float, max_units=None):
     Returns (work done, seconds, threads, description); work is FLOPs, or
     decode bytes for a decode workload."""
     import oracle   # the CPU baseline leg is one of the oracle's permitted users
+    if case.kv_form == W.PAGED:   # the oracle reads the gathered (linear) cache
+        case = W.Case(**{**case.__dict__, "kv_form": W.PADDED, "page_table": None,
+                         "k": oracle.gather_pages(case.k, case.page_table, 0, case.kv_lens),
+                         "v": oracle.gather_pages(case.v, case.page_table, 1, case.kv_lens)})
     order = sorted(range(case.batch), key=lambda b: (case.q_lens[b] * case.kv_lens[b], b))
     threads = os.cpu_count() or 1
     done_flops, spent, seqs = 0.0, 0.0, []
@@ -423,7 +437,8 @@ def main():
 
     secondary = {}
     if not args.no_secondary:
-        for idx, q in ((3, "fp8"), (4, "fp8"), (5, "fp8"), (5, "int8"), (6, "fp8"), (7, "fp8")):
+        for idx, q in ((3, "fp8"), (4, "fp8"), (5, "fp8"), (5, "int8"), (6, "fp8"), (7, "fp8"),
+                       (8, "fp8")):
             if idx == args.workload:
                 continue
             torch.cuda.empty_cache()

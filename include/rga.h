@@ -178,6 +178,46 @@ rga_status trt_quantized_attention(const rga_attention_args *args,
 rga_status trt_attention_fp8_kv(const rga_attention_args *args, const float *k_scale,
                                 const float *v_scale, cudaStream_t stream);
 
+/* Paged KV cache ("TensorRT Plugins Guide", AttentionPlugin: the decoder
+ * tensor contract's kv_page_table [N, 2, max_pages_per_sequence], a
+ * current-entry page-table view into resident paged KV pools).
+ *
+ * k_pool, v_pool: device pools of num_pages pages, each page
+ *   [kv_heads, page_size, head_dim] row-major, so a pool is
+ *   [num_pages, kv_heads, page_size, head_dim]; 16-byte aligned.
+ * kv_dtype: the pools' element type: args->dtype (F16 / BF16), or
+ *   FP8_E4M3 with k_scale / v_scale (device fp32 scalars, required then;
+ *   ignored otherwise) as in trt_attention_fp8_kv.
+ * page_table: device int32 [batch, 2, max_pages_per_seq]: row 0 of batch b
+ *   lists the K pages of its keys in order (key n is row n % page_size of
+ *   page page_table[b][0][n / page_size]), row 1 the V pages.  Entries
+ *   past a sequence's last page are never read.
+ * page_size: keys per page, a positive multiple of 32.
+ */
+typedef struct {
+    const void *k_pool, *v_pool;
+    rga_dtype kv_dtype;
+    const float *k_scale, *v_scale;
+    const int32_t *page_table;
+    int32_t num_pages, page_size, max_pages_per_seq;
+} rga_paged_kv;
+
+/* Attention over a paged KV cache.  Same as trt_attention (or
+ * trt_attention_fp8_kv for an FP8_E4M3 pool), except that the keys and
+ * values come from the pools through the page table: args->k and args->v
+ * are ignored, args->kv_form must be RGA_FORM_PADDED_BHND, args->kv_lengths
+ * (device int32 [batch]) is required, and args->kv_seq is ignored (a
+ * sequence may hold up to max_pages_per_seq * page_size keys; a mask's key
+ * dimension is 1 or at least every sequence's length, checked on the
+ * device).  Decode
+ * shapes as for trt_attention_fp8_kv; other shapes return
+ * RGA_ERR_UNSUPPORTED.  A page index outside [0, num_pages) among a
+ * sequence's pages sets *device_status to RGA_ERR_DEVICE_LENGTHS and leaves
+ * Y untouched, as bad lengths do.  Workspace: rga_attention_workspace_size
+ * of the same args with kv_seq = max_pages_per_seq * page_size. */
+rga_status trt_attention_paged_kv(const rga_attention_args *args, const rga_paged_kv *kv,
+                                  cudaStream_t stream);
+
 /* Size of the library-owned device scratch used by
  * trt_attention_static_scratch (40 MiB). */
 #define RGA_STATIC_SCRATCH_BYTES (40ull << 20)

@@ -221,5 +221,34 @@ def int8_round(x: float) -> float:
     return _load().rga_oracle_int8_round(float(x))
 
 
+def gather_pages(pool, page_table, which, kv_lens, pad=None):
+    """The linear cache [B, H, N, D] (N = max_pages * page_size) of a paged
+    KV pool ("TensorRT Plugins Guide", AttentionPlugin: kv_page_table
+    [N, 2, max_pages_per_sequence]): key n < kv_lens[b] of batch b is row
+    n % page_size of page page_table[b, which, n // page_size] of
+    pool [num_pages, H, page_size, D]; which = 0 for K, 1 for V.  Rows past
+    kv_lens[b] hold ``pad`` (default NaN, or the NaN code 0x7F for uint8 /
+    float8 codes) and page entries past a sequence's last page are not read.
+    Index work only: the element bits are copied unchanged (torch tensors in,
+    a torch tensor of the pool's dtype out)."""
+    import torch
+    pool = pool.detach().cpu()
+    pt = page_table.detach().cpu()
+    B, mp = pt.shape[0], pt.shape[2]
+    _, H, ps, D = pool.shape
+    codes = pool.dtype in (torch.uint8, torch.float8_e4m3fn)
+    out = torch.empty((B, H, mp * ps, D), dtype=pool.dtype)
+    if codes:
+        out.view(torch.uint8).fill_(0x7F if pad is None else int(pad))
+    else:
+        out.fill_(float("nan") if pad is None else float(pad))
+    for b in range(B):
+        n = int(kv_lens[b])
+        for i in range((n + ps - 1) // ps):
+            rows = min(ps, n - i * ps)
+            out[b, :, i * ps:i * ps + rows] = pool[int(pt[b, which, i]), :, :rows]
+    return out
+
+
 # TRT_KVCacheUpdate (a plain scatter; see kv_update.py)
 from .kv_update import kv_cache_update  # noqa: E402,F401

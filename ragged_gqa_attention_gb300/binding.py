@@ -37,7 +37,7 @@ FP8_CODE_DTYPES = (torch.float8_e4m3fn, torch.uint8)
 EXPORTED = ("rga_attention_workspace_size", "trt_attention", "trt_quantized_attention",
             "rga_get_device_status", "rga_status_string", "rga_abi_version",
             "trt_attention_static_scratch", "trt_kv_cache_update", "rga_selftest_wait_timeout",
-            "trt_attention_fp8_kv", "rga_selftest_e4m3_decode")
+            "trt_attention_fp8_kv", "rga_selftest_e4m3_decode", "trt_attention_paged_kv")
 
 
 class Args(ctypes.Structure):
@@ -62,6 +62,15 @@ class KvArgs(ctypes.Structure):
         ("batch", c_i32), ("heads", c_i32), ("cache_seq", c_i32), ("head_dim", c_i32),
         ("update_seq", c_i32),
         ("write_indices", c_vp), ("update_lengths", c_vp), ("device_status", c_vp),
+    ]
+
+
+class PagedKv(ctypes.Structure):
+    """Mirror of rga_paged_kv."""
+    _fields_ = [
+        ("k_pool", c_vp), ("v_pool", c_vp), ("kv_dtype", c_int),
+        ("k_scale", c_vp), ("v_scale", c_vp), ("page_table", c_vp),
+        ("num_pages", c_i32), ("page_size", c_i32), ("max_pages_per_seq", c_i32),
     ]
 
 
@@ -113,6 +122,8 @@ def load(build_if_missing: bool = False):
             lib.trt_attention_fp8_kv.argtypes = [P, c_vp, c_vp, c_vp]
             lib.rga_selftest_e4m3_decode.restype = c_int
             lib.rga_selftest_e4m3_decode.argtypes = [c_vp, c_vp, c_vp]
+            lib.trt_attention_paged_kv.restype = c_int
+            lib.trt_attention_paged_kv.argtypes = [P, ctypes.POINTER(PagedKv), c_vp]
             lib.trt_kv_cache_update.restype = c_int
             lib.trt_kv_cache_update.argtypes = [ctypes.POINTER(KvArgs), c_vp]
             _lib = lib
@@ -193,8 +204,9 @@ def _stream_handle(stream):
 
 
 def _call(kind, q, k, v, out, extra, stream, **kw):
-    """kind: 'plain' (trt_attention), 'quant' (extra = (qtype, quant_scale))
-    or 'fp8kv' (extra = (k_scale, v_scale))."""
+    """kind: 'plain' (trt_attention), 'quant' (extra = (qtype, quant_scale)),
+    'fp8kv' (extra = (k_scale, v_scale)) or 'paged' (extra = a filled
+    PagedKv, k and v being the pools)."""
     lib = load()
     y = torch.full_like(q, float("nan")) if out is None else out
     status = kw.pop("status", None)
@@ -202,6 +214,8 @@ def _call(kind, q, k, v, out, extra, stream, **kw):
         status = torch.zeros(1, dtype=torch.int32, device=q.device)
     workspace = kw.pop("workspace", None)
     a = make_args(q, k, v, y, status=status, workspace=workspace, **kw)
+    if kind == "paged":   # a sequence may hold up to max_pages_per_seq * page_size keys
+        a.kv_seq = extra.max_pages_per_seq * extra.page_size
     if workspace is None:
         n = lib.rga_attention_workspace_size(ctypes.byref(a))
         if n > 0:   # n == 0: invalid arguments; the call below reports which
@@ -217,6 +231,9 @@ def _call(kind, q, k, v, out, extra, stream, **kw):
         ks, vs = extra
         rc = lib.trt_attention_fp8_kv(ctypes.byref(a), ks.data_ptr(), vs.data_ptr(), h)
         name = "trt_attention_fp8_kv"
+    elif kind == "paged":
+        rc = lib.trt_attention_paged_kv(ctypes.byref(a), ctypes.byref(extra), h)
+        name = "trt_attention_paged_kv"
     else:
         rc = lib.trt_attention(ctypes.byref(a), h)
         name = "trt_attention"
@@ -276,6 +293,48 @@ def trt_attention_fp8_kv(q, k, v, *, k_scale, v_scale, q_form="padded", kv_form=
                   kv_form=kv_form, query_lengths=query_lengths, kv_lengths=kv_lengths,
                   mask=mask, scale=scale, causal=causal, norm=norm, workspace=workspace,
                   status=status)
+    return (y, st) if return_status else y
+
+
+def make_paged(k_pool, v_pool, page_table, *, k_scale=None, v_scale=None) -> PagedKv:
+    """rga_paged_kv for device pools [num_pages, Hkv, page_size, D] and a
+    device int32 page table [B, 2, max_pages_per_seq].  Pools of E4M3 codes
+    (float8_e4m3fn or uint8) need k_scale and v_scale."""
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("page_table", page_table)):
+        _need_cuda(name, t)
+    if k_pool.dim() != 4 or v_pool.shape != k_pool.shape:
+        raise ValueError("k_pool and v_pool must be [num_pages, Hkv, page_size, D]")
+    if page_table.dtype != torch.int32 or page_table.dim() != 3 or page_table.shape[1] != 2:
+        raise ValueError("page_table must be int32 [B, 2, max_pages_per_seq]")
+    pk = PagedKv()
+    pk.k_pool, pk.v_pool, pk.page_table = _ptr(k_pool), _ptr(v_pool), _ptr(page_table)
+    if k_pool.dtype in FP8_CODE_DTYPES:
+        if k_scale is None or v_scale is None:
+            raise ValueError("E4M3 pools need k_scale and v_scale")
+        for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+            _need_cuda(name, t)
+        pk.kv_dtype = 4
+        pk.k_scale, pk.v_scale = _ptr(k_scale), _ptr(v_scale)
+    else:
+        pk.kv_dtype = DTYPES.get(k_pool.dtype, 99)
+    pk.num_pages, pk.page_size = k_pool.shape[0], k_pool.shape[2]
+    pk.max_pages_per_seq = page_table.shape[2]
+    return pk
+
+
+def trt_attention_paged_kv(q, k_pool, v_pool, page_table, kv_lengths, *, k_scale=None,
+                           v_scale=None, q_form="padded", query_lengths=None, mask=None,
+                           scale=1.0, causal="none", norm="softmax", out=None, workspace=None,
+                           status=None, stream=None, return_status=False):
+    """Attention over a paged KV cache: pools [num_pages, Hkv, page_size, D]
+    (q's dtype, or E4M3 codes with k_scale / v_scale), an int32 page table
+    [B, 2, max_pages_per_seq] (K pages, V pages) and per-sequence key counts
+    kv_lengths [B].  Decode shapes only (see include/rga.h)."""
+    pk = make_paged(k_pool, v_pool, page_table, k_scale=k_scale, v_scale=v_scale)
+    y, st = _call("paged", q, k_pool, v_pool, out, pk, stream, q_form=q_form,
+                  kv_form="padded", query_lengths=query_lengths, kv_lengths=kv_lengths,
+                  mask=mask, scale=scale, causal=causal, norm=norm, workspace=workspace,
+                  status=status, batch=(page_table.shape[0]))
     return (y, st) if return_status else y
 
 

@@ -126,7 +126,10 @@ bool use_decode(const rga_attention_args *a, bool quant, bool kv8 = false) {
     return tiles < (int64_t(1) << 31);
 }
 
-rga_status validate(const rga_attention_args *a, bool quant) {
+// paged: K/V from page pools, whose kv_seq is a capacity rather than the
+// extent of a padded cache: a mask's key dimension is then checked against
+// every sequence's length on the device, as for packed KV.
+rga_status validate(const rga_attention_args *a, bool quant, bool paged = false) {
     if (!a) return RGA_ERR_INVALID_ARG;
     if (a->dtype != RGA_F16 && a->dtype != RGA_BF16) {
         return a->dtype == RGA_F32 ? RGA_ERR_UNSUPPORTED : RGA_ERR_INVALID_ARG;
@@ -167,7 +170,7 @@ rga_status validate(const rga_attention_args *a, bool quant) {
         if (md[1] != 1 && md[1] != a->q_heads) return RGA_ERR_INVALID_ARG;
         if (a->q_form == RGA_FORM_PADDED_BHND && md[2] != 1 && md[2] != a->q_seq)
             return RGA_ERR_INVALID_ARG;
-        if (a->kv_form == RGA_FORM_PADDED_BHND && md[3] != 1 && md[3] != a->kv_seq)
+        if (a->kv_form == RGA_FORM_PADDED_BHND && !paged && md[3] != 1 && md[3] != a->kv_seq)
             return RGA_ERR_INVALID_ARG;
     }
     return RGA_OK;
@@ -224,15 +227,15 @@ size_t workspace_bytes(const rga_attention_args *a, bool quant) {
 
 // kv8: K and V are E4M3 codes dequantised with *k_scale / *v_scale (the
 // fp8 KV cache; decode shapes only).
+// paged: K and V come from page pools (a->k / a->v point at the pools).
 rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const void *qscale,
                rga_dtype qscale_dtype, cudaStream_t stream, bool kv8 = false,
-               const float *k_scale = nullptr, const float *v_scale = nullptr) {
-    rga_status st = validate(a, quant);
+               const float *k_scale = nullptr, const float *v_scale = nullptr,
+               const rga_paged_kv *paged = nullptr) {
+    rga_status st = validate(a, quant, paged != nullptr);
     if (st != RGA_OK) return st;
-    if (kv8) {
-        if (!k_scale || !v_scale) return RGA_ERR_INVALID_ARG;
-        if (!use_decode(a, false, true)) return RGA_ERR_UNSUPPORTED;
-    }
+    if (kv8 && (!k_scale || !v_scale)) return RGA_ERR_INVALID_ARG;
+    if ((kv8 || paged) && !use_decode(a, false, kv8)) return RGA_ERR_UNSUPPORTED;
     if (quant) {
         if (qtype != RGA_QUANT_FP8_E4M3 && qtype != RGA_QUANT_INT8) return RGA_ERR_INVALID_ARG;
         if (!qscale) return RGA_ERR_INVALID_ARG;
@@ -255,6 +258,13 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
     p.kv8 = kv8;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    if (paged) {
+        p.paged = 1;
+        p.page_table = paged->page_table;
+        p.page_size = paged->page_size;
+        p.max_pages = paged->max_pages_per_seq;
+        p.num_pages = paged->num_pages;
+    }
     const int bf16 = a->dtype == RGA_BF16;
     // Zero-extent K/V (no keys anywhere): the descriptors are never read,
     // so they point at Y, which is a valid address.
@@ -265,9 +275,17 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
     std::memset(&maps, 0, sizeof(maps));
     if (!encode_q(&maps.q, p.q, p) || !encode_q(&maps.y, p.y, p))
         return RGA_ERR_CUDA;
-    if (kv8 ? !encode_kv8(&maps.k, kp, p, DEC_KEYS) || !encode_kv8(&maps.v, vp, p, DEC_KEYS)
-            : !encode_kv(&maps.k, kp, p, dec ? DEC_KEYS : BN) ||
-                  !encode_kv(&maps.v, vp, p, dec ? DEC_KEYS : BN))
+    // a paged pool has the padded layout with pages for batches and a page's
+    // keys for the sequence: [num_pages, Hkv, page_size, D]
+    AttnParams pm = p;
+    if (paged) {
+        pm.kv_packed = 0;
+        pm.B = paged->num_pages;
+        pm.kv_seq = paged->page_size;
+    }
+    if (kv8 ? !encode_kv8(&maps.k, kp, pm, DEC_KEYS) || !encode_kv8(&maps.v, vp, pm, DEC_KEYS)
+            : !encode_kv(&maps.k, kp, pm, dec ? DEC_KEYS : BN) ||
+                  !encode_kv(&maps.v, vp, pm, dec ? DEC_KEYS : BN))
         return RGA_ERR_CUDA;
     int mode;
     if (a->norm == RGA_NORM_SOFTMAX) mode = quant ? MODE_SOFTMAX_Q : MODE_SOFTMAX;
@@ -303,7 +321,11 @@ cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode, i
 extern "C" {
 
 size_t rga_attention_workspace_size(const rga_attention_args *args) {
-    if (validate(args, true) != RGA_OK && validate(args, false) != RGA_OK) return 0;
+    // (valid for any entry point: the size does not depend on the mask's
+    // key extent, which a paged call checks on the device)
+    if (validate(args, true) != RGA_OK && validate(args, false) != RGA_OK &&
+        validate(args, false, true) != RGA_OK)
+        return 0;
     const size_t a = workspace_bytes(args, false), b = workspace_bytes(args, true);
     return a > b ? a : b;
 }
@@ -321,6 +343,25 @@ rga_status trt_quantized_attention(const rga_attention_args *args, rga_quant qty
 rga_status trt_attention_fp8_kv(const rga_attention_args *args, const float *k_scale,
                                 const float *v_scale, cudaStream_t stream) {
     return run(args, false, RGA_QUANT_FP8_E4M3, nullptr, RGA_F32, stream, true, k_scale, v_scale);
+}
+
+rga_status trt_attention_paged_kv(const rga_attention_args *args, const rga_paged_kv *kv,
+                                  cudaStream_t stream) {
+    if (!args || !kv) return RGA_ERR_INVALID_ARG;
+    if (!kv->k_pool || !kv->v_pool || !kv->page_table) return RGA_ERR_INVALID_ARG;
+    if (kv->num_pages <= 0 || kv->max_pages_per_seq <= 0 || kv->page_size <= 0 ||
+        kv->page_size % DEC_KEYS != 0)
+        return RGA_ERR_INVALID_ARG;
+    if ((int64_t)kv->max_pages_per_seq * kv->page_size > INT32_MAX) return RGA_ERR_UNSUPPORTED;
+    if (args->kv_form != RGA_FORM_PADDED_BHND || !args->kv_lengths) return RGA_ERR_INVALID_ARG;
+    const bool kv8 = kv->kv_dtype == RGA_FP8_E4M3;
+    if (!kv8 && kv->kv_dtype != args->dtype) return RGA_ERR_INVALID_ARG;
+    rga_attention_args a = *args;
+    a.k = kv->k_pool;
+    a.v = kv->v_pool;
+    a.kv_seq = kv->max_pages_per_seq * kv->page_size;
+    return run(&a, false, RGA_QUANT_FP8_E4M3, nullptr, RGA_F32, stream, kv8,
+               kv8 ? kv->k_scale : nullptr, kv8 ? kv->v_scale : nullptr, kv);
 }
 
 rga_status rga_get_device_status(const int32_t *device_status, cudaStream_t stream,

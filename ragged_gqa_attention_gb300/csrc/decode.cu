@@ -88,10 +88,20 @@ __device__ __forceinline__ uint32_t swz(int row, int ch, int blk) {
     return (ch >> 3) * blk + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
 }
 
+// Loads the K and V tiles of keys [j0, j0 + DEC_KEYS) of batch b, KV head
+// g.  Paged cache: the tile lies in one page (page_size is a multiple of
+// DEC_KEYS); pk / pv are its K and V pages, looked up by the caller, and
+// the pools' tensor maps are [num_pages, Hkv, page_size, D].
 template <bool KV8>
 __device__ __forceinline__ void dec_tma(const AttnParams &p, const TensorMaps &tm,
                                         const SeqInfo &s, int b, int g, int j0, uint8_t *dst,
-                                        uint64_t *bar, int D) {
+                                        uint64_t *bar, int D, int pk, int pv) {
+    int rk = j0, rv = j0, zk = b, zv = b;   // padded / paged coordinates (row, outer)
+    if (p.paged) {
+        rk = rv = j0 % p.page_size;
+        zk = pk;
+        zv = pv;
+    }
     if constexpr (KV8) {   // one box of DEC_KEYS rows x D bytes per tensor
         const int tile = DEC_KEYS * D;
         mbar_arrive_expect_tx(bar, 2 * tile);
@@ -99,8 +109,8 @@ __device__ __forceinline__ void dec_tma(const AttnParams &p, const TensorMaps &t
             tma_load_3d(dst, &tm.k, bar, 0, g, s.kv_off + j0);
             tma_load_3d(dst + tile, &tm.v, bar, 0, g, s.kv_off + j0);
         } else {
-            tma_load_4d(dst, &tm.k, bar, 0, j0, g, b);
-            tma_load_4d(dst + tile, &tm.v, bar, 0, j0, g, b);
+            tma_load_4d(dst, &tm.k, bar, 0, rk, g, zk);
+            tma_load_4d(dst + tile, &tm.v, bar, 0, rv, g, zv);
         }
         return;
     }
@@ -113,8 +123,8 @@ __device__ __forceinline__ void dec_tma(const AttnParams &p, const TensorMaps &t
             tma_load_3d(kd, &tm.k, bar, blk * 64, g, s.kv_off + j0);
             tma_load_3d(vd, &tm.v, bar, blk * 64, g, s.kv_off + j0);
         } else {
-            tma_load_4d(kd, &tm.k, bar, blk * 64, j0, g, b);
-            tma_load_4d(vd, &tm.v, bar, blk * 64, j0, g, b);
+            tma_load_4d(kd, &tm.k, bar, blk * 64, rk, g, zk);
+            tma_load_4d(vd, &tm.v, bar, blk * 64, rv, g, zv);
         }
     }
 }
@@ -576,7 +586,15 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     }
     dec_prefix<L::THREADS>(tpre, p.B, scratch);
     dec_prefix<L::THREADS>(ppre, p.B, scratch);
-    pdl_wait();   // the tickets have been cleared
+    pdl_wait();   // the tickets have been cleared (and, paged, the pages checked)
+    if (p.paged) {
+        const volatile int *pf = reinterpret_cast<const volatile int *>(p.ws) + WS_PAGE_FLAGS;
+        const int bad = (int)threadIdx.x < dec_prep_blocks(p) ? pf[threadIdx.x] : 0;
+        if (__syncthreads_or(bad)) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) set_status(p.status, 4);
+            return;
+        }
+    }
 
     // Stream-K split of the work: all key tiles of all pairs, batch-major,
     // in one line of T tiles, cut into equal contiguous ranges, one per warp
@@ -639,11 +657,21 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         c.s = seq_info(p, b);
         dec_batch_shape<DR>(p, c.s, c.nrc, c.nt);
     };
-    auto issue = [&](const DecCur &c) {
+    // K and V pages of cursor c's tile (paged cache; lane 0 only)
+    auto pages_of = [&](const DecCur &c, int &pk, int &pv) {
+        pk = pv = 0;
+        if (p.paged && lane == 0) {
+            const int32_t *pt = p.page_table + (size_t)c.b * 2 * p.max_pages;
+            const int pg = c.tile * DEC_KEYS / p.page_size;
+            pk = __ldg(pt + pg);
+            pv = __ldg(pt + p.max_pages + pg);
+        }
+    };
+    auto issue = [&](const DecCur &c, int pk, int pv) {
         if (lane == 0) {
             fence_proxy_async_smem();   // the stage's previous tile was read by ldmatrix
             dec_tma<KV8>(p, tm, c.s, c.b, c.pib / c.nrc, c.tile * DEC_KEYS,
-                    ring + (issued % NS) * L::STAGE, &wbar[issued % NS], D);
+                    ring + (issued % NS) * L::STAGE, &wbar[issued % NS], D, pk, pv);
         }
         ++issued;
     };
@@ -660,7 +688,9 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         cc = lc;
         int next_issue = t_begin;
         for (; next_issue < t_end && next_issue < t_begin + NS; ++next_issue) {
-            issue(lc);
+            int pk, pv;
+            pages_of(lc, pk, pv);
+            issue(lc, pk, pv);
             advance(lc);
         }
         DecRow rr[2];       // this lane's two output rows
@@ -747,6 +777,9 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             const int st = c % NS;
             if (!mbar_wait(&wbar[st], (c / NS) & 1, abort)) { ok = false; break; }
             ++consumed;
+            // pages of the tile the refill below loads, read while this one computes
+            int npk = 0, npv = 0;
+            if (next_issue < t_end) pages_of(lc, npk, npv);
             const int j0 = cc.tile * DEC_KEYS;
             const uint32_t kb = ring_u32 + st * L::STAGE, vb = kb + L::TILE;
             const int rem = cc.s.kv_len - j0;
@@ -765,7 +798,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             else dec_tile<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc);
             __syncwarp();
             if (next_issue < t_end) {   // refill the stage just used
-                issue(lc);
+                issue(lc, npk, npv);
                 advance(lc);
                 ++next_issue;
             }
@@ -882,12 +915,33 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     if (lane == 0 && (!ok || *abort)) set_status(p.status, 5);
 }
 
-// Clears the merge tickets of a decode call; the decode kernel follows it as
-// a programmatic dependent.
-__global__ void decode_prep_kernel(int *tickets, int n) {
+// Clears the merge tickets of a decode call.  With a paged cache every
+// block also checks its slice of the page indices of every sequence's keys
+// (all of [0, kv_len)) and writes to its own header word whether one lies
+// outside the pools.  The decode kernel follows it as a programmatic
+// dependent and reads those words after griddepcontrol.wait, before
+// writing anything.
+__global__ void decode_prep_kernel(const __grid_constant__ AttnParams p, int n) {
     pdl_launch_dependents();
+    int *tickets = reinterpret_cast<int *>(p.ws + dec_tickets_off(p));
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
         tickets[i] = 0;
+    if (p.paged) {
+        const long long total = (long long)p.B * p.max_pages;
+        const long long cap = (long long)p.max_pages * p.page_size;
+        int bad = 0;
+        for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+             i += (long long)gridDim.x * blockDim.x) {
+            const int b = (int)(i / p.max_pages), k = (int)(i % p.max_pages);
+            const long long len = min((long long)max(p.kv_lengths[b], 0), cap);
+            if (k >= (len + p.page_size - 1) / p.page_size) continue;
+            const int32_t *pt = p.page_table + (size_t)b * 2 * p.max_pages;
+            const int a = pt[k], v = pt[p.max_pages + k];
+            if (a < 0 || a >= p.num_pages || v < 0 || v >= p.num_pages) bad = 1;
+        }
+        bad = __syncthreads_or(bad);
+        if (threadIdx.x == 0) reinterpret_cast<int *>(p.ws)[WS_PAGE_FLAGS + blockIdx.x] = bad;
+    }
 }
 
 template <int D, bool BF16, bool SOFTMAX, bool KV8>
@@ -901,8 +955,7 @@ static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStre
         attr_set = true;
     }
     const int n = p.max_pairs + 1;
-    decode_prep_kernel<<<(n + 255) / 256 < 64 ? (n + 255) / 256 : 64, 256, 0, s>>>(
-        reinterpret_cast<int *>(p.ws + dec_tickets_off(p)), n);
+    decode_prep_kernel<<<dec_prep_blocks(p), 256, 0, s>>>(p, n);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_dependent(decode_kernel<D, BF16, SOFTMAX, KV8>, p.grid, L::THREADS, L::ALLOC, s,

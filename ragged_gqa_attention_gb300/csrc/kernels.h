@@ -53,6 +53,9 @@ struct AttnParams {
     int dec_rows;                   // decode: query rows per pair (DEC_ROWS or DEC_ROWS_KV8)
     int kv8;                        // K, V hold E4M3 codes (fp8 KV cache)
     const float *k_scale, *v_scale; // fp8 KV cache: dequantisation scales (device scalars)
+    int paged;                      // K, V come from page pools (decode only)
+    const int32_t *page_table;      // paged: [B, 2, max_pages] K pages, V pages
+    int page_size, max_pages, num_pages;
     int grid;                       // decode: persistent grid size
     int32_t *status;                // device status word
     uint8_t *ws;                    // workspace base
@@ -60,6 +63,11 @@ struct AttnParams {
 
 // Workspace layout (byte offsets from ws).
 constexpr size_t WS_HEADER = 256;             // int counters
+// Paged decode: each block of the decode prep kernel checks a slice of the
+// page table and writes whether it found a page index outside the pools to
+// its own header word WS_PAGE_FLAGS + block (no word has two writers).
+constexpr int WS_PAGE_FLAGS = 8;
+constexpr int DEC_PREP_MAX = 48;              // prep blocks (WS_PAGE_FLAGS + 48 <= 64 words)
 // prefill: int4 items[max_items] after the header
 // decode: after the prefill region: int tickets[max_pairs] (256-aligned),
 // then float partial_o[dec_slots][dec_rows][D], float2 ml[dec_slots][dec_rows]
@@ -84,6 +92,18 @@ __host__ __device__ inline size_t dec_ml_off(const AttnParams &p) {
 __host__ __device__ inline size_t dec_ws_bytes(const AttnParams &p) {
     return dec_ml_off(p) + (size_t)p.dec_slots * p.dec_rows * 8;
 }
+// Blocks of the decode prep kernel (computed the same way by the launcher
+// and by the decode kernel, which reads that many page flags).
+__host__ __device__ inline int dec_prep_blocks(const AttnParams &p) {
+    long long blocks = ((long long)p.max_pairs + 1 + 255) / 256;
+    if (p.paged) {
+        const long long v = ((long long)p.B * p.max_pages + 2047) / 2048;
+        if (v > blocks) blocks = v;
+    }
+    if (blocks < 1) blocks = 1;
+    return (int)(blocks < DEC_PREP_MAX ? blocks : DEC_PREP_MAX);
+}
+
 // Largest batch the decode kernel lists in shared memory.
 constexpr int DEC_MAX_B = 4096;
 

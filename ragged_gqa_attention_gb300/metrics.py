@@ -66,7 +66,7 @@ def input_bytes(case: Case):
     """Host->device bytes of one call's inputs (Q, K, V, lengths, mask, scale)."""
     n = 0
     for t in (case.q, case.k, case.v, case.query_lengths, case.kv_lengths, case.mask,
-              case.quant_scale, *(case.kv_scales or ())):
+              case.quant_scale, case.page_table, *(case.kv_scales or ())):
         if t is not None:
             n += t.numel() * t.element_size()
     return n

@@ -29,6 +29,7 @@ import torch
 
 PADDED = "padded"
 PACKED = "packed"
+PAGED = "paged"     # K, V in page pools [num_pages, Hkv, page_size, D] + a page table
 
 
 @dataclass
@@ -52,6 +53,7 @@ class Case:
     quant: Optional[str] = None
     quant_scale: Optional[torch.Tensor] = None
     kv_scales: Optional[tuple] = None       # fp8 KV cache: (s_k, s_v) fp32 [1] tensors
+    page_table: Optional[torch.Tensor] = None   # paged: int32 [B, 2, max_pages]
     meta: dict = field(default_factory=dict)
 
     @property
@@ -59,7 +61,7 @@ class Case:
         return self.q.shape[-2] if self.q_form == PACKED else self.q.shape[1]
 
     @property
-    def kv_heads(self):
+    def kv_heads(self):   # padded [B, H, N, D], packed [T, H, D], paged pools [P, H, ps, D]
         return self.k.shape[-2] if self.kv_form == PACKED else self.k.shape[1]
 
     @property
@@ -156,6 +158,41 @@ def _to_e4m3_codes(x, s, pad):
     return codes
 
 
+def paged(case: Case, page_size: int, seed: int, spare: int = 3, pad=math.nan) -> Case:
+    """The same problem with its padded K/V cache moved into page pools:
+    each sequence's keys fill ceil(kv_len / page_size) pages, K and V pages
+    each placed at a seeded random permutation of a pool that holds
+    ``spare`` extra pages; unused pages and the rows past a sequence's end
+    hold ``pad`` (its E4M3 code for code pools); page-table entries past a
+    sequence's last page are -1 (never read).  Layout and random draws only."""
+    assert case.kv_form == PADDED and page_size % 32 == 0
+    B, H, N, D = case.k.shape
+    mp = max(1, (N + page_size - 1) // page_size)
+    need = [(n + page_size - 1) // page_size for n in case.kv_lens]
+    P = sum(need) + spare
+    g = torch.Generator("cpu").manual_seed(seed)
+    table = torch.full((B, 2, mp), -1, dtype=torch.int32)
+    pools = []
+    for which, src in enumerate((case.k, case.v)):
+        pool = torch.empty((P, H, page_size, D), dtype=src.dtype)
+        if src.dtype == torch.uint8:
+            pool.fill_(int(torch.tensor(pad, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)))
+        else:
+            pool.fill_(pad)
+        perm = torch.randperm(P, generator=g)
+        k = 0
+        for b in range(B):
+            for i in range(need[b]):
+                pg = int(perm[k])
+                k += 1
+                rows = min(page_size, N - i * page_size)
+                pool[pg, :, :rows] = src[b, :, i * page_size:i * page_size + rows]
+                table[b, which, i] = pg
+        pools.append(pool)
+    return replace(case, name=f"{case.name}_paged{page_size}", k=pools[0], v=pools[1],
+                   kv_form=PAGED, page_table=table)
+
+
 def _uniform_int(g, lo, hi, n):
     """n integers uniform on [lo, hi] (inclusive)."""
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
@@ -187,6 +224,10 @@ WORKLOADS = {
         "N=4096 with kv_len U[256,4096], B=64, Hq=64 Hkv=8 D=128, bf16 Q/Y, "
         "lower_right; K, V stored as E4M3FN codes with per-tensor scales "
         "s_k = 1/56, s_v = 1/48"),
+    8: ("decode_b64_gqa64x8_kv4096_d128_bf16_paged64",
+        "workload 4 over a paged KV cache: each sequence's keys in pages of 64 "
+        "keys placed at seeded random positions of K and V pools (16 spare "
+        "pages each), page table [64, 2, 64]"),
 }
 
 # per-tensor scales of the fp8 KV cache workload (K, V ~ N(0, 1) land near
@@ -195,7 +236,7 @@ FP8_KV_SCALES = (1.0 / 56.0, 1.0 / 48.0)
 
 
 def workload(index, *, quant="fp8", kv_pad=math.nan, seed=None):
-    """The named workload ``index`` (1..7) as a Case on host memory.
+    """The named workload ``index`` (1..8) as a Case on host memory.
 
     ``quant`` selects the fp8 or int8 variant of workload 5.
     """
@@ -227,6 +268,8 @@ def workload(index, *, quant="fp8", kv_pad=math.nan, seed=None):
                          q_form=PACKED, kv_form=PADDED, kv_seq=4096,
                          dtype=torch.bfloat16, causal="lower_right",
                          kv_pad=kv_pad, g=g)
+    if index == 8:
+        return paged(workload(4, kv_pad=kv_pad), 64, seed=8, spare=16, pad=kv_pad)
     if index == 7:
         kvls = _uniform_int(g, 256, 4096, 64)
         return make_case(name, seed, batch=64, q_heads=64, kv_heads=8,
@@ -282,4 +325,5 @@ def to_device(case: Case, device, non_blocking=False) -> Case:
                    kv_lengths=mv(case.kv_lengths), mask=mv(case.mask),
                    quant_scale=mv(case.quant_scale),
                    kv_scales=None if case.kv_scales is None else tuple(
-                       mv(t) for t in case.kv_scales))
+                       mv(t) for t in case.kv_scales),
+                   page_table=mv(case.page_table))

@@ -42,7 +42,13 @@ def run_gpu(case: W.Case, *, status=None):
     kw = dict(q_form=dc.q_form, kv_form=dc.kv_form, query_lengths=dc.query_lengths,
               kv_lengths=dc.kv_lengths, mask=dc.mask, scale=dc.scale, causal=dc.causal,
               norm=dc.norm, out=y, status=status, return_status=True)
-    if dc.kv_scales is not None:
+    if dc.kv_form == W.PAGED:
+        ks, vs = dc.kv_scales if dc.kv_scales is not None else (None, None)
+        _, st = binding.trt_attention_paged_kv(
+            dc.q, dc.k, dc.v, dc.page_table, dc.kv_lengths, k_scale=ks, v_scale=vs,
+            q_form=dc.q_form, query_lengths=dc.query_lengths, mask=dc.mask, scale=dc.scale,
+            causal=dc.causal, norm=dc.norm, out=y, status=status, return_status=True)
+    elif dc.kv_scales is not None:
         _, st = binding.trt_attention_fp8_kv(dc.q, dc.k, dc.v, k_scale=dc.kv_scales[0],
                                              v_scale=dc.kv_scales[1], **kw)
     elif dc.quant is None:
@@ -55,9 +61,15 @@ def run_gpu(case: W.Case, *, status=None):
 
 
 def run_oracle(case: W.Case):
-    """Oracle output, or (output, ambiguity bound) for the quantized op."""
+    """Oracle output, or (output, ambiguity bound) for the quantized op.  A
+    paged cache is first gathered into the linear padded cache."""
+    k, v, kv_form = case.k, case.v, case.kv_form
+    if kv_form == W.PAGED:
+        k = oracle.gather_pages(case.k, case.page_table, 0, case.kv_lens)
+        v = oracle.gather_pages(case.v, case.page_table, 1, case.kv_lens)
+        kv_form = W.PADDED
     return oracle.attention(
-        case.q, case.k, case.v, q_form=case.q_form, kv_form=case.kv_form,
+        case.q, k, v, q_form=case.q_form, kv_form=kv_form,
         query_lengths=case.query_lengths, kv_lengths=case.kv_lengths, mask=case.mask,
         scale=case.scale, causal=case.causal, norm=case.norm, quant=case.quant,
         quant_scale=case.quant_scale,

@@ -185,3 +185,30 @@ def test_fp8_codes_are_a_kv_update_element_type(lib):
 def test_e4m3_selftest_validates_its_arguments(lib):
     assert lib.rga_selftest_e4m3_decode(None, 0x20000, None) == 1
     assert lib.rga_selftest_e4m3_decode(0x20000, None, None) == 1
+
+
+def test_paged_kv_validation_without_a_device(lib):
+    def paged(**kw):
+        pk = binding.PagedKv()
+        pk.k_pool = pk.v_pool = 0x50000
+        pk.kv_dtype = 1
+        pk.page_table = 0x60000
+        pk.num_pages, pk.page_size, pk.max_pages_per_seq = 16, 64, 8
+        for k, v in kw.items():
+            setattr(pk, k, v)
+        return pk
+    # one token per sequence (decode shape), padded KV with per-batch lengths
+    a = _args(q_seq=1, kv_lengths=0x70000, workspace=0x100000, workspace_bytes=1 << 30)
+    call = lambda a, pk: lib.trt_attention_paged_kv(ctypes.byref(a), ctypes.byref(pk), None)
+    assert call(a, paged(page_size=48)) == 1            # not a multiple of 32
+    assert call(a, paged(page_size=0)) == 1
+    assert call(a, paged(k_pool=None)) == 1
+    assert call(a, paged(page_table=None)) == 1
+    assert call(a, paged(num_pages=0)) == 1
+    assert call(a, paged(kv_dtype=0)) == 1              # neither Q's dtype nor E4M3
+    assert call(a, paged(kv_dtype=4)) == 1              # E4M3 pools without scales
+    assert call(_args(q_seq=1, kv_form=1, kv_lengths=0x70000), paged()) == 1   # packed KV
+    assert call(_args(q_seq=1), paged()) == 1           # kv_lengths required
+    assert call(_args(kv_lengths=0x70000, workspace=0x100000, workspace_bytes=1 << 30),
+                paged()) == 2                           # 256 query rows: a prefill shape
+

@@ -500,3 +500,43 @@ def test_fp8_kv_zero_key_codes_give_uniform_weights():
     y = oracle.attention(q, kc, vc, kv_fp8_scales=(123.0, 0.1))
     vd = np.array([[oracle.e4m3_decode(int(c)) for c in row] for row in vc[0, 0]]) * 0.1
     np.testing.assert_allclose(y[0, 0], np.tile(vd.mean(axis=0), (N, 1)), rtol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# Paged KV cache: the gather that turns pools + page table into the linear
+# cache, pinned by brute force and by round trips through known layouts.
+# ----------------------------------------------------------------------------
+def test_gather_pages_brute_force():
+    g = torch.Generator().manual_seed(31)
+    P, H, ps, D, B, mp = 7, 2, 32, 4, 3, 3
+    pool = torch.randn(P, H, ps, D, generator=g).to(torch.float16)
+    table = torch.tensor([[[4, 0, -1], [1, 2, -1]], [[-1, -1, -1], [-1, -1, -1]],
+                          [[6, 5, 3], [0, 4, 6]]], dtype=torch.int32)
+    kv = [40, 0, 70]
+    for which in (0, 1):
+        got = oracle.gather_pages(pool, table, which, kv)
+        assert got.shape == (B, H, mp * ps, D)
+        for b in range(B):
+            for h in range(H):
+                for n in range(mp * ps):
+                    row = got[b, h, n]
+                    if n < kv[b]:
+                        src = pool[int(table[b, which, n // ps]), h, n % ps]
+                        assert torch.equal(row.view(torch.int16), src.view(torch.int16))
+                    else:
+                        assert torch.isnan(row).all()
+
+
+def test_gather_pages_inverts_the_paged_layout():
+    from ragged_gqa_attention_gb300 import workloads as W
+    c = W.make_case("g", 32, batch=4, q_heads=4, kv_heads=2, head_dim=16, q_lens=[1] * 4,
+                    kv_lens=[0, 31, 64, 100], q_form="packed", kv_form="padded", kv_seq=128,
+                    dtype=torch.bfloat16, causal="lower_right")
+    for ps in (32, 64, 128):
+        pc = W.paged(c, ps, seed=ps)
+        for which, src in ((0, c.k), (1, c.v)):
+            got = oracle.gather_pages(pc.k if which == 0 else pc.v, pc.page_table, which,
+                                      c.kv_lens)
+            for b, n in enumerate(c.kv_lens):
+                assert torch.equal(got[b, :, :n].view(torch.int16), src[b, :, :n].view(torch.int16))
+
