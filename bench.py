@@ -399,6 +399,50 @@ def measure_kv_update(stream, steps, warmup, dist_on, peaks):
                       work=work)
 
 
+def measure_rope_kv_update(stream, steps, warmup, dist_on, peaks):
+    """RoPE fused with the KV cache update: the chunked-prefill workload's new
+    K rows (packed, one chunk per sequence) rotated into its padded 8192-key
+    cache at the chunk's positions, and its 4430 x 32-head Q rotated in
+    place, in one launch.  GB/s of the rows read and written (Q twice, the
+    new keys read and written, the cos/sin table read)."""
+    import ctypes
+    c = W.workload(3, kv_pad=0.0)
+    g = torch.Generator().manual_seed(3)
+    cache = c.k.to("cuda")
+    T = sum(c.q_lens)
+    upd = torch.randn(T, c.kv_heads, c.head_dim, generator=g).to(c.k.dtype).cuda()
+    q = c.q.to("cuda")
+    cu = torch.zeros(c.batch + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(c.q_lens), 0)
+    wi = torch.tensor([kl - ql for ql, kl in zip(c.q_lens, c.kv_lens)], dtype=torch.int32)
+    pos = torch.cat([torch.arange(w, w + ql) for w, ql in zip(wi.tolist(), c.q_lens)]).to(torch.int32)
+    cs = W.rope_cos_sin(pos, c.head_dim).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib = binding.load()
+    wi_d, cu_d, pos_d = wi.cuda(), cu.cuda(), pos.cuda()   # referenced while `a`, `r` are used
+    a = binding.make_kv_args(cache, upd, cache, update_form="packed", write_indices=wi_d,
+                             update_lengths=cu_d, status=status)
+    r = binding.make_rope_args(q, None, cs, pos_d, kv_heads=c.kv_heads)
+    r.dtype, r.head_dim = a.dtype, c.head_dim
+    h = ctypes.c_void_p(stream.cuda_stream)
+
+    def run():
+        rc = lib.trt_kv_cache_update_rope(ctypes.byref(a), ctypes.byref(r), h)
+        if rc != 0:
+            raise binding.RgaError(rc, "bench rope kv update")
+
+    times, _ = device_timed(run, stream, steps, warmup, dist_on)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"rope kv update device status {int(status.item())}")
+    ms = max_over_ranks(statistics.mean(times), dist_on)
+    work = 2 * (q.numel() + upd.numel()) * q.element_size() + cs.numel() * 4
+    value = work / (ms * 1e-3) / 1e9
+    name = f"rope_kv_cache_update_packed{T}_q32_into_b16_h8_n8192_d128_bf16"
+    return name, dict(value=value, unit="GB/s", ms=ms, bound="hbm", peak=peaks["hbm_gbs"],
+                      work=work)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -450,12 +494,14 @@ def main():
                 "peak": r["peak"], "peak_source": peak_src}
             del r
         torch.cuda.empty_cache()
-        name, r = measure_kv_update(stream, max(5, args.steps // 2), 3, dist_on, peaks)
-        secondary[name] = {
-            "value": round(r["value"] * world, 3), "unit": r["unit"],
-            "ms_per_step": round(r["ms"], 4), "bound": r["bound"],
-            "frac_of_peak": round(r["value"] / r["peak"], 4),
-            "peak": r["peak"], "peak_source": peak_src}
+        for fn in (measure_kv_update, measure_rope_kv_update):
+            torch.cuda.empty_cache()
+            name, r = fn(stream, max(5, args.steps // 2), 3, dist_on, peaks)
+            secondary[name] = {
+                "value": round(r["value"] * world, 3), "unit": r["unit"],
+                "ms_per_step": round(r["ms"], 4), "bound": r["bound"],
+                "frac_of_peak": round(r["value"] / r["peak"], 4),
+                "peak": r["peak"], "peak_source": peak_src}
 
     cpu = None
     if rank == 0:

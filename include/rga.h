@@ -286,6 +286,45 @@ typedef struct {
 /* Enqueue TRT_KVCacheUpdate on `stream`; returns RGA_OK once enqueued. */
 rga_status trt_kv_cache_update(const rga_kv_update_args *args, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Rotary position embedding ("TensorRT Plugins Guide", AttentionPlugin:
+ * the plugin handles rotary positional encoding; its decoder contract
+ * passes RopeCosSin token-aligned with the physical rows, and positions
+ * with -1 marking padding rows).  For every row t of the T physical rows
+ * whose position is >= 0 (every row when positions is NULL), every head h
+ * and every i < R/2 (R = rotary_dim):
+ *     c = cos_sin[t * R + i],  s = cos_sin[t * R + R/2 + i]
+ *     x'[i]       = x[i] * c - x[i + R/2] * s
+ *     x'[i + R/2] = x[i + R/2] * c + x[i] * s
+ * (the rotate-half pairing); dims R .. D-1 are unchanged.  Computed in
+ * fp32, rounded to the element type (nearest even).  Rows with a negative
+ * position are left exactly as they are.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    void *q;                   /* [T, q_heads, D] rotated in place, or NULL */
+    void *k;                   /* [T, kv_heads, D] rotated in place, or NULL */
+    rga_dtype dtype;           /* F16 or BF16 */
+    int32_t tokens, q_heads, kv_heads, head_dim;
+    int32_t rotary_dim;        /* even multiple of 8, <= head_dim */
+    const float *cos_sin;      /* [T, rotary_dim]: the R/2 cosines, then the R/2 sines */
+    const int32_t *positions;  /* [T] or NULL */
+} rga_rope_args;
+
+/* Rotate q and/or k in place (device pointers, 8-byte aligned). */
+rga_status rga_rope_apply(const rga_rope_args *rope, cudaStream_t stream);
+
+/* RoPE fused with the KV cache update of the new keys: in one pass, rotate
+ * rope->q in place and write the update rows of kv (the new keys, packed
+ * form: kv->update is [T, heads, D] with T = rope->tokens) into the cache
+ * rotated, exactly as trt_attention would then read them; the update tensor
+ * itself is not modified.  kv must be an in-place update (y == past_cache)
+ * of the packed form with update_lengths; rope->k is ignored and
+ * rope->kv_heads must equal kv->heads.  Row t of the update is rotated with
+ * cos_sin row t (and skipped, i.e. written unrotated, when its position is
+ * negative).  Errors as for trt_kv_cache_update and rga_rope_apply. */
+rga_status trt_kv_cache_update_rope(const rga_kv_update_args *kv, const rga_rope_args *rope,
+                                    cudaStream_t stream);
+
 /* Copy *device_status to *out after the work already enqueued on `stream`
  * has finished.  This call synchronises the stream: use it in tests and
  * debugging, not on a hot path. */

@@ -252,3 +252,5 @@ def gather_pages(pool, page_table, which, kv_lens, pad=None):
 
 # TRT_KVCacheUpdate (a plain scatter; see kv_update.py)
 from .kv_update import kv_cache_update  # noqa: E402,F401
+# rotary position embedding (see rope.py)
+from .rope import rope  # noqa: E402,F401

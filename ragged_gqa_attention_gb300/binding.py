@@ -37,7 +37,8 @@ FP8_CODE_DTYPES = (torch.float8_e4m3fn, torch.uint8)
 EXPORTED = ("rga_attention_workspace_size", "trt_attention", "trt_quantized_attention",
             "rga_get_device_status", "rga_status_string", "rga_abi_version",
             "trt_attention_static_scratch", "trt_kv_cache_update", "rga_selftest_wait_timeout",
-            "trt_attention_fp8_kv", "rga_selftest_e4m3_decode", "trt_attention_paged_kv")
+            "trt_attention_fp8_kv", "rga_selftest_e4m3_decode", "trt_attention_paged_kv",
+            "rga_rope_apply", "trt_kv_cache_update_rope")
 
 
 class Args(ctypes.Structure):
@@ -71,6 +72,15 @@ class PagedKv(ctypes.Structure):
         ("k_pool", c_vp), ("v_pool", c_vp), ("kv_dtype", c_int),
         ("k_scale", c_vp), ("v_scale", c_vp), ("page_table", c_vp),
         ("num_pages", c_i32), ("page_size", c_i32), ("max_pages_per_seq", c_i32),
+    ]
+
+
+class RopeArgs(ctypes.Structure):
+    """Mirror of rga_rope_args."""
+    _fields_ = [
+        ("q", c_vp), ("k", c_vp), ("dtype", c_int),
+        ("tokens", c_i32), ("q_heads", c_i32), ("kv_heads", c_i32), ("head_dim", c_i32),
+        ("rotary_dim", c_i32), ("cos_sin", c_vp), ("positions", c_vp),
     ]
 
 
@@ -124,6 +134,11 @@ def load(build_if_missing: bool = False):
             lib.rga_selftest_e4m3_decode.argtypes = [c_vp, c_vp, c_vp]
             lib.trt_attention_paged_kv.restype = c_int
             lib.trt_attention_paged_kv.argtypes = [P, ctypes.POINTER(PagedKv), c_vp]
+            lib.rga_rope_apply.restype = c_int
+            lib.rga_rope_apply.argtypes = [ctypes.POINTER(RopeArgs), c_vp]
+            lib.trt_kv_cache_update_rope.restype = c_int
+            lib.trt_kv_cache_update_rope.argtypes = [ctypes.POINTER(KvArgs),
+                                                     ctypes.POINTER(RopeArgs), c_vp]
             lib.trt_kv_cache_update.restype = c_int
             lib.trt_kv_cache_update.argtypes = [ctypes.POINTER(KvArgs), c_vp]
             _lib = lib
@@ -399,3 +414,53 @@ def trt_kv_cache_update(past_cache, update, *, update_form="padded", write_indic
     if rc != RGA_OK:
         raise RgaError(rc, "trt_kv_cache_update")
     return (y, status) if return_status else y
+
+
+def make_rope_args(q, k, cos_sin, positions=None, kv_heads=None) -> RopeArgs:
+    """rga_rope_args for packed rows q [T, Hq, D] and/or k [T, Hkv, D] (either
+    may be None), an fp32 table cos_sin [T, R] and optional int32 positions."""
+    for name, t in (("q", q), ("k", k), ("cos_sin", cos_sin), ("positions", positions)):
+        _need_cuda(name, t)
+    x = q if q is not None else k
+    r = RopeArgs()
+    r.q, r.k = _ptr(q), _ptr(k)
+    r.dtype = DTYPES.get(x.dtype, 99) if x is not None else 99
+    if cos_sin.dtype != torch.float32 or cos_sin.dim() != 2:
+        raise ValueError("cos_sin must be fp32 [T, rotary_dim]")
+    r.tokens = cos_sin.shape[0]
+    r.q_heads = q.shape[1] if q is not None else 0
+    r.kv_heads = k.shape[1] if k is not None else (kv_heads or 0)
+    r.head_dim = x.shape[2] if x is not None else 0
+    r.rotary_dim = cos_sin.shape[1]
+    r.cos_sin, r.positions = _ptr(cos_sin), _ptr(positions)
+    return r
+
+
+def rope_apply(q=None, k=None, *, cos_sin, positions=None, stream=None):
+    """Rotary position embedding in place on q [T, Hq, D] and/or k [T, Hkv, D]."""
+    r = make_rope_args(q, k, cos_sin, positions)
+    rc = load().rga_rope_apply(ctypes.byref(r), c_vp(_stream_handle(stream)))
+    if rc != RGA_OK:
+        raise RgaError(rc, "rga_rope_apply")
+
+
+def trt_kv_cache_update_rope(past_cache, update, *, cos_sin, update_lengths, write_indices=None,
+                             q=None, positions=None, status=None, stream=None,
+                             return_status=False):
+    """TRT_KVCacheUpdate of the new keys (packed update [T, H, D]) into
+    past_cache in place, each written row rotated by RoPE, and q (packed
+    [T, Hq, D], optional) rotated in place, in one launch."""
+    lib = load()
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=past_cache.device)
+    a = make_kv_args(past_cache, update, past_cache, update_form="packed",
+                     write_indices=write_indices, update_lengths=update_lengths, status=status)
+    r = make_rope_args(q, None, cos_sin, positions, kv_heads=past_cache.shape[1])
+    r.dtype = a.dtype
+    r.head_dim = past_cache.shape[3]
+    rc = lib.trt_kv_cache_update_rope(ctypes.byref(a), ctypes.byref(r),
+                                      c_vp(_stream_handle(stream)))
+    if rc != RGA_OK:
+        raise RgaError(rc, "trt_kv_cache_update_rope")
+    return (past_cache, status) if return_status else past_cache
+

@@ -193,6 +193,19 @@ def paged(case: Case, page_size: int, seed: int, spare: int = 3, pad=math.nan) -
                    kv_form=PAGED, page_table=table)
 
 
+def rope_cos_sin(positions, rotary_dim, base=10000.0):
+    """RoPE input table [T, rotary_dim] fp32 for the given positions: the
+    cosines of angles position * base^(-2i / rotary_dim), i < rotary_dim/2,
+    then their sines (the usual rotary frequencies; rows of negative
+    positions, padding, get angle 0).  An input of the rotation, built in
+    fp64 and rounded once."""
+    pos = torch.as_tensor(positions, dtype=torch.float64).clamp(min=0.0)
+    half = rotary_dim // 2
+    inv = base ** (-2.0 * torch.arange(half, dtype=torch.float64) / rotary_dim)
+    ang = pos[:, None] * inv[None, :]
+    return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
+
+
 def _uniform_int(g, lo, hi, n):
     """n integers uniform on [lo, hi] (inclusive)."""
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]

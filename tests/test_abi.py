@@ -212,3 +212,32 @@ def test_paged_kv_validation_without_a_device(lib):
     assert call(_args(kv_lengths=0x70000, workspace=0x100000, workspace_bytes=1 << 30),
                 paged()) == 2                           # 256 query rows: a prefill shape
 
+
+def test_rope_validation_without_a_device(lib):
+    def rope(**kw):
+        r = binding.RopeArgs()
+        r.q = 0x10000
+        r.dtype, r.tokens, r.q_heads, r.kv_heads, r.head_dim, r.rotary_dim = 1, 8, 4, 2, 128, 128
+        r.cos_sin = 0x20000
+        for k, v in kw.items():
+            setattr(r, k, v)
+        return r
+    call = lambda r: lib.rga_rope_apply(ctypes.byref(r), None)
+    assert call(rope(rotary_dim=12)) == 1        # not a multiple of 8
+    assert call(rope(rotary_dim=136)) == 1       # past the head dim
+    assert call(rope(head_dim=66)) == 1
+    assert call(rope(cos_sin=None)) == 1
+    assert call(rope(cos_sin=0x20008)) == 1      # table not 16-byte aligned
+    assert call(rope(q=None)) == 1               # nothing to rotate
+    assert call(rope(q=0x10004)) == 1            # rows not 8-byte aligned
+    assert call(rope(dtype=2)) == 1
+    assert call(rope(tokens=0)) == 0             # nothing to do, nothing launched
+    kv = _kv_args(update_form=1, update_lengths=0x30000, update_seq=8, heads=2)
+    fused = lambda a, r: lib.trt_kv_cache_update_rope(ctypes.byref(a), ctypes.byref(r), None)
+    assert fused(_kv_args(update_form=0, heads=2, update_seq=8), rope()) == 1   # padded update
+    assert fused(_kv_args(update_form=1, update_lengths=0x30000, update_seq=8, heads=2,
+                          y=0x40000), rope()) == 1                              # not in place
+    assert fused(_kv_args(update_form=1, update_lengths=0x30000, update_seq=8, heads=4),
+                 rope()) == 1                                                    # heads differ
+    assert fused(kv, rope(dtype=0)) == 1                                         # dtypes differ
+
