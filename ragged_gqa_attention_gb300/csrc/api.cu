@@ -118,9 +118,10 @@ bool use_decode(const rga_attention_args *a, bool quant, bool kv8 = false) {
     (void)kv8;   // both caches take the same shapes
     if (quant || a->batch > DEC_MAX_B) return false;
     const int G = a->q_heads / a->kv_heads;
-    if (G > DEC_ROWS) return false;
+    if (G > DEC_MAX_ROWS) return false;
     const bool packed = a->q_form == RGA_FORM_PACKED_NHD;
-    if (packed ? a->q_seq > 8 * (int64_t)a->batch : (int64_t)a->q_seq * G > DEC_ROWS) return false;
+    if (packed ? a->q_seq > 8 * (int64_t)a->batch : (int64_t)a->q_seq * G > DEC_MAX_ROWS)
+        return false;
     const int64_t tiles = dec_max_pairs(a->batch, a->kv_heads, G, a->q_seq, packed, DEC_ROWS_KV8) *
                           (((int64_t)a->kv_seq + DEC_KEYS - 1) / DEC_KEYS);
     return tiles < (int64_t(1) << 31);

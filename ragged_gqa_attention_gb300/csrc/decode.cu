@@ -3,21 +3,22 @@
 // vanilla decoding attention) with the TRT_Attention semantics of
 // "TensorRT Custom Operator Schemas".
 //
-// Work: pairs (batch b, KV head g, chunk of 16 query rows), each with the
+// Work: pairs (batch b, KV head g, chunk of 8 query rows), each with the
 // 32-key tiles of the batch's key extent.  The query rows of a pair are the
-// (token, head) pairs of the G heads of g, 16 at a time (one MMA row block).
+// (token, head) pairs of the G heads of g, 8 at a time: the N = 8 of the
+// m16n8k16 MMA in the transposed products S^T = K Q^T and O^T = V^T P^T
+// (keys, then head dims, on M), so no MMA row is wasted at G = 8 and K and
+// V are read once from HBM for all G query heads of the KV head.
 // All tiles of all pairs form one batch-major line that is cut into equal
 // contiguous ranges, one per warp of the persistent grid, so that every
 // warp streams the same number of tiles and none is left finishing a long
 // unit alone at the end.  Each CTA validates the lengths and lays out the
 // line itself (no scheduler launch).  A warp streams its range's K/V tiles
 // with TMA through its own ring of a few stages (128-byte swizzle), straight
-// across pair boundaries, computes S = Q K^T and O += P V with m16n8k16 MMAs
-// (K and V are read once from HBM for all G query heads of the KV head) and
-// keeps an online softmax in fp32 registers.  A pair inside one range is
-// written to Y by its warp; a pair cut by range ends leaves a partial
-// (O, m, l) per warp, and the last of its warps to finish (atomic ticket)
-// merges them in warp order and writes Y.
+// across pair boundaries, and keeps an online softmax in fp32 registers.
+// A pair inside one range is written to Y by its warp; a pair cut by range
+// ends leaves a partial (O, m, l) per warp, and the last of its warps to
+// finish (atomic ticket) merges them in warp order and writes Y.
 //
 // FP8 KV cache ("TensorRT Plugins Guide", AttentionPlugin: kv_cache_type
 // FP8): K and V hold OCP E4M3FN codes with one dequantisation scale each.
@@ -150,114 +151,6 @@ __device__ __forceinline__ DecRow dec_row(const AttnParams &p, const SeqInfo &s,
     return r;
 }
 
-// Scale, mask and online softmax ('none': scale and mask only) of one
-// 32-key score tile held as four m16n8 accumulators: column n * 8 + 2 (lane
-// % 4) + e % 2 is key j0 + that column; rows rr[0..1] are this lane's rows
-// (lane / 4 and lane / 4 + 8).  sc: the score scale (times log2 e for
-// softmax).  Leaves P in sacc and rescales O and l.
-template <int D, bool SOFTMAX>
-__device__ __forceinline__ void dec_normalize(const AttnParams &p, const DecRow (&rr)[2],
-                                              float (&sacc)[4][4], int j0, float (&o)[D / 8][4],
-                                              float (&m_r)[2], float (&l_r)[2], float sc) {
-    constexpr int NT = D / 8;
-    const int lane = threadIdx.x & 31;
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const DecRow &R = rr[e >> 1];
-            const int j = j0 + nt * 8 + (lane & 3) * 2 + (e & 1);
-            bool ok = j <= R.lim;
-            float add = 0.f;
-            if (ok && p.mask) ok = mask_at(p, p.md[3] == 1 ? R.mrow : R.mrow + j, add);
-            const float v = sacc[nt][e] * sc + (SOFTMAX ? add * 1.4426950408889634f : add);
-            sacc[nt][e] = ok ? v : (SOFTMAX ? -INFINITY : 0.f);
-            mx[e >> 1] = fmaxf(mx[e >> 1], sacc[nt][e]);
-        }
-    if (SOFTMAX) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        }
-        // (rescaling unconditionally measured 1.5% faster here than a
-        // warp-uniform skip when no row max grew)
-        const float mn0 = fmaxf(m_r[0], mx[0]), mn1 = fmaxf(m_r[1], mx[1]);
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const float m_new = r ? mn1 : mn0;
-            const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m_r[r] - mu);
-            l_r[r] *= alpha;
-#pragma unroll
-            for (int n = 0; n < NT; ++n) { o[n][2 * r] *= alpha; o[n][2 * r + 1] *= alpha; }
-        }
-        m_r[0] = mn0;
-        m_r[1] = mn1;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const float mu = (m_r[r] == -INFINITY) ? 0.f : m_r[r];
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                sacc[nt][2 * r] = ex2(sacc[nt][2 * r] - mu);
-                sacc[nt][2 * r + 1] = ex2(sacc[nt][2 * r + 1] - mu);
-                l_r[r] += sacc[nt][2 * r] + sacc[nt][2 * r + 1];
-            }
-        }
-    }
-}
-
-// P of keys kk * 16 .. kk * 16 + 15 as the A fragment of an m16n8k16 MMA.
-template <bool BF16>
-__device__ __forceinline__ void dec_p_frag(const float (&sacc)[4][4], int kk, uint32_t (&a)[4]) {
-    a[0] = pack2<BF16>(sacc[2 * kk][0], sacc[2 * kk][1]);
-    a[1] = pack2<BF16>(sacc[2 * kk][2], sacc[2 * kk][3]);
-    a[2] = pack2<BF16>(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-    a[3] = pack2<BF16>(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
-}
-
-// One 32-key tile for the warp's 16 query rows: S = Q K^T, scale and mask,
-// online softmax (or 'none'), O += P V.  kb/vb: the tile's K and V in
-// shared memory (16-bit elements).
-template <int D, bool BF16, bool SOFTMAX>
-__device__ __forceinline__ void dec_tile(const AttnParams &p, const DecRow (&rr)[2],
-                                         const uint32_t (&qa)[D / 16][4], uint32_t kb,
-                                         uint32_t vb, int j0, float (&o)[D / 8][4],
-                                         float (&m_r)[2], float (&l_r)[2], float sc) {
-    using L = DecLayout<D, false>;
-    constexpr int NT = D / 8, KS = D / 16;
-    const int lane = threadIdx.x & 31;
-    float sacc[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ks += 2) {
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(kb + swz(nt * 8 + (lane & 7), ks * 2 + (lane >> 3), L::BLK), r0, r1, r2, r3);
-            mma16816<BF16>(sacc[nt], qa[ks], r0, r1);
-            mma16816<BF16>(sacc[nt], qa[ks + 1], r2, r3);
-        }
-    }
-    dec_normalize<D, SOFTMAX>(p, rr, sacc, j0, o, m_r, l_r, sc);
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-        uint32_t a[4];
-        dec_p_frag<BF16>(sacc, kk, a);
-#pragma unroll
-        for (int n = 0; n < NT; n += 2) {
-            uint32_t r0, r1, r2, r3;
-            const int mi = lane >> 3;
-            ldsm_x4_t(vb + swz(kk * 16 + (mi & 1) * 8 + (lane & 7), n + (mi >> 1), L::BLK),
-                      r0, r1, r2, r3);
-            mma16816<BF16>(o[n], a, r0, r1);
-            mma16816<BF16>(o[n + 1], a, r2, r3);
-        }
-    }
-}
-
 // Byte offset of 16-byte chunk `ch` of key row `row` in an fp8 tile of
 // D-byte rows as the TMA writes it: 128-byte swizzle for D = 128 (chunk
 // XOR row % 8), 64-byte swizzle for D = 64 (chunk XOR (row / 2) % 4).
@@ -279,6 +172,64 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
+}
+
+// Scale, mask and online softmax ('none': scale and mask only) of one
+// 32-key tile of a transposed product S^T (keys on M, the pair's 8 query
+// rows on N): element (mb, e) is key j0 + 16 mb + lane/4 + 8 (e / 2) of row
+// rr[e % 2] (rows 2c and 2c + 1, c = lane % 4).  Leaves P^T in sacc and
+// rescales O^T (o[m][e] belongs to row rr[e % 2]) and l.
+template <int D, bool SOFTMAX>
+__device__ __forceinline__ void dec_normalize_t(const AttnParams &p, const DecRow (&rr)[2],
+                                                float (&sacc)[2][4], int j0,
+                                                float (&o)[D / 16][4], float (&m_r)[2],
+                                                float (&l_r)[2], float sc) {
+    constexpr int NO = D / 16;
+    const int r = (threadIdx.x & 31) >> 2;
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const DecRow &R = rr[e & 1];
+            const int j = j0 + 16 * mb + r + 8 * (e >> 1);
+            bool ok = j <= R.lim;
+            float add = 0.f;
+            if (ok && p.mask) ok = mask_at(p, p.md[3] == 1 ? R.mrow : R.mrow + j, add);
+            const float v = sacc[mb][e] * sc + (SOFTMAX ? add * 1.4426950408889634f : add);
+            sacc[mb][e] = ok ? v : (SOFTMAX ? -INFINITY : 0.f);
+            mx[e & 1] = fmaxf(mx[e & 1], sacc[mb][e]);
+        }
+    if (SOFTMAX) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int m = 4; m < 32; m <<= 1) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], m));
+        // O and l need rescaling only when a row's running max grew (alpha
+        // is exactly 1 otherwise); the test is warp-uniform
+        const float mn0 = fmaxf(m_r[0], mx[0]), mn1 = fmaxf(m_r[1], mx[1]);
+        if (__any_sync(0xffffffffu, mn0 > m_r[0] || mn1 > m_r[1])) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float m_new = i ? mn1 : mn0;
+                const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+                const float alpha = ex2(m_r[i] - mu);
+                l_r[i] *= alpha;
+#pragma unroll
+                for (int m = 0; m < NO; ++m) { o[m][i] *= alpha; o[m][i + 2] *= alpha; }
+            }
+        }
+        m_r[0] = mn0;
+        m_r[1] = mn1;
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sacc[mb][e] = ex2(sacc[mb][e] - ((e & 1) ? mu1 : mu0));
+                l_r[e & 1] += sacc[mb][e];
+            }
+    }
 }
 
 // dec_tile for an fp8 KV cache, kb/vb holding E4M3 codes that each thread
@@ -333,51 +284,7 @@ __device__ __forceinline__ void dec_tile8(const AttnParams &p, const DecRow (&rr
             mma16816<false>(sacc[mb], a, qb[ks][0], qb[ks][1]);
         }
     }
-    // scale and mask: element (mb, e) is key j0 + 16 mb + r + 8 (e / 2) of row rr[e % 2]
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const DecRow &R = rr[e & 1];
-            const int j = j0 + 16 * mb + r + 8 * (e >> 1);
-            bool ok = j <= R.lim;
-            float add = 0.f;
-            if (ok && p.mask) ok = mask_at(p, p.md[3] == 1 ? R.mrow : R.mrow + j, add);
-            const float v = sacc[mb][e] * sc + (SOFTMAX ? add * 1.4426950408889634f : add);
-            sacc[mb][e] = ok ? v : (SOFTMAX ? -INFINITY : 0.f);
-            mx[e & 1] = fmaxf(mx[e & 1], sacc[mb][e]);
-        }
-    if (SOFTMAX) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int m = 4; m < 32; m <<= 1) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], m));
-        // O and l need rescaling only when a row's running max grew (alpha
-        // is exactly 1 otherwise); the test is warp-uniform
-        const float mn0 = fmaxf(m_r[0], mx[0]), mn1 = fmaxf(m_r[1], mx[1]);
-        if (__any_sync(0xffffffffu, mn0 > m_r[0] || mn1 > m_r[1])) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float m_new = i ? mn1 : mn0;
-                const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-                const float alpha = ex2(m_r[i] - mu);
-                l_r[i] *= alpha;
-#pragma unroll
-                for (int m = 0; m < NO; ++m) { o[m][i] *= alpha; o[m][i + 2] *= alpha; }
-            }
-        }
-        m_r[0] = mn0;
-        m_r[1] = mn1;
-        const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-#pragma unroll
-        for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                sacc[mb][e] = ex2(sacc[mb][e] - ((e & 1) ? mu1 : mu0));
-                l_r[e & 1] += sacc[mb][e];
-            }
-    }
+    dec_normalize_t<D, SOFTMAX>(p, rr, sacc, j0, o, m_r, l_r, sc);
     // O^T += V^T P^T over the tile's two 16-key halves
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
@@ -422,19 +329,61 @@ __device__ __forceinline__ void dec_tile8(const AttnParams &p, const DecRow (&rr
     }
 }
 
-// Y rows of this lane's output rows, scaled by f (rows outside are skipped):
-// the 16-bit tile's rows lane/4 and lane/4 + 8 in the MMA's column order;
-// the fp8 tile's rows 2c and 2c + 1, dims [(D/8) (lane/4), +D/8).
-template <int D, bool BF16, bool KV8>
+// The 16-bit tile with the transposed products of dec_tile8 (S^T = K Q^T,
+// O^T = V^T P^T; the pair's 8 query rows are the MMA's N): K blocks are the
+// A operand straight from ldmatrix, V^T blocks from ldmatrix.trans, P^T from
+// movmatrix; Q (qb) is the B operand in the natural dim order.  Accumulator
+// o[m][e] holds row 2c + e % 2, dim 16 m + lane/4 + 8 (e / 2).
+template <int D, bool BF16, bool SOFTMAX>
+__device__ __forceinline__ void dec_tile16t(const AttnParams &p, const DecRow (&rr)[2],
+                                            const uint32_t (&qb)[D / 16][2], uint32_t kb,
+                                            uint32_t vb, int j0, float (&o)[D / 16][4],
+                                            float (&m_r)[2], float (&l_r)[2], float sc) {
+    using L = DecLayout<D, false>;
+    constexpr int KS = D / 16, NO = D / 16;
+    const int lane = threadIdx.x & 31;
+    float sacc[2][4];
+#pragma unroll
+    for (int mb = 0; mb < 2; ++mb) {
+        sacc[mb][0] = sacc[mb][1] = sacc[mb][2] = sacc[mb][3] = 0.f;
+        const int key = 16 * mb + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(kb + swz(key, ks * 2 + (lane >> 4), L::BLK), a[0], a[1], a[2], a[3]);
+            mma16816<BF16>(sacc[mb], a, qb[ks][0], qb[ks][1]);
+        }
+    }
+    dec_normalize_t<D, SOFTMAX>(p, rr, sacc, j0, o, m_r, l_r, sc);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t b0 = movmatrix_trans(pack2<BF16>(sacc[kk][0], sacc[kk][1]));
+        const uint32_t b1 = movmatrix_trans(pack2<BF16>(sacc[kk][2], sacc[kk][3]));
+        const int key = 16 * kk + (lane & 7) + ((lane >> 4) & 1) * 8;
+#pragma unroll
+        for (int m = 0; m < NO; ++m) {
+            uint32_t a[4];
+            ldsm_x4_t(vb + swz(key, m * 2 + ((lane >> 3) & 1), L::BLK), a[0], a[1], a[2], a[3]);
+            mma16816<BF16>(o[m], a, b0, b1);
+        }
+    }
+}
+
+// Accumulator layouts of the two tiles (DLAY), both with rows 2c and 2c+1
+// (c = lane % 4): DLAY_FP8, dims [(D/8) (lane/4), +D/8) in order; DLAY_16T,
+// dim 16 m + lane/4 + 8 (e / 2) of o[m][e].
+constexpr int DLAY_FP8 = 1, DLAY_16T = 2;
+
+// Y rows of this lane's output rows, scaled by f (rows outside are skipped).
+template <int D, bool BF16, int DLAY>
 __device__ __forceinline__ void dec_store_y(const AttnParams &p, const DecRow (&rr)[2],
-                                            const float (&o)[KV8 ? D / 16 : D / 8][4],
-                                            const float (&f)[2]) {
+                                            const float (&o)[D / 16][4], const float (&f)[2]) {
     const int lane = threadIdx.x & 31;
     uint16_t *y = static_cast<uint16_t *>(p.y);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         if (!rr[r].valid) continue;
-        if constexpr (KV8) {
+        if constexpr (DLAY == DLAY_FP8) {
             constexpr int NO = D / 16;
             uint4 *dst = reinterpret_cast<uint4 *>(y + rr[r].qoff + (D / 8) * (lane >> 2));
 #pragma unroll
@@ -444,35 +393,36 @@ __device__ __forceinline__ void dec_store_y(const AttnParams &p, const DecRow (&
                                     pack2<BF16>(o[4 * i + 2][r] * f[r], o[4 * i + 2][r + 2] * f[r]),
                                     pack2<BF16>(o[4 * i + 3][r] * f[r], o[4 * i + 3][r + 2] * f[r]));
         } else {
+            // dims 16 m + lane/4 and + 8: one 16-bit store each (once per pair)
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                const int col = n * 8 + (lane & 3) * 2;
-                *reinterpret_cast<uint32_t *>(y + rr[r].qoff + col) =
-                    pack2<BF16>(o[n][2 * r] * f[r], o[n][2 * r + 1] * f[r]);
+            for (int m = 0; m < D / 16; ++m) {
+                const uint32_t w = pack2<BF16>(o[m][r] * f[r], o[m][r + 2] * f[r]);
+                y[rr[r].qoff + 16 * m + (lane >> 2)] = (uint16_t)(w & 0xffffu);
+                y[rr[r].qoff + 16 * m + (lane >> 2) + 8] = (uint16_t)(w >> 16);
             }
         }
     }
 }
 
 // This lane's partial O rows (unnormalised) into one partial slot.
-template <int D, bool KV8>
-__device__ __forceinline__ void dec_store_part(float *slot_rows,
-                                               const float (&o)[KV8 ? D / 16 : D / 8][4]) {
+template <int D, int DLAY>
+__device__ __forceinline__ void dec_store_part(float *slot_rows, const float (&o)[D / 16][4]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-        if constexpr (KV8) {
+        if constexpr (DLAY == DLAY_FP8) {
             float *po = slot_rows + (2 * (lane & 3) + r) * D + (D / 8) * (lane >> 2);
 #pragma unroll
             for (int i = 0; i < D / 32; ++i)
                 *reinterpret_cast<float4 *>(po + 4 * i) =
                     make_float4(o[2 * i][r], o[2 * i][r + 2], o[2 * i + 1][r], o[2 * i + 1][r + 2]);
         } else {
-            float *po = slot_rows + ((lane >> 2) + 8 * r) * D;
+            float *po = slot_rows + (2 * (lane & 3) + r) * D + (lane >> 2);
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n)
-                *reinterpret_cast<float2 *>(po + n * 8 + (lane & 3) * 2) =
-                    make_float2(o[n][2 * r], o[n][2 * r + 1]);
+            for (int m = 0; m < D / 16; ++m) {
+                po[16 * m] = o[m][r];
+                po[16 * m + 8] = o[m][r + 2];
+            }
         }
     }
 }
@@ -535,8 +485,9 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     constexpr int NW = L::NW;
     constexpr int DR = L::ROWS;                    // query rows per pair
     constexpr int NS = L::STAGES;
-    constexpr int NO = KV8 ? D / 16 : D / 8;       // O accumulator blocks
-    constexpr int QW = KV8 ? 2 : 4;                // Q fragment words per k-step
+    constexpr int DLAY = KV8 ? DLAY_FP8 : DLAY_16T;
+    constexpr int NO = D / 16;                     // O^T accumulator blocks
+    constexpr int QW = 2;                          // Q fragment words per k-step
     constexpr int KS = D / 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
@@ -701,7 +652,18 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             rows = cc.s.q_len * p.G;
             kv_hi = key_extent(p.causal, cc.s.q_len - 1, cc.s);
             const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
-            if constexpr (KV8) {
+            if constexpr (!KV8) {
+                // output rows 2c, 2c + 1; Q row lane / 4 is the B operand of
+                // S^T in the natural dim order
+                rr[0] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3), rows, kv_hi);
+                rr[1] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3) + 1, rows, kv_hi);
+                const DecRow rq = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2), rows, kv_hi);
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    qa[ks][0] = rq.valid ? q32[(rq.qoff >> 1) + 8 * ks + (lane & 3)] : 0u;
+                    qa[ks][1] = rq.valid ? q32[(rq.qoff >> 1) + 8 * ks + 4 + (lane & 3)] : 0u;
+                }
+            } else if constexpr (KV8) {
                 // output rows 2c, 2c + 1; Q row lane / 4 (the B operand of
                 // S^T), dims [c D/4, (c+1) D/4), four per k-step (the
                 // contraction order of dec_tile8)
@@ -750,17 +712,6 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                             qa[ks][i] = pack2<false>(__uint_as_float(qa[ks][i] << 16) * down,
                                                      __uint_as_float(qa[ks][i] & 0xffff0000u) * down);
                 }
-            } else {
-                rr[0] = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2), rows, kv_hi);
-                rr[1] = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2) + 8, rows, kv_hi);
-#pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int col = ks * 16 + (lane & 3) * 2;
-                    qa[ks][0] = rr[0].valid ? q32[(rr[0].qoff + col) >> 1] : 0u;
-                    qa[ks][1] = rr[1].valid ? q32[(rr[1].qoff + col) >> 1] : 0u;
-                    qa[ks][2] = rr[0].valid ? q32[(rr[0].qoff + col + 8) >> 1] : 0u;
-                    qa[ks][3] = rr[1].valid ? q32[(rr[1].qoff + col + 8) >> 1] : 0u;
-                }
             }
 #pragma unroll
             for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -792,7 +743,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                 __syncwarp();
             }
             if constexpr (KV8) dec_tile8<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc_pair);
-            else dec_tile<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc);
+            else dec_tile16t<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc);
             __syncwarp();
             if (next_issue < t_end) {   // refill the stage just used
                 issue(lc, npk, npv);
@@ -801,21 +752,14 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             }
             const bool pair_end = cc.tile + 1 == cc.nt;
             if (pair_end || t + 1 == t_end) {
-                // this range's share of the pair is done
-                // (the lanes sharing a row: lane % 4 for the 16-bit tile,
-                // lane / 4 for the fp8 one)
+                // this range's share of the pair is done (the lanes
+                // sharing a row differ in lane / 4)
                 if (SOFTMAX)
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        if constexpr (KV8) {
+                    for (int r = 0; r < 2; ++r)
 #pragma unroll
-                            for (int m = 4; m < 32; m <<= 1)
-                                l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], m);
-                        } else {
-                            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
-                            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
-                        }
-                    }
+                        for (int m = 4; m < 32; m <<= 1)
+                            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], m);
                 const int b = cc.b, g = cc.pib / cc.nrc, rc = cc.pib % cc.nrc;
                 const int ps = tpre[b] + cc.pib * cc.nt, pe = ps + cc.nt;
                 if (seg0 == ps && t + 1 == pe) {   // the whole pair: write Y
@@ -823,21 +767,16 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
                         f[r] = (SOFTMAX ? (l_r[r] > 0.f ? 1.f / l_r[r] : 0.f) : 1.f) * sv;
-                    dec_store_y<D, BF16, KV8>(p, rr, o, f);
+                    dec_store_y<D, BF16, DLAY>(p, rr, o, f);
                 } else {
                     // partial (O, m, l): slot 0 for the first pair of the
                     // range, slot 1 for the last
                     const size_t slot = (size_t)wg * 2 + (seg0 == t_begin ? 0 : 1);
-                    dec_store_part<D, KV8>(part + slot * DR * D, o);
+                    dec_store_part<D, DLAY>(part + slot * DR * D, o);
+                    if (lane < 4)
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        if constexpr (KV8) {
-                            if (lane < 4) pml[slot * DR + 2 * lane + r] = make_float2(m_r[r], l_r[r]);
-                        } else {
-                            const int row = (lane >> 2) + 8 * r;
-                            if ((lane & 3) == 0) pml[slot * DR + row] = make_float2(m_r[r], l_r[r]);
-                        }
-                    }
+                        for (int r = 0; r < 2; ++r)
+                            pml[slot * DR + 2 * lane + r] = make_float2(m_r[r], l_r[r]);
                     __threadfence();
                     __syncwarp();
                     const int w_lo = warp_of(ps), w_hi = warp_of(pe - 1);

@@ -12,18 +12,19 @@ namespace rga {
 constexpr int BM = 128;
 constexpr int BN = 128;
 
-// Decode geometry: 16 query rows per MMA row block, 32 keys per tile,
-// independent warps (4 per CTA for a 16-bit KV cache, 8 for an fp8 one,
-// whose tiles take half the bytes and more arithmetic per byte) with a
-// DEC_STAGES-deep TMA ring each; the key tiles of all work are split into
-// equal contiguous ranges, one per warp.
-constexpr int DEC_ROWS = 16;
-constexpr int DEC_ROWS_KV8 = 8;     // fp8 tiles: the 8 query rows are the MMA's N
+// Decode geometry: pairs of 8 query rows (the MMA's N of the transposed
+// products), 32 keys per tile, independent warps (6 per CTA with 2-stage
+// TMA rings for a 16-bit KV cache, 8 with 3-stage rings for an fp8 one,
+// whose tiles take half the bytes); the key tiles of all work are split
+// into equal contiguous ranges, one per warp.
+constexpr int DEC_MAX_ROWS = 16;    // decode shapes: at most 16 rows per (batch, KV head) on average
+constexpr int DEC_ROWS = 8;
+constexpr int DEC_ROWS_KV8 = 8;
 constexpr int DEC_KEYS = 32;
-constexpr int DEC_WARPS = 4;
+constexpr int DEC_WARPS = 6;
 constexpr int DEC_WARPS_KV8 = 8;
 constexpr int DEC_WARPS_MAX = 8;
-constexpr int DEC_STAGES = 3;
+constexpr int DEC_STAGES = 2;
 constexpr int DEC_STAGES_KV8 = 3;
 
 enum Mode { MODE_SOFTMAX = 0, MODE_NONE = 1, MODE_SOFTMAX_Q = 2, MODE_NONE_Q = 3 };
