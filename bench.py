@@ -53,7 +53,7 @@ def load_peaks():
 PROFILES = {   # headline kernel source and the ncu summary of it
     "prefill": ("ragged_gqa_attention_gb300/csrc/prefill.cuh",
                 "profiles/prefill_kernel_packed_ragged_prefill_gqa32x8_d128_bf16.md"),
-    "decode": ("ragged_gqa_attention_gb300/csrc/decode.cu",
+    "decode": ("ragged_gqa_attention_gb300/csrc/decode.cuh",
                "profiles/decode_kernel_decode_b64_gqa64x8_kv4096_d128_bf16.md"),
 }
 

@@ -1,4 +1,4 @@
-// decode.cu - split-KV attention for short query lengths (decode), the
+// decode.cuh - split-KV attention for short query lengths (decode), the
 // HBM-bound path of the AttentionPlugin ("TensorRT Plugins Guide":
 // vanilla decoding attention) with the TRT_Attention semantics of
 // "TensorRT Custom Operator Schemas".
@@ -27,6 +27,7 @@
 // is an f16 and a bf16 value), the K scale is folded into the softmax scale
 // and the V scale into the final 1/l.  An fp8 CTA runs 8 warps, since a
 // tile carries half the bytes and more arithmetic per byte.
+#pragma once
 #include <cuda.h>
 #include "device_common.cuh"
 #include "kernels.h"
@@ -93,12 +94,12 @@ __device__ __forceinline__ uint32_t swz(int row, int ch, int blk) {
 // g.  Paged cache: the tile lies in one page (page_size is a multiple of
 // DEC_KEYS); pk / pv are its K and V pages, looked up by the caller, and
 // the pools' tensor maps are [num_pages, Hkv, page_size, D].
-template <bool KV8>
+template <bool KV8, bool PAGED>
 __device__ __forceinline__ void dec_tma(const AttnParams &p, const TensorMaps &tm,
                                         const SeqInfo &s, int b, int g, int j0, uint8_t *dst,
                                         uint64_t *bar, int D, int pk, int pv) {
     int rk = j0, rv = j0, zk = b, zv = b;   // padded / paged coordinates (row, outer)
-    if (p.paged) {
+    if constexpr (PAGED) {
         rk = rv = j0 % p.page_size;
         zk = pk;
         zv = pv;
@@ -258,7 +259,7 @@ __device__ __forceinline__ void dec_tile8(const AttnParams &p, const DecRow (&rr
                                           const uint32_t (&qb)[D / 16][2], uint32_t kb,
                                           uint32_t vb, int j0, float (&o)[D / 16][4],
                                           float (&m_r)[2], float (&l_r)[2], float sc) {
-    constexpr int KS = D / 16, CH = D / 64, NO = D / 16, VW = D / 8;
+    constexpr int KS = D / 16, CH = D / 64, VW = D / 8;
     constexpr bool PV_BF16 = BF16 && !SOFTMAX;   // type of P and V in the P V product
     const int lane = threadIdx.x & 31, c = lane & 3, r = lane >> 2;
     float sacc[2][4];
@@ -478,7 +479,9 @@ __device__ __forceinline__ void dec_prefix(int *v, int n, int *scratch) {
     __syncthreads();
 }
 
-template <int D, bool BF16, bool SOFTMAX, bool KV8>
+// PAGED: K and V come from page pools (a compile-time choice, so that the
+// page lookups cost the linear-cache kernels nothing).
+template <int D, bool BF16, bool SOFTMAX, bool KV8, bool PAGED>
 __global__ void __launch_bounds__(DecLayout<D, KV8>::THREADS, 1)
 decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TensorMaps tm) {
     using L = DecLayout<D, KV8>;
@@ -535,7 +538,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     dec_prefix<L::THREADS>(tpre, p.B, scratch);
     dec_prefix<L::THREADS>(ppre, p.B, scratch);
     pdl_wait();   // the tickets have been cleared (and, paged, the pages checked)
-    if (p.paged) {
+    if constexpr (PAGED) {
         const volatile int *pf = reinterpret_cast<const volatile int *>(p.ws) + WS_PAGE_FLAGS;
         const int bad = (int)threadIdx.x < dec_prep_blocks(p) ? pf[threadIdx.x] : 0;
         if (__syncthreads_or(bad)) {
@@ -608,7 +611,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     // K and V pages of cursor c's tile (paged cache; lane 0 only)
     auto pages_of = [&](const DecCur &c, int &pk, int &pv) {
         pk = pv = 0;
-        if (p.paged && lane == 0) {
+        if (PAGED && lane == 0) {
             const int32_t *pt = p.page_table + (size_t)c.b * 2 * p.max_pages;
             const int pg = c.tile * DEC_KEYS / p.page_size;
             pk = __ldg(pt + pg);
@@ -618,7 +621,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
     auto issue = [&](const DecCur &c, int pk, int pv) {
         if (lane == 0) {
             fence_proxy_async_smem();   // the stage's previous tile was read by ldmatrix
-            dec_tma<KV8>(p, tm, c.s, c.b, c.pib / c.nrc, c.tile * DEC_KEYS,
+            dec_tma<KV8, PAGED>(p, tm, c.s, c.b, c.pib / c.nrc, c.tile * DEC_KEYS,
                     ring + (issued % NS) * L::STAGE, &wbar[issued % NS], D, pk, pv);
         }
         ++issued;
@@ -727,7 +730,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             ++consumed;
             // pages of the tile the refill below loads, read while this one computes
             int npk = 0, npv = 0;
-            if (next_issue < t_end) pages_of(lc, npk, npv);
+            if (PAGED && next_issue < t_end) pages_of(lc, npk, npv);
             const int j0 = cc.tile * DEC_KEYS;
             const uint32_t kb = ring_u32 + st * L::STAGE, vb = kb + L::TILE;
             const int rem = cc.s.kv_len - j0;
@@ -857,7 +860,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
 // outside the pools.  The decode kernel follows it as a programmatic
 // dependent and reads those words after griddepcontrol.wait, before
 // writing anything.
-__global__ void decode_prep_kernel(const __grid_constant__ AttnParams p, int n) {
+static __global__ void decode_prep_kernel(const __grid_constant__ AttnParams p, int n) {
     pdl_launch_dependents();
     int *tickets = reinterpret_cast<int *>(p.ws + dec_tickets_off(p));
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
@@ -880,12 +883,12 @@ __global__ void decode_prep_kernel(const __grid_constant__ AttnParams p, int n) 
     }
 }
 
-template <int D, bool BF16, bool SOFTMAX, bool KV8>
+template <int D, bool BF16, bool SOFTMAX, bool KV8, bool PAGED>
 static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStream_t s) {
     using L = DecLayout<D, KV8>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, SOFTMAX, KV8>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, SOFTMAX, KV8, PAGED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -894,25 +897,33 @@ static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStre
     decode_prep_kernel<<<dec_prep_blocks(p), 256, 0, s>>>(p, n);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_dependent(decode_kernel<D, BF16, SOFTMAX, KV8>, p.grid, L::THREADS, L::ALLOC, s,
-                            p, m);
+    return launch_dependent(decode_kernel<D, BF16, SOFTMAX, KV8, PAGED>, p.grid, L::THREADS,
+                            L::ALLOC, s, p, m);
 }
 
-template <bool KV8>
-static cudaError_t dec_launch_kv(const AttnParams &p, const TensorMaps &m, bool sm,
+template <bool KV8, bool PAGED>
+static cudaError_t dec_launch_kp(const AttnParams &p, const TensorMaps &m, bool sm,
                                  cudaStream_t s, int bf16) {
     if (p.D == 64) {
-        if (bf16) return sm ? dec_launch<64, true, true, KV8>(p, m, s) : dec_launch<64, true, false, KV8>(p, m, s);
-        return sm ? dec_launch<64, false, true, KV8>(p, m, s) : dec_launch<64, false, false, KV8>(p, m, s);
+        if (bf16) return sm ? dec_launch<64, true, true, KV8, PAGED>(p, m, s)
+                            : dec_launch<64, true, false, KV8, PAGED>(p, m, s);
+        return sm ? dec_launch<64, false, true, KV8, PAGED>(p, m, s)
+                  : dec_launch<64, false, false, KV8, PAGED>(p, m, s);
     }
-    if (bf16) return sm ? dec_launch<128, true, true, KV8>(p, m, s) : dec_launch<128, true, false, KV8>(p, m, s);
-    return sm ? dec_launch<128, false, true, KV8>(p, m, s) : dec_launch<128, false, false, KV8>(p, m, s);
+    if (bf16) return sm ? dec_launch<128, true, true, KV8, PAGED>(p, m, s)
+                        : dec_launch<128, true, false, KV8, PAGED>(p, m, s);
+    return sm ? dec_launch<128, false, true, KV8, PAGED>(p, m, s)
+              : dec_launch<128, false, false, KV8, PAGED>(p, m, s);
 }
 
-cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode, cudaStream_t s,
-                          int bf16, int kv8) {
+// The decode kernels of one KV element type (KV8: E4M3 codes), linear or
+// paged; each instantiates in its own translation unit.
+template <bool KV8>
+cudaError_t launch_decode_kv(const AttnParams &p, const TensorMaps &m, int mode,
+                             cudaStream_t s, int bf16) {
     const bool sm = (mode == MODE_SOFTMAX);
-    return kv8 ? dec_launch_kv<true>(p, m, sm, s, bf16) : dec_launch_kv<false>(p, m, sm, s, bf16);
+    return p.paged ? dec_launch_kp<KV8, true>(p, m, sm, s, bf16)
+                   : dec_launch_kp<KV8, false>(p, m, sm, s, bf16);
 }
 
 }  // namespace rga
