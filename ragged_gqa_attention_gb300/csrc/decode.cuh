@@ -886,16 +886,15 @@ static __global__ void decode_prep_kernel(const __grid_constant__ AttnParams p, 
 template <int D, bool BF16, bool SOFTMAX, bool KV8, bool PAGED>
 static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStream_t s) {
     using L = DecLayout<D, KV8>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, SOFTMAX, KV8, PAGED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = once_per_device(configured, [] {
+        return cudaFuncSetAttribute(decode_kernel<D, BF16, SOFTMAX, KV8, PAGED>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    });
+    if (e != cudaSuccess) return e;
     const int n = p.max_pairs + 1;
     decode_prep_kernel<<<dec_prep_blocks(p), 256, 0, s>>>(p, n);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_dependent(decode_kernel<D, BF16, SOFTMAX, KV8, PAGED>, p.grid, L::THREADS,
                             L::ALLOC, s, p, m);

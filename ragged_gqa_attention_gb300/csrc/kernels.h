@@ -1,6 +1,7 @@
 // kernels.h - internal launch parameters shared by the host dispatcher
 // (api.cu) and the device kernels.  Not part of the public ABI.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime_api.h>
@@ -133,6 +134,21 @@ inline cudaError_t launch_dependent(Kernel kernel, int grid, int block, int smem
 
 // SMs of the current device (0 when it cannot be read); api.cu.
 int sm_count();
+
+// Runs `set` (returning cudaError_t) once per device for the caller's flags
+// word: kernel attributes such as the dynamic shared memory limit are set
+// per device, so a process that drives several GPUs configures each of
+// them.  Idempotent, so two threads racing on the first call is harmless.
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<unsigned long long> &done, F set) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t e = set();
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_sched(const AttnParams &p, int decode, cudaStream_t s);

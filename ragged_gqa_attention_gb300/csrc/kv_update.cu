@@ -127,14 +127,13 @@ kv_update_kernel(const __grid_constant__ KvuParams p) {
 template <int V, typename I>
 static cudaError_t kvu_launch_i(const KvuParams &p, int grid, cudaStream_t s) {
     const size_t smem = (2 * (size_t)p.B + 1) * sizeof(int);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kv_update_kernel<V, I>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (2 * KVU_MAX_B + 1) * (int)sizeof(int));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = once_per_device(configured, [] {
+        return cudaFuncSetAttribute(kv_update_kernel<V, I>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (2 * KVU_MAX_B + 1) * (int)sizeof(int));
+    });
+    if (e != cudaSuccess) return e;
     kv_update_kernel<V, I><<<grid, KVU_THREADS, smem, s>>>(p);
     return cudaGetLastError();
 }

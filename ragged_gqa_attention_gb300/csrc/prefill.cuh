@@ -1228,18 +1228,17 @@ template <int D, int MODE, bool BF16>
 static cudaError_t launch_one(const AttnParams &p, const TensorMaps &m, int grid,
                               cudaStream_t s) {
     using L = PfLayout<D>;
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = once_per_device(configured, [] {
         // the register split needs exactly the launch allocation it was sized for
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MODE, BF16>);
-        if (e != cudaSuccess) return e;
+        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<D, MODE, BF16>);
+        if (r != cudaSuccess) return r;
         if (fa.numRegs != PF_LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(prefill_kernel<D, MODE, BF16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+        return cudaFuncSetAttribute(prefill_kernel<D, MODE, BF16>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    });
+    if (e != cudaSuccess) return e;
     return launch_dependent(prefill_kernel<D, MODE, BF16>, grid, PF_THREADS, L::ALLOC, s, p, m);
 }
 

@@ -195,14 +195,13 @@ static rga_status rope_launch(const RopeParams &p, bool bf16, long long units, c
     if (grid < 1) grid = 1;
     const size_t smem = FUSED ? (2 * (size_t)p.B + 1) * sizeof(int) : 0;
     if (FUSED) {
-        static bool attr_set[2] = {false, false};
-        if (!attr_set[bf16]) {
-            cudaError_t e = cudaFuncSetAttribute(
-                bf16 ? rope_kernel<true, true> : rope_kernel<false, true>,
-                cudaFuncAttributeMaxDynamicSharedMemorySize, (2 * ROPE_MAX_B + 1) * (int)sizeof(int));
-            if (e != cudaSuccess) return RGA_ERR_CUDA;
-            attr_set[bf16] = true;
-        }
+        static std::atomic<unsigned long long> configured[2] = {{0}, {0}};
+        const cudaError_t e = once_per_device(configured[bf16], [bf16] {
+            return cudaFuncSetAttribute(bf16 ? rope_kernel<true, true> : rope_kernel<false, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (2 * ROPE_MAX_B + 1) * (int)sizeof(int));
+        });
+        if (e != cudaSuccess) return RGA_ERR_CUDA;
     }
     if (bf16) rope_kernel<true, FUSED><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
     else rope_kernel<false, FUSED><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
