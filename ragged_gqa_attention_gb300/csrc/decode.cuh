@@ -262,6 +262,30 @@ __device__ __forceinline__ void dec_tile8(const AttnParams &p, const DecRow (&rr
     constexpr int KS = D / 16, CH = D / 64, VW = D / 8;
     constexpr bool PV_BF16 = BF16 && !SOFTMAX;   // type of P and V in the P V product
     const int lane = threadIdx.x & 31, c = lane & 3, r = lane >> 2;
+    // V codes of keys 0..15 (rows 2c, 2c+1, 2c+8, 2c+9), loaded before the
+    // S^T product so that their latency hides behind it
+    uint32_t pv0[VW / 4], pv1[VW / 4], pv8[VW / 4], pv9[VW / 4];
+    if constexpr (D == 128) {
+        uint32_t w[4];
+        lds128(vb + off8<D>(2 * c, r), w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pv0[i] = w[i];
+        lds128(vb + off8<D>(2 * c + 1, r), w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pv1[i] = w[i];
+        lds128(vb + off8<D>(2 * c + 8, r), w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pv8[i] = w[i];
+        lds128(vb + off8<D>(2 * c + 9, r), w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pv9[i] = w[i];
+    } else {
+        const int ch = r >> 1, half = (r & 1) * 8;
+        lds64(vb + off8<D>(2 * c, ch) + half, pv0[0], pv0[1]);
+        lds64(vb + off8<D>(2 * c + 1, ch) + half, pv1[0], pv1[1]);
+        lds64(vb + off8<D>(2 * c + 8, ch) + half, pv8[0], pv8[1]);
+        lds64(vb + off8<D>(2 * c + 9, ch) + half, pv9[0], pv9[1]);
+    }
     float sacc[2][4];
 #pragma unroll
     for (int mb = 0; mb < 2; ++mb) {
@@ -294,7 +318,12 @@ __device__ __forceinline__ void dec_tile8(const AttnParams &p, const DecRow (&rr
         // key rows k0, k0 + 1 (a0, a1) and k0 + 8, k0 + 9 (a2, a3); codes [VW r, VW r + VW)
         const int k0 = kk * 16 + 2 * c;
         uint32_t v0[VW / 4], v1[VW / 4], v8[VW / 4], v9[VW / 4];
-        if constexpr (D == 128) {
+        if (kk == 0) {
+#pragma unroll
+            for (int i = 0; i < VW / 4; ++i) {
+                v0[i] = pv0[i]; v1[i] = pv1[i]; v8[i] = pv8[i]; v9[i] = pv9[i];
+            }
+        } else if constexpr (D == 128) {
             uint32_t w[4];
             lds128(vb + off8<D>(k0, r), w);
 #pragma unroll
