@@ -241,3 +241,25 @@ def test_rope_validation_without_a_device(lib):
                  rope()) == 1                                                    # heads differ
     assert fused(kv, rope(dtype=0)) == 1                                         # dtypes differ
 
+
+
+def test_fp8_and_paged_report_a_small_workspace_before_any_device_work(lib):
+    # one token per sequence: a decode shape; the workspace is checked after
+    # the arguments and before anything is enqueued
+    a = _args(q_seq=1, kv_lengths=0x70000)
+    need = lib.rga_attention_workspace_size(ctypes.byref(a))
+    assert need >= 256 and need % 256 == 0
+    a.workspace, a.workspace_bytes = 0x100000, need - 256
+    assert lib.trt_attention_fp8_kv(ctypes.byref(a), 0x40000, 0x40010, None) == 6
+    pk = binding.PagedKv()
+    pk.k_pool = pk.v_pool = 0x50000
+    pk.kv_dtype = 1
+    pk.page_table = 0x60000
+    pk.num_pages, pk.page_size, pk.max_pages_per_seq = 16, 64, 4
+    a.kv_seq = 4 * 64
+    need = lib.rga_attention_workspace_size(ctypes.byref(a))
+    a.workspace_bytes = need - 256
+    assert lib.trt_attention_paged_kv(ctypes.byref(a), ctypes.byref(pk), None) == 6
+    a.workspace = 0x100010          # not 256-byte aligned
+    a.workspace_bytes = need
+    assert lib.trt_attention_paged_kv(ctypes.byref(a), ctypes.byref(pk), None) == 6
