@@ -110,7 +110,8 @@ static int64_t dec_max_pairs(int64_t B, int64_t Hkv, int64_t G, int64_t q_seq, b
 // Decode (split-KV) path: short query rows per (batch, KV head) -- one
 // token each in vanilla decoding, a few draft tokens in tree decoding (at
 // most 8 per sequence on average for packed Q; the decode kernel streams the
-// keys once per chunk of 16 query rows, 8 for an fp8 cache) -- no Q/DQ, and
+// keys once per chunk of 16 query rows, or of 8 for an fp8 cache and where a
+// KV head has at most 8) -- no Q/DQ, and
 // every key tile of the work countable in 32 bits.  (Tree decoding with 64
 // rows per (batch, KV head) measured slower on the prefill kernel: it has no
 // split over the keys, so the longest cache sets its time.)
@@ -205,7 +206,13 @@ AttnParams make_params(const rga_attention_args *a, bool quant, bool kv8 = false
         p.max_items = p.Hkv * ((p.q_seq + it - 1) / it + p.B);
     else
         p.max_items = p.Hkv * p.B * ((p.q_seq + it - 1) / it);
-    p.dec_rows = kv8 ? DEC_ROWS_KV8 : DEC_ROWS;
+    // rows per decode pair: 8 for the fp8 tile; the 16-bit tile takes 16 (two
+    // N-blocks sharing every K/V fragment) where a (batch, KV head) holds
+    // more than 8 query rows on average (q_seq is per batch for padded Q,
+    // the total for packed Q)
+    const int64_t qrows = (int64_t)p.q_seq * p.G;
+    const bool wide = p.q_packed ? qrows > 8LL * p.B : qrows > 8;
+    p.dec_rows = kv8 ? DEC_ROWS_KV8 : (wide ? DEC_ROWS_WIDE : DEC_ROWS);
     p.max_pairs = (int)dec_max_pairs(p.B, p.Hkv, p.G, p.q_seq, p.q_packed != 0, p.dec_rows);
     p.dec_slots = 2 * DEC_WARPS_MAX * (sm_count() > 0 ? sm_count() : 1);
     p.status = a->device_status;

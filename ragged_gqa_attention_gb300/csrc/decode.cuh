@@ -3,12 +3,15 @@
 // vanilla decoding attention) with the TRT_Attention semantics of
 // "TensorRT Custom Operator Schemas".
 //
-// Work: pairs (batch b, KV head g, chunk of 8 query rows), each with the
-// 32-key tiles of the batch's key extent.  The query rows of a pair are the
-// (token, head) pairs of the G heads of g, 8 at a time: the N = 8 of the
+// Work: pairs (batch b, KV head g, chunk of 8 or 16 query rows), each with
+// the 32-key tiles of the batch's key extent.  The query rows of a pair are
+// the (token, head) pairs of the G heads of g, 8 at a time: the N = 8 of the
 // m16n8k16 MMA in the transposed products S^T = K Q^T and O^T = V^T P^T
 // (keys, then head dims, on M), so no MMA row is wasted at G = 8 and K and
-// V are read once from HBM for all G query heads of the KV head.
+// V are read once from HBM for all G query heads of the KV head.  Where a
+// (batch, KV head) holds more than 8 rows (tree decoding, G = 16), the
+// 16-bit tile takes 16 rows per pair as two N-blocks that share every K and
+// V fragment, so the keys are streamed half as often.
 // All tiles of all pairs form one batch-major line that is cut into equal
 // contiguous ranges, one per warp of the persistent grid, so that every
 // warp streams the same number of tiles and none is left finishing a long
@@ -40,7 +43,6 @@ template <int D, bool KV8>
 struct DecLayout {
     static constexpr int NW = KV8 ? DEC_WARPS_KV8 : DEC_WARPS;   // warps per CTA
     static constexpr int THREADS = NW * 32;
-    static constexpr int ROWS = KV8 ? DEC_ROWS_KV8 : DEC_ROWS;     // query rows per pair
     static constexpr int STAGES = KV8 ? DEC_STAGES_KV8 : DEC_STAGES;
     static constexpr int BLK = DEC_KEYS * 128;          // 16-bit: 32 rows x 64 columns x 2 bytes
     static constexpr int TILE = KV8 ? DEC_KEYS * D : (D / 64) * BLK;   // one K or V tile
@@ -360,41 +362,53 @@ __device__ __forceinline__ void dec_tile8(const AttnParams &p, const DecRow (&rr
 }
 
 // The 16-bit tile with the transposed products of dec_tile8 (S^T = K Q^T,
-// O^T = V^T P^T; the pair's 8 query rows are the MMA's N): K blocks are the
-// A operand straight from ldmatrix, V^T blocks from ldmatrix.trans, P^T from
-// movmatrix; Q (qb) is the B operand in the natural dim order.  Accumulator
-// o[m][e] holds row 2c + e % 2, dim 16 m + lane/4 + 8 (e / 2).
-template <int D, bool BF16, bool SOFTMAX>
-__device__ __forceinline__ void dec_tile16t(const AttnParams &p, const DecRow (&rr)[2],
-                                            const uint32_t (&qb)[D / 16][2], uint32_t kb,
-                                            uint32_t vb, int j0, float (&o)[D / 16][4],
-                                            float (&m_r)[2], float (&l_r)[2], float sc) {
+// O^T = V^T P^T; each N-block of 8 query rows is the MMA's N): K blocks are
+// the A operand straight from ldmatrix, V^T blocks from ldmatrix.trans, P^T
+// from movmatrix; Q (qb[nb]) is the B operand in the natural dim order.
+// The NB N-blocks (8 NB rows of the pair) share every A fragment.
+// Accumulator o[nb][m][e] holds row 8 nb + 2c + e % 2, dim 16 m + lane/4 +
+// 8 (e / 2).
+template <int D, bool BF16, bool SOFTMAX, int NB>
+__device__ __forceinline__ void dec_tile16t(const AttnParams &p, const DecRow (&rr)[NB][2],
+                                            const uint32_t (&qb)[NB][D / 16][2], uint32_t kb,
+                                            uint32_t vb, int j0, float (&o)[NB][D / 16][4],
+                                            float (&m_r)[NB][2], float (&l_r)[NB][2], float sc) {
     using L = DecLayout<D, false>;
     constexpr int KS = D / 16, NO = D / 16;
     const int lane = threadIdx.x & 31;
-    float sacc[2][4];
+    float sacc[NB][2][4];
 #pragma unroll
     for (int mb = 0; mb < 2; ++mb) {
-        sacc[mb][0] = sacc[mb][1] = sacc[mb][2] = sacc[mb][3] = 0.f;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+            sacc[nb][mb][0] = sacc[nb][mb][1] = sacc[nb][mb][2] = sacc[nb][mb][3] = 0.f;
         const int key = 16 * mb + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             uint32_t a[4];
             ldsm_x4(kb + swz(key, ks * 2 + (lane >> 4), L::BLK), a[0], a[1], a[2], a[3]);
-            mma16816<BF16>(sacc[mb], a, qb[ks][0], qb[ks][1]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma16816<BF16>(sacc[nb][mb], a, qb[nb][ks][0], qb[nb][ks][1]);
         }
     }
-    dec_normalize_t<D, SOFTMAX>(p, rr, sacc, j0, o, m_r, l_r, sc);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+        dec_normalize_t<D, SOFTMAX>(p, rr[nb], sacc[nb], j0, o[nb], m_r[nb], l_r[nb], sc);
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
-        const uint32_t b0 = movmatrix_trans(pack2<BF16>(sacc[kk][0], sacc[kk][1]));
-        const uint32_t b1 = movmatrix_trans(pack2<BF16>(sacc[kk][2], sacc[kk][3]));
+        uint32_t b0[NB], b1[NB];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            b0[nb] = movmatrix_trans(pack2<BF16>(sacc[nb][kk][0], sacc[nb][kk][1]));
+            b1[nb] = movmatrix_trans(pack2<BF16>(sacc[nb][kk][2], sacc[nb][kk][3]));
+        }
         const int key = 16 * kk + (lane & 7) + ((lane >> 4) & 1) * 8;
 #pragma unroll
         for (int m = 0; m < NO; ++m) {
             uint32_t a[4];
             ldsm_x4_t(vb + swz(key, m * 2 + ((lane >> 3) & 1), L::BLK), a[0], a[1], a[2], a[3]);
-            mma16816<BF16>(o[m], a, b0, b1);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma16816<BF16>(o[nb][m], a, b0[nb], b1[nb]);
         }
     }
 }
@@ -509,13 +523,16 @@ __device__ __forceinline__ void dec_prefix(int *v, int n, int *scratch) {
 }
 
 // PAGED: K and V come from page pools (a compile-time choice, so that the
-// page lookups cost the linear-cache kernels nothing).
-template <int D, bool BF16, bool SOFTMAX, bool KV8, bool PAGED>
+// page lookups cost the linear-cache kernels nothing).  NB: N-blocks of 8
+// query rows per pair (16-bit cache: 1 or 2; fp8 cache: 1); the launcher
+// takes it from p.dec_rows, which also sized the partial slots.
+template <int D, bool BF16, bool SOFTMAX, bool KV8, bool PAGED, int NB>
 __global__ void __launch_bounds__(DecLayout<D, KV8>::THREADS, 1)
 decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TensorMaps tm) {
+    static_assert(NB == 1 || (NB == 2 && !KV8), "N-blocks per pair");
     using L = DecLayout<D, KV8>;
     constexpr int NW = L::NW;
-    constexpr int DR = L::ROWS;                    // query rows per pair
+    constexpr int DR = 8 * NB;                     // query rows per pair
     constexpr int NS = L::STAGES;
     constexpr int DLAY = KV8 ? DLAY_FP8 : DLAY_16T;
     constexpr int NO = D / 16;                     // O^T accumulator blocks
@@ -673,10 +690,10 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             issue(lc, pk, pv);
             advance(lc);
         }
-        DecRow rr[2];       // this lane's two output rows
-        uint32_t qa[KS][QW];
-        float o[NO][4];
-        float m_r[2], l_r[2];
+        DecRow rr[NB][2];   // this lane's two output rows of each N-block
+        uint32_t qa[NB][KS][QW];
+        float o[NB][NO][4];
+        float m_r[NB][2], l_r[NB][2];
         int seg0 = t_begin;    // first tile of the current pair in this range
         int kv_hi = 0, rows = 0;
         auto start_pair = [&]() {
@@ -685,22 +702,26 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
             kv_hi = key_extent(p.causal, cc.s.q_len - 1, cc.s);
             const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
             if constexpr (!KV8) {
-                // output rows 2c, 2c + 1; Q row lane / 4 is the B operand of
-                // S^T in the natural dim order
-                rr[0] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3), rows, kv_hi);
-                rr[1] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3) + 1, rows, kv_hi);
-                const DecRow rq = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2), rows, kv_hi);
+                // N-block nb: output rows 8 nb + 2c, 8 nb + 2c + 1; Q row
+                // 8 nb + lane / 4 is the B operand of S^T in the natural dim order
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    qa[ks][0] = rq.valid ? q32[(rq.qoff >> 1) + 8 * ks + (lane & 3)] : 0u;
-                    qa[ks][1] = rq.valid ? q32[(rq.qoff >> 1) + 8 * ks + 4 + (lane & 3)] : 0u;
+                for (int nb = 0; nb < NB; ++nb) {
+                    const int r0 = rc * DR + 8 * nb;
+                    rr[nb][0] = dec_row(p, cc.s, cc.b, g, r0 + 2 * (lane & 3), rows, kv_hi);
+                    rr[nb][1] = dec_row(p, cc.s, cc.b, g, r0 + 2 * (lane & 3) + 1, rows, kv_hi);
+                    const DecRow rq = dec_row(p, cc.s, cc.b, g, r0 + (lane >> 2), rows, kv_hi);
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        qa[nb][ks][0] = rq.valid ? q32[(rq.qoff >> 1) + 8 * ks + (lane & 3)] : 0u;
+                        qa[nb][ks][1] = rq.valid ? q32[(rq.qoff >> 1) + 8 * ks + 4 + (lane & 3)] : 0u;
+                    }
                 }
             } else if constexpr (KV8) {
                 // output rows 2c, 2c + 1; Q row lane / 4 (the B operand of
                 // S^T), dims [c D/4, (c+1) D/4), four per k-step (the
                 // contraction order of dec_tile8)
-                rr[0] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3), rows, kv_hi);
-                rr[1] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3) + 1, rows, kv_hi);
+                rr[0][0] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3), rows, kv_hi);
+                rr[0][1] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3) + 1, rows, kv_hi);
                 const DecRow rq = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2), rows, kv_hi);
                 uint32_t w[D / 8];
                 const uint4 *src = reinterpret_cast<const uint4 *>(
@@ -712,8 +733,8 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                 }
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    qa[ks][0] = w[2 * ks];
-                    qa[ks][1] = w[2 * ks + 1];
+                    qa[0][ks][0] = w[2 * ks];
+                    qa[0][ks][1] = w[2 * ks + 1];
                 }
                 if constexpr (BF16) {
                     // bf16 -> f16 for the f16 S product: scale the warp's
@@ -729,8 +750,8 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
                         for (int i = 0; i < QW; ++i)
-                            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(qa[ks][i] << 16)),
-                                                 fabsf(__uint_as_float(qa[ks][i] & 0xffff0000u))));
+                            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(qa[0][ks][i] << 16)),
+                                                 fabsf(__uint_as_float(qa[0][ks][i] & 0xffff0000u))));
 #pragma unroll
                     for (int m = 1; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
                     int e = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xff) - 127 - 14 : 0;
@@ -741,14 +762,17 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
                         for (int i = 0; i < QW; ++i)
-                            qa[ks][i] = pack2<false>(__uint_as_float(qa[ks][i] << 16) * down,
-                                                     __uint_as_float(qa[ks][i] & 0xffff0000u) * down);
+                            qa[0][ks][i] = pack2<false>(__uint_as_float(qa[0][ks][i] << 16) * down,
+                                                        __uint_as_float(qa[0][ks][i] & 0xffff0000u) * down);
                 }
             }
 #pragma unroll
-            for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-            m_r[0] = m_r[1] = -INFINITY;
-            l_r[0] = l_r[1] = 0.f;
+            for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+                for (int n = 0; n < NO; ++n) o[nb][n][0] = o[nb][n][1] = o[nb][n][2] = o[nb][n][3] = 0.f;
+                m_r[nb][0] = m_r[nb][1] = -INFINITY;
+                l_r[nb][0] = l_r[nb][1] = 0.f;
+            }
         };
         start_pair();
 
@@ -774,8 +798,9 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                 }
                 __syncwarp();
             }
-            if constexpr (KV8) dec_tile8<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc_pair);
-            else dec_tile16t<D, BF16, SOFTMAX>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc);
+            if constexpr (KV8)
+                dec_tile8<D, BF16, SOFTMAX>(p, rr[0], qa[0], kb, vb, j0, o[0], m_r[0], l_r[0], sc_pair);
+            else dec_tile16t<D, BF16, SOFTMAX, NB>(p, rr, qa, kb, vb, j0, o, m_r, l_r, sc);
             __syncwarp();
             if (next_issue < t_end) {   // refill the stage just used
                 issue(lc, npk, npv);
@@ -788,27 +813,35 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                 // sharing a row differ in lane / 4)
                 if (SOFTMAX)
 #pragma unroll
-                    for (int r = 0; r < 2; ++r)
+                    for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-                        for (int m = 4; m < 32; m <<= 1)
-                            l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], m);
+                        for (int r = 0; r < 2; ++r)
+#pragma unroll
+                            for (int m = 4; m < 32; m <<= 1)
+                                l_r[nb][r] += __shfl_xor_sync(0xffffffffu, l_r[nb][r], m);
                 const int b = cc.b, g = cc.pib / cc.nrc, rc = cc.pib % cc.nrc;
                 const int ps = tpre[b] + cc.pib * cc.nt, pe = ps + cc.nt;
                 if (seg0 == ps && t + 1 == pe) {   // the whole pair: write Y
-                    float f[2];
 #pragma unroll
-                    for (int r = 0; r < 2; ++r)
-                        f[r] = (SOFTMAX ? (l_r[r] > 0.f ? 1.f / l_r[r] : 0.f) : 1.f) * sv;
-                    dec_store_y<D, BF16, DLAY>(p, rr, o, f);
-                } else {
-                    // partial (O, m, l): slot 0 for the first pair of the
-                    // range, slot 1 for the last
-                    const size_t slot = (size_t)wg * 2 + (seg0 == t_begin ? 0 : 1);
-                    dec_store_part<D, DLAY>(part + slot * DR * D, o);
-                    if (lane < 4)
+                    for (int nb = 0; nb < NB; ++nb) {
+                        float f[2];
 #pragma unroll
                         for (int r = 0; r < 2; ++r)
-                            pml[slot * DR + 2 * lane + r] = make_float2(m_r[r], l_r[r]);
+                            f[r] = (SOFTMAX ? (l_r[nb][r] > 0.f ? 1.f / l_r[nb][r] : 0.f) : 1.f) * sv;
+                        dec_store_y<D, BF16, DLAY>(p, rr[nb], o[nb], f);
+                    }
+                } else {
+                    // partial (O, m, l): slot 0 for the first pair of the
+                    // range, slot 1 for the last; N-block nb holds rows 8 nb ..
+                    const size_t slot = (size_t)wg * 2 + (seg0 == t_begin ? 0 : 1);
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) {
+                        dec_store_part<D, DLAY>(part + (slot * DR + 8 * nb) * D, o[nb]);
+                        if (lane < 4)
+#pragma unroll
+                            for (int r = 0; r < 2; ++r)
+                                pml[slot * DR + 8 * nb + 2 * lane + r] = make_float2(m_r[nb][r], l_r[nb][r]);
+                    }
                     __threadfence();
                     __syncwarp();
                     const int w_lo = warp_of(ps), w_hi = warp_of(pe - 1);
@@ -818,8 +851,9 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                     tk = __shfl_sync(0xffffffffu, tk, 0);
                     if (tk == w_hi - w_lo) {   // the last of the pair's warps: merge
                         __threadfence();
-                        // LPR lanes per row, each with D / LPR dims
-                        constexpr int LPR = 32 / DR, DL = D / LPR;
+                        // LPR lanes per row, each with D / LPR dims, merged
+                        // MC dims at a time
+                        constexpr int LPR = 32 / DR, DL = D / LPR, MC = DL < 32 ? DL : 32;
                         const int row = lane / LPR, c0 = (lane % LPR) * DL;
                         // the first warp's share is its slot 1 unless the pair
                         // starts its range; every later warp's share is its slot 0
@@ -830,38 +864,43 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                         if (SOFTMAX)
                             for (int w = w_lo; w <= w_hi; ++w)
                                 M = fmaxf(M, __ldcg(&pml[slot_of(w) * DR + row].x));
-                        float acc[DL];
-#pragma unroll
-                        for (int k = 0; k < DL; ++k) acc[k] = 0.f;
-                        float Lsum = 0.f;
-                        for (int w = w_lo; w <= w_hi; ++w) {
-                            const size_t sl = slot_of(w);
-                            float wt = 1.f;
-                            if (SOFTMAX) {
-                                const float2 v = __ldcg(&pml[sl * DR + row]);
-                                wt = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
-                                Lsum += v.y * wt;
-                            }
-                            const float4 *src = reinterpret_cast<const float4 *>(part + (sl * DR + row) * D + c0);
-#pragma unroll
-                            for (int k = 0; k < DL / 4; ++k) {
-                                const float4 x4 = __ldcg(src + k);
-                                acc[4 * k] += x4.x * wt;
-                                acc[4 * k + 1] += x4.y * wt;
-                                acc[4 * k + 2] += x4.z * wt;
-                                acc[4 * k + 3] += x4.w * wt;
-                            }
-                        }
                         const DecRow R = dec_row(p, cc.s, b, g, rc * DR + row, rows, kv_hi);
-                        if (R.valid) {
-                            const float f = (SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f) * sv;
-                            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff + c0);
+#pragma unroll 1
+                        for (int h = 0; h < DL / MC; ++h) {
+                            float acc[MC];
 #pragma unroll
-                            for (int k = 0; k < DL / 8; ++k)
-                                dst[k] = make_uint4(pack2<BF16>(acc[8 * k] * f, acc[8 * k + 1] * f),
-                                                    pack2<BF16>(acc[8 * k + 2] * f, acc[8 * k + 3] * f),
-                                                    pack2<BF16>(acc[8 * k + 4] * f, acc[8 * k + 5] * f),
-                                                    pack2<BF16>(acc[8 * k + 6] * f, acc[8 * k + 7] * f));
+                            for (int k = 0; k < MC; ++k) acc[k] = 0.f;
+                            float Lsum = 0.f;
+                            for (int w = w_lo; w <= w_hi; ++w) {
+                                const size_t sl = slot_of(w);
+                                float wt = 1.f;
+                                if (SOFTMAX) {
+                                    const float2 v = __ldcg(&pml[sl * DR + row]);
+                                    wt = (v.x == -INFINITY) ? 0.f : ex2(v.x - M);
+                                    Lsum += v.y * wt;
+                                }
+                                const float4 *src = reinterpret_cast<const float4 *>(
+                                    part + (sl * DR + row) * D + c0 + h * MC);
+#pragma unroll
+                                for (int k = 0; k < MC / 4; ++k) {
+                                    const float4 x4 = __ldcg(src + k);
+                                    acc[4 * k] += x4.x * wt;
+                                    acc[4 * k + 1] += x4.y * wt;
+                                    acc[4 * k + 2] += x4.z * wt;
+                                    acc[4 * k + 3] += x4.w * wt;
+                                }
+                            }
+                            if (R.valid) {
+                                const float f = (SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f) * sv;
+                                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) +
+                                                                       R.qoff + c0 + h * MC);
+#pragma unroll
+                                for (int k = 0; k < MC / 8; ++k)
+                                    dst[k] = make_uint4(pack2<BF16>(acc[8 * k] * f, acc[8 * k + 1] * f),
+                                                        pack2<BF16>(acc[8 * k + 2] * f, acc[8 * k + 3] * f),
+                                                        pack2<BF16>(acc[8 * k + 4] * f, acc[8 * k + 5] * f),
+                                                        pack2<BF16>(acc[8 * k + 6] * f, acc[8 * k + 7] * f));
+                            }
                         }
                         if (lane == 0) tickets[pidx] = 0;   // ready for the next call
                     }
@@ -912,12 +951,12 @@ static __global__ void decode_prep_kernel(const __grid_constant__ AttnParams p, 
     }
 }
 
-template <int D, bool BF16, bool SOFTMAX, bool KV8, bool PAGED>
+template <int D, bool BF16, bool SOFTMAX, bool KV8, bool PAGED, int NB>
 static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStream_t s) {
     using L = DecLayout<D, KV8>;
     static std::atomic<unsigned long long> configured{0};
     cudaError_t e = once_per_device(configured, [] {
-        return cudaFuncSetAttribute(decode_kernel<D, BF16, SOFTMAX, KV8, PAGED>,
+        return cudaFuncSetAttribute(decode_kernel<D, BF16, SOFTMAX, KV8, PAGED, NB>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     });
     if (e != cudaSuccess) return e;
@@ -925,33 +964,35 @@ static cudaError_t dec_launch(const AttnParams &p, const TensorMaps &m, cudaStre
     decode_prep_kernel<<<dec_prep_blocks(p), 256, 0, s>>>(p, n);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_dependent(decode_kernel<D, BF16, SOFTMAX, KV8, PAGED>, p.grid, L::THREADS,
+    return launch_dependent(decode_kernel<D, BF16, SOFTMAX, KV8, PAGED, NB>, p.grid, L::THREADS,
                             L::ALLOC, s, p, m);
 }
 
-template <bool KV8, bool PAGED>
+template <bool KV8, bool PAGED, int NB>
 static cudaError_t dec_launch_kp(const AttnParams &p, const TensorMaps &m, bool sm,
                                  cudaStream_t s, int bf16) {
     if (p.D == 64) {
-        if (bf16) return sm ? dec_launch<64, true, true, KV8, PAGED>(p, m, s)
-                            : dec_launch<64, true, false, KV8, PAGED>(p, m, s);
-        return sm ? dec_launch<64, false, true, KV8, PAGED>(p, m, s)
-                  : dec_launch<64, false, false, KV8, PAGED>(p, m, s);
+        if (bf16) return sm ? dec_launch<64, true, true, KV8, PAGED, NB>(p, m, s)
+                            : dec_launch<64, true, false, KV8, PAGED, NB>(p, m, s);
+        return sm ? dec_launch<64, false, true, KV8, PAGED, NB>(p, m, s)
+                  : dec_launch<64, false, false, KV8, PAGED, NB>(p, m, s);
     }
-    if (bf16) return sm ? dec_launch<128, true, true, KV8, PAGED>(p, m, s)
-                        : dec_launch<128, true, false, KV8, PAGED>(p, m, s);
-    return sm ? dec_launch<128, false, true, KV8, PAGED>(p, m, s)
-              : dec_launch<128, false, false, KV8, PAGED>(p, m, s);
+    if (bf16) return sm ? dec_launch<128, true, true, KV8, PAGED, NB>(p, m, s)
+                        : dec_launch<128, true, false, KV8, PAGED, NB>(p, m, s);
+    return sm ? dec_launch<128, false, true, KV8, PAGED, NB>(p, m, s)
+              : dec_launch<128, false, false, KV8, PAGED, NB>(p, m, s);
 }
 
-// The decode kernels of one KV element type (KV8: E4M3 codes), linear or
-// paged; each instantiates in its own translation unit.
-template <bool KV8>
+// The decode kernels of one KV element type (KV8: E4M3 codes) and one
+// number of N-blocks per pair, linear or paged; each instantiates in its own
+// translation unit.  p.dec_rows (which sized the partial slots) must be 8 NB.
+template <bool KV8, int NB>
 cudaError_t launch_decode_kv(const AttnParams &p, const TensorMaps &m, int mode,
                              cudaStream_t s, int bf16) {
+    if (p.dec_rows != 8 * NB) return cudaErrorInvalidValue;
     const bool sm = (mode == MODE_SOFTMAX);
-    return p.paged ? dec_launch_kp<KV8, true>(p, m, sm, s, bf16)
-                   : dec_launch_kp<KV8, false>(p, m, sm, s, bf16);
+    return p.paged ? dec_launch_kp<KV8, true, NB>(p, m, sm, s, bf16)
+                   : dec_launch_kp<KV8, false, NB>(p, m, sm, s, bf16);
 }
 
 }  // namespace rga

@@ -1,19 +1,23 @@
-// decode_kv16.cu - the decode kernels over a 16-bit (f16 / bf16) KV cache,
-// linear or paged (decode.cuh), and the decode entry of the launchers.
+// decode_kv16.cu - the decode kernels over a 16-bit (f16 / bf16) KV cache
+// with one N-block of 8 query rows per pair, linear or paged (decode.cuh),
+// and the decode entry of the launchers.
 #include "decode.cuh"
 
 namespace rga {
 
-// the fp8 kernels are instantiated in decode_kv8.cu
-extern template cudaError_t launch_decode_kv<true>(const AttnParams &, const TensorMaps &, int,
-                                                   cudaStream_t, int);
-template cudaError_t launch_decode_kv<false>(const AttnParams &, const TensorMaps &, int,
-                                            cudaStream_t, int);
+// instantiated in decode_kv16w.cu (two N-blocks) and decode_kv8.cu (fp8)
+extern template cudaError_t launch_decode_kv<false, 2>(const AttnParams &, const TensorMaps &,
+                                                       int, cudaStream_t, int);
+extern template cudaError_t launch_decode_kv<true, 1>(const AttnParams &, const TensorMaps &,
+                                                      int, cudaStream_t, int);
+template cudaError_t launch_decode_kv<false, 1>(const AttnParams &, const TensorMaps &, int,
+                                                cudaStream_t, int);
 
 cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode, cudaStream_t s,
                           int bf16, int kv8) {
-    return kv8 ? launch_decode_kv<true>(p, m, mode, s, bf16)
-               : launch_decode_kv<false>(p, m, mode, s, bf16);
+    if (kv8) return launch_decode_kv<true, 1>(p, m, mode, s, bf16);
+    return p.dec_rows == DEC_ROWS_WIDE ? launch_decode_kv<false, 2>(p, m, mode, s, bf16)
+                                       : launch_decode_kv<false, 1>(p, m, mode, s, bf16);
 }
 
 }  // namespace rga

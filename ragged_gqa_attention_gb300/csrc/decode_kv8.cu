@@ -4,7 +4,7 @@
 
 namespace rga {
 
-template cudaError_t launch_decode_kv<true>(const AttnParams &, const TensorMaps &, int,
-                                           cudaStream_t, int);
+template cudaError_t launch_decode_kv<true, 1>(const AttnParams &, const TensorMaps &, int,
+                                               cudaStream_t, int);
 
 }  // namespace rga

@@ -14,12 +14,14 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 
 // Decode geometry: pairs of 8 query rows (the MMA's N of the transposed
-// products), 32 keys per tile, independent warps (6 per CTA with 2-stage
-// TMA rings for a 16-bit KV cache, 8 with 3-stage rings for an fp8 one,
-// whose tiles take half the bytes); the key tiles of all work are split
-// into equal contiguous ranges, one per warp.
+// products), or 16 as two N-blocks where a (batch, KV head) holds more than
+// 8 rows on average (16-bit cache only), 32 keys per tile, independent
+// warps (6 per CTA with 2-stage TMA rings for a 16-bit KV cache, 8 with
+// 3-stage rings for an fp8 one, whose tiles take half the bytes); the key
+// tiles of all work are split into equal contiguous ranges, one per warp.
 constexpr int DEC_MAX_ROWS = 16;    // decode shapes: at most 16 rows per (batch, KV head) on average
 constexpr int DEC_ROWS = 8;
+constexpr int DEC_ROWS_WIDE = 16;
 constexpr int DEC_ROWS_KV8 = 8;
 constexpr int DEC_KEYS = 32;
 constexpr int DEC_WARPS = 6;
@@ -52,7 +54,7 @@ struct AttnParams {
     int max_items;                  // capacity of the work list
     int max_pairs;                  // decode: bound on (batch, KV head, row chunk) pairs
     int dec_slots;                  // decode: partial slots (2 per warp of the grid)
-    int dec_rows;                   // decode: query rows per pair (DEC_ROWS or DEC_ROWS_KV8)
+    int dec_rows;                   // decode: query rows per pair (DEC_ROWS, DEC_ROWS_WIDE or DEC_ROWS_KV8)
     int kv8;                        // K, V hold E4M3 codes (fp8 KV cache)
     const float *k_scale, *v_scale; // fp8 KV cache: dequantisation scales (device scalars)
     int paged;                      // K, V come from page pools (decode only)

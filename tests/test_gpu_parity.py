@@ -215,6 +215,26 @@ def test_decode_masks_and_none():
     _parity(c)
 
 
+@pytest.mark.parametrize("D,dtype", [(64, torch.float16), (128, torch.bfloat16)])
+@pytest.mark.parametrize("norm", ["softmax", "none"])
+@pytest.mark.parametrize("q_form", ["packed", "padded"])
+def test_decode_sixteen_row_pairs(D, dtype, norm, q_form):
+    # more than 8 query rows per (batch, KV head) on average: the 16-bit
+    # decode tile takes 16 rows per pair as two N-blocks.  G = 4 with 3, 1,
+    # 2 and 3 tokens gives 12, 4, 8 and 12 rows: second N-blocks that are
+    # half full or empty, a first row that sees no key (2 keys for 3 tokens,
+    # lower right) and pairs that the stream-K ranges cut.  'none' sums up to
+    # 2049 unnormalised terms: scale 0.001 keeps |y| below 2, where bf16
+    # output rounding stays inside the tolerance
+    kw = dict(q_seq=3, pass_query_lengths=True) if q_form == "padded" else dict(tail=3)
+    c = W.make_case("dec16", 30 + D + (norm == "none") + 2 * (q_form == "padded"), batch=4,
+                    q_heads=8, kv_heads=2, head_dim=D, q_lens=[3, 1, 2, 3],
+                    kv_lens=[2, 33, 700, 2049], q_form=q_form, kv_form="padded", kv_seq=2100,
+                    dtype=dtype, causal="lower_right", norm=norm,
+                    scale=0.001 if norm == "none" else None, **kw)
+    _parity(c)
+
+
 @pytest.mark.parametrize("G", [2, 8])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 def test_tree_decoding(G, dtype):
