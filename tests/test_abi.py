@@ -263,3 +263,18 @@ def test_fp8_and_paged_report_a_small_workspace_before_any_device_work(lib):
     a.workspace = 0x100010          # not 256-byte aligned
     a.workspace_bytes = need
     assert lib.trt_attention_paged_kv(ctypes.byref(a), ctypes.byref(pk), None) == 6
+
+
+def test_decode_pairs_take_sixteen_rows_past_eight_rows_per_kv_head(lib):
+    # a (batch, KV head) with more than 8 query rows takes pairs of 16 rows
+    # (two N-blocks) on a 16-bit cache: the partial slots of the workspace
+    # double.  Padded Q, 2 KV heads: 16 query heads (G = 8) with 1 token and
+    # 8 (G = 4) with 2 tokens are 8 rows; 16 heads with 2 tokens and 8 with 3
+    # are 16 and 12 rows.  (The fp8 layout, also sized by the query, keeps 8.)
+    def need(q_seq, q_heads):
+        return lib.rga_attention_workspace_size(ctypes.byref(_args(q_seq=q_seq, q_heads=q_heads)))
+    eight = need(1, 16)
+    assert eight == need(2, 8)
+    slot_rows = 16 * 8 * 128 * 4   # at least 16 slots of 8 more rows of 128 fp32 dims
+    assert need(2, 16) - eight >= slot_rows
+    assert need(3, 8) - eight >= slot_rows
