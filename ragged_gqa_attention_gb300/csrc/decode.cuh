@@ -9,10 +9,9 @@
 // m16n8k16 MMA in the transposed products S^T = K Q^T and O^T = V^T P^T
 // (keys, then head dims, on M), so no MMA row is wasted at G = 8 and K and
 // V are read once from HBM for all G query heads of the KV head.  Where a
-// (batch, KV head) holds more than 8 rows on average (tree decoding, G =
-// 16), the 16-bit tile takes 16 rows per pair as two N-blocks that share
-// every K and V fragment, so the keys are streamed half as often (the fp8
-// tile, at 246 registers, keeps one N-block).
+// (batch, KV head) holds more than 8 rows (tree decoding, G = 16), the
+// 16-bit tile takes 16 rows per pair as two N-blocks that share every K and
+// V fragment, so the keys are streamed half as often.
 // All tiles of all pairs form one batch-major line that is cut into equal
 // contiguous ranges, one per warp of the persistent grid, so that every
 // warp streams the same number of tiles and none is left finishing a long
