@@ -143,11 +143,16 @@ static double qdq(double p, int quant, double s)
     return rga_oracle_int8_round(x) * s;
 }
 
-/* Where floating point decides a quantised code, a value within a relative
- * distance eps of a rounding midpoint may round either way in any other
- * correct evaluation order.  Returns the change of the dequantised value
- * if such a code flipped (one quantisation step times s), or 0 when the
- * decision is clear. */
+/* Where floating point decides a quantised code, a value x = |p / s| within
+ * eps * x of a rounding midpoint may round either way in another correct
+ * evaluation (another precision or order).  The window is relative to x:
+ * after softmax, x is an exponential of the scores, so an error in the
+ * scores moves it by a relative amount.  (Under 'none', x is the score
+ * itself, and near a cancellation in the dot product the error of another
+ * evaluation is larger than eps * x; such codes sit next to zero, where the
+ * first midpoint lies far away.)  Returns the change of the dequantised
+ * value if such a code flipped (one quantisation step times s), or 0 when
+ * the decision is clear. */
 static double qdq_ambiguity(double p, int quant, double s, double eps)
 {
     double x = fabs(p / s), step, t;
@@ -169,7 +174,7 @@ static double qdq_ambiguity(double p, int quant, double s, double eps)
         step = 1.0;
     }
     t = x / step - floor(x / step);      /* position inside the step */
-    if (fabs(t - 0.5) * step <= eps * (x > 1.0 ? x : 1.0))
+    if (fabs(t - 0.5) * step <= eps * x)
         return step * s;
     return 0.0;
 }

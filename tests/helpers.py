@@ -17,14 +17,21 @@ SENTINEL = 0x7FDA                # a NaN bit pattern in both fp16 and bf16
 
 TOL = {None: (1e-2, 1e-3), "fp8": (3e-2, 3e-3), "int8": (3e-2, 3e-3)}
 
-# A quantised code is decided from fp32 scores on the GPU and fp64 scores in
-# the oracle; a code whose pre-quantisation value lies within
-# AMBIGUITY_EPS * max(|x|, 1) of a rounding midpoint may round either way.
-# fp32 accumulation of 128 products and exp2 put the GPU's x within a few
-# 1e-6 relative (and ~1e-4 absolute near 0) of the exact value; 2^-13 covers
-# that with margin.  Such flips are allowed on top of the tolerance, by the
-# bound the oracle computes for them.
-AMBIGUITY_EPS = 2.0 ** -13
+# Allowance for quantised codes that may legitimately round either way.  The
+# kernel decides each code from x = 2^(S*c - lam) in fp32: S is the tensor
+# core's fp32 dot product of 16-bit values, c = scale*log2(e), lam = m +
+# log2(l) + log2(s_q) with l an fp32 sum of exponentials.  Its relative error
+# is ln2 * |error of S*c - lam| plus the error of the hardware exp2 (about
+# 2^-22).  Emulating that arithmetic on the CPU (fp32 dot products, fp32 sums
+# in the kernel's order) over 1.1 M codes of the 4 x 16 x 4096 quantized
+# workload gave at most 2.7e-6 (2^-18.5).  AMBIGUITY_EPS = 2^-16 is about six
+# times that, for the tensor core's own accumulation order and the exp2.  It
+# is relative, with no absolute floor: the oracle marks a code only when x
+# lies within AMBIGUITY_EPS * x of a rounding midpoint.  test_gpu_code_flips
+# reads the kernel's codes directly and checks that every code that differs
+# from the oracle's is one of those.  Tests assert the raw error (no
+# allowance) against the tolerance too.
+AMBIGUITY_EPS = 2.0 ** -16
 
 
 def guarded_output(q):
@@ -91,7 +98,11 @@ def valid_row_mask(case: W.Case):
 
 
 def check(case: W.Case, y_gpu, raw, y_ref, tol=None):
-    """Element-wise parity on valid rows; bit-exact sentinel elsewhere."""
+    """Element-wise parity on valid rows; bit-exact sentinel elsewhere.
+
+    For the quantized op the raw error (no allowance) must meet the
+    tolerance, and so must the error less the oracle's ambiguity bound.
+    Returns the raw max-abs error."""
     atol_max, atol_mean = tol or TOL[case.quant]
     amb = None
     if isinstance(y_ref, tuple):
@@ -100,10 +111,14 @@ def check(case: W.Case, y_gpu, raw, y_ref, tol=None):
     g, r = y_gpu[rows], y_ref[rows]
     assert np.isfinite(g).all(), "non-finite output in a valid row"
     err = np.abs(g - r)
-    if amb is not None:   # allowed rounding flips of ambiguous codes
-        err = np.maximum(err - amb[rows], 0.0)
     if err.size:
-        assert err.max() <= atol_max, f"max abs err {err.max():.3e} > {atol_max}"
+        note = ""
+        if amb is not None:   # allowed rounding flips of ambiguous codes
+            a = amb[rows]
+            adj = np.maximum(err - a, 0.0)
+            note = f" (allowance max {a.max():.3e}, error less allowance {adj.max():.3e})"
+            assert adj.max() <= atol_max, f"max abs err less allowance {adj.max():.3e}{note}"
+        assert err.max() <= atol_max, f"raw max abs err {err.max():.3e} > {atol_max}{note}"
         assert err.mean() <= atol_mean, f"mean abs err {err.mean():.3e} > {atol_mean}"
     # untouched: invalid rows and the guard bands keep the sentinel bits
     body = raw[GUARD:GUARD + case.q.numel()].reshape(case.q.shape)

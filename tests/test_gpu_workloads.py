@@ -94,9 +94,16 @@ def test_workload_full_size_sampled(index, quant):
             yref, amb = yref
         got = gpu_rows(c, y, b, g)
         err = np.abs(got - ref_rows(c, yref, b))
+        note = ""
         if amb is not None:
-            err = np.maximum(err - ref_rows(c, amb, b), 0.0)
+            # quantized P: the error less the allowance for codes within
+            # AMBIGUITY_EPS of a rounding midpoint meets the bar, and so does
+            # the raw error with no allowance
+            a = ref_rows(c, amb, b)
+            adj = np.maximum(err - a, 0.0)
+            note = f"allowance max {a.max():.3e}, error less allowance {adj.max():.3e}"
+            assert adj.max() <= amax, (b, g, note)
         errs.append(err)
-        assert err.max() <= amax, (b, g, err.max())
+        assert err.max() <= amax, (b, g, f"raw max abs err {err.max():.3e}", note)
     allerr = np.concatenate([e.ravel() for e in errs])
     assert allerr.mean() <= amean
