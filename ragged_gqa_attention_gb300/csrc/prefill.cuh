@@ -468,11 +468,17 @@ __device__ __forceinline__ float ld_as_float(const void *base, long long e) {
     else return __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[e]);
 }
 
+// Marker of an excluded pair in 'none' scores: a NaN whose bits no
+// arithmetic produces (the GPU's arithmetic NaN is 0x7fffffff), so that an
+// allowed pair whose additive mask value is -inf keeps its -inf score, as
+// the plain formula does, while excluded pairs contribute 0.
+constexpr uint32_t NONE_EXCLUDED = 0xffc0dead;
+
 // Chunk c (keys j0 + 32c .. j0 + 32c + 31) of a partial tile, scaled and
 // masked in place.  Key kk = 32c + k is allowed when kk <= rem (causal and
 // length limits) and its bit is set: bit (kk >> 2) of word (kk & 3).
-// Writes log2-domain scores (softmax) or natural-unit scores ('none'), and
-// -inf where the pair is excluded.
+// Writes log2-domain scores (softmax), where an excluded pair is -inf, or
+// natural-unit scores ('none'), where it is NONE_EXCLUDED.
 template <bool LOG2, int MK>
 __device__ __forceinline__ void mask_chunk(const AttnParams &p, float (&v)[32], int c, int rem,
                                            const uint32_t (&bits)[4], long long mrow, int j0) {
@@ -495,7 +501,7 @@ __device__ __forceinline__ void mask_chunk(const AttnParams &p, float (&v)[32], 
                 val += LOG2 ? add * LOG2E : add;
             }
         }
-        v[k] = ok ? val : -INFINITY;
+        v[k] = ok ? val : (LOG2 ? -INFINITY : __uint_as_float(NONE_EXCLUDED));
     }
 }
 
@@ -1077,8 +1083,8 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                             else acc0 = fadd2(acc0, f2_pack(pa, pb));
                         }
                     } else {
-                        pa = (pa == -INFINITY) ? 0.f : pa * mul;
-                        pb = (pb == -INFINITY) ? 0.f : pb * mul;
+                        pa = (__float_as_uint(pa) == NONE_EXCLUDED) ? 0.f : pa * mul;
+                        pb = (__float_as_uint(pb) == NONE_EXCLUDED) ? 0.f : pb * mul;
                         if (MODE == MODE_NONE_Q) {
                             pa *= inv_qs;
                             pb *= inv_qs;

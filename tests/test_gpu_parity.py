@@ -15,7 +15,7 @@ import torch
 from ragged_gqa_attention_gb300 import binding
 from ragged_gqa_attention_gb300 import workloads as W
 
-from helpers import check, run_gpu, run_oracle
+from helpers import check, run_gpu, run_oracle, valid_row_mask
 
 pytestmark = pytest.mark.gpu
 
@@ -120,6 +120,59 @@ def test_prefill_norm_none(causal):
                     q_lens=[130, 64], kv_lens=[130, 250], dtype=torch.float16,
                     causal=causal, norm="none", scale=0.01, pass_query_lengths=True)
     _parity(c)
+
+
+def _minus_inf_mask(B, H, Nq, Nkv, q_lens, kv_lens, seed):
+    """Additive fp32 mask [B, H, Nq, Nkv]: zeros, with -inf at a few allowed
+    pairs (inside both lengths) and +inf at one."""
+    rng = np.random.default_rng(seed)
+    m = torch.zeros(B, H, Nq, Nkv, dtype=torch.float32)
+    for b in range(B):
+        for _ in range(3):
+            m[b, int(rng.integers(H)), int(rng.integers(q_lens[b])),
+              int(rng.integers(kv_lens[b]))] = -math.inf
+    m[0, 0, int(rng.integers(q_lens[0])), int(rng.integers(kv_lens[0]))] = math.inf
+    return m
+
+
+@pytest.mark.parametrize("path", ["prefill", "decode", "quantized"])
+def test_none_with_infinite_mask_values_follows_the_formula(path):
+    """Under 'none' the additive mask value is added to the scaled score and
+    the sum multiplies V with no normalisation ("TensorRT Custom Operator
+    Schemas", TRT_Attention: attn_mask, TRT_normalization_op).  An allowed
+    pair whose value is -inf (or +inf) therefore gives a non-finite output
+    row, as in the oracle; under the quantized op the infinite score
+    saturates to the largest code and the row stays finite.  Excluded pairs
+    (past the lengths) still contribute 0."""
+    if path == "decode":
+        B, H, N = 3, 8, 300
+        q_lens, kv_lens = [1] * B, [300, 120, 299]
+        mask = _minus_inf_mask(B, H, 1, N, q_lens, kv_lens, 31)
+        c = W.make_case("none_inf_dec", 31, batch=B, q_heads=H, kv_heads=2, head_dim=128,
+                        q_lens=q_lens, kv_lens=kv_lens, q_form="packed", kv_form="padded",
+                        kv_seq=N, dtype=torch.float16, norm="none", scale=0.01, mask=mask)
+    else:
+        B, H = 2, 4
+        q_lens, kv_lens = [130, 70], [200, 90]
+        mask = _minus_inf_mask(B, H, 130, 200, q_lens, kv_lens, 32)
+        c = W.make_case("none_inf", 32, batch=B, q_heads=H, kv_heads=H, head_dim=64,
+                        q_lens=q_lens, kv_lens=kv_lens, dtype=torch.float16, norm="none",
+                        scale=0.01, mask=mask, pass_query_lengths=True,
+                        quant="int8" if path == "quantized" else None,
+                        quant_scale=torch.tensor(1 / 127) if path == "quantized" else None)
+    y, raw, st = run_gpu(c)
+    assert binding.device_status(st) == 0
+    ref = run_oracle(c)
+    if path == "quantized":
+        check(c, y, raw, ref)
+        return
+    rows = valid_row_mask(c)
+    g, r = y[rows], ref[rows]
+    bad = ~np.isfinite(r)
+    assert bad.any(), "the case must produce non-finite oracle rows"
+    np.testing.assert_array_equal(~np.isfinite(g), bad)
+    err = np.abs(g[~bad] - r[~bad])
+    assert err.max() <= 1e-2 and err.mean() <= 1e-3, err.max()
 
 
 # --------------------------------------------------------------------------
