@@ -230,14 +230,16 @@ rga_status trt_attention_paged_kv(const rga_attention_args *args, const rga_page
  *
  * Same arguments and results as trt_attention, except that args->workspace
  * and args->workspace_bytes are ignored: the scratch is a 40 MiB device
- * array inside the library, held on every GPU that loads the library until
- * the process exits.  Inputs, Y and device_status are still the caller's.
- * Allocates nothing (no cudaMalloc, no allocating library routine).
+ * array inside the library, held on a GPU from the first call made on it
+ * (from context creation when CUDA loads modules eagerly) until the process
+ * exits.  Inputs, Y and device_status are still the caller's.  Allocates
+ * nothing (no cudaMalloc, no allocating library routine).
  *
  * Returns RGA_ERR_WORKSPACE when rga_attention_workspace_size(args) exceeds
- * RGA_STATIC_SCRATCH_BYTES.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every call shares the
+ * RGA_STATIC_SCRATCH_BYTES.  Every call looks up the array's device address
+ * in the current context (cudaGetSymbolAddress, with the caller's device
+ * current); the first call on a device also loads the array there, so make
+ * that first call before any stream capture.  Every call shares the
  * one array: calls that overlap on the device race and give wrong results,
  * so serialise them (one stream, or events).  Each call rewrites all the
  * scratch it reads, so what a previous call left there does not matter. */

@@ -4,39 +4,31 @@
 //
 // The scratch that trt_attention normally takes from the caller (the
 // scheduler's work list, and for decode the split partials and tickets)
-// comes here from one file-scope device array owned by the library.  Every
-// GPU that loads the library holds that array until the process exits.
+// comes here from one file-scope device array owned by the library.  A GPU
+// holds that array from the first call made on it (when CUDA loads modules
+// lazily, its default; from context creation when it loads them eagerly)
+// until the process exits.
 //
 // Host code cannot use `g_rga_scratch` as an address: on the host the name
 // stands for a host-side shadow, and a kernel given it would fault or, where
-// the GPU can reach host memory, quietly use the wrong memory.  The device
-// address is looked up with cudaGetSymbolAddress once per device, with that
-// device current, on the first call made on it.
-#include <mutex>
+// the GPU can reach host memory, quietly use the wrong memory.  Every call
+// looks up the device address with cudaGetSymbolAddress, with the caller's
+// device current, so the address always belongs to the current context (a
+// context re-created after cudaDeviceReset may place the array elsewhere).
+// The first call on a device also loads the array's module there.
 #include "rga.h"
 
 namespace {
 
 constexpr size_t kScratchBytes = RGA_STATIC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_rga_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void *g_addr[kMaxDevices];
-
-// Device address of the scratch array on the current device (set up once).
+// Device address of the scratch array in the current context.
 rga_status scratch_address(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return RGA_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_rga_scratch) != cudaSuccess || !p) return RGA_ERR_CUDA;
-        g_addr[dev] = p;
-    }
-    *out = g_addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_rga_scratch) != cudaSuccess || !p) return RGA_ERR_CUDA;
+    *out = p;
     return RGA_OK;
 }
 

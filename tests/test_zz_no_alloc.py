@@ -42,10 +42,16 @@ def test_static_scratch_matches_trt_attention(name):
         y = torch.full_like(c.q, float("nan"))
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         a = binding.make_args(c.q, c.k, c.v, y, status=status, **kw)
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         rc = lib.trt_attention_static_scratch(ctypes.byref(a),
                                               ctypes.c_void_p(stream.cuda_stream))
         assert rc == 0, binding.STATUS_NAMES.get(rc, rc)
         torch.cuda.synchronize()
+        if call == 1:
+            # the first call may load the library's modules on this device;
+            # after that a call takes no device memory at all
+            assert torch.cuda.mem_get_info()[0] == free_before, "the call allocated device memory"
         assert int(status.item()) == 0
         rows = torch.isfinite(ref)
         assert torch.equal(torch.isfinite(y), rows), f"call {call}: written rows differ"
