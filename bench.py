@@ -211,7 +211,7 @@ def device_timed(run, stream, steps, warmup, dist_on, sampler_index=None):
     the call."""
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")   # 256 MiB
     clean = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device="cuda")   # 256 MiB
-    sink = torch.empty(1, dtype=torch.float32, device="cuda")
+    sink = torch.empty((), dtype=torch.float32, device="cuda")   # 0-d: the sum's shape
 
     def l2_flush():
         flush.zero_()
