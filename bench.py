@@ -310,18 +310,19 @@ def e2e_timed(case: W.Case, stream, steps, warmup, dist_on):
     return t0.elapsed_time(t1) / steps, bi, bo
 
 
-def oracle_sample(case: W.Case, budget_s: float, max_units=None):
+def oracle_sample(case: W.Case, budget_s: float, max_units=None, threads=None):
     """Time the CPU oracle, as it stands, on whole sequences of the workload
-    (all heads), shortest first, until ``budget_s`` seconds have been spent.
-    Returns (work done, seconds, threads, description); work is FLOPs, or
-    decode bytes for a decode workload."""
+    (all heads), shortest first, until ``budget_s`` seconds have been spent,
+    with ``threads`` worker threads (default: one per host core).  Returns
+    (work done, seconds, threads, description); work is FLOPs, or decode
+    bytes for a decode workload."""
     import oracle   # the CPU baseline leg is one of the oracle's permitted users
     if case.kv_form == W.PAGED:   # the oracle reads the gathered (linear) cache
         case = W.Case(**{**case.__dict__, "kv_form": W.PADDED, "page_table": None,
                          "k": oracle.gather_pages(case.k, case.page_table, 0, case.kv_lens),
                          "v": oracle.gather_pages(case.v, case.page_table, 1, case.kv_lens)})
     order = sorted(range(case.batch), key=lambda b: (case.q_lens[b] * case.kv_lens[b], b))
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     done_flops, spent, seqs = 0.0, 0.0, []
     for b in order:
         sub = single_sequence(case, b)
@@ -509,7 +510,7 @@ def main():
     secondary = {}
     if not args.no_secondary:
         for idx, q in ((3, "fp8"), (4, "fp8"), (5, "fp8"), (5, "int8"), (6, "fp8"), (7, "fp8"),
-                       (8, "fp8")):
+                       (8, "fp8"), (9, "fp8"), (10, "fp8")):
             if idx == args.workload:
                 continue
             torch.cuda.empty_cache()
@@ -532,9 +533,14 @@ def main():
 
     cpu = None
     if rank == 0:
+        # the oracle with one thread per host core, then single-threaded
         f, s, thr, desc = oracle_sample(case, args.cpu_budget)
+        f1, s1, _, desc1 = oracle_sample(case, args.cpu_budget / 2, threads=1)
         cpu = {"value": (f / s / scale) if s > 0 else None, "unit": head["unit"],
-               "cores": thr, "kind": "oracle", "sample": desc, "seconds": round(s, 2)}
+               "cores": thr, "kind": "oracle", "sample": desc, "seconds": round(s, 2),
+               "single_thread": {"value": (f1 / s1 / scale) if s1 > 0 else None,
+                                 "unit": head["unit"], "cores": 1, "sample": desc1,
+                                 "seconds": round(s1, 2)}}
 
     if rank == 0:
         value = head["value"] * world

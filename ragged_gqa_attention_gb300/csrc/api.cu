@@ -84,9 +84,14 @@ bool encode_kv(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t r
     return encode(m, base, 4, d, b);
 }
 
-// fp8 K or V (one byte per element): a box is `rows` whole D-byte rows.
-bool encode_kv8(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t rows) {
-    const CUtensorMapSwizzle sw = p.D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+// fp8 K or V (one byte per element): a box is `rows` whole D-byte rows,
+// swizzled as the decode kernel reads them, or unswizzled (`plain`) for the
+// prefill kernel's converter warps.
+bool encode_kv8(CUtensorMap *m, const void *base, const AttnParams &p, uint32_t rows,
+                bool plain = false) {
+    const CUtensorMapSwizzle sw = plain ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                  : p.D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                               : CU_TENSOR_MAP_SWIZZLE_64B;
     if (p.kv_packed) {
         const uint64_t d[3] = {(uint64_t)p.D, (uint64_t)p.Hkv, (uint64_t)p.kv_seq};
         const uint32_t b[3] = {(uint32_t)p.D, 1, rows};
@@ -243,7 +248,9 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
     rga_status st = validate(a, quant, paged != nullptr);
     if (st != RGA_OK) return st;
     if (kv8 && (!k_scale || !v_scale)) return RGA_ERR_INVALID_ARG;
-    if ((kv8 || paged) && !use_decode(a, false, kv8)) return RGA_ERR_UNSUPPORTED;
+    // (an FP8 or paged cache serves the unquantized op: decode shapes on the
+    // split-KV kernel, any other shape on the prefill kernel)
+    if ((kv8 || paged) && quant) return RGA_ERR_UNSUPPORTED;
     if (quant) {
         if (qtype != RGA_QUANT_FP8_E4M3 && qtype != RGA_QUANT_INT8) return RGA_ERR_INVALID_ARG;
         if (!qscale) return RGA_ERR_INVALID_ARG;
@@ -291,9 +298,11 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
         pm.B = paged->num_pages;
         pm.kv_seq = paged->page_size;
     }
-    if (kv8 ? !encode_kv8(&maps.k, kp, pm, DEC_KEYS) || !encode_kv8(&maps.v, vp, pm, DEC_KEYS)
-            : !encode_kv(&maps.k, kp, pm, dec ? DEC_KEYS : BN) ||
-                  !encode_kv(&maps.v, vp, pm, dec ? DEC_KEYS : BN))
+    // key rows per box: decode tiles of DEC_KEYS; prefill tiles of BN, as
+    // boxes of pf_page_rows() rows (each inside one page) for a paged cache
+    const uint32_t rows = dec ? DEC_KEYS : paged ? pf_page_rows(paged->page_size) : BN;
+    if (kv8 ? !encode_kv8(&maps.k, kp, pm, rows, !dec) || !encode_kv8(&maps.v, vp, pm, rows, !dec)
+            : !encode_kv(&maps.k, kp, pm, rows) || !encode_kv(&maps.v, vp, pm, rows))
         return RGA_ERR_CUDA;
     int mode;
     if (a->norm == RGA_NORM_SOFTMAX) mode = quant ? MODE_SOFTMAX_Q : MODE_SOFTMAX;
@@ -311,7 +320,7 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
         if (grid <= 0) return RGA_ERR_CUDA;
         if (grid > p.max_items) grid = p.max_items;
         if (grid < 1) grid = 1;
-        e = launch_prefill(p, maps, mode, grid, stream, bf16);
+        e = launch_prefill(p, maps, mode, grid, stream, bf16, kv8);
     }
     return e == cudaSuccess ? RGA_OK : RGA_ERR_CUDA;
 }
@@ -320,7 +329,10 @@ rga_status run(const rga_attention_args *a, bool quant, rga_quant qtype, const v
 
 namespace rga {
 cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode, int grid,
-                           cudaStream_t s, int bf16) {
+                           cudaStream_t s, int bf16, int kv8) {
+    if (kv8)
+        return bf16 ? launch_prefill_kv8_typed<true>(p, m, mode, grid, s)
+                    : launch_prefill_kv8_typed<false>(p, m, mode, grid, s);
     return bf16 ? launch_prefill_typed<true>(p, m, mode, grid, s)
                 : launch_prefill_typed<false>(p, m, mode, grid, s);
 }

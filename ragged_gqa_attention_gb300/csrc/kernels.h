@@ -57,7 +57,7 @@ struct AttnParams {
     int dec_rows;                   // decode: query rows per pair (DEC_ROWS, DEC_ROWS_WIDE or DEC_ROWS_KV8)
     int kv8;                        // K, V hold E4M3 codes (fp8 KV cache)
     const float *k_scale, *v_scale; // fp8 KV cache: dequantisation scales (device scalars)
-    int paged;                      // K, V come from page pools (decode only)
+    int paged;                      // K, V come from page pools
     const int32_t *page_table;      // paged: [B, 2, max_pages] K pages, V pages
     int page_size, max_pages, num_pages;
     int grid;                       // decode: persistent grid size
@@ -106,6 +106,13 @@ __host__ __device__ inline int dec_prep_blocks(const AttnParams &p) {
     }
     if (blocks < 1) blocks = 1;
     return (int)(blocks < DEC_PREP_MAX ? blocks : DEC_PREP_MAX);
+}
+
+// Rows of one TMA box of a paged cache in the prefill kernel: the largest of
+// 128, 64, 32 that divides the page size (a multiple of 32), so that each
+// box lies inside one page and a 128-key tile is a whole number of boxes.
+__host__ __device__ inline int pf_page_rows(int page_size) {
+    return (page_size & 127) == 0 ? 128 : (page_size & 63) == 0 ? 64 : 32;
 }
 
 // Largest batch the decode kernel lists in shared memory.
@@ -157,8 +164,11 @@ cudaError_t launch_sched(const AttnParams &p, int decode, cudaStream_t s);
 template <bool BF16>
 cudaError_t launch_prefill_typed(const AttnParams &p, const TensorMaps &m, int mode, int grid,
                                  cudaStream_t s);
+template <bool BF16>
+cudaError_t launch_prefill_kv8_typed(const AttnParams &p, const TensorMaps &m, int mode, int grid,
+                                     cudaStream_t s);
 cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode, int grid,
-                           cudaStream_t s, int bf16);
+                           cudaStream_t s, int bf16, int kv8);
 cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode,
                           cudaStream_t s, int bf16, int kv8);
 

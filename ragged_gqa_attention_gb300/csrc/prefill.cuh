@@ -80,24 +80,35 @@ struct Item {
 constexpr int IRING = 4;
 constexpr int ITEM_CONSUMERS = 1 + 8;   // the MMA warp and the 8 softmax warps
 
-template <int D>
+// KV8: K and V hold E4M3 codes (an FP8 KV cache).  The producer lands each
+// 128-key tile as bytes (128 rows x D bytes, unswizzled) and the two
+// converter warps expand it into the 16-bit, 128-byte-swizzled tile the
+// tensor core reads.  For D = 128 the bytes land in the second 64-column
+// block of the 16-bit stage itself (the expansion writes row r of a block
+// only over byte row r, which the same warp has already read); for D = 64
+// they land in buffers of their own.
+template <int D, bool KV8 = false>
 struct PfLayout {
     static constexpr int KST = D == 128 ? 2 : 3;         // K ring stages
     static constexpr int VST = D == 128 ? 2 : 3;         // V ring stages
     static constexpr int BLK = 128 * 128;                // one 64-column block of 128 rows
     static constexpr int NBLK = D / 64;
     static constexpr int TILE = NBLK * BLK;              // 128 rows x D x 2 bytes
+    static constexpr int RAW_TILE = 128 * D;             // 128 rows x D bytes (KV8)
     static constexpr int Q_OFF = 0;                      // two Q tiles
     static constexpr int K_OFF = Q_OFF + 2 * TILE;
     static constexpr int V_OFF = K_OFF + KST * TILE;
     // epilogue staging: 32 rows x 128 bytes per softmax warp (8 warps)
     static constexpr int STG_OFF = V_OFF + VST * TILE;
     static constexpr int STG_WARP = 32 * 128;
-    static constexpr int BAR_OFF = STG_OFF + 8 * STG_WARP;
+    // KV8 byte tiles of their own (D = 64 only)
+    static constexpr bool RAW_SEP = KV8 && D != 128;
+    static constexpr int RAW_OFF = STG_OFF + 8 * STG_WARP;
+    static constexpr int BAR_OFF = RAW_OFF + (RAW_SEP ? (KST + VST) * RAW_TILE : 0);
     // barriers: q_full, q_empty, k_full[KST], k_empty[KST], v_full[VST],
     // v_empty[VST], s_full[2], p_full[2], o_done[2], v_part,
-    // item_full[IRING], item_empty[IRING]
-    static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 7 + 2 * IRING;
+    // item_full[IRING], item_empty[IRING], kraw_full[KST], vraw_full[VST]
+    static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 7 + 2 * IRING + KST + VST;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     // misc: TMEM address (+0), abort flag (+8), item ring (+64)
     static constexpr int RING_OFF = 64;
@@ -106,17 +117,24 @@ struct PfLayout {
     // (and one 512-column TMEM allocation) is resident per SM
     static constexpr int ALLOC = (BYTES + 1024) > 120 * 1024 ? (BYTES + 1024) : 120 * 1024;
     static_assert(ALLOC <= 232448, "shared memory per CTA");
+    // byte tile of K stage s / V stage s (KV8)
+    __host__ __device__ static constexpr int raw_k(int st) {
+        return RAW_SEP ? RAW_OFF + st * RAW_TILE : K_OFF + st * TILE + BLK;
+    }
+    __host__ __device__ static constexpr int raw_v(int st) {
+        return RAW_SEP ? RAW_OFF + (KST + st) * RAW_TILE : V_OFF + st * TILE + BLK;
+    }
 };
 
 struct PfBars {
     uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full,
-        *o_done, *v_part, *item_full, *item_empty;
+        *o_done, *v_part, *item_full, *item_empty, *kraw_full, *vraw_full;
     Item *ring;   // IRING items
 };
 
-template <int D>
+template <int D, bool KV8>
 __device__ __forceinline__ PfBars pf_bars(uint8_t *base) {
-    using L = PfLayout<D>;
+    using L = PfLayout<D, KV8>;
     uint64_t *b = reinterpret_cast<uint64_t *>(base);
     PfBars r;
     r.q_full = b;
@@ -131,6 +149,8 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *base) {
     r.v_part = r.o_done + 2;
     r.item_full = r.v_part + 1;
     r.item_empty = r.item_full + IRING;
+    r.kraw_full = r.item_empty + IRING;
+    r.vraw_full = r.kraw_full + L::KST;
     static_assert(L::RING_OFF + IRING * sizeof(Item) <= 256, "item ring fits the misc area");
     r.ring = reinterpret_cast<Item *>(base + (L::MISC_OFF - L::BAR_OFF) + L::RING_OFF);
     return r;
@@ -219,14 +239,64 @@ __device__ __forceinline__ void tma_kv(const AttnParams &p, const CUtensorMap *m
         tma_load_4d(dst, map, bar, d0, j0, m.g, m.b);
 }
 
-// ------------------------------------------------------------------ producer
-template <int D, int MODE>
+// Pool page of each pr-row sub-box of key tile j0 of a paged cache: lane i
+// (i < BN / pr) gets the page holding keys j0 + i * pr .. + pr - 1 (table
+// row `which`: 0 K, 1 V), or -1 past the sequence's last page, where the
+// TMA copy reads out of bounds and fills zeros.  (The scheduler checked
+// every page index the sequence's keys use.)
+__device__ __forceinline__ int tile_page(const AttnParams &p, const Item &m, int which, int j0,
+                                         int pr) {
+    const int lane = threadIdx.x & 31;
+    int pg = -1;
+    if (lane < BN / pr) {
+        const int idx = (j0 + lane * pr) / p.page_size;
+        const int npages = (m.s.kv_len + p.page_size - 1) / p.page_size;
+        if (idx < npages)
+            pg = __ldg(p.page_table + ((size_t)m.b * 2 + which) * p.max_pages + idx);
+    }
+    return pg;
+}
+
+// Key tile j0 of K (which = 0) or V (which = 1) into dst, every copy
+// completing on `bar` (whose transaction count lane 0 sets to `bytes`).
+// 16-bit: NBLK boxes of 64 columns x 128 rows, 128-byte swizzled; KV8: one
+// box of D bytes x 128 rows, unswizzled.  A paged cache takes the tile as
+// BN / pr boxes of pr rows, each inside one page.  The whole warp calls it.
+template <int D, bool KV8>
+__device__ __forceinline__ void load_kv_tile(const AttnParams &p, const CUtensorMap *map,
+                                             const Item &m, int which, int j0, uint8_t *dst,
+                                             uint64_t *bar, uint32_t bytes) {
+    using L = PfLayout<D, KV8>;
+    const int lane = threadIdx.x & 31;
+    const int pr = p.paged ? pf_page_rows(p.page_size) : BN;
+    const int pg = p.paged ? tile_page(p, m, which, j0, pr) : 0;
+    if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+    for (int i = 0; i < BN / pr; ++i) {
+        const int page = __shfl_sync(0xffffffffu, pg, i);
+        if (lane != 0) continue;
+        const int key = j0 + i * pr;
+        if (KV8) {
+            uint8_t *d = dst + i * pr * D;
+            if (p.paged) tma_load_4d(d, map, bar, 0, key % p.page_size, m.g, page);
+            else if (p.kv_packed) tma_load_3d(d, map, bar, 0, m.g, m.s.kv_off + key);
+            else tma_load_4d(d, map, bar, 0, key, m.g, m.b);
+        } else {
+            for (int blk = 0; blk < L::NBLK; ++blk) {
+                uint8_t *d = dst + blk * L::BLK + i * pr * 128;
+                if (p.paged) tma_load_4d(d, map, bar, blk * 64, key % p.page_size, m.g, page);
+                else tma_kv(p, map, m, key, d, bar, blk * 64);
+            }
+        }
+    }
+}
+
+template <int D, int MODE, bool KV8>
 __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorMaps &tm, uint8_t *sm,
                               const PfBars &bar, volatile int *abort, int n_items) {
-    using L = PfLayout<D>;
+    using L = PfLayout<D, KV8>;
     const int lane = threadIdx.x & 31;
     const uint32_t q_bytes = (uint32_t)(2 * L::NBLK * p.G * p.tq * 128);
-    const uint32_t kv_bytes = (uint32_t)L::TILE;
+    const uint32_t kv_bytes = (uint32_t)(KV8 ? L::RAW_TILE : L::TILE);
     uint32_t kc = 0, vc = 0, qc = 0, vpc = 0;   // running ring / barrier counters
     int *counter = reinterpret_cast<int *>(p.ws) + 1;
     int next = blockIdx.x;                      // lane 0: the next item to hand out
@@ -259,32 +329,28 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
             const int j0 = key_tile<MODE>(m, t) * BN;
             const int ks = kc % L::KST;
             if (kc >= L::KST && !mbar_wait(&bar.k_empty[ks], ((kc / L::KST) - 1) & 1, abort)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bar.k_full[ks], kv_bytes);
-                for (int blk = 0; blk < L::NBLK; ++blk)
-                    tma_kv(p, &tm.k, m, j0, sm + L::K_OFF + ks * L::TILE + blk * L::BLK,
-                           &bar.k_full[ks], blk * 64);
-            }
+            if (KV8)   // bytes for the converter warps
+                load_kv_tile<D, true>(p, &tm.k, m, 0, j0, sm + L::raw_k(ks), &bar.kraw_full[ks],
+                                      kv_bytes);
+            else
+                load_kv_tile<D, false>(p, &tm.k, m, 0, j0, sm + L::K_OFF + ks * L::TILE,
+                                       &bar.k_full[ks], kv_bytes);
             ++kc;
             if (!is_pv<MODE>(m, t)) continue;
             const int vs = vc % L::VST;
             if (vc >= L::VST && !mbar_wait(&bar.v_empty[vs], ((vc / L::VST) - 1) & 1, abort)) break;
             uint8_t *vdst = sm + L::V_OFF + vs * L::TILE;
             const int rem = m.s.kv_len - j0;
-            if (rem >= BN) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bar.v_full[vs], kv_bytes);
-                    for (int blk = 0; blk < L::NBLK; ++blk)
-                        tma_kv(p, &tm.v, m, j0, vdst + blk * L::BLK, &bar.v_full[vs], blk * 64);
-                }
+            if (KV8) {
+                // the converter warps zero the rows past the sequence end
+                load_kv_tile<D, true>(p, &tm.v, m, 1, j0, sm + L::raw_v(vs), &bar.vraw_full[vs],
+                                      kv_bytes);
+            } else if (rem >= BN) {
+                load_kv_tile<D, false>(p, &tm.v, m, 1, j0, vdst, &bar.v_full[vs], kv_bytes);
             } else {
                 // the tile runs past the sequence end: land it, clear the
                 // rows past the end, then publish it
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar.v_part, kv_bytes);
-                    for (int blk = 0; blk < L::NBLK; ++blk)
-                        tma_kv(p, &tm.v, m, j0, vdst + blk * L::BLK, bar.v_part, blk * 64);
-                }
+                load_kv_tile<D, false>(p, &tm.v, m, 1, j0, vdst, bar.v_part, kv_bytes);
                 const bool landed = mbar_wait(bar.v_part, vpc & 1, abort);
                 ++vpc;
                 if (!landed) break;
@@ -295,12 +361,89 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
         }
     }
     // Before the CTA exits, let every copy this warp started land.
+    uint64_t *k_land = KV8 ? bar.kraw_full : bar.k_full;
+    uint64_t *v_land = KV8 ? bar.vraw_full : bar.v_full;
     for (uint32_t c = kc > L::KST ? kc - L::KST : 0; c < kc; ++c)
-        mbar_wait_drain(&bar.k_full[c % L::KST], (c / L::KST) & 1);
+        mbar_wait_drain(&k_land[c % L::KST], (c / L::KST) & 1);
     for (uint32_t c = vc > L::VST ? vc - L::VST : 0; c < vc; ++c)
-        mbar_wait_drain(&bar.v_full[c % L::VST], (c / L::VST) & 1);
+        mbar_wait_drain(&v_land[c % L::VST], (c / L::VST) & 1);
     if (qc > 0) mbar_wait_drain(bar.q_full, (qc - 1) & 1);
     if (vpc > 0) mbar_wait_drain(bar.v_part, (vpc - 1) & 1);
+}
+
+// ------------------------------------------------------------------ converter (KV8)
+// Expands a byte tile of E4M3 codes (128 rows x D bytes) into the 16-bit tile
+// a TMA load of 16-bit values would have produced: NBLK blocks of 128 rows x
+// 128 bytes, 16-byte chunks swizzled with the row's low three bits.  Lane l
+// of converter warp w takes, per step, row r = r0 + l / (D/16) and its
+// 16-byte chunk c = l % (D/16) (codes 16c .. 16c+15, exactly converted to
+// f16 or bf16), which land in block c / 4 as the logical chunks 2(c%4) and
+// 2(c%4)+1 of the row.  Rows from `zero_from` on are written as zeros.  The
+// warp reads all its rows' bytes before it writes, so the expansion may
+// overwrite the byte tile in place (D = 128: each 16-bit row of the second
+// block covers exactly the byte row of the same index).
+template <int D, bool BF16>
+__device__ __forceinline__ void expand_tile(const uint8_t *raw, uint8_t *dst, int zero_from,
+                                            int w) {
+    constexpr int CPR = D / 16;     // 16-byte chunks per byte row
+    constexpr int RPS = 32 / CPR;   // rows per warp step
+    const int lane = threadIdx.x & 31;
+    const int c = lane % CPR;
+    const int l0 = 2 * (c % 4);
+#pragma unroll 2
+    for (int r0 = w * RPS; r0 < BN; r0 += 2 * RPS) {
+        const int r = r0 + lane / CPR;
+        const uint4 b = *reinterpret_cast<const uint4 *>(raw + r * D + c * 16);
+        __syncwarp();
+        uint32_t h[8];
+        e4m3x4_to_x2<BF16>(b.x, h[0], h[1]);
+        e4m3x4_to_x2<BF16>(b.y, h[2], h[3]);
+        e4m3x4_to_x2<BF16>(b.z, h[4], h[5]);
+        e4m3x4_to_x2<BF16>(b.w, h[6], h[7]);
+        if (r >= zero_from) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) h[k] = 0u;
+        }
+        uint8_t *row = dst + (c / 4) * PfLayout<D>::BLK + r * 128;
+        *reinterpret_cast<uint4 *>(row + ((l0 ^ (r & 7)) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(row + (((l0 + 1) ^ (r & 7)) * 16)) =
+            make_uint4(h[4], h[5], h[6], h[7]);
+    }
+}
+
+// Converter warp w (0 or 1) of an FP8 KV cache: follows the producer's K and
+// V tiles item by item, expands each landed byte tile (each warp half the
+// rows) and publishes it to the tensor core (k_full / v_full take one
+// arrival per converter warp).  V rows past the sequence end become zeros
+// (their codes may be NaN, and 0 * NaN would reach O).
+template <int D, bool BF16>
+__device__ __forceinline__ void convert_role(const AttnParams &p, uint8_t *sm, const PfBars &bar,
+                                             volatile int *abort, int w) {
+    using L = PfLayout<D, true>;
+    const int lane = threadIdx.x & 31;
+    uint32_t kc = 0, vc = 0;
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+        Item m;
+        if (!next_item(bar, n, abort, true, m)) break;
+        for (int t = 0; t < m.ntiles; ++t) {
+            const int ks = kc % L::KST;
+            if (!mbar_wait(&bar.kraw_full[ks], (kc / L::KST) & 1, abort)) { ok = false; break; }
+            expand_tile<D, BF16>(sm + L::raw_k(ks), sm + L::K_OFF + ks * L::TILE, BN, w);
+            fence_proxy_async_smem();   // the tensor core reads what the generic proxy wrote
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.k_full[ks]);
+            ++kc;
+            const int vs = vc % L::VST;
+            if (!mbar_wait(&bar.vraw_full[vs], (vc / L::VST) & 1, abort)) { ok = false; break; }
+            expand_tile<D, BF16>(sm + L::raw_v(vs), sm + L::V_OFF + vs * L::TILE,
+                                 m.s.kv_len - t * BN, w);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.v_full[vs]);
+            ++vc;
+        }
+    }
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -479,10 +622,11 @@ constexpr uint32_t NONE_EXCLUDED = 0xffc0dead;
 // length limits) and its bit is set: bit (kk >> 2) of word (kk & 3).
 // Writes log2-domain scores (softmax), where an excluded pair is -inf, or
 // natural-unit scores ('none'), where it is NONE_EXCLUDED.
+// sc: the score scale (log2 units for softmax; times s_k for an FP8 cache).
 template <bool LOG2, int MK>
 __device__ __forceinline__ void mask_chunk(const AttnParams &p, float (&v)[32], int c, int rem,
-                                           const uint32_t (&bits)[4], long long mrow, int j0) {
-    const float sc = LOG2 ? p.scale_log2 : p.scale;
+                                           const uint32_t (&bits)[4], long long mrow, int j0,
+                                           float sc) {
     const bool keyb = p.md[3] == 1;
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
@@ -508,12 +652,12 @@ __device__ __forceinline__ void mask_chunk(const AttnParams &p, float (&v)[32], 
 template <bool LOG2>
 __device__ __forceinline__ void mask_chunk_any(const AttnParams &p, int mk, float (&v)[32], int c,
                                                int rem, const uint32_t (&bits)[4],
-                                               long long mrow, int j0) {
+                                               long long mrow, int j0, float sc) {
     switch (mk) {
-    case MK_ADD_F16: mask_chunk<LOG2, MK_ADD_F16>(p, v, c, rem, bits, mrow, j0); break;
-    case MK_ADD_BF16: mask_chunk<LOG2, MK_ADD_BF16>(p, v, c, rem, bits, mrow, j0); break;
-    case MK_ADD_F32: mask_chunk<LOG2, MK_ADD_F32>(p, v, c, rem, bits, mrow, j0); break;
-    default: mask_chunk<LOG2, MK_BITS>(p, v, c, rem, bits, mrow, j0); break;
+    case MK_ADD_F16: mask_chunk<LOG2, MK_ADD_F16>(p, v, c, rem, bits, mrow, j0, sc); break;
+    case MK_ADD_BF16: mask_chunk<LOG2, MK_ADD_BF16>(p, v, c, rem, bits, mrow, j0, sc); break;
+    case MK_ADD_F32: mask_chunk<LOG2, MK_ADD_F32>(p, v, c, rem, bits, mrow, j0, sc); break;
+    default: mask_chunk<LOG2, MK_BITS>(p, v, c, rem, bits, mrow, j0, sc); break;
     }
 }
 
@@ -775,7 +919,7 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&r)[32], uint32_t s_addr
     tmem_st16(s_addr + c * 16, w);
 }
 
-template <int D, int MODE, bool BF16>
+template <int D, int MODE, bool BF16, bool KV8>
 __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMaps &tm,
                                              const PfBars &bar, volatile int *abort,
                                              int n_items, uint32_t tmem, int a, uint8_t *stg) {
@@ -791,7 +935,9 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
     const bool in_tile = r < G * TQ;
     const float qs = QUANT ? load_qscale(p) : 1.f;
     const float inv_qs = 1.f / qs;
-    const float sc = SOFTMAX ? p.scale_log2 : p.scale;
+    // score scale; an FP8 cache folds s_k into it and s_v into the epilogue
+    const float sc = (SOFTMAX ? p.scale_log2 : p.scale) * (KV8 ? __ldg(p.k_scale) : 1.f);
+    const float sv = KV8 ? __ldg(p.v_scale) : 1.f;
     const bool use_mask = p.mask != nullptr;
     const bool bool_mask = use_mask && p.mask_dtype == 3;
     const bool row_indep = bool_mask && p.md[1] == 1 && p.md[2] == 1;
@@ -1018,7 +1164,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
 #pragma unroll
                     for (int c = 0; c < BN / 32; ++c)
                         mask_chunk<SOFTMAX, MK_BITS>(p, *reinterpret_cast<float(*)[32]>(&x[c * 32]),
-                                                     c, rem, bits, mrow, j0);
+                                                     c, rem, bits, mrow, j0, sc);
             } else {   // additive mask: scale and mask a chunk at a time
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
@@ -1029,7 +1175,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                     float v[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(rr[k]);
-                    mask_chunk_any<SOFTMAX>(p, mk, v, c, rem, bits, mrow, j0);
+                    mask_chunk_any<SOFTMAX>(p, mk, v, c, rem, bits, mrow, j0, sc);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) x[c * 32 + k] = v[k];
                 }
@@ -1154,8 +1300,8 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
         ++pvw;
         tc_fence_after();
         float f;
-        if (MODE == MODE_SOFTMAX) f = (l > 0.f) ? 1.f / l : 0.f;
-        else f = qs;    // 'none': 1; quantized: the Q/DQ scale
+        if (MODE == MODE_SOFTMAX) f = (l > 0.f) ? sv / l : 0.f;
+        else f = qs * sv;    // 'none': 1 (s_v); quantized: the Q/DQ scale
         store_rows<D, BF16>(p, tm, m, a, o_addr, f, false, stg, pending);
         tc_fence_before();
     }
@@ -1163,14 +1309,15 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int MODE, bool BF16>
+// KV8: K and V are E4M3 codes (FP8 KV cache), expanded by warps 10-11.
+template <int D, int MODE, bool BF16, bool KV8>
 __global__ void __launch_bounds__(PF_THREADS, 1)
 prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TensorMaps tm) {
-    using L = PfLayout<D>;
+    using L = PfLayout<D, KV8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const PfBars bar = pf_bars<D>(sm + L::BAR_OFF);
+    const PfBars bar = pf_bars<D, KV8>(sm + L::BAR_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF);
     volatile int *abort = reinterpret_cast<volatile int *>(sm + L::MISC_OFF + 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1178,8 +1325,18 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     if (threadIdx.x == 0) {
         mbar_init(bar.q_full, 1);
         mbar_init(bar.q_empty, 1);
-        for (int s = 0; s < L::KST; ++s) { mbar_init(&bar.k_full[s], 1); mbar_init(&bar.k_empty[s], 1); }
-        for (int s = 0; s < L::VST; ++s) { mbar_init(&bar.v_full[s], 1); mbar_init(&bar.v_empty[s], 1); }
+        // with an FP8 cache the two converter warps publish each K and V tile
+        const int pub = KV8 ? 2 : 1;
+        for (int s = 0; s < L::KST; ++s) {
+            mbar_init(&bar.k_full[s], pub);
+            mbar_init(&bar.k_empty[s], 1);
+            mbar_init(&bar.kraw_full[s], 1);
+        }
+        for (int s = 0; s < L::VST; ++s) {
+            mbar_init(&bar.v_full[s], pub);
+            mbar_init(&bar.v_empty[s], 1);
+            mbar_init(&bar.vraw_full[s], 1);
+        }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar.s_full[s], 1);
             mbar_init(&bar.p_full[s], 128);
@@ -1188,7 +1345,7 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
         mbar_init(bar.v_part, 1);
         for (int s = 0; s < IRING; ++s) {
             mbar_init(&bar.item_full[s], 1);
-            mbar_init(&bar.item_empty[s], ITEM_CONSUMERS);
+            mbar_init(&bar.item_empty[s], ITEM_CONSUMERS + (KV8 ? 2 : 0));
         }
         *abort = 0;
         fence_mbar_init();
@@ -1211,8 +1368,8 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
 
     if (warp < 8) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(PF_SOFTMAX_REGS));
-        softmax_role<D, MODE, BF16>(p, tm, bar, abort, n_items, tmem, warp >> 2,
-                                    sm + L::STG_OFF + (warp >> 2) * 4 * L::STG_WARP);
+        softmax_role<D, MODE, BF16, KV8>(p, tm, bar, abort, n_items, tmem, warp >> 2,
+                                         sm + L::STG_OFF + (warp >> 2) * 4 * L::STG_WARP);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(PF_AUX_REGS));
     }
@@ -1220,7 +1377,9 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     } else if (warp == 8) {
         mma_role<D, MODE, BF16>(p, sm, bar, abort, tmem);
     } else if (warp == 9) {
-        producer_role<D, MODE>(p, tm, sm, bar, abort, n_items);
+        producer_role<D, MODE, KV8>(p, tm, sm, bar, abort, n_items);
+    } else if (KV8) {
+        convert_role<D, BF16>(p, sm, bar, abort, warp - 10);
     }
 
     tc_fence_before();
@@ -1230,32 +1389,33 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     if (threadIdx.x == 0 && *abort) set_status(p.status, 5);
 }
 
-template <int D, int MODE, bool BF16>
+template <int D, int MODE, bool BF16, bool KV8>
 static cudaError_t launch_one(const AttnParams &p, const TensorMaps &m, int grid,
                               cudaStream_t s) {
-    using L = PfLayout<D>;
+    using L = PfLayout<D, KV8>;
     static std::atomic<unsigned long long> configured{0};
     cudaError_t e = once_per_device(configured, [] {
         // the register split needs exactly the launch allocation it was sized for
         cudaFuncAttributes fa;
-        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<D, MODE, BF16>);
+        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_kernel<D, MODE, BF16, KV8>);
         if (r != cudaSuccess) return r;
         if (fa.numRegs != PF_LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(prefill_kernel<D, MODE, BF16>,
+        return cudaFuncSetAttribute(prefill_kernel<D, MODE, BF16, KV8>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     });
     if (e != cudaSuccess) return e;
-    return launch_dependent(prefill_kernel<D, MODE, BF16>, grid, PF_THREADS, L::ALLOC, s, p, m);
+    return launch_dependent(prefill_kernel<D, MODE, BF16, KV8>, grid, PF_THREADS, L::ALLOC, s, p,
+                            m);
 }
 
 template <int D, bool BF16>
 static cudaError_t launch_mode(const AttnParams &p, const TensorMaps &m, int mode, int grid,
                                cudaStream_t s) {
     switch (mode) {
-    case MODE_SOFTMAX: return launch_one<D, MODE_SOFTMAX, BF16>(p, m, grid, s);
-    case MODE_NONE: return launch_one<D, MODE_NONE, BF16>(p, m, grid, s);
-    case MODE_SOFTMAX_Q: return launch_one<D, MODE_SOFTMAX_Q, BF16>(p, m, grid, s);
-    default: return launch_one<D, MODE_NONE_Q, BF16>(p, m, grid, s);
+    case MODE_SOFTMAX: return launch_one<D, MODE_SOFTMAX, BF16, false>(p, m, grid, s);
+    case MODE_NONE: return launch_one<D, MODE_NONE, BF16, false>(p, m, grid, s);
+    case MODE_SOFTMAX_Q: return launch_one<D, MODE_SOFTMAX_Q, BF16, false>(p, m, grid, s);
+    default: return launch_one<D, MODE_NONE_Q, BF16, false>(p, m, grid, s);
     }
 }
 
@@ -1266,6 +1426,20 @@ cudaError_t launch_prefill_typed(const AttnParams &p, const TensorMaps &m, int m
                                  cudaStream_t s) {
     if (p.D == 64) return launch_mode<64, BF16>(p, m, mode, grid, s);
     return launch_mode<128, BF16>(p, m, mode, grid, s);
+}
+
+// Over an FP8 KV cache (softmax or 'none'; the quantized op has no FP8
+// cache form), instantiated in prefill_kv8.cu.
+template <bool BF16>
+cudaError_t launch_prefill_kv8_typed(const AttnParams &p, const TensorMaps &m, int mode, int grid,
+                                     cudaStream_t s) {
+    if (mode != MODE_SOFTMAX && mode != MODE_NONE) return cudaErrorInvalidValue;
+    const bool sm = mode == MODE_SOFTMAX;
+    if (p.D == 64)
+        return sm ? launch_one<64, MODE_SOFTMAX, BF16, true>(p, m, grid, s)
+                  : launch_one<64, MODE_NONE, BF16, true>(p, m, grid, s);
+    return sm ? launch_one<128, MODE_SOFTMAX, BF16, true>(p, m, grid, s)
+              : launch_one<128, MODE_NONE, BF16, true>(p, m, grid, s);
 }
 
 }  // namespace rga

@@ -10,7 +10,8 @@
 // Work-list layout in the workspace: int n_items at byte 0, the attention
 // kernel's next-item counter (cleared here) at byte 4, int4 items from
 // byte WS_HEADER.  On bad lengths it writes RGA_ERR_DEVICE_LENGTHS (4) to
-// the status word and an empty list, so no attention work runs.
+// the status word and an empty list, so no attention work runs; the same
+// for a page index outside the pools of a paged cache.
 #include "device_common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -89,6 +90,20 @@ sched_kernel(AttnParams p, int decode) {
             if (p.md[3] != 1 && p.md[3] < s.kv_len) ok = false;
         }
         if (!ok) atomicOr(&bad, 1);
+    }
+    // a paged cache: every page index a sequence's keys use must lie in the
+    // pools (entries past the last page are never read)
+    if (p.paged) {
+        const long long total = (long long)p.B * p.max_pages;
+        const long long cap = (long long)p.max_pages * p.page_size;
+        for (long long i = tid; i < total; i += SCHED_THREADS) {
+            const int b = (int)(i / p.max_pages), k = (int)(i % p.max_pages);
+            const long long len = min((long long)max(p.kv_lengths[b], 0), cap);
+            if (k >= (len + p.page_size - 1) / p.page_size) continue;
+            const int32_t *pt = p.page_table + (size_t)b * 2 * p.max_pages;
+            const int a = pt[k], v = pt[p.max_pages + k];
+            if (a < 0 || a >= p.num_pages || v < 0 || v >= p.num_pages) atomicOr(&bad, 1);
+        }
     }
     __syncthreads();
     if (bad) {

@@ -241,6 +241,13 @@ WORKLOADS = {
         "workload 4 over a paged KV cache: each sequence's keys in pages of 64 "
         "keys placed at seeded random positions of K and V pools (16 spare "
         "pages each), page table [64, 2, 64]"),
+    9: ("chunked_packedq_fp8kv8192_gqa32x8_d128_bf16",
+        "workload 3 (its draws) over an FP8 (E4M3) KV cache: K and V stored as "
+        "E4M3FN codes with per-tensor scales s_k = 1/56, s_v = 1/48; bf16 Q and Y"),
+    10: ("chunked_packedq_paddedkv8192_gqa32x8_d128_bf16_paged64",
+         "workload 3 over a paged KV cache: each sequence's keys in pages of 64 "
+         "keys at seeded random positions of K and V pools (16 spare pages each), "
+         "page table [16, 2, 128]"),
 }
 
 # per-tensor scales of the fp8 KV cache workload (K, V ~ N(0, 1) land near
@@ -249,7 +256,7 @@ FP8_KV_SCALES = (1.0 / 56.0, 1.0 / 48.0)
 
 
 def workload(index, *, quant="fp8", kv_pad=math.nan, seed=None):
-    """The named workload ``index`` (1..8) as a Case on host memory.
+    """The named workload ``index`` (1..10) as a Case on host memory.
 
     ``quant`` selects the fp8 or int8 variant of workload 5.
     """
@@ -266,14 +273,18 @@ def workload(index, *, quant="fp8", kv_pad=math.nan, seed=None):
                          head_dim=128, q_lens=lens, kv_lens=lens,
                          q_form=PACKED, kv_form=PACKED, dtype=torch.bfloat16,
                          causal="upper_left", kv_pad=kv_pad, g=g)
-    if index == 3:
+    if index in (3, 9):
+        if index == 9:   # workload 3's draws
+            g = torch.Generator("cpu").manual_seed(3)
         qls = _uniform_int(g, 64, 512, 16)
         kvls = [_uniform_int(g, ql, 8192, 1)[0] for ql in qls]
         return make_case(name, seed, batch=16, q_heads=32, kv_heads=8,
                          head_dim=128, q_lens=qls, kv_lens=kvls,
                          q_form=PACKED, kv_form=PADDED, kv_seq=8192,
                          dtype=torch.bfloat16, causal="lower_right",
-                         kv_pad=kv_pad, g=g)
+                         kv_pad=kv_pad, g=g, kv_fp8=FP8_KV_SCALES if index == 9 else None)
+    if index == 10:
+        return paged(workload(3, kv_pad=kv_pad), 64, seed=10, spare=16, pad=kv_pad)
     if index == 4:
         kvls = _uniform_int(g, 256, 4096, 64)
         return make_case(name, seed, batch=64, q_heads=64, kv_heads=8,

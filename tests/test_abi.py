@@ -167,8 +167,9 @@ def test_fp8_kv_validation_without_a_device(lib):
     a = _args(workspace=0x100000, workspace_bytes=1 << 30)
     assert lib.trt_attention_fp8_kv(ctypes.byref(a), None, 0x40000, None) == 1   # k_scale
     assert lib.trt_attention_fp8_kv(ctypes.byref(a), 0x40000, None, None) == 1   # v_scale
-    # prefill shapes (256 query rows per sequence) are not on the fp8 path
-    assert lib.trt_attention_fp8_kv(ctypes.byref(a), 0x40000, 0x40010, None) == 2
+    # prefill shapes (256 query rows per sequence) pass validation and go to
+    # the prefill kernel: with no device here, the launch set-up fails
+    assert lib.trt_attention_fp8_kv(ctypes.byref(a), 0x40000, 0x40010, None) == 3
     # argument errors come first, as for trt_attention
     a = _args(q_heads=6, kv_heads=4)
     assert lib.trt_attention_fp8_kv(ctypes.byref(a), 0x40000, 0x40010, None) == 1
@@ -209,8 +210,9 @@ def test_paged_kv_validation_without_a_device(lib):
     assert call(a, paged(kv_dtype=4)) == 1              # E4M3 pools without scales
     assert call(_args(q_seq=1, kv_form=1, kv_lengths=0x70000), paged()) == 1   # packed KV
     assert call(_args(q_seq=1), paged()) == 1           # kv_lengths required
+    # 256 query rows: a prefill shape, accepted (no device here: launch set-up fails)
     assert call(_args(kv_lengths=0x70000, workspace=0x100000, workspace_bytes=1 << 30),
-                paged()) == 2                           # 256 query rows: a prefill shape
+                paged()) == 3
 
 
 def test_rope_validation_without_a_device(lib):

@@ -7,7 +7,9 @@ and both normalisations, with empty, one-key and ragged key ranges and NaN
 codes in every padding row; GQA group sizes 1, 4 and 16; long key ranges
 that the stream-K split cuts across warps; tree decoding with a bool mask;
 agreement with the 16-bit path on a cache whose dequantised values are
-exactly bf16; and the shapes the path rejects."""
+exactly bf16.  Prefill and chunked-prefill shapes run on the prefill kernel:
+both Q and KV forms, every causal kind, masks, 'none', GQA group sizes 1 to
+16, and bit-for-bit agreement with the 16-bit prefill on exact values."""
 import dataclasses
 import math
 
@@ -124,10 +126,75 @@ def test_matches_16bit_path_on_exact_values():
     assert np.abs(y8 - y16).max() <= 4e-3
 
 
-def test_prefill_shapes_are_unsupported():
-    c = W.make_case("fp8kv_prefill", 180, batch=2, q_heads=8, kv_heads=2, head_dim=128,
-                    q_lens=[64, 64], kv_lens=[64, 64], dtype=torch.bfloat16,
-                    causal="upper_left", kv_fp8=W.FP8_KV_SCALES)
-    with pytest.raises(binding.RgaError) as e:
-        run_gpu(c)
-    assert e.value.code == 2
+# --------------------------------------------------------------------------
+# prefill and chunked-prefill shapes: the tcgen05 prefill kernel, whose
+# converter warps expand each landed tile of codes into 16-bit values
+# --------------------------------------------------------------------------
+def _prefill_case(seed, *, D=128, dtype=torch.bfloat16, q_form="packed", kv_form="padded",
+                  causal="lower_right", norm="softmax", G=4, q_lens=(100, 257, 1, 64, 130),
+                  kv_lens=(612, 257, 300, 64, 1000), mask=None, scales=W.FP8_KV_SCALES):
+    B = len(q_lens)
+    kw = {"kv_seq": max(kv_lens) + 40} if kv_form == "padded" else {"tail": 7}
+    return W.make_case(f"fp8kv_prefill_{seed}", seed, batch=B, q_heads=2 * G, kv_heads=2,
+                       head_dim=D, q_lens=list(q_lens), kv_lens=list(kv_lens), q_form=q_form,
+                       kv_form=kv_form, dtype=dtype, causal=causal, norm=norm, mask=mask,
+                       # 'none' sums s * v over up to 1000 keys unnormalised: a small
+                       # score scale keeps |y| below 4, where bf16 output rounding
+                       # stays inside the tolerance
+                       kv_fp8=scales, scale=0.002 if norm == "none" else None,
+                       pass_query_lengths=True, **kw)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("kv_form", ["padded", "packed"])
+def test_chunked_prefill(D, dtype, kv_form):
+    seed = 300 + D + (dtype == torch.bfloat16) * 3 + (kv_form == "packed") * 5
+    _parity(_prefill_case(seed, D=D, dtype=dtype, kv_form=kv_form))
+
+
+@pytest.mark.parametrize("causal", ["none", "upper_left"])
+@pytest.mark.parametrize("q_form", ["packed", "padded"])
+def test_prefill_causal_kinds_and_forms(causal, q_form):
+    q_lens = (130, 64, 300) if causal == "upper_left" else (100, 17, 300)
+    kv_lens = (130, 64, 300) if causal == "upper_left" else (50, 400, 129)
+    _parity(_prefill_case(320 + len(causal) + len(q_form), q_form=q_form, causal=causal,
+                          q_lens=q_lens, kv_lens=kv_lens))
+
+
+@pytest.mark.parametrize("G", [1, 8, 16])
+def test_prefill_group_sizes(G):
+    _parity(_prefill_case(340 + G, G=G, q_lens=(70, 200), kv_lens=(333, 200)))
+
+
+def test_prefill_none_and_masks():
+    _parity(_prefill_case(350, norm="none", causal="none", q_lens=(90, 140), kv_lens=(300, 140)))
+    B, N = 2, 340   # the mask's key dim is the padded cache's extent (300 + 40)
+    _parity(_prefill_case(351, causal="none", q_lens=(90, 140), kv_lens=(300, 140),
+                          mask=lambda g: torch.rand((B, 1, 140, N), generator=g) > 0.3))
+    _parity(_prefill_case(352, causal="none", q_lens=(90, 140), kv_lens=(300, 140),
+                          mask=lambda g: torch.randn((B, 8, 140, N), generator=g)))
+
+
+def test_prefill_scales_of_other_magnitudes():
+    _parity(_prefill_case(360, scales=(1.0 / 448.0, 3.0)))
+    _parity(_prefill_case(361, scales=(0.25, 1.0 / 1000.0)))
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_prefill_matches_16bit_path_bit_for_bit(dtype):
+    """Power-of-two scales make every dequantised value a 16-bit value, and
+    scaling by a power of two commutes with every rounding on the way: the
+    prefill kernel over the codes computes exactly what it computes over the
+    dequantised 16-bit cache."""
+    c = _prefill_case(370, dtype=dtype, scales=(1.0 / 64.0, 1.0 / 32.0))
+    y8, _, st = run_gpu(c)
+    assert binding.device_status(st) == 0
+    kd = torch.from_numpy(oracle.dequant_e4m3(c.k, c.kv_scales[0])).to(dtype)
+    vd = torch.from_numpy(oracle.dequant_e4m3(c.v, c.kv_scales[1])).to(dtype)
+    c16 = dataclasses.replace(c, k=torch.nan_to_num(kd), v=torch.nan_to_num(vd), kv_scales=None)
+    y16, _, st = run_gpu(c16)
+    assert binding.device_status(st) == 0
+    rows = np.isfinite(y16)
+    assert np.array_equal(np.isfinite(y8), rows)
+    assert np.array_equal(y8[rows], y16[rows])

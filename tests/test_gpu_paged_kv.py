@@ -8,7 +8,9 @@ page-table entries past a sequence's last page are -1.  Covers page sizes 32
 to 256, both dtypes and head dims, fp8 (E4M3) pools, tree decoding, empty
 sequences, identity paging against the linear cache (bit for bit: the same
 tiles in the same order), and a page index outside the pools (device status
-4, Y untouched)."""
+4, Y untouched).  Chunked-prefill shapes run on the prefill kernel with page
+sizes 32 to 256 (96 included: tiles that straddle pages), 16-bit and fp8
+pools, and the same identity and bad-page checks."""
 import dataclasses
 
 import numpy as np
@@ -100,10 +102,63 @@ def test_page_outside_the_pools_sets_status_and_leaves_y_untouched():
         assert (raw == np.int16(SENTINEL)).all()
 
 
-def test_prefill_shapes_are_unsupported():
-    c = W.make_case("paged_prefill", 260, batch=2, q_heads=8, kv_heads=2, head_dim=128,
-                    q_lens=[64, 64], kv_lens=[64, 64], dtype=torch.bfloat16,
-                    causal="upper_left", kv_seq=64)
-    with pytest.raises(binding.RgaError) as e:
-        run_gpu(W.paged(c, 64, seed=12))
-    assert e.value.code == 2
+# --------------------------------------------------------------------------
+# prefill and chunked-prefill shapes: the prefill kernel loads each 128-key
+# tile as boxes of pf_page_rows(page_size) rows, one page each
+# --------------------------------------------------------------------------
+# Chunks of a longer context (every row attends at least 64 keys), as the
+# prefill of a paged cache sees them.  (Rows that attend one or two keys
+# return about one V row, |y| up to ~3.5, where bf16 output rounding alone
+# reaches 7.8e-3 of the 1e-2 bar; the linear-cache tests and the
+# self-attention case below cover such rows.)
+def _chunked(seed, *, D=128, dtype=torch.bfloat16, fp8=False, G=4,
+             q_lens=(100, 257, 1, 64, 130), kv_lens=(612, 321, 300, 128, 1000), causal="lower_right",
+             kv_seq=None):
+    B = len(q_lens)
+    return W.make_case(f"paged_prefill_{seed}", seed, batch=B, q_heads=2 * G, kv_heads=2,
+                       head_dim=D, q_lens=list(q_lens), kv_lens=list(kv_lens), q_form="packed",
+                       kv_form="padded", kv_seq=kv_seq or max(kv_lens) + 40, dtype=dtype,
+                       causal=causal,
+                       kv_fp8=W.FP8_KV_SCALES if fp8 else None)
+
+
+@pytest.mark.parametrize("page_size", [32, 64, 96, 128, 256])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_paged_chunked_prefill(page_size, dtype):
+    _parity(W.paged(_chunked(270 + page_size, dtype=dtype), page_size, seed=13))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("page_size", [64, 128])
+def test_paged_prefill_fp8_pools(D, page_size):
+    _parity(W.paged(_chunked(280 + D + page_size, D=D, fp8=True), page_size, seed=14))
+
+
+def test_paged_prefill_self_attention():
+    c = _chunked(290, q_lens=(300, 77, 129), kv_lens=(300, 77, 129), causal="upper_left", G=8)
+    _parity(W.paged(c, 64, seed=15))
+
+
+def test_paged_prefill_identity_pages_match_the_linear_cache_bit_for_bit():
+    ps = 64
+    c = _chunked(295, q_lens=(100, 64, 300), kv_lens=(640, 64, 333), kv_seq=640)
+    B, H, N, D = c.k.shape
+    assert N % ps == 0
+    pools = [t.reshape(B, H, N // ps, ps, D).permute(0, 2, 1, 3, 4).reshape(B * N // ps, H, ps, D)
+             .contiguous() for t in (c.k, c.v)]
+    table = torch.arange(B * N // ps, dtype=torch.int32).reshape(B, 1, N // ps).repeat(1, 2, 1)
+    pc = dataclasses.replace(c, k=pools[0], v=pools[1], kv_form=W.PAGED, page_table=table)
+    y_lin, _, st1 = run_gpu(c)
+    y_pag, _, st2 = run_gpu(pc)
+    assert binding.device_status(st1) == 0 and binding.device_status(st2) == 0
+    assert np.array_equal(y_lin.view(np.int64), y_pag.view(np.int64))
+
+
+def test_paged_prefill_page_outside_the_pools_sets_status():
+    c = W.paged(_chunked(297), 64, seed=16)
+    for bad in (-1, c.k.shape[0]):
+        t = c.page_table.clone()
+        t[4, 0, 9] = bad          # K page of keys 576..639 of sequence 4 (1000 keys)
+        y, raw, st = run_gpu(dataclasses.replace(c, page_table=t))
+        assert binding.device_status(st) == 4
+        assert (raw == np.int16(SENTINEL)).all()

@@ -1,4 +1,4 @@
-"""The named workloads (2 to 7) at full size, run on the GPU exactly as the
+"""The named workloads (2 to 10) at full size, run on the GPU exactly as the
 benchmark launches them; the oracle checks sampled (batch, KV head) pairs
 (each one a complete sub-problem it can finish in seconds), and every row
 outside the sequences is checked for its sentinel bits."""
@@ -32,10 +32,17 @@ def sub_problem(c: W.Case, b: int, g: int):
     else:
         q = c.q[b:b + 1, hs]
         qlen = torch.tensor([0, ql], dtype=torch.int32)
+    kv_form = c.kv_form
     if c.kv_form == W.PACKED:
         ko = int(c.kv_lengths[b])
         k, v = c.k[ko:ko + kl, g:g + 1], c.v[ko:ko + kl, g:g + 1]
         klen = torch.tensor([0, kl], dtype=torch.int32)
+    elif c.kv_form == W.PAGED:   # sequence b's pages gathered into a linear cache
+        t = c.page_table[b:b + 1]
+        k = oracle.gather_pages(c.k, t, 0, [kl])[:, g:g + 1]
+        v = oracle.gather_pages(c.v, t, 1, [kl])[:, g:g + 1]
+        klen = torch.tensor([kl], dtype=torch.int32)
+        kv_form = W.PADDED
     else:
         k, v = c.k[b:b + 1, g:g + 1], c.v[b:b + 1, g:g + 1]
         klen = torch.tensor([kl], dtype=torch.int32)
@@ -45,7 +52,7 @@ def sub_problem(c: W.Case, b: int, g: int):
         m = m[b:b + 1] if m.shape[0] > 1 else m
         m = m[:, hs] if m.shape[1] > 1 else m
         mask = m
-    return oracle.attention(q, k, v, q_form=c.q_form, kv_form=c.kv_form, query_lengths=qlen,
+    return oracle.attention(q, k, v, q_form=c.q_form, kv_form=kv_form, query_lengths=qlen,
                             kv_lengths=klen, mask=mask, scale=c.scale, causal=c.causal,
                             norm=c.norm, quant=c.quant, quant_scale=c.quant_scale,
                             ambiguity_eps=AMBIGUITY_EPS if c.quant else None,
@@ -68,7 +75,8 @@ def ref_rows(c: W.Case, yref, b):
     return yref[:, :, :c.q_lens[b]]
 
 
-CASES = [(2, None), (3, None), (4, None), (5, "fp8"), (5, "int8"), (6, None), (7, None)]
+CASES = [(2, None), (3, None), (4, None), (5, "fp8"), (5, "int8"), (6, None), (7, None), (8, None),
+         (9, None), (10, None)]
 
 
 @pytest.mark.parametrize("index,quant", CASES, ids=[f"w{i}-{q}" for i, q in CASES])
