@@ -160,7 +160,8 @@ rga_status trt_quantized_attention(const rga_attention_args *args,
                                    cudaStream_t stream);
 
 /* Attention over an FP8 KV cache ("TensorRT Plugins Guide",
- * AttentionPlugin: kv_cache_type FP8, vanilla and tree decoding).  Same as
+ * AttentionPlugin: kv_cache_type FP8; prefill, chunked prefill, vanilla and
+ * tree decoding).  Same as
  * trt_attention, except that args->k and args->v hold OCP E4M3FN codes (one
  * byte per element, same shapes and forms as there) and the keys and values
  * attended are
@@ -169,11 +170,11 @@ rga_status trt_quantized_attention(const rga_attention_args *args,
  * float each, required).  args->dtype is the type of q and y (F16 or BF16);
  * k and v must be 16-byte aligned.  The codes past a sequence's kv length
  * may hold any bits, NaN codes included.
- * Supported for decode shapes: q_heads / kv_heads <= 16 and either padded q
- * with q_seq * (q_heads / kv_heads) <= 16 or packed q with q_seq <= 8 *
- * batch (one token per sequence, or up to 8 draft tokens per sequence on
- * average for tree decoding with a bool mask).  Other shapes return
- * RGA_ERR_UNSUPPORTED.  Workspace:
+ * Every shape and option of trt_attention: decode shapes (q_heads /
+ * kv_heads <= 16 and either padded q with q_seq * (q_heads / kv_heads) <=
+ * 16 or packed q with q_seq <= 8 * batch) run on the split-KV decode
+ * kernel, every other shape on the prefill kernel, which expands each tile
+ * of codes to 16-bit values in shared memory.  Workspace:
  * rga_attention_workspace_size(args) bytes. */
 rga_status trt_attention_fp8_kv(const rga_attention_args *args, const float *k_scale,
                                 const float *v_scale, cudaStream_t stream);
@@ -209,9 +210,10 @@ typedef struct {
  * (device int32 [batch]) is required, and args->kv_seq is ignored (a
  * sequence may hold up to max_pages_per_seq * page_size keys; a mask's key
  * dimension is 1 or at least every sequence's length, checked on the
- * device).  Decode
- * shapes as for trt_attention_fp8_kv; other shapes return
- * RGA_ERR_UNSUPPORTED.  A page index outside [0, num_pages) among a
+ * device).  Every shape, as for trt_attention_fp8_kv (the prefill kernel
+ * loads a 128-key tile as boxes of 128, 64 or 32 rows, the largest that
+ * divides page_size, each inside one page).  A page index outside
+ * [0, num_pages) among a
  * sequence's pages sets *device_status to RGA_ERR_DEVICE_LENGTHS and leaves
  * Y untouched, as bad lengths do.  Workspace: rga_attention_workspace_size
  * of the same args with kv_seq = max_pages_per_seq * page_size. */
