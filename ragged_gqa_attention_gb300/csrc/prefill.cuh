@@ -258,39 +258,58 @@ __device__ __forceinline__ int tile_page(const AttnParams &p, const Item &m, int
 }
 
 // Key tile j0 of K (which = 0) or V (which = 1) into dst, every copy
-// completing on `bar` (whose transaction count lane 0 sets to `bytes`).
-// 16-bit: NBLK boxes of 64 columns x 128 rows, 128-byte swizzled; KV8: one
-// box of D bytes x 128 rows, unswizzled.  A paged cache takes the tile as
-// BN / pr boxes of pr rows, each inside one page.  The whole warp calls it.
-template <int D, bool KV8>
+// completing on `bar` (whose transaction count is set to `bytes`).  16-bit:
+// NBLK boxes of 64 columns x 128 rows, 128-byte swizzled; KV8: one box of D
+// bytes x 128 rows, unswizzled.  A paged cache takes the tile as BN / pr
+// boxes of pr rows, each inside one page, whose page ids the warp's lanes
+// read together.  The whole warp calls it; lane 0 issues.  (The producer's
+// issue latency is on the pipeline's critical path: a linear tile is two or
+// three instructions from lane 0, with no shuffles.)
+template <int D, bool KV8, bool PAGED>
 __device__ __forceinline__ void load_kv_tile(const AttnParams &p, const CUtensorMap *map,
                                              const Item &m, int which, int j0, uint8_t *dst,
                                              uint64_t *bar, uint32_t bytes) {
     using L = PfLayout<D, KV8>;
     const int lane = threadIdx.x & 31;
-    const int pr = p.paged ? pf_page_rows(p.page_size) : BN;
-    const int pg = p.paged ? tile_page(p, m, which, j0, pr) : 0;
-    if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-    for (int i = 0; i < BN / pr; ++i) {
-        const int page = __shfl_sync(0xffffffffu, pg, i);
-        if (lane != 0) continue;
-        const int key = j0 + i * pr;
-        if (KV8) {
-            uint8_t *d = dst + i * pr * D;
-            if (p.paged) tma_load_4d(d, map, bar, 0, key % p.page_size, m.g, page);
-            else if (p.kv_packed) tma_load_3d(d, map, bar, 0, m.g, m.s.kv_off + key);
-            else tma_load_4d(d, map, bar, 0, key, m.g, m.b);
-        } else {
-            for (int blk = 0; blk < L::NBLK; ++blk) {
-                uint8_t *d = dst + blk * L::BLK + i * pr * 128;
-                if (p.paged) tma_load_4d(d, map, bar, blk * 64, key % p.page_size, m.g, page);
-                else tma_kv(p, map, m, key, d, bar, blk * 64);
+    if (!PAGED) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, bytes);
+            if (KV8) {
+                if (p.kv_packed) tma_load_3d(dst, map, bar, 0, m.g, m.s.kv_off + j0);
+                else tma_load_4d(dst, map, bar, 0, j0, m.g, m.b);
+            } else {
+                for (int blk = 0; blk < L::NBLK; ++blk)
+                    tma_kv(p, map, m, j0, dst + blk * L::BLK, bar, blk * 64);
+            }
+        }
+        return;
+    }
+    const int pr = pf_page_rows(p.page_size);
+    const int mine = tile_page(p, m, which, j0, pr);
+    int pg[BN / 32];
+#pragma unroll
+    for (int i = 0; i < BN / 32; ++i) pg[i] = __shfl_sync(0xffffffffu, mine, i);
+    if (lane == 0) {
+        mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+        for (int i = 0; i < BN / 32; ++i) {
+            if (i * pr >= BN) break;
+            const int key = j0 + i * pr, row = key % p.page_size;
+            if (KV8) {
+                tma_load_4d(dst + i * pr * D, map, bar, 0, row, m.g, pg[i]);
+            } else {
+                for (int blk = 0; blk < L::NBLK; ++blk)
+                    tma_load_4d(dst + blk * L::BLK + i * pr * 128, map, bar, blk * 64, row, m.g,
+                                pg[i]);
             }
         }
     }
 }
 
-template <int D, int MODE, bool KV8>
+// PAGED: K and V come from page pools (both forms are compiled into every
+// kernel and the producer picks one at the start, so the linear form's loop
+// carries no page logic).
+template <int D, int MODE, bool KV8, bool PAGED>
 __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorMaps &tm, uint8_t *sm,
                               const PfBars &bar, volatile int *abort, int n_items) {
     using L = PfLayout<D, KV8>;
@@ -330,10 +349,10 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
             const int ks = kc % L::KST;
             if (kc >= L::KST && !mbar_wait(&bar.k_empty[ks], ((kc / L::KST) - 1) & 1, abort)) break;
             if (KV8)   // bytes for the converter warps
-                load_kv_tile<D, true>(p, &tm.k, m, 0, j0, sm + L::raw_k(ks), &bar.kraw_full[ks],
+                load_kv_tile<D, true, PAGED>(p, &tm.k, m, 0, j0, sm + L::raw_k(ks), &bar.kraw_full[ks],
                                       kv_bytes);
             else
-                load_kv_tile<D, false>(p, &tm.k, m, 0, j0, sm + L::K_OFF + ks * L::TILE,
+                load_kv_tile<D, false, PAGED>(p, &tm.k, m, 0, j0, sm + L::K_OFF + ks * L::TILE,
                                        &bar.k_full[ks], kv_bytes);
             ++kc;
             if (!is_pv<MODE>(m, t)) continue;
@@ -343,14 +362,14 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
             const int rem = m.s.kv_len - j0;
             if (KV8) {
                 // the converter warps zero the rows past the sequence end
-                load_kv_tile<D, true>(p, &tm.v, m, 1, j0, sm + L::raw_v(vs), &bar.vraw_full[vs],
+                load_kv_tile<D, true, PAGED>(p, &tm.v, m, 1, j0, sm + L::raw_v(vs), &bar.vraw_full[vs],
                                       kv_bytes);
             } else if (rem >= BN) {
-                load_kv_tile<D, false>(p, &tm.v, m, 1, j0, vdst, &bar.v_full[vs], kv_bytes);
+                load_kv_tile<D, false, PAGED>(p, &tm.v, m, 1, j0, vdst, &bar.v_full[vs], kv_bytes);
             } else {
                 // the tile runs past the sequence end: land it, clear the
                 // rows past the end, then publish it
-                load_kv_tile<D, false>(p, &tm.v, m, 1, j0, vdst, bar.v_part, kv_bytes);
+                load_kv_tile<D, false, PAGED>(p, &tm.v, m, 1, j0, vdst, bar.v_part, kv_bytes);
                 const bool landed = mbar_wait(bar.v_part, vpc & 1, abort);
                 ++vpc;
                 if (!landed) break;
@@ -943,7 +962,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
     const bool row_indep = bool_mask && p.md[1] == 1 && p.md[2] == 1;
     const int mk = !use_mask || bool_mask ? MK_BITS
                    : p.mask_dtype == 0 ? MK_ADD_F16 : p.mask_dtype == 1 ? MK_ADD_BF16 : MK_ADD_F32;
-    uint32_t tc = 0, pvw = 0;                        // steps seen, BMM2 completions waited
+    uint32_t tc = 0, npv = 0;                        // steps seen; BMM2s of this tile so far
     bool ok = true, pending = false;
 
     for (uint32_t n = 0; ok; ++n) {
@@ -1046,14 +1065,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                         continue;
                     }
                     // pass 2: p / s_q = 2^(s sc - lse2), quantized (0 for an
-                    // excluded key or a row with no key: lse2 is +inf there).
-                    // Take the previous BMM2's completion in turn (it is done:
-                    // S(t) follows it), so that the epilogue's parity wait
-                    // finds exactly the last one outstanding.
-                    if (u > 0) {
-                        if (!mbar_wait(&bar.o_done[a], pvw & 1, abort)) { ok = false; break; }
-                        ++pvw;
-                    }
+                    // excluded key or a row with no key: lse2 is +inf there)
                     const uint64_t neg2 = f2_pack(-lse2, -lse2);
                     p_chunk_q<BF16>(ra[0], s_addr, 0, mul2, neg2, p.quant);
                     p_chunk_q<BF16>(ra[1], s_addr, 1, mul2, neg2, p.quant);
@@ -1119,11 +1131,10 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                 f2_unpack(acc0, s0, s1);
                 f2_unpack(acc1, s2, s3);
                 l += (s0 + s1) + (s2 + s3);
-                if (u > 0) {   // BMM2 of the previous step must be done before O is touched
-                    if (!mbar_wait(&bar.o_done[a], pvw & 1, abort)) { ok = false; break; }
-                    ++pvw;
+                // O holds the earlier BMM2s, all complete: S of this step was
+                // issued after them, and its completion covers them
+                if (u > 0) {
                     if (__any_sync(0xffffffffu, need)) {
-                        tc_fence_after();
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t o[32];
@@ -1270,11 +1281,9 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                 continue;
             }
             if (MODE == MODE_SOFTMAX) l += psum;
-            if (u > 0) {   // BMM2 of the previous step must be done before O is touched
-                if (!mbar_wait(&bar.o_done[a], pvw & 1, abort)) { ok = false; break; }
-                ++pvw;
+            // O holds the earlier BMM2s, all complete (S of this step follows them)
+            if (u > 0) {
                 if (MODE == MODE_SOFTMAX && __any_sync(0xffffffffu, need)) {
-                    tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
@@ -1295,9 +1304,11 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
             ++tc;
         }
         if (!ok) break;
-        // epilogue: after the item's last BMM2
-        if (!mbar_wait(&bar.o_done[a], pvw & 1, abort)) { ok = false; break; }
-        ++pvw;
+        // epilogue: after the item's last BMM2.  o_done completes a phase per
+        // BMM2; every earlier one had completed before the last S did, so
+        // only the last can still be outstanding and its parity is awaited.
+        npv += (MODE == MODE_SOFTMAX_Q) ? m.nkt : m.ntiles;
+        if (!mbar_wait(&bar.o_done[a], (npv - 1) & 1, abort)) { ok = false; break; }
         tc_fence_after();
         float f;
         if (MODE == MODE_SOFTMAX) f = (l > 0.f) ? sv / l : 0.f;
@@ -1377,7 +1388,8 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     } else if (warp == 8) {
         mma_role<D, MODE, BF16>(p, sm, bar, abort, tmem);
     } else if (warp == 9) {
-        producer_role<D, MODE, KV8>(p, tm, sm, bar, abort, n_items);
+        if (p.paged) producer_role<D, MODE, KV8, true>(p, tm, sm, bar, abort, n_items);
+        else producer_role<D, MODE, KV8, false>(p, tm, sm, bar, abort, n_items);
     } else if (KV8) {
         convert_role<D, BF16>(p, sm, bar, abort, warp - 10);
     }
