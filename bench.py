@@ -239,12 +239,46 @@ def device_timed(run, stream, steps, warmup, dist_on, sampler_index=None):
     return times, (sampler.summary() if sampler else None)
 
 
+UPLOAD_STREAMS = 4
+
+
+def h2d_peak_gbs(nbytes=512 << 20, streams=(1, UPLOAD_STREAMS), reps=3):
+    """Best pinned host->device copy rate of this machine (GB/s), one large
+    buffer split evenly over 1 or several copy streams: the link the e2e
+    number is judged against."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = {}
+    for ns in streams:
+        ss = [torch.cuda.Stream() for _ in range(ns)]
+        chunk = nbytes // ns
+        best = 0.0
+        for _ in range(reps):
+            start = torch.cuda.Event(enable_timing=True)
+            ends = [torch.cuda.Event(enable_timing=True) for _ in ss]
+            torch.cuda.synchronize()
+            start.record(ss[0])
+            for i, st in enumerate(ss):
+                st.wait_event(start)
+                with torch.cuda.stream(st):
+                    dst[i * chunk:(i + 1) * chunk].copy_(src[i * chunk:(i + 1) * chunk],
+                                                         non_blocking=True)
+                ends[i].record(st)
+            torch.cuda.synchronize()
+            ms = max(start.elapsed_time(e) for e in ends)
+            best = max(best, nbytes / (ms * 1e-3) / 1e9)
+        out[f"{ns}_stream" + ("s" if ns > 1 else "")] = round(best, 1)
+    del src, dst
+    return out
+
+
 def e2e_timed(case: W.Case, stream, steps, warmup, dist_on):
     """The public call from pinned host buffers, every step: H2D of all its
     inputs, the attention call, D2H of Y.  Steps are pipelined over two sets
-    of device buffers and three streams (uploads, calls, downloads), so that
-    step i+1's upload and step i-1's download overlap step i's call, as a
-    serving loop would run them; each step still moves all its own bytes.
+    of device buffers and streams for uploads (each input split evenly over
+    UPLOAD_STREAMS copy streams), calls and downloads, so that step i+1's
+    upload and step i-1's download overlap step i's call, as a serving loop
+    would run them; each step still moves all its own bytes.
     Returns (ms per step over the timed steps, bytes in, bytes out)."""
     host = {}
     for name in ("q", "k", "v", "query_lengths", "kv_lengths", "mask", "quant_scale",
@@ -264,23 +298,42 @@ def e2e_timed(case: W.Case, stream, steps, warmup, dist_on):
         run = Runner(W.Case(**{**case.__dict__, **fields}), stream)
         y_host = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
         sets.append((dev, run, y_host))
-    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ups = [torch.cuda.Stream() for _ in range(UPLOAD_STREAMS)]
+    up = ups[0]
+    down = torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
-    uploaded, computed, downloaded = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    uploaded = [[ev() for _ in ups], [ev() for _ in ups]]
+    computed, downloaded = [ev(), ev()], [ev(), ev()]
     used = [False, False]
+    # each input in UPLOAD_STREAMS contiguous byte ranges, one per copy stream
+    parts = {}
+    for n, t in host.items():
+        if t is None:
+            continue
+        nb = t.numel() * t.element_size()
+        cut = [(nb * k // UPLOAD_STREAMS) // 16 * 16 for k in range(UPLOAD_STREAMS)] + [nb]
+        parts[n] = cut
 
     def step(i):
         b = i % 2
         dev, run, y_host = sets[b]
         if used[b]:   # buffers b were last used by step i-2
-            up.wait_event(computed[b])
+            for u in ups:
+                u.wait_event(computed[b])
             stream.wait_event(downloaded[b])
-        with torch.cuda.stream(up):
-            for n, t in host.items():
-                if t is not None:
-                    dev[n].copy_(t, non_blocking=True)
-            uploaded[b].record(up)
-        stream.wait_event(uploaded[b])
+        for k, u in enumerate(ups):
+            with torch.cuda.stream(u):
+                for n, t in host.items():
+                    if t is None:
+                        continue
+                    lo, hi = parts[n][k], parts[n][k + 1]
+                    if hi > lo:
+                        dst = dev[n].view(-1).view(torch.uint8)
+                        src = t.view(-1).view(torch.uint8)
+                        dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+                uploaded[b][k].record(u)
+        for k in range(len(ups)):
+            stream.wait_event(uploaded[b][k])
         with torch.cuda.stream(stream):
             run()
             computed[b].record(stream)
@@ -296,6 +349,8 @@ def e2e_timed(case: W.Case, stream, steps, warmup, dist_on):
     barrier(dist_on)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(up)
+    for u in ups[1:]:
+        u.wait_event(t0)
     for i in range(warmup, warmup + steps):
         step(i)
     last = (warmup + steps - 1) % 2
@@ -503,6 +558,7 @@ def main():
                    clocks=True)
     case = head["case"]
     e2e_step_ms, bi, bo = e2e_timed(case, stream, max(3, args.steps // 2), 3, dist_on)
+    h2d_peak = h2d_peak_gbs()
     e2e_ms = max_over_ranks(e2e_step_ms, dist_on)
     scale = 1e12 if head["unit"] == "TFLOP/s" else 1e9
     e2e_val = head["work"] / (e2e_ms * 1e-3) / scale
@@ -566,7 +622,9 @@ def main():
                                  "call (scheduler + attention kernel)"},
             "e2e": {"value": round(e2e_val * world, 3), "unit": head["unit"],
                     "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-                    "ms_per_step": round(e2e_ms, 4)},
+                    "ms_per_step": round(e2e_ms, 4),
+                    "h2d_gbs_achieved": round(bi / (e2e_ms * 1e-3) / 1e9, 1),
+                    "h2d_peak_gbs": h2d_peak, "upload_streams": UPLOAD_STREAMS},
             "gpu_launches": head["launches_per_step"] * args.steps,
             "clocks": head["clocks"],
             "cpu_baseline": cpu,

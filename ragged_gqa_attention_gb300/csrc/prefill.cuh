@@ -107,10 +107,13 @@ struct PfLayout {
     static constexpr int BAR_OFF = RAW_OFF + (RAW_SEP ? (KST + VST) * RAW_TILE : 0);
     // barriers: q_full, q_empty, k_full[KST], k_empty[KST], v_full[VST],
     // v_empty[VST], s_full[2], p_full[2], o_done[2], v_part,
-    // item_full[IRING], item_empty[IRING], kraw_full[KST], vraw_full[VST]
-    static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 7 + 2 * IRING + KST + VST;
+    // item_full[IRING], item_empty[IRING], kraw_full[KST], vraw_full[VST],
+    // q_conv
+    static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 7 + 2 * IRING + KST + VST + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    // misc: TMEM address (+0), abort flag (+8), item ring (+64)
+    // misc: TMEM address (+0), abort flag (+8), the Q tiles' score factors
+    // 2^s (+16, +20; FP8 cache with bf16 queries), the converter warps' Q
+    // maxima (+24..+39), item ring (+64)
     static constexpr int RING_OFF = 64;
     static constexpr int BYTES = MISC_OFF + 256;
     // room to align the base to 1024; at least 120 KB so that only one CTA
@@ -128,7 +131,7 @@ struct PfLayout {
 
 struct PfBars {
     uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full,
-        *o_done, *v_part, *item_full, *item_empty, *kraw_full, *vraw_full;
+        *o_done, *v_part, *item_full, *item_empty, *kraw_full, *vraw_full, *q_conv;
     Item *ring;   // IRING items
 };
 
@@ -151,6 +154,7 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *base) {
     r.item_empty = r.item_full + IRING;
     r.kraw_full = r.item_empty + IRING;
     r.vraw_full = r.kraw_full + L::KST;
+    r.q_conv = r.vraw_full + L::VST;
     static_assert(L::RING_OFF + IRING * sizeof(Item) <= 256, "item ring fits the misc area");
     r.ring = reinterpret_cast<Item *>(base + (L::MISC_OFF - L::BAR_OFF) + L::RING_OFF);
     return r;
@@ -430,33 +434,116 @@ __device__ __forceinline__ void expand_tile(const uint8_t *raw, uint8_t *dst, in
     }
 }
 
+// Largest finite |x| of a converter warp's rows (64 of 128) of a bf16 Q tile,
+// as bf16 magnitude bits (non-finite values, such as NaN padding rows, are
+// left out).  Lane l reads 16-byte chunks l, l + 32, ... of the rows.
+template <int D>
+__device__ __forceinline__ uint32_t q_tile_max(const uint8_t *tile, int w) {
+    constexpr int CHUNKS = 64 * D * 2 / 16;    // 16-byte chunks in 64 rows
+    const int lane = threadIdx.x & 31;
+    uint32_t mx = 0;
+    for (int c = lane; c < CHUNKS; c += 32) {
+        // row r = 64 w + c / (D / 8) lies in 64-column block (c % (D/8)) / 8
+        const int r = 64 * w + c / (D / 8), cc = c % (D / 8);
+        const uint4 v = *reinterpret_cast<const uint4 *>(tile + (cc / 8) * PfLayout<D>::BLK +
+                                                         r * 128 + (cc % 8) * 16);
+        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                const uint32_t m16 = (ws[k] >> (16 * hlf)) & 0x7fffu;
+                if ((m16 & 0x7f80u) != 0x7f80u && m16 > mx) mx = m16;
+            }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    return mx;
+}
+
+// Power-of-two exponent s that puts the largest |q| (bf16 bits m16) in
+// [2^14, 2^15): every component above 2^-28 of it is then an exact f16.
+__device__ __forceinline__ int q_shift(uint32_t m16) {
+    if (m16 == 0) return 0;
+    const int e = (int)(m16 >> 7) - 127;       // floor(log2) of a normal bf16 (subnormal: -127)
+    const int sft = 14 - e;
+    return sft > 126 ? 126 : sft;
+}
+
+// In place: the converter warp's rows of a bf16 Q tile become f16 values of
+// q * 2^s (elementwise on 16-byte chunks, so the 128-byte swizzle is kept).
+template <int D>
+__device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int w, float scale) {
+    constexpr int CHUNKS = 64 * D * 2 / 16;
+    const int lane = threadIdx.x & 31;
+    for (int c = lane; c < CHUNKS; c += 32) {
+        const int r = 64 * w + c / (D / 8), cc = c % (D / 8);
+        uint4 *ptr = reinterpret_cast<uint4 *>(tile + (cc / 8) * PfLayout<D>::BLK + r * 128 +
+                                               (cc % 8) * 16);
+        uint4 v = *ptr;
+        uint32_t *ws = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(ws[k] << 16) * scale;
+            const float hi = __uint_as_float(ws[k] & 0xffff0000u) * scale;
+            __half2 hh = __floats2half2_rn(lo, hi);
+            ws[k] = *reinterpret_cast<uint32_t *>(&hh);
+        }
+        *ptr = v;
+    }
+}
+
 // Converter warp w (0 or 1) of an FP8 KV cache: follows the producer's K and
 // V tiles item by item, expands each landed byte tile (each warp half the
-// rows) and publishes it to the tensor core (k_full / v_full take one
-// arrival per converter warp).  V rows past the sequence end become zeros
-// (their codes may be NaN, and 0 * NaN would reach O).
-template <int D, bool BF16>
+// rows) into OPB (bf16) or f16 values and publishes it to the tensor core
+// (k_full / v_full take one arrival per converter warp).  V rows past the
+// sequence end become zeros (their codes may be NaN, and 0 * NaN would reach
+// O).  QCONV (softmax with bf16 queries): the tensor core then multiplies in
+// f16, so once per item the warps also turn both bf16 Q tiles into f16 in
+// place, each scaled by a power of two 2^s chosen from the tile's largest
+// finite |q|; 2^-s goes to shared memory for the softmax's score scale, and
+// q_conv (one arrival per converter warp) publishes the tiles.
+template <int D, bool OPB, bool QCONV>
 __device__ __forceinline__ void convert_role(const AttnParams &p, uint8_t *sm, const PfBars &bar,
                                              volatile int *abort, int w) {
     using L = PfLayout<D, true>;
     const int lane = threadIdx.x & 31;
-    uint32_t kc = 0, vc = 0;
+    float *qf = reinterpret_cast<float *>(sm + L::MISC_OFF + 16);
+    uint32_t *qmax = reinterpret_cast<uint32_t *>(sm + L::MISC_OFF + 24);   // [warp][tile]
+    uint32_t kc = 0, vc = 0, qc = 0;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
         Item m;
         if (!next_item(bar, n, abort, true, m)) break;
+        if (QCONV && m.nkt > 0) {
+            if (!mbar_wait(bar.q_full, qc & 1, abort)) break;
+            ++qc;
+            for (int a = 0; a < 2; ++a) {
+                const uint32_t mx = q_tile_max<D>(sm + L::Q_OFF + a * L::TILE, w);
+                if (lane == 0) qmax[w * 2 + a] = mx;
+            }
+            asm volatile("bar.sync 7, 64;" ::: "memory");   // both converter warps
+            for (int a = 0; a < 2; ++a) {
+                const int sft = q_shift(max(qmax[a], qmax[2 + a]));
+                q_tile_to_f16<D>(sm + L::Q_OFF + a * L::TILE, w, ldexpf(1.f, sft));
+                if (w == 0 && lane == 0) qf[a] = ldexpf(1.f, -sft);
+            }
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 7, 64;" ::: "memory");   // the maxima are read; Q is written
+            if (lane == 0) mbar_arrive(bar.q_conv);
+        }
         for (int t = 0; t < m.ntiles; ++t) {
             const int ks = kc % L::KST;
             if (!mbar_wait(&bar.kraw_full[ks], (kc / L::KST) & 1, abort)) { ok = false; break; }
-            expand_tile<D, BF16>(sm + L::raw_k(ks), sm + L::K_OFF + ks * L::TILE, BN, w);
+            expand_tile<D, OPB>(sm + L::raw_k(ks), sm + L::K_OFF + ks * L::TILE, BN, w);
             fence_proxy_async_smem();   // the tensor core reads what the generic proxy wrote
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.k_full[ks]);
             ++kc;
             const int vs = vc % L::VST;
             if (!mbar_wait(&bar.vraw_full[vs], (vc / L::VST) & 1, abort)) { ok = false; break; }
-            expand_tile<D, BF16>(sm + L::raw_v(vs), sm + L::V_OFF + vs * L::TILE,
-                                 m.s.kv_len - t * BN, w);
+            expand_tile<D, OPB>(sm + L::raw_v(vs), sm + L::V_OFF + vs * L::TILE,
+                                m.s.kv_len - t * BN, w);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.v_full[vs]);
@@ -477,12 +564,14 @@ __device__ __forceinline__ void convert_role(const AttnParams &p, uint8_t *sm, c
 // additions of constants, and the barriers the next step starts with (P_0
 // and the V tile) are tested before the last MMA of S_1, while the queued
 // MMAs still keep the pipe busy.
-template <int D, int MODE, bool BF16>
+// OPB: the products' operand type is bf16 (else f16).  QCONV: the Q tiles
+// are ready when the converter warps have turned them into f16 (q_conv).
+template <int D, int MODE, bool OPB, bool QCONV>
 __device__ __forceinline__ void mma_role(const AttnParams &p, uint8_t *sm, const PfBars &bar,
                          volatile int *abort, uint32_t tmem) {
     using L = PfLayout<D>;
-    constexpr uint32_t ID_S = idesc_f16(BF16 ? 1 : 0, 128, BN, 0, 0);   // Q K-major, K K-major
-    constexpr uint32_t ID_O = idesc_f16(BF16 ? 1 : 0, 128, D, 0, 1);    // P from TMEM, V MN-major
+    constexpr uint32_t ID_S = idesc_f16(OPB ? 1 : 0, 128, BN, 0, 0);   // Q K-major, K K-major
+    constexpr uint32_t ID_O = idesc_f16(OPB ? 1 : 0, 128, D, 0, 1);    // P from TMEM, V MN-major
     constexpr int NS = D / 16;      // MMAs of one BMM1 (16 of the head dimension each)
     constexpr int NO = BN / 16;     // MMAs of one BMM2 (16 keys each)
     // A descriptor's start-address field holds addr >> 4, so a byte offset
@@ -517,7 +606,7 @@ __device__ __forceinline__ void mma_role(const AttnParams &p, uint8_t *sm, const
         Item m;
         if (!next_item(bar, n, abort, true, m)) break;
         if (m.nkt == 0) continue;
-        if (!wwait(bar.q_full, qc & 1, abort)) break;
+        if (!wwait(QCONV ? bar.q_conv : bar.q_full, qc & 1, abort)) break;
         ++qc;
         // S0(0), S1(0)
         int ks = kc % L::KST;
@@ -944,6 +1033,10 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                                              int n_items, uint32_t tmem, int a, uint8_t *stg) {
     constexpr bool SOFTMAX = (MODE == MODE_SOFTMAX || MODE == MODE_SOFTMAX_Q);
     constexpr bool QUANT = (MODE == MODE_SOFTMAX_Q || MODE == MODE_NONE_Q);
+    // P's type for BMM2, and whether the converter warps scale Q (FP8 cache,
+    // softmax, bf16 queries: the products run in f16)
+    constexpr bool OPB = BF16 && !(KV8 && MODE == MODE_SOFTMAX);
+    constexpr bool QCONV = KV8 && BF16 && MODE == MODE_SOFTMAX;
     const int r = threadIdx.x & 127;                 // row = TMEM lane
     const uint32_t lane_base = (uint32_t)((r & ~31) << 16);
     const uint32_t s_addr = tmem + lane_base + S_COL0 + a * 128;
@@ -955,7 +1048,9 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
     const float qs = QUANT ? load_qscale(p) : 1.f;
     const float inv_qs = 1.f / qs;
     // score scale; an FP8 cache folds s_k into it and s_v into the epilogue
-    const float sc = (SOFTMAX ? p.scale_log2 : p.scale) * (KV8 ? __ldg(p.k_scale) : 1.f);
+    const float sc0 = (SOFTMAX ? p.scale_log2 : p.scale) * (KV8 ? __ldg(p.k_scale) : 1.f);
+    float sc = sc0;   // per item: times 2^-s of the tile's Q scaling (QCONV)
+    uint32_t qcv = 0;
     const float sv = KV8 ? __ldg(p.v_scale) : 1.f;
     const bool use_mask = p.mask != nullptr;
     const bool bool_mask = use_mask && p.mask_dtype == 3;
@@ -975,6 +1070,13 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
         if (m.nkt == 0) {                            // no attendable key: the rows are zero
             store_rows<D, BF16>(p, tm, m, a, 0, 0.f, true, stg, pending);
             continue;
+        }
+        if (QCONV) {   // this tile's Q scaling, once the converter warps are done
+            if (!mbar_wait(bar.q_conv, qcv & 1, abort)) { ok = false; break; }
+            ++qcv;
+            sc = sc0 * reinterpret_cast<const volatile float *>(
+                           reinterpret_cast<const uint8_t *>(bar.q_full) +
+                           (PfLayout<D, KV8>::MISC_OFF - PfLayout<D, KV8>::BAR_OFF) + 16)[a];
         }
         const int lim = row_ok ? min(causal_limit(p.causal, i, m.s), m.s.kv_len - 1) : -1;
         const int lim_first = min(causal_limit(p.causal, m.i0 + a * TQ, m.s), m.s.kv_len - 1);
@@ -1067,10 +1169,10 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                     // pass 2: p / s_q = 2^(s sc - lse2), quantized (0 for an
                     // excluded key or a row with no key: lse2 is +inf there)
                     const uint64_t neg2 = f2_pack(-lse2, -lse2);
-                    p_chunk_q<BF16>(ra[0], s_addr, 0, mul2, neg2, p.quant);
-                    p_chunk_q<BF16>(ra[1], s_addr, 1, mul2, neg2, p.quant);
-                    p_chunk_q<BF16>(rb[0], s_addr, 2, mul2, neg2, p.quant);
-                    p_chunk_q<BF16>(rb[1], s_addr, 3, mul2, neg2, p.quant);
+                    p_chunk_q<OPB>(ra[0], s_addr, 0, mul2, neg2, p.quant);
+                    p_chunk_q<OPB>(ra[1], s_addr, 1, mul2, neg2, p.quant);
+                    p_chunk_q<OPB>(rb[0], s_addr, 2, mul2, neg2, p.quant);
+                    p_chunk_q<OPB>(rb[1], s_addr, 3, mul2, neg2, p.quant);
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(&bar.p_full[a]);
@@ -1087,15 +1189,15 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                 const float ref0 = (row_ok && m_ref != -INFINITY) ? m_ref : 0.f;
                 uint64_t neg2 = f2_pack(-ref0, -ref0);
                 uint64_t acc0 = 0, acc1 = 0;
-                p_chunk<BF16>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
-                p_chunk<BF16>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1);
+                p_chunk<OPB>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
+                p_chunk<OPB>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1);
                 tmem_wait_ld();
                 if (!lim_full) {
                     mask_after(rb[0], rem - 64);
                     mask_after(rb[1], rem - 96);
                 }
-                p_chunk<BF16>(rb[0], s_addr, 2, mul2, neg2, acc0, acc1);
-                p_chunk<BF16>(rb[1], s_addr, 3, mul2, neg2, acc0, acc1);
+                p_chunk<OPB>(rb[0], s_addr, 2, mul2, neg2, acc0, acc1);
+                p_chunk<OPB>(rb[1], s_addr, 3, mul2, neg2, acc0, acc1);
                 // No probability can pass 2^threshold while their sum stays
                 // below it, so the row max is only needed (to decide on a
                 // new reference) when the sum is that large.
@@ -1122,10 +1224,10 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                     const float ref1 = row_ok ? m_ref : 0.f;
                     neg2 = f2_pack(-ref1, -ref1);
                     acc0 = acc1 = 0;
-                    p_chunk<BF16>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
-                    p_chunk<BF16>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1);
-                    p_chunk<BF16>(rb[0], s_addr, 2, mul2, neg2, acc0, acc1);
-                    p_chunk<BF16>(rb[1], s_addr, 3, mul2, neg2, acc0, acc1);
+                    p_chunk<OPB>(ra[0], s_addr, 0, mul2, neg2, acc0, acc1);
+                    p_chunk<OPB>(ra[1], s_addr, 1, mul2, neg2, acc0, acc1);
+                    p_chunk<OPB>(rb[0], s_addr, 2, mul2, neg2, acc0, acc1);
+                    p_chunk<OPB>(rb[1], s_addr, 3, mul2, neg2, acc0, acc1);
                 }
                 float s0, s1, s2, s3;
                 f2_unpack(acc0, s0, s1);
@@ -1257,7 +1359,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                             pb = int8_round(pb);
                         }
                     }
-                    w[k] = pack2<BF16>(pa, pb);
+                    w[k] = pack2<OPB>(pa, pb);
                 }
                 if (!stat) tmem_st16(s_addr + c * 16, w);
             }
@@ -1354,6 +1456,7 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
             mbar_init(&bar.o_done[s], 1);
         }
         mbar_init(bar.v_part, 1);
+        mbar_init(bar.q_conv, 2);   // one arrival per converter warp
         for (int s = 0; s < IRING; ++s) {
             mbar_init(&bar.item_full[s], 1);
             mbar_init(&bar.item_empty[s], ITEM_CONSUMERS + (KV8 ? 2 : 0));
@@ -1386,12 +1489,14 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
     }
     if (warp < 8) {
     } else if (warp == 8) {
-        mma_role<D, MODE, BF16>(p, sm, bar, abort, tmem);
+        mma_role<D, MODE, BF16 && !(KV8 && MODE == MODE_SOFTMAX), KV8 && BF16 && MODE == MODE_SOFTMAX>(
+            p, sm, bar, abort, tmem);
     } else if (warp == 9) {
         if (p.paged) producer_role<D, MODE, KV8, true>(p, tm, sm, bar, abort, n_items);
         else producer_role<D, MODE, KV8, false>(p, tm, sm, bar, abort, n_items);
     } else if (KV8) {
-        convert_role<D, BF16>(p, sm, bar, abort, warp - 10);
+        convert_role<D, BF16 && MODE != MODE_SOFTMAX, BF16 && MODE == MODE_SOFTMAX>(
+            p, sm, bar, abort, warp - 10);
     }
 
     tc_fence_before();

@@ -182,11 +182,14 @@ def test_prefill_scales_of_other_magnitudes():
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-def test_prefill_matches_16bit_path_bit_for_bit(dtype):
+def test_prefill_matches_16bit_path_on_exact_values(dtype):
     """Power-of-two scales make every dequantised value a 16-bit value, and
-    scaling by a power of two commutes with every rounding on the way: the
-    prefill kernel over the codes computes exactly what it computes over the
-    dequantised 16-bit cache."""
+    scaling by a power of two commutes with every rounding on the way.  With
+    f16 queries the prefill kernel over the codes computes exactly what it
+    computes over the dequantised 16-bit cache (bit for bit).  With bf16
+    queries the softmax's products run in f16 over a cache of codes (Q
+    scaled by a power of two, P rounded to f16 rather than bf16), so the two
+    agree to P's rounding."""
     c = _prefill_case(370, dtype=dtype, scales=(1.0 / 64.0, 1.0 / 32.0))
     y8, _, st = run_gpu(c)
     assert binding.device_status(st) == 0
@@ -197,4 +200,8 @@ def test_prefill_matches_16bit_path_bit_for_bit(dtype):
     assert binding.device_status(st) == 0
     rows = np.isfinite(y16)
     assert np.array_equal(np.isfinite(y8), rows)
-    assert np.array_equal(y8[rows], y16[rows])
+    if dtype == torch.float16:
+        assert np.array_equal(y8[rows], y16[rows])
+    else:   # P's rounding, and one bf16 ulp of the output where it falls differently
+        d = np.abs(y8[rows] - y16[rows])
+        assert (d <= 4e-3 + 2.0 ** -7 * np.abs(y16[rows])).all(), d.max()
