@@ -169,6 +169,10 @@ cudaError_t launch_prefill_kv8_typed(const AttnParams &p, const TensorMaps &m, i
                                      cudaStream_t s);
 cudaError_t launch_prefill(const AttnParams &p, const TensorMaps &m, int mode, int grid,
                            cudaStream_t s, int bf16, int kv8);
+// Decode over a 16-bit cache with several 16-row chunks per (batch, KV
+// head) (tree decoding): warps in groups of four sharing each K/V tile.
+cudaError_t launch_decode_group(const AttnParams &p, const TensorMaps &m, int mode,
+                                cudaStream_t s, int bf16);
 cudaError_t launch_decode(const AttnParams &p, const TensorMaps &m, int mode,
                           cudaStream_t s, int bf16, int kv8);
 

@@ -304,6 +304,46 @@ def test_tree_decoding(G, dtype):
     _parity(c)
 
 
+@pytest.mark.parametrize("shape", ["rounds", "partial_round", "long", "d64_none", "padded_q"])
+def test_grouped_decode(shape):
+    """More than two 16-row chunks per (batch, KV head) on average: warps in
+    groups of four share each K/V tile (one chunk each), units with more than
+    four chunks take several rounds, and units cut by the groups' ranges are
+    merged from partials."""
+    from helpers import tree_mask
+    D, dtype, norm, q_form = 128, torch.bfloat16, "softmax", "packed"
+    if shape == "rounds":          # 16 x 8 = 128 rows: 8 chunks, two rounds
+        G, T, cache = 16, 8, [40, 700, 129]
+    elif shape == "partial_round":   # 8 x 5 = 40 rows: 3 chunks, the last half full
+        G, T, cache = 8, 5, [0, 333, 1025, 64]
+    elif shape == "long":          # few units over long caches: ranges cut them
+        G, T, cache = 8, 8, [3900, 2500]
+    elif shape == "d64_none":
+        G, T, cache, D, dtype, norm = 8, 8, [100, 517, 31], 64, torch.float16, "none"
+    else:
+        G, T, cache, q_form = 8, 6, [77, 640, 1], "padded"
+    B = len(cache)
+    N = max(cache) + T + 5
+    kw = dict(q_seq=T, pass_query_lengths=True) if q_form == "padded" else {}
+    c = W.make_case(f"grp_{shape}", 60 + len(shape), batch=B, q_heads=2 * G, kv_heads=2,
+                    head_dim=D, q_lens=[T] * B, kv_lens=[x + T for x in cache], q_form=q_form,
+                    kv_form="padded", kv_seq=N, dtype=dtype, norm=norm,
+                    scale=0.002 if norm == "none" else None, mask=tree_mask(B, T, N, cache), **kw)
+    _parity(c)
+
+
+def test_grouped_decode_paged():
+    from helpers import tree_mask
+    B, T, G = 3, 8, 8
+    cache = [40, 1500, 129]
+    N = max(cache) + T + 5
+    c = W.make_case("grp_paged", 77, batch=B, q_heads=2 * G, kv_heads=2, head_dim=128,
+                    q_lens=[T] * B, kv_lens=[x + T for x in cache], q_form="packed",
+                    kv_form="padded", kv_seq=N, dtype=torch.bfloat16,
+                    mask=tree_mask(B, T, N, cache))
+    _parity(W.paged(c, 64, seed=17))
+
+
 # --------------------------------------------------------------------------
 # degenerate shapes and device-side length errors
 # --------------------------------------------------------------------------
