@@ -45,7 +45,9 @@ typedef enum {
     RGA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
     RGA_ERR_DEVICE_LENGTHS = 4,  /* device-side: inconsistent length inputs */
     RGA_ERR_TIMEOUT = 5,         /* device-side: a bounded wait ran out */
-    RGA_ERR_WORKSPACE = 6        /* workspace missing or too small */
+    RGA_ERR_WORKSPACE = 6,       /* workspace missing or too small */
+    RGA_ERR_DEBUG_BOUNDS = 7     /* device-side, debug-checks builds only: an access
+                                    outside its tensor was caught and skipped */
 } rga_status;
 
 /* IO forms (TRT_Attention attributes query_form / kv_form):
@@ -352,6 +354,20 @@ rga_status rga_selftest_wait_timeout(int32_t *device_status, int64_t wait_cycles
  * to out_bf16[c] (device arrays of 256 uint16 each, owned by the caller).
  * Returns RGA_ERR_INVALID_ARG for a null pointer. */
 rga_status rga_selftest_e4m3_decode(uint16_t *out_f16, uint16_t *out_bf16, cudaStream_t stream);
+
+/* Self-test of the debug-checks build (librga_debug.so, built with
+ * RGA_DEBUG_CHECKS).  Its kernels check every TMA start coordinate against
+ * its tensor's extent and every direct global read or write against its
+ * buffer; an access outside is skipped and RGA_ERR_DEBUG_BOUNDS written to
+ * the device status word (a skipped TMA load still completes its
+ * mbarrier's transaction count, so no wait hangs).  This call asks one
+ * thread for a store to element `index` of the device int32 buffer `buf` of
+ * `n` elements through the same check: with index >= n the store is
+ * skipped and *device_status becomes RGA_ERR_DEBUG_BOUNDS; otherwise buf
+ * [index] = 1.  Returns RGA_ERR_UNSUPPORTED in the ordinary build, whose
+ * kernels carry no checks.  Stream-ordered, no synchronisation. */
+rga_status rga_selftest_bounds_check(int32_t *buf, int64_t n, int64_t index,
+                                     int32_t *device_status, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *rga_status_string(rga_status status);

@@ -24,7 +24,7 @@ c_vp, c_size, c_float = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
 RGA_OK = 0
 STATUS_NAMES = {0: "RGA_OK", 1: "RGA_ERR_INVALID_ARG", 2: "RGA_ERR_UNSUPPORTED",
                 3: "RGA_ERR_CUDA", 4: "RGA_ERR_DEVICE_LENGTHS", 5: "RGA_ERR_TIMEOUT",
-                6: "RGA_ERR_WORKSPACE"}
+                6: "RGA_ERR_WORKSPACE", 7: "RGA_ERR_DEBUG_BOUNDS"}
 FORMS = {"padded": 0, "padded_bhnd": 0, "packed": 1, "packed_nhd": 1}
 CAUSAL = {"none": 0, "upper_left": 1, "lower_right": 2}
 NORM = {"softmax": 0, "none": 1}
@@ -38,7 +38,7 @@ EXPORTED = ("rga_attention_workspace_size", "trt_attention", "trt_quantized_atte
             "rga_get_device_status", "rga_status_string", "rga_abi_version",
             "trt_attention_static_scratch", "trt_kv_cache_update", "rga_selftest_wait_timeout",
             "trt_attention_fp8_kv", "rga_selftest_e4m3_decode", "trt_attention_paged_kv",
-            "rga_rope_apply", "trt_kv_cache_update_rope")
+            "rga_rope_apply", "trt_kv_cache_update_rope", "rga_selftest_bounds_check")
 
 
 class Args(ctypes.Structure):
@@ -94,18 +94,25 @@ _lib = None
 _lock = threading.Lock()
 
 
+def debug_checks() -> bool:
+    """RGA_DEBUG_CHECKS=1 in the environment selects librga_debug.so, the
+    build whose kernels check their accesses (status 7 on a violation)."""
+    return os.environ.get("RGA_DEBUG_CHECKS", "0") not in ("", "0")
+
+
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if debug_checks() else _build.LIB_PATH
 
 
 def load(build_if_missing: bool = False):
-    """Load librga.so (optionally building it first)."""
+    """Load librga.so, or librga_debug.so (RGA_DEBUG_CHECKS=1), optionally
+    building it first."""
     global _lib
     with _lock:
         if _lib is None:
             path = library_path()
             if build_if_missing:
-                _build.build()
+                _build.build(debug_checks=debug_checks())
             if not os.path.exists(path):
                 raise RuntimeError(
                     f"the CUDA library {path} is not built; run "
@@ -132,6 +139,8 @@ def load(build_if_missing: bool = False):
             lib.trt_attention_fp8_kv.argtypes = [P, c_vp, c_vp, c_vp]
             lib.rga_selftest_e4m3_decode.restype = c_int
             lib.rga_selftest_e4m3_decode.argtypes = [c_vp, c_vp, c_vp]
+            lib.rga_selftest_bounds_check.restype = c_int
+            lib.rga_selftest_bounds_check.argtypes = [c_vp, c_i64, c_i64, c_vp, c_vp]
             lib.trt_attention_paged_kv.restype = c_int
             lib.trt_attention_paged_kv.argtypes = [P, ctypes.POINTER(PagedKv), c_vp]
             lib.rga_rope_apply.restype = c_int
@@ -344,7 +353,8 @@ def trt_attention_paged_kv(q, k_pool, v_pool, page_table, kv_lengths, *, k_scale
     """Attention over a paged KV cache: pools [num_pages, Hkv, page_size, D]
     (q's dtype, or E4M3 codes with k_scale / v_scale), an int32 page table
     [B, 2, max_pages_per_seq] (K pages, V pages) and per-sequence key counts
-    kv_lengths [B].  Decode shapes only (see include/rga.h)."""
+    kv_lengths [B].  Every shape: decode shapes run the decode kernels,
+    the others the prefill kernel."""
     pk = make_paged(k_pool, v_pool, page_table, k_scale=k_scale, v_scale=v_scale)
     y, st = _call("paged", q, k_pool, v_pool, out, pk, stream, q_form=q_form,
                   kv_form="padded", query_lengths=query_lengths, kv_lengths=kv_lengths,
@@ -364,6 +374,15 @@ def selftest_e4m3_decode(device=None):
     if rc != RGA_OK:
         raise RgaError(rc, "rga_selftest_e4m3_decode")
     return f16, bf16
+
+
+def selftest_bounds_check(buf, index, status, stream=None) -> int:
+    """One store of 1 to element `index` of the int32 CUDA tensor `buf`
+    through the debug-checks build's bounds check (status 7 and no store
+    when index is outside).  Returns the call's status: RGA_ERR_UNSUPPORTED
+    (2) from the ordinary build."""
+    return load().rga_selftest_bounds_check(buf.data_ptr(), buf.numel(), index,
+                                            status.data_ptr(), c_vp(_stream_handle(stream)))
 
 
 def device_status(status, stream=None) -> int:

@@ -403,6 +403,7 @@ const char *rga_status_string(rga_status s) {
     case RGA_ERR_DEVICE_LENGTHS: return "RGA_ERR_DEVICE_LENGTHS";
     case RGA_ERR_TIMEOUT: return "RGA_ERR_TIMEOUT";
     case RGA_ERR_WORKSPACE: return "RGA_ERR_WORKSPACE";
+    case RGA_ERR_DEBUG_BOUNDS: return "RGA_ERR_DEBUG_BOUNDS";
     }
     return "RGA_ERR_UNKNOWN";
 }

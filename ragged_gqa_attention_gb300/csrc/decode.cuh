@@ -106,6 +106,17 @@ __device__ __forceinline__ void dec_tma(const AttnParams &p, const TensorMaps &t
         zk = pk;
         zv = pv;
     }
+    // (debug checks) the tile starts inside the sequence, in the cache or in
+    // pages of the pools; a skipped load still completes its transactions
+    if (!dbg_ok(j0 >= 0 && j0 < s.kv_len && g >= 0 && g < p.Hkv &&
+                (PAGED ? pk >= 0 && pk < p.num_pages && pv >= 0 && pv < p.num_pages
+                       : p.kv_packed ? s.kv_off + j0 < p.kv_seq : j0 < p.kv_seq && b < p.B),
+                p.status)) {
+        const uint32_t bytes = 2 * (KV8 ? DEC_KEYS * D : (D / 64) * DEC_KEYS * 128);
+        mbar_arrive_expect_tx(bar, bytes);
+        mbar_complete_tx(bar, bytes);
+        return;
+    }
     if constexpr (KV8) {   // one box of DEC_KEYS rows x D bytes per tensor
         const int tile = DEC_KEYS * D;
         mbar_arrive_expect_tx(bar, 2 * tile);
@@ -427,6 +438,7 @@ __device__ __forceinline__ void dec_store_y(const AttnParams &p, const DecRow (&
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         if (!rr[r].valid) continue;
+        if (!dbg_ok(rr[r].qoff >= 0 && rr[r].qoff + D <= q_elems(p), p.status)) continue;
         if constexpr (DLAY == DLAY_FP8) {
             constexpr int NO = D / 16;
             uint4 *dst = reinterpret_cast<uint4 *>(y + rr[r].qoff + (D / 8) * (lane >> 2));
@@ -618,6 +630,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
         const int rows = s.q_len * p.G;
         for (int r = lane; r < p.Hkv * rows; r += 32) {
             const DecRow R = dec_row(p, s, b, r / rows, r % rows, rows, 0);
+            if (!dbg_ok(R.qoff >= 0 && R.qoff + D <= q_elems(p), p.status)) continue;
             uint4 *y = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff);
             for (int c = 0; c < D / 8; ++c) y[c] = make_uint4(0, 0, 0, 0);
         }
@@ -709,7 +722,9 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                     const int r0 = rc * DR + 8 * nb;
                     rr[nb][0] = dec_row(p, cc.s, cc.b, g, r0 + 2 * (lane & 3), rows, kv_hi);
                     rr[nb][1] = dec_row(p, cc.s, cc.b, g, r0 + 2 * (lane & 3) + 1, rows, kv_hi);
-                    const DecRow rq = dec_row(p, cc.s, cc.b, g, r0 + (lane >> 2), rows, kv_hi);
+                    DecRow rq = dec_row(p, cc.s, cc.b, g, r0 + (lane >> 2), rows, kv_hi);
+                    rq.valid = rq.valid &&
+                               dbg_ok(rq.qoff >= 0 && rq.qoff + D <= q_elems(p), p.status);
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) {
                         qa[nb][ks][0] = rq.valid ? q32[(rq.qoff >> 1) + 8 * ks + (lane & 3)] : 0u;
@@ -722,7 +737,8 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                 // contraction order of dec_tile8)
                 rr[0][0] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3), rows, kv_hi);
                 rr[0][1] = dec_row(p, cc.s, cc.b, g, rc * DR + 2 * (lane & 3) + 1, rows, kv_hi);
-                const DecRow rq = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2), rows, kv_hi);
+                DecRow rq = dec_row(p, cc.s, cc.b, g, rc * DR + (lane >> 2), rows, kv_hi);
+                rq.valid = rq.valid && dbg_ok(rq.qoff >= 0 && rq.qoff + D <= q_elems(p), p.status);
                 uint32_t w[D / 8];
                 const uint4 *src = reinterpret_cast<const uint4 *>(
                     static_cast<const uint16_t *>(p.q) + rq.qoff + (lane & 3) * (D / 4));
@@ -836,6 +852,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                     const size_t slot = (size_t)wg * 2 + (seg0 == t_begin ? 0 : 1);
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) {
+                        if (!dbg_ok(slot < (size_t)p.dec_slots && DR == p.dec_rows, p.status)) break;
                         dec_store_part<D, DLAY>(part + (slot * DR + 8 * nb) * D, o[nb]);
                         if (lane < 4)
 #pragma unroll
@@ -847,7 +864,8 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                     const int w_lo = warp_of(ps), w_hi = warp_of(pe - 1);
                     const int pidx = ppre[b] + cc.pib;
                     int tk = 0;
-                    if (lane == 0) tk = atomicAdd(&tickets[pidx], 1);
+                    if (lane == 0 && dbg_ok(pidx >= 0 && pidx <= p.max_pairs, p.status))
+                        tk = atomicAdd(&tickets[pidx], 1);
                     tk = __shfl_sync(0xffffffffu, tk, 0);
                     if (tk == w_hi - w_lo) {   // the last of the pair's warps: merge
                         __threadfence();
@@ -890,7 +908,7 @@ decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Tens
                                     acc[4 * k + 3] += x4.w * wt;
                                 }
                             }
-                            if (R.valid) {
+                            if (R.valid && dbg_ok(R.qoff >= 0 && R.qoff + D <= q_elems(p), p.status)) {
                                 const float f = (SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f) * sv;
                                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) +
                                                                        R.qoff + c0 + h * MC);

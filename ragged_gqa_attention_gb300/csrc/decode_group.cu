@@ -146,6 +146,7 @@ decode_group_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const int rows = s.q_len * p.G;
         for (int r = lane; r < p.Hkv * rows; r += 32) {
             const DecRow R = dec_row(p, s, b, r / rows, r % rows, rows, 0);
+            if (!dbg_ok(R.qoff >= 0 && R.qoff + D <= q_elems(p), p.status)) continue;
             uint4 *y = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) + R.qoff);
             for (int c = 0; c < D / 8; ++c) y[c] = make_uint4(0, 0, 0, 0);
         }
@@ -228,7 +229,8 @@ decode_group_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
                 const int r0 = chunk * DR + 8 * nb;
                 rr[nb][0] = dec_row(p, cc.s, cc.b, g, r0 + 2 * (lane & 3), rows, kv_hi);
                 rr[nb][1] = dec_row(p, cc.s, cc.b, g, r0 + 2 * (lane & 3) + 1, rows, kv_hi);
-                const DecRow rq = dec_row(p, cc.s, cc.b, g, r0 + (lane >> 2), rows, kv_hi);
+                DecRow rq = dec_row(p, cc.s, cc.b, g, r0 + (lane >> 2), rows, kv_hi);
+                rq.valid = rq.valid && dbg_ok(rq.qoff >= 0 && rq.qoff + D <= q_elems(p), p.status);
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     qa[nb][ks][0] = rq.valid ? q32[(rq.qoff >> 1) + 8 * ks + (lane & 3)] : 0u;
@@ -302,6 +304,7 @@ decode_group_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
                     const size_t slot = slot_base(vg) + (seg0 == t_begin ? 0 : 1);
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) {
+                        if (!dbg_ok(slot < (size_t)p.dec_slots && p.dec_rows == DR, p.status)) break;
                         dec_store_part<D, DLAY>(part + (slot * DR + 8 * nb) * D, o[nb]);
                         if (lane < 4)
 #pragma unroll
@@ -313,7 +316,8 @@ decode_group_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
                     const int v_lo = group_of(us), v_hi = group_of(ue - 1);
                     const int pidx = ppre[b] + g * cc.nrc + chunk;
                     int tk = 0;
-                    if (lane == 0) tk = atomicAdd(&tickets[pidx], 1);
+                    if (lane == 0 && dbg_ok(pidx >= 0 && pidx <= p.max_pairs, p.status))
+                        tk = atomicAdd(&tickets[pidx], 1);
                     tk = __shfl_sync(0xffffffffu, tk, 0);
                     if (tk == v_hi - v_lo) {   // the last of the chunk's warps: merge
                         __threadfence();
@@ -354,7 +358,7 @@ decode_group_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
                                     acc[4 * k + 3] += x4.w * wt;
                                 }
                             }
-                            if (R.valid) {
+                            if (R.valid && dbg_ok(R.qoff >= 0 && R.qoff + D <= q_elems(p), p.status)) {
                                 const float f = SOFTMAX ? (Lsum > 0.f ? 1.f / Lsum : 0.f) : 1.f;
                                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.y) +
                                                                        R.qoff + c0 + h * MC);

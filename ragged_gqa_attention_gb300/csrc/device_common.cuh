@@ -53,6 +53,33 @@ __device__ __forceinline__ int key_extent(int causal, int i_last, const SeqInfo 
     return (int)lim;
 }
 
+// Record an error code in the status word unless one is already there.
+__device__ __forceinline__ void set_status(int32_t *status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+// Debug-checks builds (RGA_DEBUG_CHECKS): dbg_ok(ok, status) is false when
+// an access failed its bounds check, after recording status 7 (the caller
+// then skips the access).  Ordinary builds carry no checks: it is true and
+// the condition is not evaluated.
+#ifdef RGA_DEBUG_CHECKS
+constexpr bool RGA_DEBUG = true;
+#else
+constexpr bool RGA_DEBUG = false;
+#endif
+constexpr int RGA_STATUS_BOUNDS = 7;
+#define dbg_ok(cond, status)                                                   \
+    (!::rga::RGA_DEBUG || (cond) ||                                            \
+     (::rga::set_status((status), ::rga::RGA_STATUS_BOUNDS), false))
+
+// Elements of the tensors a call reads and writes (for the checks).
+__device__ __forceinline__ long long q_elems(const AttnParams &p) {
+    return (long long)(p.q_packed ? p.q_seq : (long long)p.B * p.q_seq) * p.Hq * p.D;
+}
+__device__ __forceinline__ long long mask_elems(const AttnParams &p) {
+    return p.md[0] * p.md[1] * p.md[2] * p.md[3];
+}
+
 // Flat offset of mask row (b, h, i) under right-aligned broadcast.
 __device__ __forceinline__ long long mask_row(const AttnParams &p, int b, int h, int i) {
     long long ib = p.md[0] == 1 ? 0 : b;
@@ -64,6 +91,10 @@ __device__ __forceinline__ long long mask_row(const AttnParams &p, int b, int h,
 // Read mask element at flat index e: returns whether the pair may attend
 // and the additive term (natural units).
 __device__ __forceinline__ bool mask_at(const AttnParams &p, long long e, float &add) {
+    if (!dbg_ok(e >= 0 && e < mask_elems(p), p.status)) {
+        add = 0.f;
+        return false;
+    }
     switch (p.mask_dtype) {
     case 3:  // bool
         add = 0.f;
@@ -86,11 +117,6 @@ __device__ __forceinline__ float load_qscale(const AttnParams &p) {
     if (p.qscale_dtype == 1)
         return __bfloat162float(*static_cast<const __nv_bfloat16 *>(p.qscale));
     return *static_cast<const float *>(p.qscale);
-}
-
-// Record an error code in the status word unless one is already there.
-__device__ __forceinline__ void set_status(int32_t *status, int code) {
-    atomicCAS(status, 0, code);
 }
 
 }  // namespace rga

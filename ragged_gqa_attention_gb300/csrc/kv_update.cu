@@ -70,7 +70,16 @@ kv_update_kernel(const __grid_constant__ KvuParams p) {
     const int64_t row = (int64_t)p.D * p.esize;       // bytes per row
     const I vpr = (I)(row / V);                        // vectors per row
     const I stride = (I)gridDim.x * KVU_THREADS;
+    const int64_t cache_bytes = (int64_t)p.B * p.H * p.N * row;
+    const int64_t upd_bytes = p.packed ? (int64_t)s_cu[p.B] * p.H * row
+                                       : (int64_t)p.B * p.H * p.nu * row;
     auto copy = [&](const uint8_t *src, uint8_t *dst) {
+        // debug-checks builds: the destination lies in the cache, the source
+        // in the update tensor or the cache
+        const int64_t di = dst - p.y;
+        const bool src_ok = (src >= p.update && src - p.update + V <= upd_bytes) ||
+                            (p.cache && src >= p.cache && src - p.cache + V <= cache_bytes);
+        if (!dbg_ok(di >= 0 && di + V <= cache_bytes && src_ok, p.status)) return;
         if constexpr (V == 16) *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
         else if constexpr (V == 4) *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(src);
         else if constexpr (V == 2) *reinterpret_cast<uint16_t *>(dst) = *reinterpret_cast<const uint16_t *>(src);

@@ -179,7 +179,9 @@ __device__ __forceinline__ bool next_item(const PfBars &bar, uint32_t n, volatil
 
 template <int MODE>
 __device__ __forceinline__ Item load_item(const AttnParams &p, int idx) {
-    const int4 it = reinterpret_cast<const int4 *>(p.ws + WS_HEADER)[idx];
+    int4 it = make_int4(0, 0, 0, 0);   // (debug checks) inside the work list
+    if (dbg_ok(idx >= 0 && idx < p.max_items, p.status))
+        it = reinterpret_cast<const int4 *>(p.ws + WS_HEADER)[idx];
     Item m;
     m.b = it.x;
     m.qt = it.y;
@@ -278,6 +280,13 @@ __device__ __forceinline__ void load_kv_tile(const AttnParams &p, const CUtensor
     if (!PAGED) {
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, bytes);
+            // (debug checks) the tile starts inside the sequence and the cache
+            if (!dbg_ok(j0 >= 0 && j0 < m.s.kv_len && m.g < p.Hkv &&
+                        (p.kv_packed ? m.s.kv_off + j0 < p.kv_seq : j0 < p.kv_seq && m.b < p.B),
+                        p.status)) {
+                mbar_complete_tx(bar, bytes);
+                return;
+            }
             if (KV8) {
                 if (p.kv_packed) tma_load_3d(dst, map, bar, 0, m.g, m.s.kv_off + j0);
                 else tma_load_4d(dst, map, bar, 0, j0, m.g, m.b);
@@ -299,6 +308,14 @@ __device__ __forceinline__ void load_kv_tile(const AttnParams &p, const CUtensor
         for (int i = 0; i < BN / 32; ++i) {
             if (i * pr >= BN) break;
             const int key = j0 + i * pr, row = key % p.page_size;
+            // (debug checks) a box in one of the sequence's pages lies in the
+            // pools; boxes past its last page read out of bounds (-1)
+            if (!dbg_ok(key / p.page_size >= (m.s.kv_len + p.page_size - 1) / p.page_size
+                            ? pg[i] == -1 : (pg[i] >= 0 && pg[i] < p.num_pages),
+                        p.status)) {
+                mbar_complete_tx(bar, bytes / (BN / pr));
+                continue;
+            }
             if (KV8) {
                 tma_load_4d(dst + i * pr * D, map, bar, 0, row, m.g, pg[i]);
             } else {
@@ -342,10 +359,22 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
         if (qc > 0 && !mbar_wait(bar.q_empty, (qc - 1) & 1, abort)) break;
         if (lane == 0) {
             mbar_arrive_expect_tx(bar.q_full, q_bytes);
-            for (int a = 0; a < 2; ++a)
-                for (int blk = 0; blk < L::NBLK; ++blk)
-                    tma_q(p, &tm.q, m, a, sm + L::Q_OFF + a * L::TILE + blk * L::BLK, bar.q_full,
-                          blk * 64);
+            for (int a = 0; a < 2; ++a) {
+                // (debug checks) a tile with valid rows starts inside Q; a
+                // tile past the item's tokens is loaded knowingly and unused
+                const int tok = m.i0 + a * p.tq;
+                const bool inside = tok >= m.ntok + m.i0 ||
+                    dbg_ok(tok >= 0 && (p.q_packed ? m.s.q_off + tok < p.q_seq
+                                                   : tok < p.q_seq && m.b < p.B) &&
+                           (m.g + 1) * p.G <= p.Hq, p.status);
+                for (int blk = 0; blk < L::NBLK; ++blk) {
+                    if (inside)
+                        tma_q(p, &tm.q, m, a, sm + L::Q_OFF + a * L::TILE + blk * L::BLK,
+                              bar.q_full, blk * 64);
+                    else
+                        mbar_complete_tx(bar.q_full, q_bytes / (2 * L::NBLK));
+                }
+            }
         }
         ++qc;
         for (int t = 0; t < m.ntiles && !*abort; ++t) {
@@ -746,6 +775,10 @@ __device__ __forceinline__ void mask_chunk(const AttnParams &p, float (&v)[32], 
         } else {
             if (ok) {
                 const long long e = keyb ? mrow : mrow + j0 + kk;
+                ok = dbg_ok(e >= 0 && e < mask_elems(p), p.status);
+            }
+            if (ok) {
+                const long long e = keyb ? mrow : mrow + j0 + kk;
                 float add;
                 if constexpr (MK == MK_ADD_F16) add = ld_as_float<__half>(p.mask, e);
                 else if constexpr (MK == MK_ADD_BF16) add = ld_as_float<__nv_bfloat16>(p.mask, e);
@@ -799,7 +832,9 @@ __device__ __forceinline__ void mask_bits(const AttnParams &p, bool row_indep, l
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int j = j0 + lane * 4 + k;
-            const bool ok = j < kv_len && mk[keyb ? mrow : mrow + j] != 0;
+            const long long e = keyb ? mrow : mrow + j;
+            const bool ok = j < kv_len && dbg_ok(e >= 0 && e < mask_elems(p), p.status) &&
+                            mk[e] != 0;
             bits[k] = __ballot_sync(0xffffffffu, ok);
         }
         return;
@@ -809,7 +844,8 @@ __device__ __forceinline__ void mask_bits(const AttnParams &p, bool row_indep, l
     if (!row_ok) return;
     const uint8_t *src = mk + (keyb ? mrow : mrow + j0);
     if (!keyb && j0 + BN <= kv_len && j0 + BN <= p.md[3] &&
-        (reinterpret_cast<uintptr_t>(src) & 7) == 0) {
+        (reinterpret_cast<uintptr_t>(src) & 7) == 0 &&
+        dbg_ok(mrow + j0 >= 0 && mrow + j0 + BN <= mask_elems(p), p.status)) {
         // the tile lies inside the mask row and the sequence: 16 loads of 8
         // key bytes each; key 8q + e lands in bits[e & 3], bit 2q + (e >> 2)
 #pragma unroll
@@ -826,7 +862,8 @@ __device__ __forceinline__ void mask_bits(const AttnParams &p, bool row_indep, l
 #pragma unroll 1
     for (int c = 0; c < BN; ++c) {
         const int j = j0 + c;
-        if (j < kv_len && mk[keyb ? mrow : mrow + j] != 0) {
+        const long long e = keyb ? mrow : mrow + j;
+        if (j < kv_len && dbg_ok(e >= 0 && e < mask_elems(p), p.status) && mk[e] != 0) {
             const uint32_t bit = 1u << (c >> 2);
             switch (c & 3) {   // a switch keeps bits[] in registers
             case 0: bits[0] |= bit; break;
@@ -907,8 +944,12 @@ __device__ __forceinline__ void store_rows(const AttnParams &p, const TensorMaps
         if (whole) {
             fence_proxy_async_smem();
             named_sync(1 + a, 128);
-            if (r == 0) {
-                const int tok = m.i0 + a * p.tq;
+            const int tok = m.i0 + a * p.tq;
+            // (debug checks) the stored tile lies inside the sequence and Y
+            if (r == 0 &&
+                dbg_ok(tok >= 0 && tok + p.tq <= m.s.q_len && (m.g + 1) * p.G <= p.Hq &&
+                       (p.q_packed ? m.s.q_off + tok + p.tq <= p.q_seq
+                                   : tok + p.tq <= p.q_seq && m.b < p.B), p.status)) {
                 if (p.q_packed)
                     tma_store_3d(&tm.y, stg_wg, half * 64, m.g * p.G, m.s.q_off + tok);
                 else
@@ -925,7 +966,9 @@ __device__ __forceinline__ void store_rows(const AttnParams &p, const TensorMaps
                 const RowOut o = row_out(p, m, a, wr0 + lr);
                 const uint4 val =
                     *reinterpret_cast<const uint4 *>(stg + lr * 128 + ((q ^ (lr & 7)) * 16));
-                if (o.ok) *reinterpret_cast<uint4 *>(y + o.off + half * 64 + q * 8) = val;
+                const long long e = o.off + half * 64 + q * 8;
+                if (o.ok && dbg_ok(e >= 0 && e + 8 <= q_elems(p), p.status))
+                    *reinterpret_cast<uint4 *>(y + e) = val;
             }
             __syncwarp();
         }

@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(const __grid_constan
             const long long r = j / G4;            // (t, h) row
             const int t = (int)(r / H);
             if (p.pos && p.pos[t] < 0) continue;   // padding row: left as it is
+            if (!dbg_ok(t < p.T && 8 * u + 8 <= p.R, p.status)) continue;
             uint16_t *row = (isq ? p.q : p.k) + r * p.D;
             rope_group<BF16>(row, row, p.cs + (long long)t * p.R, p.R, u, true);
         } else {             // fused: the new keys into their cache rows
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(const __grid_constan
                 if (s_cu[mid] <= tg) lo = mid; else hi = mid;
             }
             const int n = s_w[lo] + (tg - s_cu[lo]);
+            if (!dbg_ok(tg < p.T && n >= 0 && n < p.N, p.status)) continue;
             const uint16_t *src = p.upd + r * p.D;
             uint16_t *dst = p.cache + (((long long)lo * p.Hk + h) * p.N + n) * p.D;
             if (u < G4) {

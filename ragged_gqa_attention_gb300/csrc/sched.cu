@@ -199,7 +199,9 @@ sched_kernel(AttnParams p, int decode) {
             const SeqInfo s = seq_info(p, b);
             const int cost = item_cost(p, s, qt);
             const int pos = atomicAdd(&hist[min(cost, COST_BUCKETS - 1)], p.Hkv);
-            for (int g = 0; g < p.Hkv; ++g) items[pos + g] = make_int4(b, qt, g, cost);
+            for (int g = 0; g < p.Hkv; ++g)
+                if (dbg_ok(pos + g < p.max_items, p.status))
+                    items[pos + g] = make_int4(b, qt, g, cost);
         }
     } else {
         for (int b = tid; b < p.B; b += SCHED_THREADS) {
@@ -208,7 +210,9 @@ sched_kernel(AttnParams p, int decode) {
             for (int qt = nqt - 1; qt >= 0; --qt) {
                 const int cost = item_cost(p, s, qt);
                 const int pos = atomicAdd(&hist[min(cost, COST_BUCKETS - 1)], p.Hkv);
-                for (int g = 0; g < p.Hkv; ++g) items[pos + g] = make_int4(b, qt, g, cost);
+                for (int g = 0; g < p.Hkv; ++g)
+                    if (dbg_ok(pos + g < p.max_items, p.status))
+                        items[pos + g] = make_int4(b, qt, g, cost);
             }
         }
     }

@@ -7,7 +7,8 @@
 // stays usable.
 //
 // It also exposes the fp8 KV cache's in-register E4M3 decoding, so that a
-// test can compare all 256 codes with the oracle's decoder.
+// test can compare all 256 codes with the oracle's decoder, and one store
+// through the bounds check of the debug-checks build.
 #include <cuda_runtime.h>
 #include "rga.h"
 #include "device_common.cuh"
@@ -44,7 +45,23 @@ __global__ void selftest_e4m3_kernel(uint16_t *out_f16, uint16_t *out_bf16) {
     out_bf16[4 * l + 2] = hi & 0xffff; out_bf16[4 * l + 3] = hi >> 16;
 }
 
+// One store through the debug-checks build's bounds check: buf[index] = 1
+// when 0 <= index < n, else the store is skipped and the status recorded.
+__global__ void selftest_bounds_kernel(int32_t *buf, long long n, long long index,
+                                       int32_t *status) {
+    if (dbg_ok(index >= 0 && index < n, status)) buf[index] = 1;
+}
+
 }  // namespace rga
+
+extern "C" rga_status rga_selftest_bounds_check(int32_t *buf, int64_t n, int64_t index,
+                                                 int32_t *device_status, cudaStream_t stream) {
+    if (!rga::RGA_DEBUG) return RGA_ERR_UNSUPPORTED;
+    if (!buf || !device_status || n <= 0) return RGA_ERR_INVALID_ARG;
+    rga::selftest_bounds_kernel<<<1, 1, 0, stream>>>(buf, (long long)n, (long long)index,
+                                                      device_status);
+    return cudaGetLastError() == cudaSuccess ? RGA_OK : RGA_ERR_CUDA;
+}
 
 extern "C" rga_status rga_selftest_e4m3_decode(uint16_t *out_f16, uint16_t *out_bf16,
                                                 cudaStream_t stream) {
