@@ -537,6 +537,10 @@ def main():
                     help="skip the other workloads (headline only)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle CPU work for cpu_baseline")
+    ap.add_argument("--quant", choices=["fp8", "int8"], default="fp8",
+                    help="P's quantisation when --workload is the quantized workload (5)")
+    ap.add_argument("--aux", choices=["kv_update", "rope_kv_update"],
+                    help="time only this cache-update kernel and print its line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
@@ -554,7 +558,22 @@ def main():
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream()
 
-    head = measure(args.workload, "fp8", stream, args.steps, args.warmup, dist_on, peaks, rank,
+    if args.aux:
+        fn = measure_kv_update if args.aux == "kv_update" else measure_rope_kv_update
+        name, r = fn(stream, args.steps, args.warmup, dist_on, peaks)
+        if rank == 0:
+            print(json.dumps({"metric": f"{args.aux} GB/s", "value": round(r["value"] * world, 3),
+                              "unit": r["unit"], "n_gpus": world, "steps": args.steps,
+                              "warmup": args.warmup, "ms_per_step": round(r["ms"], 4),
+                              "config": {"workload": name},
+                              "frac_of_peak": round(r["value"] / r["peak"], 4),
+                              "peak": r["peak"], "peak_source": peak_src}), flush=True)
+        if dist_on:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
+
+    head = measure(args.workload, args.quant, stream, args.steps, args.warmup, dist_on, peaks, rank,
                    clocks=True)
     case = head["case"]
     e2e_step_ms, bi, bo = e2e_timed(case, stream, max(3, args.steps // 2), 3, dist_on)
