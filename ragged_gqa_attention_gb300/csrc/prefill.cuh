@@ -431,35 +431,49 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
 // 16-byte chunk c = l % (D/16) (codes 16c .. 16c+15, exactly converted to
 // f16 or bf16), which land in block c / 4 as the logical chunks 2(c%4) and
 // 2(c%4)+1 of the row.  Rows from `zero_from` on are written as zeros.  The
-// warp reads all its rows' bytes before it writes, so the expansion may
-// overwrite the byte tile in place (D = 128: each 16-bit row of the second
-// block covers exactly the byte row of the same index).
+// warp reads the bytes of EB steps' rows before it writes any of them (the
+// loads overlap instead of each waiting out the one before), so the
+// expansion may overwrite the byte tile in place (D = 128: each 16-bit row
+// of the second block covers exactly the byte row of the same index, and
+// each row belongs to one warp and one batch).
 template <int D, bool BF16>
 __device__ __forceinline__ void expand_tile(const uint8_t *raw, uint8_t *dst, int zero_from,
                                             int w) {
-    constexpr int CPR = D / 16;     // 16-byte chunks per byte row
-    constexpr int RPS = 32 / CPR;   // rows per warp step
+    constexpr int CPR = D / 16;             // 16-byte chunks per byte row
+    constexpr int RPS = 32 / CPR;           // rows per warp step
+    constexpr int STEPS = BN / (2 * RPS);   // steps of one warp (two warps per tile)
+    constexpr int EB = D == 128 ? 8 : 4;    // steps per batch of loads
+    static_assert(STEPS % EB == 0, "whole batches");
     const int lane = threadIdx.x & 31;
     const int c = lane % CPR;
     const int l0 = 2 * (c % 4);
-#pragma unroll 2
-    for (int r0 = w * RPS; r0 < BN; r0 += 2 * RPS) {
-        const int r = r0 + lane / CPR;
-        const uint4 b = *reinterpret_cast<const uint4 *>(raw + r * D + c * 16);
-        __syncwarp();
-        uint32_t h[8];
-        e4m3x4_to_x2<BF16>(b.x, h[0], h[1]);
-        e4m3x4_to_x2<BF16>(b.y, h[2], h[3]);
-        e4m3x4_to_x2<BF16>(b.z, h[4], h[5]);
-        e4m3x4_to_x2<BF16>(b.w, h[6], h[7]);
-        if (r >= zero_from) {
+#pragma unroll 1
+    for (int s0 = 0; s0 < STEPS; s0 += EB) {
+        uint4 b[EB];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) h[k] = 0u;
+        for (int i = 0; i < EB; ++i) {
+            const int r = (w + 2 * (s0 + i)) * RPS + lane / CPR;
+            b[i] = *reinterpret_cast<const uint4 *>(raw + r * D + c * 16);
         }
-        uint8_t *row = dst + (c / 4) * PfLayout<D>::BLK + r * 128;
-        *reinterpret_cast<uint4 *>(row + ((l0 ^ (r & 7)) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(row + (((l0 + 1) ^ (r & 7)) * 16)) =
-            make_uint4(h[4], h[5], h[6], h[7]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < EB; ++i) {
+            const int r = (w + 2 * (s0 + i)) * RPS + lane / CPR;
+            uint32_t h[8];
+            e4m3x4_to_x2<BF16>(b[i].x, h[0], h[1]);
+            e4m3x4_to_x2<BF16>(b[i].y, h[2], h[3]);
+            e4m3x4_to_x2<BF16>(b[i].z, h[4], h[5]);
+            e4m3x4_to_x2<BF16>(b[i].w, h[6], h[7]);
+            if (r >= zero_from) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) h[k] = 0u;
+            }
+            uint8_t *row = dst + (c / 4) * PfLayout<D>::BLK + r * 128;
+            *reinterpret_cast<uint4 *>(row + ((l0 ^ (r & 7)) * 16)) =
+                make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4 *>(row + (((l0 + 1) ^ (r & 7)) * 16)) =
+                make_uint4(h[4], h[5], h[6], h[7]);
+        }
     }
 }
 
@@ -501,24 +515,37 @@ __device__ __forceinline__ int q_shift(uint32_t m16) {
 
 // In place: the converter warp's rows of a bf16 Q tile become f16 values of
 // q * 2^s (elementwise on 16-byte chunks, so the 128-byte swizzle is kept).
+// Eight chunks are read before any is written back, so the loads overlap.
 template <int D>
 __device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int w, float scale) {
     constexpr int CHUNKS = 64 * D * 2 / 16;
+    constexpr int QB = 8;
+    static_assert(CHUNKS % (32 * QB) == 0, "whole batches");
     const int lane = threadIdx.x & 31;
-    for (int c = lane; c < CHUNKS; c += 32) {
-        const int r = 64 * w + c / (D / 8), cc = c % (D / 8);
-        uint4 *ptr = reinterpret_cast<uint4 *>(tile + (cc / 8) * PfLayout<D>::BLK + r * 128 +
-                                               (cc % 8) * 16);
-        uint4 v = *ptr;
-        uint32_t *ws = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll 1
+    for (int c0 = lane; c0 < CHUNKS; c0 += 32 * QB) {
+        uint4 *ptr[QB];
+        uint4 v[QB];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float lo = __uint_as_float(ws[k] << 16) * scale;
-            const float hi = __uint_as_float(ws[k] & 0xffff0000u) * scale;
-            __half2 hh = __floats2half2_rn(lo, hi);
-            ws[k] = *reinterpret_cast<uint32_t *>(&hh);
+        for (int i = 0; i < QB; ++i) {
+            const int c = c0 + 32 * i;
+            const int r = 64 * w + c / (D / 8), cc = c % (D / 8);
+            ptr[i] = reinterpret_cast<uint4 *>(tile + (cc / 8) * PfLayout<D>::BLK + r * 128 +
+                                               (cc % 8) * 16);
+            v[i] = *ptr[i];
         }
-        *ptr = v;
+#pragma unroll
+        for (int i = 0; i < QB; ++i) {
+            uint32_t *ws = reinterpret_cast<uint32_t *>(&v[i]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float lo = __uint_as_float(ws[k] << 16) * scale;
+                const float hi = __uint_as_float(ws[k] & 0xffff0000u) * scale;
+                __half2 hh = __floats2half2_rn(lo, hi);
+                ws[k] = *reinterpret_cast<uint32_t *>(&hh);
+            }
+            *ptr[i] = v[i];
+        }
     }
 }
 
