@@ -305,7 +305,8 @@ def trt_attention_fp8_kv(q, k, v, *, k_scale, v_scale, q_form="padded", kv_form=
     """Attention over an FP8 KV cache: ``k`` and ``v`` hold E4M3 codes
     (torch.float8_e4m3fn, or uint8 holding the codes), dequantised with the
     one-element fp32 CUDA tensors ``k_scale`` and ``v_scale``; ``q`` and the
-    returned Y are f16 or bf16.  Decode shapes only (see include/rga.h)."""
+    returned Y are f16 or bf16.  Every shape: decode shapes run the decode
+    kernels, the others the prefill kernel."""
     for name, t in (("k", k), ("v", v)):
         if t.dtype not in FP8_CODE_DTYPES:
             raise ValueError(f"{name} must hold E4M3 codes (float8_e4m3fn or uint8)")

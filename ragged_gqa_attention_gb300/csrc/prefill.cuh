@@ -430,7 +430,12 @@ __device__ __forceinline__ void producer_role(const AttnParams &p, const TensorM
 // of converter warp w takes, per step, row r = r0 + l / (D/16) and its
 // 16-byte chunk c = l % (D/16) (codes 16c .. 16c+15, exactly converted to
 // f16 or bf16), which land in block c / 4 as the logical chunks 2(c%4) and
-// 2(c%4)+1 of the row.  Rows from `zero_from` on are written as zeros.  The
+// 2(c%4)+1 of the row.  (D = 128: the four rows of a step are permuted
+// among the quarter warps, row dr(l) = (q & 2) + ((q ^ (c >> 2)) & 1) with
+// q = l / 8, so that the 8 lanes the shared memory serves together read 128
+// distinct bytes and write to blocks 0 and 1 of two rows of opposite
+// swizzle parity: no bank conflicts either way.)  Rows from `zero_from` on
+// are written as zeros.  The
 // warp reads the bytes of EB steps' rows before it writes any of them (the
 // loads overlap instead of each waiting out the one before), so the
 // expansion may overwrite the byte tile in place (D = 128: each 16-bit row
@@ -447,18 +452,20 @@ __device__ __forceinline__ void expand_tile(const uint8_t *raw, uint8_t *dst, in
     const int lane = threadIdx.x & 31;
     const int c = lane % CPR;
     const int l0 = 2 * (c % 4);
+    const int q = lane / CPR;
+    const int dr = D == 128 ? (q & 2) + ((q ^ (c >> 2)) & 1) : q;   // row within the step
 #pragma unroll 1
     for (int s0 = 0; s0 < STEPS; s0 += EB) {
         uint4 b[EB];
 #pragma unroll
         for (int i = 0; i < EB; ++i) {
-            const int r = (w + 2 * (s0 + i)) * RPS + lane / CPR;
+            const int r = (w + 2 * (s0 + i)) * RPS + dr;
             b[i] = *reinterpret_cast<const uint4 *>(raw + r * D + c * 16);
         }
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < EB; ++i) {
-            const int r = (w + 2 * (s0 + i)) * RPS + lane / CPR;
+            const int r = (w + 2 * (s0 + i)) * RPS + dr;
             uint32_t h[8];
             e4m3x4_to_x2<BF16>(b[i].x, h[0], h[1]);
             e4m3x4_to_x2<BF16>(b[i].y, h[2], h[3]);
