@@ -486,17 +486,36 @@ __device__ __forceinline__ void expand_tile(const uint8_t *raw, uint8_t *dst, in
 
 // Largest finite |x| of a converter warp's rows (64 of 128) of a bf16 Q tile,
 // as bf16 magnitude bits (non-finite values, such as NaN padding rows, are
-// left out).  Lane l reads 16-byte chunks l, l + 32, ... of the rows.
+// left out).  Lane l reads 16-byte chunks l, l + 32, ... of the rows.  A
+// first pass takes the largest magnitude bits of every element two at a
+// time (max.u16x2); only when that finds a non-finite value does a second
+// pass compare element by element and leave those out.
 template <int D>
 __device__ __forceinline__ uint32_t q_tile_max(const uint8_t *tile, int w) {
     constexpr int CHUNKS = 64 * D * 2 / 16;    // 16-byte chunks in 64 rows
     const int lane = threadIdx.x & 31;
-    uint32_t mx = 0;
-    for (int c = lane; c < CHUNKS; c += 32) {
+    auto chunk = [&](int c) {
         // row r = 64 w + c / (D / 8) lies in 64-column block (c % (D/8)) / 8
         const int r = 64 * w + c / (D / 8), cc = c % (D / 8);
-        const uint4 v = *reinterpret_cast<const uint4 *>(tile + (cc / 8) * PfLayout<D>::BLK +
-                                                         r * 128 + (cc % 8) * 16);
+        return *reinterpret_cast<const uint4 *>(tile + (cc / 8) * PfLayout<D>::BLK + r * 128 +
+                                                (cc % 8) * 16);
+    };
+    uint32_t acc = 0;
+#pragma unroll 4
+    for (int c = lane; c < CHUNKS; c += 32) {
+        const uint4 v = chunk(c);
+        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            asm("max.u16x2 %0, %0, %1;" : "+r"(acc) : "r"(ws[k] & 0x7fff7fffu));
+    }
+    uint32_t mx = max(acc & 0xffffu, acc >> 16);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (mx < 0x7f80u) return mx;              // every element finite
+    mx = 0;
+    for (int c = lane; c < CHUNKS; c += 32) {
+        const uint4 v = chunk(c);
         const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -529,6 +548,8 @@ __device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int w, float scale)
     constexpr int QB = 8;
     static_assert(CHUNKS % (32 * QB) == 0, "whole batches");
     const int lane = threadIdx.x & 31;
+    uint64_t sc2;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(sc2) : "f"(scale));
 #pragma unroll 1
     for (int c0 = lane; c0 < CHUNKS; c0 += 32 * QB) {
         uint4 *ptr[QB];
@@ -546,8 +567,12 @@ __device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int w, float scale)
             uint32_t *ws = reinterpret_cast<uint32_t *>(&v[i]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float lo = __uint_as_float(ws[k] << 16) * scale;
-                const float hi = __uint_as_float(ws[k] & 0xffff0000u) * scale;
+                // both halves as f32, times 2^s in one packed multiply
+                uint64_t x;
+                asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(ws[k] << 16), "r"(ws[k] & 0xffff0000u));
+                asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(sc2));
+                float lo, hi;
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
                 __half2 hh = __floats2half2_rn(lo, hi);
                 ws[k] = *reinterpret_cast<uint32_t *>(&hh);
             }
