@@ -1196,6 +1196,10 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
             const bool stat = (MODE == MODE_SOFTMAX_Q) && t < m.nkt;
             uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
             if (bool_mask && !full) mask_bits(p, row_indep, mrow, j0, m.s.kv_len, row_ok, bits);
+            // a row-independent bool mask that keeps every key of the tile
+            // needs no per-score test (warp-uniform: the bits are the warp's)
+            const bool mask_part =
+                use_mask && (!row_indep || (bits[0] & bits[1] & bits[2] & bits[3]) != 0xffffffffu);
 
             // Softmax without an explicit mask (and the quantized op's
             // statistics and quantized passes, also under a bool mask that
@@ -1225,7 +1229,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                     mask_after(ra[0], rem);
                     mask_after(ra[1], rem - 32);
                 }
-                if (MODE == MODE_SOFTMAX_Q && use_mask) {
+                if (MODE == MODE_SOFTMAX_Q && mask_part) {
                     mask_keys(ra[0], bits, 0);
                     mask_keys(ra[1], bits, 1);
                 }
@@ -1237,21 +1241,27 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                         mask_after(rb[0], rem - 64);
                         mask_after(rb[1], rem - 96);
                     }
-                    if (use_mask) {
+                    if (mask_part) {
                         mask_keys(rb[0], bits, 2);
                         mask_keys(rb[1], bits, 3);
                     }
                     if (stat) {
                         // pass 1: S is in registers, so the tensor core may
-                        // already write the next S over it; exact max and sum
+                        // already write the next S over it.  The row sum is
+                        // taken against a running reference, as in the
+                        // softmax pass: a row's first visible scores set it
+                        // (their max); the tile max is needed again only
+                        // when the sum shows a score above the reference by
+                        // more than the threshold, and then the sum is
+                        // retaken against the new max.  lse2 = ref + log2 l.
                         tc_fence_before();
                         mbar_arrive(&bar.p_full[a]);
-                        const float mraw = fmaxf(fmaxf(reg_max(ra[0]), reg_max(ra[1])),
-                                                 fmaxf(reg_max(rb[0]), reg_max(rb[1])));
-                        const float mx = row_ok ? mraw * sc : -INFINITY;
-                        const float m_new = fmaxf(m_ref, mx);
-                        if (m_new != -INFINITY) {
-                            const uint64_t neg2 = f2_pack(-m_new, -m_new);
+                        auto tile_max = [&]() {
+                            return fmaxf(fmaxf(reg_max(ra[0]), reg_max(ra[1])),
+                                         fmaxf(reg_max(rb[0]), reg_max(rb[1])));
+                        };
+                        auto tile_sum = [&](float ref) {
+                            const uint64_t neg2 = f2_pack(-ref, -ref);
                             uint64_t acc0 = 0, acc1 = 0;
                             sum_chunk(ra[0], mul2, neg2, acc0, acc1);
                             sum_chunk(ra[1], mul2, neg2, acc0, acc1);
@@ -1260,9 +1270,27 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                             float s0, s1, s2, s3;
                             f2_unpack(acc0, s0, s1);
                             f2_unpack(acc1, s2, s3);
-                            l = l * ex2(m_ref - m_new) + ((s0 + s1) + (s2 + s3));
-                            m_ref = m_new;
+                            return (s0 + s1) + (s2 + s3);
+                        };
+                        if (__any_sync(0xffffffffu, row_ok && m_ref == -INFINITY)) {
+                            const float mx = tile_max() * sc;   // -inf: nothing visible yet
+                            if (row_ok && m_ref == -INFINITY) m_ref = mx;
                         }
+                        const bool has_ref = row_ok && m_ref != -INFINITY;
+                        float ref = has_ref ? m_ref : 0.f;
+                        float sum = tile_sum(ref);
+                        const bool big = has_ref && !(sum <= RESCALE_SUM);
+                        if (__any_sync(0xffffffffu, big)) {
+                            const float mx = tile_max() * sc;
+                            const bool grow = big && mx > m_ref;
+                            if (grow) {
+                                l *= ex2(m_ref - mx);
+                                m_ref = mx;
+                                ref = mx;
+                            }
+                            if (__any_sync(0xffffffffu, grow)) sum = tile_sum(ref);
+                        }
+                        if (has_ref) l += sum;
                         if (t == m.nkt - 1)
                             lse2 = (l > 0.f) ? m_ref + log2f(l) + log2f(qs) : INFINITY;
                         ++tc;
