@@ -1188,14 +1188,15 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
         float m_ref = -INFINITY, l = 0.f, lse2 = 0.f;
         int u = 0;
         for (int t = 0; t < m.ntiles; ++t) {
+            const int j0 = key_tile<MODE>(m, t) * BN;
+            // the bool mask's bits of the tile, read while S is computed
+            uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+            if (bool_mask) mask_bits(p, row_indep, mrow, j0, m.s.kv_len, row_ok, bits);
             if (!mbar_wait(&bar.s_full[a], tc & 1, abort)) { ok = false; break; }
             tc_fence_after();
-            const int j0 = key_tile<MODE>(m, t) * BN;
             const int rem = lim - j0;
             const bool full = !use_mask && j0 + BN - 1 <= lim_first && sc > 0.f;
             const bool stat = (MODE == MODE_SOFTMAX_Q) && t < m.nkt;
-            uint32_t bits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-            if (bool_mask && !full) mask_bits(p, row_indep, mrow, j0, m.s.kv_len, row_ok, bits);
             // a row-independent bool mask that keeps every key of the tile
             // needs no per-score test (warp-uniform: the bits are the warp's)
             const bool mask_part =
