@@ -23,6 +23,7 @@
 namespace rga {
 
 constexpr int KVU_THREADS = 256;
+constexpr int KVU_UNROLL = 4;   // vectors a lane reads before it writes (packed, in place)
 constexpr int KVU_MAX_B = 8192;
 
 struct KvuParams {
@@ -96,18 +97,48 @@ kv_update_kernel(const __grid_constant__ KvuParams p) {
 
     if (p.in_place) {
         if (p.packed) {
-            const I total = (I)s_cu[p.B] * p.H * vpr;
-            for (I v = (I)blockIdx.x * KVU_THREADS + threadIdx.x; v < total; v += stride) {
-                const I r = v / vpr, c = v % vpr;
-                const int tg = (int)(r / p.H), h = (int)(r % p.H);
+            // one warp per update token: its H rows are one contiguous block
+            // of the update tensor; the token's batch is found once, and the
+            // lane's vectors are read before any is written (KVU_UNROLL at a
+            // time), so their loads overlap
+            const int lane = threadIdx.x & 31;
+            const int wpb = KVU_THREADS / 32;
+            const int per = p.H * (int)vpr;   // vectors of one token
+            for (int tg = (int)blockIdx.x * wpb + (threadIdx.x >> 5); tg < s_cu[p.B];
+                 tg += (int)gridDim.x * wpb) {
                 int lo = 0, hi = p.B;   // s_cu[lo] <= tg < s_cu[lo + 1]
                 while (hi - lo > 1) {
                     const int mid = (lo + hi) >> 1;
                     if (s_cu[mid] <= tg) lo = mid; else hi = mid;
                 }
-                const int t = tg - s_cu[lo];
-                copy(p.update + ((int64_t)tg * p.H + h) * row + (int64_t)c * V,
-                     p.y + cache_row(lo, h, s_w[lo] + t) + (int64_t)c * V);
+                const int n = s_w[lo] + (tg - s_cu[lo]);
+                const uint8_t *src = p.update + (int64_t)tg * p.H * row;
+                for (int v0 = lane; v0 < per; v0 += 32 * KVU_UNROLL) {
+                    uint4 buf[KVU_UNROLL];
+                    const uint8_t *sp[KVU_UNROLL];
+                    uint8_t *dp[KVU_UNROLL];
+#pragma unroll
+                    for (int k = 0; k < KVU_UNROLL; ++k) {
+                        const int v = v0 + 32 * k;
+                        const int h = v / (int)vpr, c = v - h * (int)vpr;
+                        sp[k] = v < per ? src + (int64_t)v * V : nullptr;
+                        dp[k] = v < per ? p.y + cache_row(lo, h, n) + (int64_t)c * V : nullptr;
+                        if constexpr (V == 16)
+                            if (sp[k]) buf[k] = *reinterpret_cast<const uint4 *>(sp[k]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < KVU_UNROLL; ++k) {
+                        if (!sp[k]) continue;
+                        if constexpr (V == 16) {
+                            const int64_t di = dp[k] - p.y;
+                            if (dbg_ok(di >= 0 && di + V <= cache_bytes &&
+                                       sp[k] - p.update + V <= upd_bytes, p.status))
+                                *reinterpret_cast<uint4 *>(dp[k]) = buf[k];
+                        } else {
+                            copy(sp[k], dp[k]);
+                        }
+                    }
+                }
             }
         } else {
             const I total = (I)p.B * p.H * p.nu * vpr;

@@ -98,7 +98,9 @@ __device__ __forceinline__ void rope_group(const uint16_t *src, uint16_t *dst, c
     *reinterpret_cast<uint2 *>(dst + 4 * u + h) = pack4<BF16>(yo);
 }
 
-template <bool BF16, bool FUSED>
+// I: the index type of the unit loop (32-bit whenever every unit index and
+// row offset fits: the divisions that map a unit to its row are then cheap).
+template <bool BF16, bool FUSED, typename I>
 __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(const __grid_constant__ RopeParams p) {
     extern __shared__ int rope_smem[];
     int *s_cu = rope_smem;            // fused: [B + 1] cumulative update rows
@@ -127,29 +129,29 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(const __grid_constan
     }
     const int G4 = p.R / 8;                       // rotated 4-pair groups per row
     const int CG = FUSED ? (p.D - p.R) / 4 : 0;   // copied 4-element groups (fused keys)
-    const long long nq = p.q ? (long long)p.T * p.Hq * G4 : 0;
-    const long long nk = (!FUSED && p.k) ? (long long)p.T * p.Hk * G4 : 0;
-    const long long nu = FUSED ? (long long)s_cu[p.B] * p.Hk * (G4 + CG) : 0;
-    const long long total = nq + nk + nu;
-    for (long long i = (long long)blockIdx.x * ROPE_THREADS + threadIdx.x; i < total;
-         i += (long long)gridDim.x * ROPE_THREADS) {
+    const I nq = p.q ? (I)p.T * p.Hq * G4 : 0;
+    const I nk = (!FUSED && p.k) ? (I)p.T * p.Hk * G4 : 0;
+    const I nu = FUSED ? (I)s_cu[p.B] * p.Hk * (G4 + CG) : 0;
+    const I total = nq + nk + nu;
+    for (I i = (I)blockIdx.x * ROPE_THREADS + threadIdx.x; i < total;
+         i += (I)gridDim.x * ROPE_THREADS) {
         if (i < nq + nk) {   // in place on Q (then K)
             const bool isq = i < nq;
-            const long long j = isq ? i : i - nq;
+            const I j = isq ? i : i - nq;
             const int H = isq ? p.Hq : p.Hk;
-            const int u = (int)(j % G4);
-            const long long r = j / G4;            // (t, h) row
-            const int t = (int)(r / H);
+            const int u = (int)(j % (I)G4);
+            const I r = j / (I)G4;                 // (t, h) row
+            const int t = (int)(r / (I)H);
             if (p.pos && p.pos[t] < 0) continue;   // padding row: left as it is
             if (!dbg_ok(t < p.T && 8 * u + 8 <= p.R, p.status)) continue;
-            uint16_t *row = (isq ? p.q : p.k) + r * p.D;
+            uint16_t *row = (isq ? p.q : p.k) + (long long)r * p.D;
             rope_group<BF16>(row, row, p.cs + (long long)t * p.R, p.R, u, true);
         } else {             // fused: the new keys into their cache rows
-            const long long j = i - nq;
+            const I j = i - nq;
             const int per = G4 + CG;
-            const int u = (int)(j % per);
-            const long long r = j / per;           // (update row, head)
-            const int tg = (int)(r / p.Hk), h = (int)(r % p.Hk);
+            const int u = (int)(j % (I)per);
+            const I r = j / (I)per;                // (update row, head)
+            const int tg = (int)(r / (I)p.Hk), h = (int)(r % (I)p.Hk);
             int lo = 0, hi = p.B;                  // s_cu[lo] <= tg < s_cu[lo + 1]
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(const __grid_constan
             }
             const int n = s_w[lo] + (tg - s_cu[lo]);
             if (!dbg_ok(tg < p.T && n >= 0 && n < p.N, p.status)) continue;
-            const uint16_t *src = p.upd + r * p.D;
+            const uint16_t *src = p.upd + (long long)r * p.D;
             uint16_t *dst = p.cache + (((long long)lo * p.Hk + h) * p.N + n) * p.D;
             if (u < G4) {
                 const bool rot = !(p.pos && p.pos[tg] < 0);
@@ -196,17 +198,25 @@ static rga_status rope_launch(const RopeParams &p, bool bf16, long long units, c
     if (grid > 4LL * sms) grid = 4LL * sms;
     if (grid < 1) grid = 1;
     const size_t smem = FUSED ? (2 * (size_t)p.B + 1) * sizeof(int) : 0;
+    // 32-bit unit indices when every unit (plus one grid stride) fits
+    const bool narrow = units + grid * ROPE_THREADS < INT32_MAX;
     if (FUSED) {
-        static std::atomic<unsigned long long> configured[2] = {{0}, {0}};
-        const cudaError_t e = once_per_device(configured[bf16], [bf16] {
-            return cudaFuncSetAttribute(bf16 ? rope_kernel<true, true> : rope_kernel<false, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static std::atomic<unsigned long long> configured[4] = {{0}, {0}, {0}, {0}};
+        const cudaError_t e = once_per_device(configured[2 * bf16 + narrow], [bf16, narrow] {
+            auto k = bf16 ? (narrow ? rope_kernel<true, true, int> : rope_kernel<true, true, long long>)
+                          : (narrow ? rope_kernel<false, true, int> : rope_kernel<false, true, long long>);
+            return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (2 * ROPE_MAX_B + 1) * (int)sizeof(int));
         });
         if (e != cudaSuccess) return RGA_ERR_CUDA;
     }
-    if (bf16) rope_kernel<true, FUSED><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
-    else rope_kernel<false, FUSED><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
+    if (bf16) {
+        if (narrow) rope_kernel<true, FUSED, int><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
+        else rope_kernel<true, FUSED, long long><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
+    } else {
+        if (narrow) rope_kernel<false, FUSED, int><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
+        else rope_kernel<false, FUSED, long long><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
+    }
     return cudaGetLastError() == cudaSuccess ? RGA_OK : RGA_ERR_CUDA;
 }
 
