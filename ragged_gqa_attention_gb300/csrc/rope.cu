@@ -6,9 +6,11 @@
 //
 // Row t, head h, pair i < R/2 (R = rotary_dim) with c, s from row t of the
 // cos/sin table:  x'[i] = x[i] c - x[i + R/2] s,  x'[i + R/2] = x[i + R/2] c
-// + x[i] s.  HBM-bound elementwise work: one unit is four consecutive pairs
-// of one (row, head) (8-byte loads of each half, 16-byte loads of the
-// cosines and sines); in the fused form a unit of the new keys writes its
+// + x[i] s.  HBM-bound elementwise work: one unit is eight consecutive
+// pairs of one (row, head) (16-byte loads of each half and of the cosines
+// and sines), or four (8-byte loads) where the rotary dims, the head dim or
+// a base address do not allow 16-byte vectors; in the fused form a unit of
+// the new keys writes its
 // rotated (or, past the rotary dims, copied) elements straight into the
 // cache row the update lands in.  The fused form checks every window first,
 // in every CTA, so that a bad call changes nothing (status 4).
@@ -38,11 +40,17 @@ struct RopeParams {
     int32_t *status;
 };
 
-template <bool BF16>
-__device__ __forceinline__ void unpack4(uint2 w, float (&x)[4]) {
-    const uint32_t u[2] = {w.x, w.y};
+// P consecutive 16-bit elements (P = 4: 8 bytes, P = 8: 16 bytes) as one
+// vector, unpacked to and packed from fp32.
+template <int P> struct Vec;
+template <> struct Vec<4> { using T = uint2; };
+template <> struct Vec<8> { using T = uint4; };
+
+template <bool BF16, int P>
+__device__ __forceinline__ void unpack(const typename Vec<P>::T &w, float (&x)[P]) {
+    const uint32_t *u = reinterpret_cast<const uint32_t *>(&w);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < P / 2; ++i) {
         if constexpr (BF16) {
             x[2 * i] = __uint_as_float(u[i] << 16);
             x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
@@ -54,11 +62,12 @@ __device__ __forceinline__ void unpack4(uint2 w, float (&x)[4]) {
     }
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint2 pack4(const float (&x)[4]) {
-    uint32_t u[2];
+template <bool BF16, int P>
+__device__ __forceinline__ typename Vec<P>::T pack(const float (&x)[P]) {
+    typename Vec<P>::T w;
+    uint32_t *u = reinterpret_cast<uint32_t *>(&w);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < P / 2; ++i) {
         if constexpr (BF16) {
             __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
             u[i] = *reinterpret_cast<uint32_t *>(&h);
@@ -67,40 +76,48 @@ __device__ __forceinline__ uint2 pack4(const float (&x)[4]) {
             u[i] = *reinterpret_cast<uint32_t *>(&h);
         }
     }
-    return make_uint2(u[0], u[1]);
+    return w;
 }
 
-// Pairs 4u .. 4u + 3 of one row: src -> dst (may alias), rotated with the
-// table row cs, or copied unchanged when !rotate.
-template <bool BF16>
+// Pairs P u .. P u + P - 1 of one row: src -> dst (may alias), rotated with
+// the table row cs, or copied unchanged when !rotate.
+template <bool BF16, int P>
 __device__ __forceinline__ void rope_group(const uint16_t *src, uint16_t *dst, const float *cs,
                                            int R, int u, bool rotate) {
+    using V = typename Vec<P>::T;
     const int h = R / 2;
-    const uint2 a = *reinterpret_cast<const uint2 *>(src + 4 * u);
-    const uint2 b = *reinterpret_cast<const uint2 *>(src + 4 * u + h);
+    const V a = *reinterpret_cast<const V *>(src + P * u);
+    const V b = *reinterpret_cast<const V *>(src + P * u + h);
     if (!rotate) {
-        *reinterpret_cast<uint2 *>(dst + 4 * u) = a;
-        *reinterpret_cast<uint2 *>(dst + 4 * u + h) = b;
+        *reinterpret_cast<V *>(dst + P * u) = a;
+        *reinterpret_cast<V *>(dst + P * u + h) = b;
         return;
     }
-    const float4 c4 = *reinterpret_cast<const float4 *>(cs + 4 * u);
-    const float4 s4 = *reinterpret_cast<const float4 *>(cs + h + 4 * u);
-    const float c[4] = {c4.x, c4.y, c4.z, c4.w}, s[4] = {s4.x, s4.y, s4.z, s4.w};
-    float x[4], y[4], xo[4], yo[4];
-    unpack4<BF16>(a, x);
-    unpack4<BF16>(b, y);
+    float c[P], sn[P];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        xo[e] = fmaf(x[e], c[e], -(y[e] * s[e]));
-        yo[e] = fmaf(y[e], c[e], x[e] * s[e]);
+    for (int q = 0; q < P / 4; ++q) {
+        const float4 c4 = *reinterpret_cast<const float4 *>(cs + P * u + 4 * q);
+        const float4 s4 = *reinterpret_cast<const float4 *>(cs + h + P * u + 4 * q);
+        c[4 * q] = c4.x; c[4 * q + 1] = c4.y; c[4 * q + 2] = c4.z; c[4 * q + 3] = c4.w;
+        sn[4 * q] = s4.x; sn[4 * q + 1] = s4.y; sn[4 * q + 2] = s4.z; sn[4 * q + 3] = s4.w;
     }
-    *reinterpret_cast<uint2 *>(dst + 4 * u) = pack4<BF16>(xo);
-    *reinterpret_cast<uint2 *>(dst + 4 * u + h) = pack4<BF16>(yo);
+    float x[P], y[P], xo[P], yo[P];
+    unpack<BF16, P>(a, x);
+    unpack<BF16, P>(b, y);
+#pragma unroll
+    for (int e = 0; e < P; ++e) {
+        xo[e] = fmaf(x[e], c[e], -(y[e] * sn[e]));
+        yo[e] = fmaf(y[e], c[e], x[e] * sn[e]);
+    }
+    *reinterpret_cast<V *>(dst + P * u) = pack<BF16, P>(xo);
+    *reinterpret_cast<V *>(dst + P * u + h) = pack<BF16, P>(yo);
 }
 
 // I: the index type of the unit loop (32-bit whenever every unit index and
 // row offset fits: the divisions that map a unit to its row are then cheap).
-template <bool BF16, bool FUSED, typename I>
+// P: pairs per unit (8 when the rotary dims, the head dim and every base
+// address allow 16-byte vectors, else 4).
+template <bool BF16, bool FUSED, typename I, int P>
 __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(const __grid_constant__ RopeParams p) {
     extern __shared__ int rope_smem[];
     int *s_cu = rope_smem;            // fused: [B + 1] cumulative update rows
@@ -127,8 +144,8 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(const __grid_constan
             return;
         }
     }
-    const int G4 = p.R / 8;                       // rotated 4-pair groups per row
-    const int CG = FUSED ? (p.D - p.R) / 4 : 0;   // copied 4-element groups (fused keys)
+    const int G4 = p.R / (2 * P);                 // rotated P-pair groups per row
+    const int CG = FUSED ? (p.D - p.R) / P : 0;   // copied P-element groups (fused keys)
     const I nq = p.q ? (I)p.T * p.Hq * G4 : 0;
     const I nk = (!FUSED && p.k) ? (I)p.T * p.Hk * G4 : 0;
     const I nu = FUSED ? (I)s_cu[p.B] * p.Hk * (G4 + CG) : 0;
@@ -143,9 +160,9 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(const __grid_constan
             const I r = j / (I)G4;                 // (t, h) row
             const int t = (int)(r / (I)H);
             if (p.pos && p.pos[t] < 0) continue;   // padding row: left as it is
-            if (!dbg_ok(t < p.T && 8 * u + 8 <= p.R, p.status)) continue;
+            if (!dbg_ok(t < p.T && 2 * P * (u + 1) <= p.R, p.status)) continue;
             uint16_t *row = (isq ? p.q : p.k) + (long long)r * p.D;
-            rope_group<BF16>(row, row, p.cs + (long long)t * p.R, p.R, u, true);
+            rope_group<BF16, P>(row, row, p.cs + (long long)t * p.R, p.R, u, true);
         } else {             // fused: the new keys into their cache rows
             const I j = i - nq;
             const int per = G4 + CG;
@@ -163,10 +180,11 @@ __global__ void __launch_bounds__(ROPE_THREADS) rope_kernel(const __grid_constan
             uint16_t *dst = p.cache + (((long long)lo * p.Hk + h) * p.N + n) * p.D;
             if (u < G4) {
                 const bool rot = !(p.pos && p.pos[tg] < 0);
-                rope_group<BF16>(src, dst, p.cs + (long long)tg * p.R, p.R, u, rot);
+                rope_group<BF16, P>(src, dst, p.cs + (long long)tg * p.R, p.R, u, rot);
             } else {
-                const int d0 = p.R + 4 * (u - G4);
-                *reinterpret_cast<uint2 *>(dst + d0) = *reinterpret_cast<const uint2 *>(src + d0);
+                using V = typename Vec<P>::T;
+                const int d0 = p.R + P * (u - G4);
+                *reinterpret_cast<V *>(dst + d0) = *reinterpret_cast<const V *>(src + d0);
             }
         }
     }
@@ -190,33 +208,35 @@ static rga_status check_rope(const rga_rope_args *r, bool need_qk) {
 }
 
 template <bool FUSED>
-static rga_status rope_launch(const RopeParams &p, bool bf16, long long units, cudaStream_t s) {
-    if (units <= 0 && !FUSED) return RGA_OK;
+static rga_status rope_launch(const RopeParams &p, bool bf16, bool wide, long long units4,
+                              cudaStream_t s) {
+    if (units4 <= 0 && !FUSED) return RGA_OK;
     const int sms = sm_count();
     if (sms <= 0) return RGA_ERR_CUDA;
+    // P = 8 pairs per unit (16-byte vectors) halves the units of P = 4
+    const long long units = wide ? (units4 + 1) / 2 : units4;
     long long grid = (units + ROPE_THREADS - 1) / ROPE_THREADS;
     if (grid > 4LL * sms) grid = 4LL * sms;
     if (grid < 1) grid = 1;
     const size_t smem = FUSED ? (2 * (size_t)p.B + 1) * sizeof(int) : 0;
     // 32-bit unit indices when every unit (plus one grid stride) fits
-    const bool narrow = units + grid * ROPE_THREADS < INT32_MAX;
+    const bool narrow = units4 + grid * ROPE_THREADS < INT32_MAX;
+    const int which = (bf16 ? 4 : 0) + (narrow ? 2 : 0) + (wide ? 1 : 0);
+    using K = void (*)(RopeParams);
+    static const K kernels[8] = {
+        rope_kernel<false, FUSED, long long, 4>, rope_kernel<false, FUSED, long long, 8>,
+        rope_kernel<false, FUSED, int, 4>,       rope_kernel<false, FUSED, int, 8>,
+        rope_kernel<true, FUSED, long long, 4>,  rope_kernel<true, FUSED, long long, 8>,
+        rope_kernel<true, FUSED, int, 4>,        rope_kernel<true, FUSED, int, 8>};
     if (FUSED) {
-        static std::atomic<unsigned long long> configured[4] = {{0}, {0}, {0}, {0}};
-        const cudaError_t e = once_per_device(configured[2 * bf16 + narrow], [bf16, narrow] {
-            auto k = bf16 ? (narrow ? rope_kernel<true, true, int> : rope_kernel<true, true, long long>)
-                          : (narrow ? rope_kernel<false, true, int> : rope_kernel<false, true, long long>);
-            return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static std::atomic<unsigned long long> configured[8] = {};
+        const cudaError_t e = once_per_device(configured[which], [which] {
+            return cudaFuncSetAttribute(kernels[which], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (2 * ROPE_MAX_B + 1) * (int)sizeof(int));
         });
         if (e != cudaSuccess) return RGA_ERR_CUDA;
     }
-    if (bf16) {
-        if (narrow) rope_kernel<true, FUSED, int><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
-        else rope_kernel<true, FUSED, long long><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
-    } else {
-        if (narrow) rope_kernel<false, FUSED, int><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
-        else rope_kernel<false, FUSED, long long><<<(int)grid, ROPE_THREADS, smem, s>>>(p);
-    }
+    kernels[which]<<<(int)grid, ROPE_THREADS, smem, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? RGA_OK : RGA_ERR_CUDA;
 }
 
@@ -237,7 +257,9 @@ extern "C" rga_status rga_rope_apply(const rga_rope_args *r, cudaStream_t stream
     p.cs = r->cos_sin;
     p.pos = r->positions;
     const long long units = (long long)p.T * ((p.q ? p.Hq : 0) + (p.k ? p.Hk : 0)) * (p.R / 8);
-    return rope_launch<false>(p, r->dtype == RGA_BF16, units, stream);
+    const bool wide = p.R % 16 == 0 && p.D % 8 == 0 && (!p.q || aligned(p.q, 16)) &&
+                      (!p.k || aligned(p.k, 16));
+    return rope_launch<false>(p, r->dtype == RGA_BF16, wide, units, stream);
 }
 
 extern "C" rga_status trt_kv_cache_update_rope(const rga_kv_update_args *kv,
@@ -279,5 +301,7 @@ extern "C" rga_status trt_kv_cache_update_rope(const rga_kv_update_args *kv,
     p.status = kv->device_status;
     const long long units = (long long)p.T * ((p.q ? p.Hq : 0) * (p.R / 8) +
                                              p.Hk * (p.R / 8 + (p.D - p.R) / 4));
-    return rope_launch<true>(p, r->dtype == RGA_BF16, units, stream);
+    const bool wide = p.R % 16 == 0 && p.D % 8 == 0 && (!p.q || aligned(p.q, 16)) &&
+                      aligned(p.upd, 16) && aligned(p.cache, 16);
+    return rope_launch<true>(p, r->dtype == RGA_BF16, wide, units, stream);
 }
