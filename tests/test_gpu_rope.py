@@ -33,7 +33,10 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
-@pytest.mark.parametrize("D,R", [(128, 128), (128, 64), (64, 64)])
+# (the kernel takes eight pairs per unit where the rotary dims are a multiple
+# of 16 and every base address 16-byte aligned, else four: R = 24 and 40
+# take the four-pair units)
+@pytest.mark.parametrize("D,R", [(128, 128), (128, 64), (64, 64), (128, 24), (64, 40)])
 def test_rope_in_place(dtype, D, R):
     g = torch.Generator().manual_seed(D + R)
     T, Hq, Hk = 37, 8, 2
@@ -54,7 +57,7 @@ def test_rope_in_place(dtype, D, R):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
-@pytest.mark.parametrize("R", [128, 32])
+@pytest.mark.parametrize("R", [128, 32, 40])
 def test_fused_kv_update_rope(dtype, R):
     g = torch.Generator().manual_seed(7 + R)
     B, H, N, D, Hq = 5, 2, 96, 128, 8
@@ -94,6 +97,23 @@ def test_fused_kv_update_rope(dtype, R):
                                 update_lengths=cu.cuda())
     torch.cuda.synchronize()
     assert np.array_equal(_bits(cache2), _bits(cd))
+
+
+def test_rope_in_place_on_8_byte_aligned_rows():
+    # Q and K views that start 8 bytes into their buffers: the four-pair units
+    g = torch.Generator().manual_seed(11)
+    T, Hq, Hk, D, R = 19, 4, 2, 64, 64
+    qb = torch.randn(T * Hq * D + 4, generator=g).to(torch.bfloat16)
+    kb = torch.randn(T * Hk * D + 4, generator=g).to(torch.bfloat16)
+    pos = torch.randint(0, 4096, (T,), generator=g, dtype=torch.int32)
+    cs = W.rope_cos_sin(pos, R)
+    qd, kd = qb.cuda()[4:].view(T, Hq, D), kb.cuda()[4:].view(T, Hk, D)
+    assert qd.data_ptr() % 16 == 8
+    q0, k0 = qd.cpu().clone(), kd.cpu().clone()
+    binding.rope_apply(qd, kd, cos_sin=cs.cuda(), positions=pos.cuda())
+    torch.cuda.synchronize()
+    _close(qd, oracle.rope(q0, cs, pos), torch.bfloat16)
+    _close(kd, oracle.rope(k0, cs, pos), torch.bfloat16)
 
 
 def test_fused_bad_window_changes_nothing():
