@@ -18,8 +18,11 @@
 
 namespace rga {
 
-constexpr int SCHED_THREADS = 1024;
-constexpr int COST_BUCKETS = 1024;
+#ifndef RGA_SCHED_THREADS
+#define RGA_SCHED_THREADS 256
+#endif
+constexpr int SCHED_THREADS = RGA_SCHED_THREADS;
+constexpr int COST_BUCKETS = SCHED_THREADS;
 constexpr int SCHED_MAX_B = 4096;   // per-batch prefix in shared memory up to this batch
 static_assert(COST_BUCKETS == SCHED_THREADS, "one bucket per thread in the scan");
 
@@ -43,7 +46,7 @@ __device__ __forceinline__ int block_excl_scan(int x, int *warp_sum, int *total)
     if (lane == 31) warp_sum[w] = v;
     __syncthreads();
     if (w == 0) {
-        int t = warp_sum[lane];
+        int t = lane < SCHED_THREADS / 32 ? warp_sum[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, t, o);
