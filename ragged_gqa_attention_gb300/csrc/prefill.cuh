@@ -1072,14 +1072,19 @@ template <bool BF16>
 __device__ __forceinline__ void p_chunk_q(const uint32_t (&r)[32], uint32_t s_addr, int c,
                                           uint64_t mul2, uint64_t neg2, int quant) {
     uint32_t w[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        float pa, pb;
+    auto p2 = [&](int k, float &pa, float &pb) {
         f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])), mul2, neg2),
                   pa, pb);
         pa = ex2(pa);
         pb = ex2(pb);
-        if (quant == 0) {
+    };
+    // (one loop per grid: a branch inside the loop would leave both roundings
+    // in every iteration's instruction stream)
+    if (quant == 0) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            float pa, pb;
+            p2(k, pa, pb);
             uint16_t q;
             uint32_t h;
             asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(pb), "f"(pa));
@@ -1090,7 +1095,12 @@ __device__ __forceinline__ void p_chunk_q(const uint32_t (&r)[32], uint32_t s_ad
             } else {
                 w[k] = h;
             }
-        } else {
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            float pa, pb;
+            p2(k, pa, pb);
             w[k] = pack2<BF16>(int8_round(pa), int8_round(pb));
         }
     }

@@ -336,9 +336,16 @@ __device__ __forceinline__ float2 e4m3_round2(float a, float b) {
 
 // int8 QuantizeLinear (zero point 0): round half to even, clamp to [-128, 127].
 __device__ __forceinline__ float int8_round(float x) {
+    // clamp to [-128, 127] (a NaN becomes -128), then round to the nearest
+    // integer, ties to even, by adding and subtracting 1.5 * 2^23: near that
+    // constant the fp32 spacing is 1, so the rounded sum is an integer and
+    // the difference is exact (|x| <= 128).  The same as rounding first and
+    // clamping after, on the FMA pipe instead of the conversion unit.
+    const float c = fminf(fmaxf(x, -128.f), 127.f);
     float r;
-    asm("cvt.rni.f32.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return fminf(fmaxf(r, -128.f), 127.f);
+    asm("add.rn.f32 %0, %1, 0f4B400000;" : "=f"(r) : "f"(c));   // + 12582912
+    asm("sub.rn.f32 %0, %0, 0f4B400000;" : "+f"(r));
+    return r;
 }
 
 // Four E4M3 codes (bytes 0..3 of w) as two words of 16-bit values: lo holds
