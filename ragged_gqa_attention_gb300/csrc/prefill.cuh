@@ -1465,45 +1465,52 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                 ref = lse2;   // pass 2: p / s_q directly
             }
 
-            // probabilities (or only the row sum, for a statistics step)
+            // probabilities (or only the row sum, for a statistics step);
+            // the P grid (QK: 0 fp8, 1 int8) is a constant of each copy of
+            // the loop, so that no iteration carries the other rounding
             const uint64_t mul2 = f2_pack(mul, mul), neg2 = f2_pack(-ref, -ref);
             uint64_t acc0 = 0, acc1 = 0;
+            auto probs = [&](auto qk) {
+                constexpr int QK = decltype(qk)::value;
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t w[16];
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t w[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    float pa = x[c * 32 + 2 * k], pb = x[c * 32 + 2 * k + 1];
-                    if (SOFTMAX) {
-                        f2_unpack(ffma2(f2_pack(pa, pb), mul2, neg2), pa, pb);
-                        pa = ex2(pa);
-                        pb = ex2(pb);
-                        if (MODE == MODE_SOFTMAX || stat) {
-                            if (k & 1) acc1 = fadd2(acc1, f2_pack(pa, pb));
-                            else acc0 = fadd2(acc0, f2_pack(pa, pb));
-                        }
-                    } else {
-                        pa = (__float_as_uint(pa) == NONE_EXCLUDED) ? 0.f : pa * mul;
-                        pb = (__float_as_uint(pb) == NONE_EXCLUDED) ? 0.f : pb * mul;
-                        if (MODE == MODE_NONE_Q) {
-                            pa *= inv_qs;
-                            pb *= inv_qs;
-                        }
-                    }
-                    if (QUANT && !stat) {
-                        if (p.quant == 0) {
-                            const float2 e = e4m3_round2(pa, pb);
-                            pa = e.x;
-                            pb = e.y;
+                    for (int k = 0; k < 16; ++k) {
+                        float pa = x[c * 32 + 2 * k], pb = x[c * 32 + 2 * k + 1];
+                        if (SOFTMAX) {
+                            f2_unpack(ffma2(f2_pack(pa, pb), mul2, neg2), pa, pb);
+                            pa = ex2(pa);
+                            pb = ex2(pb);
+                            if (MODE == MODE_SOFTMAX || stat) {
+                                if (k & 1) acc1 = fadd2(acc1, f2_pack(pa, pb));
+                                else acc0 = fadd2(acc0, f2_pack(pa, pb));
+                            }
                         } else {
-                            pa = int8_round(pa);
-                            pb = int8_round(pb);
+                            pa = (__float_as_uint(pa) == NONE_EXCLUDED) ? 0.f : pa * mul;
+                            pb = (__float_as_uint(pb) == NONE_EXCLUDED) ? 0.f : pb * mul;
+                            if (MODE == MODE_NONE_Q) {
+                                pa *= inv_qs;
+                                pb *= inv_qs;
+                            }
                         }
+                        if (QUANT && !stat) {
+                            if constexpr (QK == 0) {
+                                const float2 e = e4m3_round2(pa, pb);
+                                pa = e.x;
+                                pb = e.y;
+                            } else {
+                                pa = int8_round(pa);
+                                pb = int8_round(pb);
+                            }
+                        }
+                        w[k] = pack2<OPB>(pa, pb);
                     }
-                    w[k] = pack2<OPB>(pa, pb);
+                    if (!stat) tmem_st16(s_addr + c * 16, w);
                 }
-                if (!stat) tmem_st16(s_addr + c * 16, w);
-            }
+            };
+            if (QUANT && p.quant != 0) probs(std::integral_constant<int, 1>{});
+            else probs(std::integral_constant<int, 0>{});
             float s0, s1, s2, s3;
             f2_unpack(acc0, s0, s1);
             f2_unpack(acc1, s2, s3);
