@@ -31,6 +31,7 @@
 // and the V scale into the final 1/l.  An fp8 CTA runs 8 warps, since a
 // tile carries half the bytes and more arithmetic per byte.
 #pragma once
+#include <type_traits>
 #include <cuda.h>
 #include "device_common.cuh"
 #include "kernels.h"
@@ -201,19 +202,30 @@ __device__ __forceinline__ void dec_normalize_t(const AttnParams &p, const DecRo
     constexpr int NO = D / 16;
     const int r = (threadIdx.x & 31) >> 2;
     float mx[2] = {-INFINITY, -INFINITY};
+    // one copy of the loop per mask type (MK: -1 none, else the rga_dtype),
+    // so that no iteration carries the loads of the other types
+    auto scores = [&](auto mk) {
+        constexpr int MK = decltype(mk)::value;
 #pragma unroll
-    for (int mb = 0; mb < 2; ++mb)
+        for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const DecRow &R = rr[e & 1];
-            const int j = j0 + 16 * mb + r + 8 * (e >> 1);
-            bool ok = j <= R.lim;
-            float add = 0.f;
-            if (ok && p.mask) ok = mask_at(p, p.md[3] == 1 ? R.mrow : R.mrow + j, add);
-            const float v = sacc[mb][e] * sc + (SOFTMAX ? add * 1.4426950408889634f : add);
-            sacc[mb][e] = ok ? v : (SOFTMAX ? -INFINITY : 0.f);
-            mx[e & 1] = fmaxf(mx[e & 1], sacc[mb][e]);
-        }
+            for (int e = 0; e < 4; ++e) {
+                const DecRow &R = rr[e & 1];
+                const int j = j0 + 16 * mb + r + 8 * (e >> 1);
+                bool ok = j <= R.lim;
+                float add = 0.f;
+                if constexpr (MK >= 0)
+                    if (ok) ok = mask_at_t<MK>(p, p.md[3] == 1 ? R.mrow : R.mrow + j, add);
+                const float v = sacc[mb][e] * sc + (SOFTMAX ? add * 1.4426950408889634f : add);
+                sacc[mb][e] = ok ? v : (SOFTMAX ? -INFINITY : 0.f);
+                mx[e & 1] = fmaxf(mx[e & 1], sacc[mb][e]);
+            }
+    };
+    if (!p.mask) scores(std::integral_constant<int, -1>{});
+    else if (p.mask_dtype == 3) scores(std::integral_constant<int, 3>{});
+    else if (p.mask_dtype == 0) scores(std::integral_constant<int, 0>{});
+    else if (p.mask_dtype == 1) scores(std::integral_constant<int, 1>{});
+    else scores(std::integral_constant<int, 2>{});
     if (SOFTMAX) {
 #pragma unroll
         for (int i = 0; i < 2; ++i)

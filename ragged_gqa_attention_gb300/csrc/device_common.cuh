@@ -112,6 +112,27 @@ __device__ __forceinline__ bool mask_at(const AttnParams &p, long long e, float 
 }
 
 
+// mask_at for a mask type known at compile time (MK: the rga_dtype of the
+// mask, 3 bool), for loops that would otherwise carry every type's load.
+template <int MK>
+__device__ __forceinline__ bool mask_at_t(const AttnParams &p, long long e, float &add) {
+    if (!dbg_ok(e >= 0 && e < mask_elems(p), p.status)) {
+        add = 0.f;
+        return false;
+    }
+    if constexpr (MK == 3) {
+        add = 0.f;
+        return static_cast<const uint8_t *>(p.mask)[e] != 0;
+    } else if constexpr (MK == 0) {
+        add = __half2float(static_cast<const __half *>(p.mask)[e]);
+    } else if constexpr (MK == 1) {
+        add = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.mask)[e]);
+    } else {
+        add = static_cast<const float *>(p.mask)[e];
+    }
+    return true;
+}
+
 __device__ __forceinline__ float load_qscale(const AttnParams &p) {
     if (p.qscale_dtype == 0) return __half2float(*static_cast<const __half *>(p.qscale));
     if (p.qscale_dtype == 1)
