@@ -239,13 +239,13 @@ def device_timed(run, stream, steps, warmup, dist_on, sampler_index=None):
     return times, (sampler.summary() if sampler else None)
 
 
-UPLOAD_STREAMS = 4
+UPLOAD_STREAMS = 1
 
 
 def h2d_peak_gbs(nbytes=512 << 20, streams=(1, UPLOAD_STREAMS), reps=3):
-    """Best pinned host->device copy rate of this machine (GB/s), one large
-    buffer split evenly over 1 or several copy streams: the link the e2e
-    number is judged against."""
+    """Best pinned copy rates of this machine (GB/s): host->device with one large
+    buffer split evenly over 1 or several copy streams, device->host, and
+    both directions at once: the link the e2e number is judged against."""
     src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     out = {}
@@ -268,7 +268,39 @@ def h2d_peak_gbs(nbytes=512 << 20, streams=(1, UPLOAD_STREAMS), reps=3):
             ms = max(start.elapsed_time(e) for e in ends)
             best = max(best, nbytes / (ms * 1e-3) / 1e9)
         out[f"{ns}_stream" + ("s" if ns > 1 else "")] = round(best, 1)
-    del src, dst
+    # device->host alone, and both directions at once (as in the e2e loop,
+    # whose uploads and downloads overlap): host->device into one half of
+    # the device buffer while the other half goes back, bytes of both over
+    # the time of both
+    back = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    half = nbytes // 2
+    best_d2h = best_both = 0.0
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(down)
+        with torch.cuda.stream(down):
+            back.copy_(dst, non_blocking=True)
+        end.record(down)
+        torch.cuda.synchronize()
+        best_d2h = max(best_d2h, nbytes / (start.elapsed_time(end) * 1e-3) / 1e9)
+        start = torch.cuda.Event(enable_timing=True)
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        start.record(up)
+        down.wait_event(start)
+        with torch.cuda.stream(up):
+            dst[:half].copy_(src[:half], non_blocking=True)
+        ends[0].record(up)
+        with torch.cuda.stream(down):
+            back[half:].copy_(dst[half:], non_blocking=True)
+        ends[1].record(down)
+        torch.cuda.synchronize()
+        ms = max(start.elapsed_time(e) for e in ends)
+        best_both = max(best_both, 2 * half / (ms * 1e-3) / 1e9)
+    out["d2h_1_stream"] = round(best_d2h, 1)
+    out["both_directions"] = round(best_both, 1)
+    del src, dst, back
     return out
 
 
