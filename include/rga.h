@@ -16,7 +16,7 @@
  * Conventions shared by every entry point:
  *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
  *    library never allocates, frees or synchronises; all work is enqueued on
- *    the caller's stream, so a call can be captured into a CUDA graph.
+ *    the caller's stream.
  *  - Synchronous argument errors are returned as an rga_status and nothing
  *    is launched.  Errors that depend on device data (the length inputs) are
  *    detected on the device: the affected call writes a non-zero code to
@@ -242,9 +242,8 @@ rga_status trt_attention_paged_kv(const rga_attention_args *args, const rga_page
  * Returns RGA_ERR_WORKSPACE when rga_attention_workspace_size(args) exceeds
  * RGA_STATIC_SCRATCH_BYTES.  Every call looks up the array's device address
  * in the current context (cudaGetSymbolAddress, with the caller's device
- * current); the first call on a device also loads the array there, so make
- * that first call before any stream capture.  Every call shares the
- * one array: calls that overlap on the device race and give wrong results,
+ * current); the first call on a device also loads the array there.  Every
+ * call shares the one array: calls that overlap on the device race and give wrong results,
  * so serialise them (one stream, or events).  Each call rewrites all the
  * scratch it reads, so what a previous call left there does not matter. */
 rga_status trt_attention_static_scratch(const rga_attention_args *args, cudaStream_t stream);
