@@ -195,6 +195,25 @@ def test_quantized(quant, norm, dtype):
     _parity(c)
 
 
+@pytest.mark.parametrize("quant", ["fp8", "int8"])
+@pytest.mark.parametrize("kind", ["bool_rows", "additive"])
+def test_quantized_softmax_under_row_masks(quant, kind):
+    # masks that depend on the query row take the kernel's general path for
+    # both passes of the quantized softmax (each P grid in its own copy of
+    # the probability loop)
+    B, H, Nq, N = 2, 4, 200, 260
+
+    def mk(gen):
+        if kind == "bool_rows":
+            return torch.rand((B, 1, Nq, N), generator=gen) > 0.25
+        return (torch.randn((B, H, Nq, N), generator=gen) * 2).to(torch.float16)
+
+    c = W.make_case("qrows", 41 + (kind == "additive"), batch=B, q_heads=H, kv_heads=2,
+                    head_dim=128, q_lens=[Nq, 131], kv_lens=[N, 190], q_seq=Nq, kv_seq=N,
+                    dtype=torch.float16, mask=mk, quant=quant, pass_query_lengths=True)
+    _parity(c)
+
+
 @pytest.mark.parametrize("sdtype", [torch.float16, torch.bfloat16])
 def test_quantized_scale_dtypes(sdtype):
     c = W.make_case("qs", 12, batch=1, q_heads=2, kv_heads=1, head_dim=64,
