@@ -1065,26 +1065,21 @@ __device__ __forceinline__ void sum_chunk(const uint32_t (&r)[32], uint64_t mul2
 }
 
 // One 32-column chunk of the quantized pass: x = 2^(s * mul - ref) (with
-// ref = log2 of l * s_q, x is p / s_q), rounded to the fp8 E4M3 (quant 0)
-// or int8 (quant 1) grid, stored as 16-bit pairs into TMEM columns
+// ref = log2 of l * s_q, x is p / s_q), rounded to the fp8 E4M3 (QK 0)
+// or int8 (QK 1) grid, stored as 16-bit pairs into TMEM columns
 // [16c, 16c+16) of the S buffer (every code is exact in f16 and bf16).
-template <bool BF16>
+template <bool BF16, int QK>
 __device__ __forceinline__ void p_chunk_q(const uint32_t (&r)[32], uint32_t s_addr, int c,
-                                          uint64_t mul2, uint64_t neg2, int quant) {
+                                          uint64_t mul2, uint64_t neg2) {
     uint32_t w[16];
-    auto p2 = [&](int k, float &pa, float &pb) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        float pa, pb;
         f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])), mul2, neg2),
                   pa, pb);
         pa = ex2(pa);
         pb = ex2(pb);
-    };
-    // (one loop per grid: a branch inside the loop would leave both roundings
-    // in every iteration's instruction stream)
-    if (quant == 0) {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            float pa, pb;
-            p2(k, pa, pb);
+        if constexpr (QK == 0) {
             uint16_t q;
             uint32_t h;
             asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(pb), "f"(pa));
@@ -1095,13 +1090,9 @@ __device__ __forceinline__ void p_chunk_q(const uint32_t (&r)[32], uint32_t s_ad
             } else {
                 w[k] = h;
             }
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            float pa, pb;
-            p2(k, pa, pb);
-            w[k] = pack2<BF16>(int8_round(pa), int8_round(pb));
+        } else {
+            int8_round2(pa, pb);
+            w[k] = pack2<BF16>(pa, pb);
         }
     }
     tmem_st16(s_addr + c * 16, w);
@@ -1139,7 +1130,10 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&r)[32], uint32_t s_addr
     tmem_st16(s_addr + c * 16, w);
 }
 
-template <int D, int MODE, bool BF16, bool KV8>
+// QK: the quantized op's P grid (0 fp8, 1 int8; 0 for the other modes), a
+// constant of each copy of this role so that no loop carries the other
+// grid's rounding.
+template <int D, int MODE, bool BF16, bool KV8, int QK>
 __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMaps &tm,
                                              const PfBars &bar, volatile int *abort,
                                              int n_items, uint32_t tmem, int a, uint8_t *stg) {
@@ -1310,10 +1304,10 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                     // pass 2: p / s_q = 2^(s sc - lse2), quantized (0 for an
                     // excluded key or a row with no key: lse2 is +inf there)
                     const uint64_t neg2 = f2_pack(-lse2, -lse2);
-                    p_chunk_q<OPB>(ra[0], s_addr, 0, mul2, neg2, p.quant);
-                    p_chunk_q<OPB>(ra[1], s_addr, 1, mul2, neg2, p.quant);
-                    p_chunk_q<OPB>(rb[0], s_addr, 2, mul2, neg2, p.quant);
-                    p_chunk_q<OPB>(rb[1], s_addr, 3, mul2, neg2, p.quant);
+                    p_chunk_q<OPB, QK>(ra[0], s_addr, 0, mul2, neg2);
+                    p_chunk_q<OPB, QK>(ra[1], s_addr, 1, mul2, neg2);
+                    p_chunk_q<OPB, QK>(rb[0], s_addr, 2, mul2, neg2);
+                    p_chunk_q<OPB, QK>(rb[1], s_addr, 3, mul2, neg2);
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(&bar.p_full[a]);
@@ -1471,7 +1465,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
             const uint64_t mul2 = f2_pack(mul, mul), neg2 = f2_pack(-ref, -ref);
             uint64_t acc0 = 0, acc1 = 0;
             auto probs = [&](auto qk) {
-                constexpr int QK = decltype(qk)::value;
+                constexpr int QG = decltype(qk)::value;
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t w[16];
@@ -1495,13 +1489,12 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                             }
                         }
                         if (QUANT && !stat) {
-                            if constexpr (QK == 0) {
+                            if constexpr (QG == 0) {
                                 const float2 e = e4m3_round2(pa, pb);
                                 pa = e.x;
                                 pb = e.y;
                             } else {
-                                pa = int8_round(pa);
-                                pb = int8_round(pb);
+                                int8_round2(pa, pb);
                             }
                         }
                         w[k] = pack2<OPB>(pa, pb);
@@ -1509,8 +1502,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
                     if (!stat) tmem_st16(s_addr + c * 16, w);
                 }
             };
-            if (QUANT && p.quant != 0) probs(std::integral_constant<int, 1>{});
-            else probs(std::integral_constant<int, 0>{});
+            probs(std::integral_constant<int, QK>{});
             float s0, s1, s2, s3;
             f2_unpack(acc0, s0, s1);
             f2_unpack(acc1, s2, s3);
@@ -1574,6 +1566,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
 template <int D, int MODE, bool BF16, bool KV8>
 __global__ void __launch_bounds__(PF_THREADS, 1)
 prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TensorMaps tm) {
+    constexpr bool QUANT_MODE = MODE == MODE_SOFTMAX_Q || MODE == MODE_NONE_Q;
     using L = PfLayout<D, KV8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
@@ -1630,8 +1623,11 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
 
     if (warp < 8) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(PF_SOFTMAX_REGS));
-        softmax_role<D, MODE, BF16, KV8>(p, tm, bar, abort, n_items, tmem, warp >> 2,
-                                         sm + L::STG_OFF + (warp >> 2) * 4 * L::STG_WARP);
+        uint8_t *stg = sm + L::STG_OFF + (warp >> 2) * 4 * L::STG_WARP;
+        if (QUANT_MODE && p.quant != 0)
+            softmax_role<D, MODE, BF16, KV8, 1>(p, tm, bar, abort, n_items, tmem, warp >> 2, stg);
+        else
+            softmax_role<D, MODE, BF16, KV8, 0>(p, tm, bar, abort, n_items, tmem, warp >> 2, stg);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(PF_AUX_REGS));
     }

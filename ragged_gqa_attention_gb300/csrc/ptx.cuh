@@ -334,18 +334,22 @@ __device__ __forceinline__ float2 e4m3_round2(float a, float b) {
     return __half22float2(hh);
 }
 
-// int8 QuantizeLinear (zero point 0): round half to even, clamp to [-128, 127].
-__device__ __forceinline__ float int8_round(float x) {
-    // clamp to [-128, 127] (a NaN becomes -128), then round to the nearest
-    // integer, ties to even, by adding and subtracting 1.5 * 2^23: near that
-    // constant the fp32 spacing is 1, so the rounded sum is an integer and
-    // the difference is exact (|x| <= 128).  The same as rounding first and
-    // clamping after, on the FMA pipe instead of the conversion unit.
-    const float c = fminf(fmaxf(x, -128.f), 127.f);
-    float r;
-    asm("add.rn.f32 %0, %1, 0f4B400000;" : "=f"(r) : "f"(c));   // + 12582912
-    asm("sub.rn.f32 %0, %0, 0f4B400000;" : "+f"(r));
-    return r;
+// int8 QuantizeLinear (zero point 0) of two values: round half to even,
+// clamp to [-128, 127].  Each value is clamped first (a NaN becomes -128),
+// then rounded to the nearest integer, ties to even, by adding and
+// subtracting 1.5 * 2^23 (near that constant the fp32 spacing is 1, so the
+// rounded sum is an integer and the difference is exact for |x| <= 128):
+// the same as rounding first and clamping after, on the FMA pipe instead of
+// the conversion unit, both values in one packed f32x2 add and subtract
+// (flushing a subnormal to zero changes nothing: it rounds to 0 either way).
+__device__ __forceinline__ void int8_round2(float &a, float &b) {
+    const float ca = fminf(fmaxf(a, -128.f), 127.f), cb = fminf(fmaxf(b, -128.f), 127.f);
+    uint64_t x;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(ca), "f"(cb));
+    const uint64_t magic = 0x4B4000004B400000ull;   // 1.5 * 2^23 in both halves
+    asm("add.rn.ftz.f32x2 %0, %0, %1;" : "+l"(x) : "l"(magic));
+    asm("sub.rn.ftz.f32x2 %0, %0, %1;" : "+l"(x) : "l"(magic));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
 }
 
 // Four E4M3 codes (bytes 0..3 of w) as two words of 16-bit values: lo holds
