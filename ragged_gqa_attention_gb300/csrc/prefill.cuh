@@ -1132,8 +1132,9 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&r)[32], uint32_t s_addr
 
 // QK: the quantized op's P grid (0 fp8, 1 int8; 0 for the other modes), a
 // constant of each copy of this role so that no loop carries the other
-// grid's rounding.
-template <int D, int MODE, bool BF16, bool KV8, int QK>
+// grid's rounding.  PLAIN: softmax with no mask and a positive score scale,
+// where every tile takes the register path: that copy holds no general path.
+template <int D, int MODE, bool BF16, bool KV8, int QK, bool PLAIN = false>
 __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMaps &tm,
                                              const PfBars &bar, volatile int *abort,
                                              int n_items, uint32_t tmem, int a, uint8_t *stg) {
@@ -1158,7 +1159,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
     float sc = sc0;   // per item: times 2^-s of the tile's Q scaling (QCONV)
     uint32_t qcv = 0;
     const float sv = KV8 ? __ldg(p.v_scale) : 1.f;
-    const bool use_mask = p.mask != nullptr;
+    const bool use_mask = !PLAIN && p.mask != nullptr;
     const bool bool_mask = use_mask && p.mask_dtype == 3;
     const bool row_indep = bool_mask && p.md[1] == 1 && p.md[2] == 1;
     const int mk = !use_mask || bool_mask ? MK_BITS
@@ -1199,7 +1200,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
             if (!mbar_wait(&bar.s_full[a], tc & 1, abort)) { ok = false; break; }
             tc_fence_after();
             const int rem = lim - j0;
-            const bool full = !use_mask && j0 + BN - 1 <= lim_first && sc > 0.f;
+            const bool full = !use_mask && j0 + BN - 1 <= lim_first && (PLAIN || sc > 0.f);
             const bool stat = (MODE == MODE_SOFTMAX_Q) && t < m.nkt;
             // a row-independent bool mask that keeps every key of the tile
             // needs no per-score test (warp-uniform: the bits are the warp's)
@@ -1217,7 +1218,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMa
             // without a reference yet takes the max of its first 64 visible
             // scores (none visible: all its p are 0).
             if (((MODE == MODE_SOFTMAX && !use_mask) ||
-                 (MODE == MODE_SOFTMAX_Q && (!use_mask || row_indep))) && sc > 0.f) {
+                 (MODE == MODE_SOFTMAX_Q && (!use_mask || row_indep))) && (PLAIN || sc > 0.f)) {
                 const bool lim_full = j0 + BN - 1 <= lim_first;   // no causal/length limit in the tile
                 const uint64_t mul2 = f2_pack(sc, sc);
                 uint32_t ra[2][32], rb[2][32];
@@ -1626,6 +1627,9 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
         uint8_t *stg = sm + L::STG_OFF + (warp >> 2) * 4 * L::STG_WARP;
         if (QUANT_MODE && p.quant != 0)
             softmax_role<D, MODE, BF16, KV8, 1>(p, tm, bar, abort, n_items, tmem, warp >> 2, stg);
+        else if (MODE == MODE_SOFTMAX && !KV8 && !p.mask && p.scale > 0.f)
+            softmax_role<D, MODE, BF16, KV8, 0, MODE == MODE_SOFTMAX>(p, tm, bar, abort, n_items,
+                                                                     tmem, warp >> 2, stg);
         else
             softmax_role<D, MODE, BF16, KV8, 0>(p, tm, bar, abort, n_items, tmem, warp >> 2, stg);
     } else {
