@@ -1132,8 +1132,9 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&r)[32], uint32_t s_addr
 
 // QK: the quantized op's P grid (0 fp8, 1 int8; 0 for the other modes), a
 // constant of each copy of this role so that no loop carries the other
-// grid's rounding.  PLAIN: softmax with no mask and a positive score scale,
-// where every tile takes the register path: that copy holds no general path.
+// grid's rounding.  PLAIN: softmax with no mask and a positive score scale
+// (times the FP8 cache's s_k), where every tile takes the register path:
+// that copy holds no general path.
 template <int D, int MODE, bool BF16, bool KV8, int QK, bool PLAIN = false>
 __device__ __forceinline__ void softmax_role(const AttnParams &p, const TensorMaps &tm,
                                              const PfBars &bar, volatile int *abort,
@@ -1627,7 +1628,8 @@ prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ Ten
         uint8_t *stg = sm + L::STG_OFF + (warp >> 2) * 4 * L::STG_WARP;
         if (QUANT_MODE && p.quant != 0)
             softmax_role<D, MODE, BF16, KV8, 1>(p, tm, bar, abort, n_items, tmem, warp >> 2, stg);
-        else if (MODE == MODE_SOFTMAX && !KV8 && !p.mask && p.scale > 0.f)
+        else if (MODE == MODE_SOFTMAX && !p.mask && p.scale > 0.f &&
+                 (!KV8 || __ldg(p.k_scale) > 0.f))
             softmax_role<D, MODE, BF16, KV8, 0, MODE == MODE_SOFTMAX>(p, tm, bar, abort, n_items,
                                                                      tmem, warp >> 2, stg);
         else
